@@ -1,0 +1,433 @@
+"""Benchmark: paged decode / verify attention over a quantized paged KV cache.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
+
+One step is one pass of the whole path over one synthetic batch: pa_plan
+(device planner, plus the max|k_scale| reduction for per-channel scales),
+pa_run (split-KV attention) and pa_combine (log-sum-exp merge), captured in a
+CUDA graph and replayed.  L2 is flushed (a 256 MiB write) before every step,
+outside the timed events.  `value` is the effective KV bandwidth: the bytes a
+single pass must read (real tokens only, codes + scales, K and V once) divided
+by the device time of the step.
+
+The default workload is the bf16 GQA decode batch (B=64, L~U[512,8192], 32 q /
+8 kv heads, D=128, bs=16).  The other workloads of the library can be timed
+with --workload (tiny, e4m3, int8, int4).
+
+With N > 1 (torchrun, one rank per GPU) every rank times its own replica of
+the batch (requests are independent, nothing is exchanged): weak scaling,
+`value` is the sum over ranks of the bytes each processed / the slowest rank.
+
+--impl reference times the CPU fp64 oracle on the host cores instead, each
+step a bounded sample of rows of the same workload, in the same unit.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "paged-attn: effective KV HBM GB/s (% of GB300 peak) and query rows/sec"
+WORKLOAD_TEXT = {
+    "tiny": "tiny fp16 decode: B=2, L={37,70}, 4 q / 1 kv heads, D=64, bs=16, 12 blocks, fp32 out",
+    "bf16": "bf16 GQA decode: B=64, L~U[512,8192], next_n=1, 32 q / 8 kv heads, D=128, bs=16, "
+            "pool = pages + 10% slack, shuffled ids, bf16 out",
+    "e4m3": "FP8 E4M3 verify: B=32, L~U[1024,32768], next_n=4 causal, 32 q / 8 kv heads, D=256, bs=32, "
+            "per-tensor scales 0.05, NaN-poisoned null/slack/padding, bf16 out",
+    "int8": "INT8 per-channel KV: B=128, L~U[2048,16384], next_n=1, 64 q / 8 kv heads, D=128, bs=16, "
+            "k/v scales log-uniform [1e-2,1e3], q~N(0,100^2) fp16, fp32 out",
+    "int4": "INT4 per-channel KV (packed 2/byte): B=128, L~U[2048,16384], next_n=1, 64 q / 8 kv heads, "
+            "D=128, bs=16, k/v scales log-uniform [1e-2,1e3], q~N(0,100^2) fp16, fp32 out",
+}
+COMPUTE_DTYPE = {"tiny": "f16", "bf16": "bf16", "e4m3": "f16", "int8": "f16", "int4": "f16"}
+L2_FLUSH_BYTES = 256 << 20
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def _kernel_sha() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "paged_attention_quantized_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def _traffic(workload: str):
+    """DRAM bytes per attention launch from a committed ncu summary, only if it
+    was taken on the current kernel sources."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)[workload]
+        if d.get("kernel_sha") == _kernel_sha():
+            return d.get("dram_bytes_per_launch")
+    except Exception:
+        pass
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples while the timed region runs."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.t.join(timeout=2)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 6:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[2:6]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# -------------------------------------------------------------- GPU arm
+
+
+def gpu_arm(args, rank, world, local_rank):
+    import torch
+    import paged_attention_quantized_gb300 as pa
+    from paged_attention_quantized_gb300 import build as pabuild
+    from paged_attention_quantized_gb300 import workloads as W
+
+    pabuild.build()
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    w = W.make(args.workload, device=dev)
+    p = pa.problem(w)
+    out, lse, ws = pa.alloc(w, p, device=dev)
+    B = pa.binding()
+    eff_bytes = w.effective_kv_bytes()
+    rows = w.B * w.n * w.Hq
+    query_rows = w.B * w.n
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    s = torch.cuda.Stream(device=dev)
+    launches_per_step = 3 if w.k_scale_mode == "channel" else 2
+    launches_per_step += 1  # combine
+
+    def dist_barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    # correctness before timing (one sampled oracle check on rank 0)
+    with torch.cuda.stream(s):
+        pa.run(w, p, out, ws, lse, stream=s)
+    torch.cuda.synchronize()
+    bits = B.pa_get_error(ws.data_ptr(), int(s.cuda_stream))
+    if bits:
+        raise RuntimeError(f"device error bits {bits:#x}")
+    if not torch.isfinite(out.float()).all():
+        raise RuntimeError("non-finite output")
+
+    # capture one step
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        pa.run(w, p, out, ws, lse, stream=s)
+    torch.cuda.synchronize()
+
+    def flush_l2():
+        flush.fill_(1)
+
+    with torch.cuda.stream(s):
+        for _ in range(args.warmup):
+            flush_l2()
+            g.replay()
+    torch.cuda.synchronize()
+
+    clocks = ClockSampler(int(os.environ.get("CUDA_VISIBLE_DEVICES", str(local_rank)).split(",")[0])
+                          if os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",")[0].isdigit() else local_rank)
+    clocks.start()
+    time.sleep(0.3)
+    ev0 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ev1 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    dist_barrier()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(s):
+        for k in range(args.steps):
+            flush_l2()
+            ev0[k].record(s)
+            g.replay()
+            ev1[k].record(s)
+    torch.cuda.synchronize()
+    dist_barrier()
+    step_ms = [a.elapsed_time(b) for a, b in zip(ev0, ev1)]
+
+    # the attention kernel alone, eager launches on the same stream
+    a0 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    a1 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    with torch.cuda.stream(s):
+        for k in range(args.steps):
+            flush_l2()
+            pa.run(w, p, out, ws, lse, stream=s, steps="plan")
+            a0[k].record(s)
+            pa.run(w, p, out, ws, lse, stream=s, steps="run")
+            a1[k].record(s)
+            pa.run(w, p, out, ws, lse, stream=s, steps="combine")
+    torch.cuda.synchronize()
+    time.sleep(0.2)
+    clk = clocks.stop()
+    attn_ms = [a.elapsed_time(b) for a, b in zip(a0, a1)]
+
+    # end to end through the public call with host buffers: q, block_table and
+    # context_lens copied in from pinned memory, out copied back, every step
+    hq = w.q.cpu().pin_memory()
+    ht = w.block_table.cpu().pin_memory()
+    hl = w.context_lens.cpu().pin_memory()
+    ho = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(s):
+        for _ in range(max(1, args.warmup)):
+            w.q.copy_(hq, non_blocking=True)
+            pa.run(w, p, out, ws, lse, stream=s)
+    torch.cuda.synchronize()
+    dist_barrier()
+    e2e_ms = []
+    with torch.cuda.stream(s):
+        for k in range(args.steps):
+            flush_l2()
+            e0.record(s)
+            w.q.copy_(hq, non_blocking=True)
+            w.block_table.copy_(ht, non_blocking=True)
+            w.context_lens.copy_(hl, non_blocking=True)
+            pa.run(w, p, out, ws, lse, stream=s)
+            ho.copy_(out, non_blocking=True)
+            e1.record(s)
+            e1.synchronize()
+            e2e_ms.append(e0.elapsed_time(e1))
+    h2d = hq.numel() * hq.element_size() + ht.numel() * 4 + hl.numel() * 4
+    d2h = ho.numel() * ho.element_size()
+
+    total_ms = sum(step_ms)
+    attn_avg = sum(attn_ms) / len(attn_ms)
+    e2e_avg = sum(e2e_ms) / len(e2e_ms)
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([total_ms, attn_avg, e2e_avg], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms, attn_avg, e2e_avg = t.tolist()
+    ms_per_step = total_ms / args.steps
+    value = world * eff_bytes / (ms_per_step * 1e-3) / 1e9
+    peak, peak_kind = _peaks()
+    achieved = eff_bytes / (attn_avg * 1e-3) / 1e9
+    traffic = _traffic(args.workload)
+    return {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_per_step, 5),
+        "median_ms_per_step": round(statistics.median(step_ms), 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": COMPUTE_DTYPE[args.workload],
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD_TEXT[args.workload], "name": args.workload, "batch": w.B,
+                   "next_n": w.n, "total_tokens": int(w.context_lens.sum().item()),
+                   "effective_kv_bytes": eff_bytes, "l2": "flushed before every step (256 MiB write)",
+                   "parallelism": f"replicas x{world}"},
+        "query_rows_per_s": round(world * query_rows / (ms_per_step * 1e-3), 1),
+        "head_rows_per_s": round(world * rows / (ms_per_step * 1e-3), 1),
+        "pct_of_hbm_peak": round(100.0 * value / world / peak, 2),
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "traffic": traffic,
+                     "kernel": "pa_attn_kernel", "peak_source": f"{peak_kind} hbm_gbs",
+                     "attn_ms": round(attn_avg, 5)},
+        "e2e": {"value": round(world * eff_bytes / (e2e_avg * 1e-3) / 1e9, 2), "unit": "GB/s",
+                "ms_per_step": round(e2e_avg, 5), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clk,
+    }, w
+
+
+# ---------------------------------------------------------- CPU oracle arm
+
+
+def oracle_rate(w, budget_s: float, seed: int = 0):
+    """Time the oracle on a bounded, seeded sample of rows of workload w.
+    Returns (GB/s equivalent, rows/s, rows timed, seconds, threads)."""
+    import numpy as np
+    import oracle
+    host = oracle.HostArrays(w)
+    threads = len(os.sched_getaffinity(0))
+    allrows = np.stack(np.meshgrid(np.arange(w.B), np.arange(w.n), np.arange(w.Hq), indexing="ij"), -1).reshape(-1, 3)
+    rng = np.random.default_rng(seed)
+    perm = rng.permutation(len(allrows))
+    # calibrate on a few rows, then size the sample to the budget
+    n0 = min(len(allrows), max(threads, 8))
+    t0 = time.perf_counter()
+    oracle.attention(w, rows=allrows[perm[:n0]], host=host, threads=threads)
+    dt = max(1e-6, time.perf_counter() - t0)
+    n = int(min(len(allrows), max(n0, n0 * budget_s / dt)))
+    rows = allrows[perm[:n]]
+    t0 = time.perf_counter()
+    oracle.attention(w, rows=rows, host=host, threads=threads)
+    dt = time.perf_counter() - t0
+    eff = w.effective_kv_bytes() * (n / len(allrows))
+    return eff / dt / 1e9, n / dt, n, dt, threads
+
+
+def cpu_model() -> str:
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True).stdout
+        for ln in out.splitlines():
+            if ln.startswith("Model name"):
+                return ln.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    return "unknown"
+
+
+def reference_arm(args):
+    from paged_attention_quantized_gb300 import workloads as W
+    w = W.make(args.workload, device="cpu")
+    for _ in range(args.warmup):
+        oracle_rate(w, budget_s=0.5)
+    vals, rows_s, secs = [], [], []
+    n_rows = 0
+    threads = 1
+    for k in range(args.steps):
+        v, r, n, dt, threads = oracle_rate(w, budget_s=args.ref_step_s, seed=k)
+        vals.append(v)
+        rows_s.append(r)
+        secs.append(dt)
+        n_rows = n
+    value = statistics.median(vals)
+    total_rows = w.B * w.n * w.Hq
+    sample = (f"{n_rows} of {total_rows} (b, j, h) rows per step, seeded; GB/s scaled by the sampled share "
+              f"of the workload's effective KV bytes; {cpu_model()}")
+    return {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": round(value, 4),
+        "unit": "GB/s",
+        "n_gpus": args.gpus,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(1e3 * statistics.median(secs), 3),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD_TEXT[args.workload], "name": args.workload},
+        "query_rows_per_s": round(statistics.median(rows_s) / w.Hq, 3),
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+# -------------------------------------------------------------------- main
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--workload", default="bf16", choices=sorted(WORKLOAD_TEXT))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--ref-step-s", type=float, default=2.0, help="oracle seconds per reference step")
+    ap.add_argument("--cpu-baseline-s", type=float, default=12.0, help="oracle seconds for cpu_baseline")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        print(json.dumps(reference_arm(args)), flush=True)
+        return
+
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    line, w = gpu_arm(args, rank, world, local_rank)
+    if rank == 0 and not args.no_cpu_baseline:
+        from paged_attention_quantized_gb300 import workloads as W
+        wc = W.make(args.workload, device="cpu")
+        v, r, n, dt, threads = oracle_rate(wc, budget_s=args.cpu_baseline_s)
+        line["cpu_baseline"] = {"value": round(v, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
+                                "sample": f"{n} of {wc.B * wc.n * wc.Hq} (b, j, h) rows, seeded, {dt:.1f} s; "
+                                          f"GB/s scaled by the sampled share of the effective KV bytes; "
+                                          f"{cpu_model()}",
+                                "query_rows_per_s": round(r / wc.Hq, 3)}
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,218 @@
+/*
+ * pa.h -- paged decode / verify attention over a quantized paged KV cache.
+ *
+ * C ABI of the GB300 (sm_103a) library `libpa.so`.  Plain pointers and sizes
+ * only.  Every call enqueues work on the caller's CUDA stream and returns
+ * without synchronising (except pa_get_error), so a pa_plan -> pa_run ->
+ * pa_combine sequence can be captured in a CUDA graph.
+ *
+ * The operation (for request b, query row j < next_n, query head h, kv head
+ * g = h / (Hq / Hkv)):
+ *
+ *   vis   = causal ? L_b - (next_n - 1 - j) : L_b
+ *   k^_t  = dec(K[block_table[b][t / bs], g, t % bs, :]) * k_scale
+ *   v^_t  = dec(V[block_table[b][t / bs], g, t % bs, :]) * v_scale
+ *   out   = softmax_t( softmax_scale * q[b, j, h, :] . k^_t ) . v^_t   for t < vis
+ *   lse   = ln sum_t exp(softmax_scale * q . k^_t)                   (optional)
+ *   vis <= 0 gives out = 0 and lse = -inf.
+ *
+ * Sources (page title, section):
+ *  - FlashInfer docs, "flashinfer.fp4_paged_mqa_logits", Parameters: the
+ *    problem statement -- q [batch, next_n, heads, dim], a paged pool indexed by
+ *    block_table [batch, max_blocks_per_seq] int32, context_lens [batch] int32
+ *    bounded by max_context_len, a device-side schedule that is only valid for
+ *    the context_lens it was computed from, and a preallocated `out`.
+ *  - onnxruntime PR #32520, "[CUDA] Normalize the PER_CHANNEL K scale folded into
+ *    Q for paged XQA", Description / Approach: FP8 / INT8 / INT4 caches with a
+ *    per-tensor or per-(kv head, channel) scale; a single-block max|k_scale|
+ *    reduction, launched on the device so the step stays capturable, whose
+ *    result normalises the scale folded into q.
+ *  - 1Cat-vLLM PR #494, "[Bugfix][SM70] Stabilize QSA page4 order under KV
+ *    relocation", Summary / Contract and limits: work is ordered by logical
+ *    token position; results are bitwise identical when pages are relocated.
+ *  - 1Cat-vLLM PR #647, "[Bugfix][SM70] Stop grouped-page4 null-block padding
+ *    from leaking E4M3 NaN", Root cause / Fix: block 0 is the null block;
+ *    padding and unused slots never reach P.V (0 * NaN = NaN).
+ *
+ * ------------------------------------------------------------------ layouts
+ *  q            [batch][next_n][Hq][Dk]   fp16 or bf16, contiguous.
+ *  k_pool       [num_blocks] blocks; each block is [Hkv][bs][row bytes] codes,
+ *               followed -- only with PA_SCALE_TOKEN -- by [Hkv][bs] fp32
+ *               per-token scales.  Row bytes = Dk * bits / 8 (fp16/bf16 16,
+ *               E4M3/INT8 8, INT4 4).  INT4: two's-complement nibbles, channel
+ *               2i in the low nibble of byte i.  INT8: two's complement.
+ *               E4M3: the "fn" FP8 format (0x7F / 0xFF are NaN).
+ *               Base address 16-byte aligned.
+ *  v_pool       the same with Dv, or NULL when v_is_k_prefix (V is then the
+ *               first Dv channels of the K plane and uses K's scales).
+ *  block_table  [batch][max_blocks_per_seq] int32 physical block ids.  Columns
+ *               p < ceil(L_b / bs) must hold ids in [1, num_blocks); block 0 is
+ *               the null block.  Other columns are never read.
+ *  context_lens [batch] int32, 0 <= L_b <= max_context_len.
+ *  k_scale      PA_SCALE_NONE: NULL.  TENSOR: 1 fp32.  CHANNEL: [Hkv][Dk] fp32.
+ *               TOKEN: NULL (the scales live in the pool blocks).
+ *  v_scale      as k_scale with Dv (NULL when v_is_k_prefix).
+ *  out          [batch][next_n][Hq][Dv] of out_dtype (f32 / f16 / bf16).
+ *  lse          optional [batch][next_n][Hq] fp32 (natural log), or NULL.
+ *  workspace    caller-owned device memory of pa_workspace_size() bytes,
+ *               256-byte aligned.  It holds the plan, the split partials and a
+ *               device error word; its layout is reported by
+ *               pa_workspace_layout().
+ *
+ * ---------------------------------------------------------------- ownership
+ *  The caller owns every buffer.  The library allocates no memory, keeps no
+ *  per-call state outside the workspace, and reads device pointers only from
+ *  kernels.  All calls for one workspace must be ordered on one stream.
+ *  A plan is valid only for the context_lens it was made from: re-run pa_plan
+ *  (into the same workspace) whenever they change, e.g. before every replay of
+ *  a captured step.
+ *
+ * ------------------------------------------------------------------- errors
+ *  Host-detectable problems return a status and launch nothing.
+ *  Contract violations only visible on the device (a block id outside
+ *  [1, num_blocks) at a visible position, L_b outside [0, max_context_len] or
+ *  needing more than max_blocks_per_seq columns, context_lens changed since
+ *  pa_plan) set bits in the workspace's device error word and fill the
+ *  affected request's output rows with NaN.  The kernels never trap and every
+ *  wait they contain is bounded; a wait that runs out sets PA_DEV_ERR_TIMEOUT.
+ */
+#ifndef PA_H_
+#define PA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define PA_API __attribute__((visibility("default")))
+#else
+#define PA_API
+#endif
+
+/* A cudaStream_t (NULL = the legacy default stream). */
+typedef struct CUstream_st *pa_stream_t;
+
+typedef enum {
+    PA_OK = 0,
+    PA_ERR_INVALID_ARG = 1, /* bad size, NULL or misaligned pointer, bad enum */
+    PA_ERR_UNSUPPORTED = 2, /* valid problem this build has no kernel for */
+    PA_ERR_WORKSPACE = 3,   /* workspace NULL, misaligned or too small */
+    PA_ERR_CUDA = 4         /* a CUDA runtime call or launch failed */
+} pa_status;
+
+typedef enum { PA_F32 = 0, PA_F16 = 1, PA_BF16 = 2, PA_E4M3 = 3, PA_INT8 = 4, PA_INT4 = 5 } pa_dtype;
+
+typedef enum {
+    PA_SCALE_NONE = 0,    /* codes are the values */
+    PA_SCALE_TENSOR = 1,  /* one fp32 scalar */
+    PA_SCALE_CHANNEL = 2, /* one fp32 per (kv head, channel) */
+    PA_SCALE_TOKEN = 3    /* one fp32 per (block, kv head, slot), inside the block */
+} pa_scale_mode;
+
+/* Bits of the device error word (pa_get_error). */
+#define PA_DEV_ERR_BLOCK_ID 0x1u    /* visible position mapped to an id outside [1, num_blocks) */
+#define PA_DEV_ERR_CONTEXT_LEN 0x2u /* L_b < 0, > max_context_len, or > max_blocks_per_seq pages */
+#define PA_DEV_ERR_STALE_PLAN 0x4u  /* context_lens differ from the ones pa_plan saw */
+#define PA_DEV_ERR_TIMEOUT 0x8u     /* a bounded wait inside a kernel ran out */
+#define PA_DEV_ERR_PLAN_OVERFLOW 0x10u
+
+typedef struct pa_problem {
+    int32_t batch;              /* B >= 0 requests */
+    int32_t next_n;             /* query rows per request, >= 1 */
+    int32_t num_q_heads;        /* Hq */
+    int32_t num_kv_heads;       /* Hkv, divides Hq */
+    int32_t head_dim_k;         /* Dk */
+    int32_t head_dim_v;         /* Dv */
+    int32_t block_size;         /* bs, tokens per block */
+    int32_t num_blocks;         /* blocks in the pool (block 0 = null block) */
+    int32_t max_blocks_per_seq; /* block_table columns */
+    int32_t max_context_len;    /* bound on every context_lens entry */
+    int32_t q_dtype;            /* PA_F16 or PA_BF16 */
+    int32_t kv_dtype;           /* PA_F16, PA_BF16, PA_E4M3, PA_INT8, PA_INT4 */
+    int32_t out_dtype;          /* PA_F32, PA_F16, PA_BF16 */
+    int32_t k_scale_mode;       /* pa_scale_mode */
+    int32_t v_scale_mode;       /* pa_scale_mode (ignored when v_is_k_prefix) */
+    int32_t causal;             /* 1: row j sees tokens [0, L_b - next_n + j] */
+    int32_t v_is_k_prefix;      /* 1: V = first Dv channels of the K plane */
+    int32_t num_sms;            /* planner target width; 0 = current device's SM count */
+    int32_t split_target;       /* CTAs the planner aims for; 0 = library default */
+    int32_t split_pages;        /* > 0: force this many pages per split (tests) */
+    float softmax_scale;        /* e.g. 1/sqrt(Dk) */
+} pa_problem;
+
+/* Byte offsets inside the workspace (all 256-byte aligned) and the effective
+ * planner parameters.  Header words (uint32): [0] device error bits,
+ * [1] number of work units, [2] pages per split, [3] max|k_scale| (fp32 bits).
+ * Request records (int32 x4 per request): {L_b seen by pa_plan, splits S_b,
+ * first split index, flags}.  Unit records (int32 x4): {b, kv_head << 16 |
+ * split, first page, end page}; unit u = first_split_index(b) * Hkv +
+ * kv_head * S_b + split.  Partials: fp32 [max_units][rows_per_kv_head][Dv]
+ * normalised outputs and fp32 [max_units][rows_per_kv_head] log-sum-exp, row
+ * r = j * (Hq / Hkv) + (h mod (Hq / Hkv)). */
+typedef struct pa_layout {
+    size_t total_bytes;
+    size_t header_offset;
+    size_t requests_offset;
+    size_t units_offset;
+    size_t partial_o_offset;
+    size_t partial_lse_offset;
+    int32_t max_units;
+    int32_t rows_per_kv_head;
+    int32_t row_blocks;      /* CTAs per unit along the rows */
+    int32_t num_sms;         /* effective */
+    int32_t split_target;    /* effective */
+    int32_t min_split_pages; /* effective */
+} pa_layout;
+
+/* Library version: major * 10000 + minor * 100 + patch. */
+PA_API int pa_version(void);
+
+/* Human-readable name of a status code (static string). */
+PA_API const char *pa_status_string(pa_status s);
+
+/* Workspace bytes needed by pa_plan / pa_run / pa_combine for problem *p.
+ * Host only; with p->num_sms == 0 it queries the current device. */
+PA_API pa_status pa_workspace_size(const pa_problem *p, size_t *bytes);
+
+/* Workspace layout for *p (host only, as pa_workspace_size). */
+PA_API pa_status pa_workspace_layout(const pa_problem *p, pa_layout *layout);
+
+/* Plan the work for the current context_lens (device pointer).  With
+ * PA_SCALE_CHANNEL K scales, also reduces max|k_scale| over every (kv head,
+ * channel) on the device (k_scale: device [Hkv][Dk] fp32); otherwise k_scale
+ * may be NULL.  Clears the device error word.  Launches 1-2 kernels. */
+PA_API pa_status pa_plan(const pa_problem *p, const int32_t *context_lens, const float *k_scale,
+                         void *workspace, size_t workspace_bytes, pa_stream_t stream);
+
+/* The attention itself over the planned units.  Requests with one split write
+ * `out` (and `lse` if not NULL) directly; split requests write partials into
+ * the workspace for pa_combine.  All pointers are device pointers. */
+PA_API pa_status pa_run(const pa_problem *p, const void *q, const void *k_pool, const void *v_pool,
+                        const int32_t *block_table, const int32_t *context_lens,
+                        const float *k_scale, const float *v_scale, void *workspace,
+                        size_t workspace_bytes, void *out, float *lse, pa_stream_t stream);
+
+/* Merge the partials of split requests (log-sum-exp, ascending split order),
+ * apply the V scale and write `out` / `lse` for them.  Requests with one
+ * split are left untouched. */
+PA_API pa_status pa_combine(const pa_problem *p, const float *v_scale, void *workspace,
+                            size_t workspace_bytes, void *out, float *lse, pa_stream_t stream);
+
+/* pa_plan + pa_run + pa_combine in one call (same arguments). */
+PA_API pa_status pa_attention(const pa_problem *p, const void *q, const void *k_pool,
+                              const void *v_pool, const int32_t *block_table,
+                              const int32_t *context_lens, const float *k_scale,
+                              const float *v_scale, void *workspace, size_t workspace_bytes,
+                              void *out, float *lse, pa_stream_t stream);
+
+/* Copy the device error word to *bits.  Synchronises `stream`. */
+PA_API pa_status pa_get_error(const void *workspace, uint32_t *bits, pa_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PA_H_ */

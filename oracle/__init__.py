@@ -43,7 +43,7 @@ _ERR = {0: "ok", 1: "bad argument", 2: "block id out of range", 3: "out of memor
 class _Problem(ctypes.Structure):
     _fields_ = [(k, ctypes.c_int32) for k in
                 ("B", "n", "Hq", "Hkv", "Dk", "Dv", "bs", "num_blocks", "max_blocks_per_seq",
-                 "q_dtype", "kv_dtype", "k_scale_mode", "v_scale_mode", "v_is_k_prefix")] + \
+                 "q_dtype", "kv_dtype", "k_scale_mode", "v_scale_mode", "v_is_k_prefix", "causal")] + \
               [("softmax_scale", ctypes.c_double)]
 
 
@@ -110,7 +110,8 @@ def _problem(w) -> _Problem:
                     num_blocks=w.num_blocks, max_blocks_per_seq=w.max_blocks_per_seq,
                     q_dtype=_DT[w.q_dtype], kv_dtype=_DT[w.kv_dtype],
                     k_scale_mode=_SM[w.k_scale_mode], v_scale_mode=_SM[w.v_scale_mode],
-                    v_is_k_prefix=int(bool(w.v_is_k_prefix)), softmax_scale=float(w.softmax_scale))
+                    v_is_k_prefix=int(bool(w.v_is_k_prefix)), causal=int(bool(w.causal)),
+                    softmax_scale=float(w.softmax_scale))
 
 
 class HostArrays:

@@ -10,8 +10,9 @@
  *
  *   For request b, query row j in [0, n) and query head h, with kv head
  *   g = h / (Hq / Hkv):
- *     vis      = L_b - (n - 1 - j)             (row j sits at logical position
+ *     vis      = L_b - (n - 1 - j)  if causal   (row j sits at logical position
  *                                               L_b - n + j and sees tokens up to it)
+ *              = L_b                otherwise
  *     for t in [0, vis):
  *        blk   = block_table[b][t / bs],  slot = t % bs
  *        k^[d] = dec(Kcode[blk, g, slot, d]) * ks(g, d, blk, slot)
@@ -70,6 +71,7 @@ typedef struct {
     int32_t q_dtype, kv_dtype;
     int32_t k_scale_mode, v_scale_mode;
     int32_t v_is_k_prefix;
+    int32_t causal;
     double softmax_scale;
 } orc_problem;
 
@@ -193,7 +195,7 @@ static int one_row(const orc_job *J, int b, int j, int h, double *out, double *l
     const int G = p->Hq / p->Hkv;
     const int g = h / G;
     const int L = J->context_lens[b];
-    const int vis = L - (p->n - 1 - j);
+    const int vis = p->causal ? L - (p->n - 1 - j) : L;
     const int k_tok = p->k_scale_mode == ORC_SCALE_TOKEN;
     const int v_from_k = p->v_is_k_prefix != 0;
     const int v_mode = v_from_k ? p->k_scale_mode : p->v_scale_mode;
@@ -369,7 +371,7 @@ int orc_row_ties(const orc_problem *p, const void *q, const void *k_pool, const 
     J.k_scale = k_scale;
     J.v_scale = v_scale;
     const int L = context_lens[b];
-    const int vis = L - (p->n - 1 - j);
+    const int vis = p->causal ? L - (p->n - 1 - j) : L;
     *count = 0;
     *gap = INFINITY;
     for (int d = 0; d < p->Dv; ++d) { vmin[d] = INFINITY; vmax[d] = -INFINITY; }

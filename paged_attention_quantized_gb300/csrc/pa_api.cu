@@ -1,0 +1,385 @@
+// Host side of the C ABI declared in include/pa.h: argument validation,
+// workspace layout, tensor-map encoding and kernel dispatch.  No allocation,
+// no synchronisation (except pa_get_error), no global state beyond cached
+// driver entry points and per-device SM counts.
+#include <cudaTypedefs.h>
+
+#include <atomic>
+#include <cmath>
+#include <cstring>
+#include <mutex>
+
+#include "pa_attn_launch.cuh"
+
+namespace pa {
+cudaError_t launch_plan(const PlanParams &P, const float *k_scale, int k_count, cudaStream_t s);
+cudaError_t launch_combine(const CombineParams &P, cudaStream_t s);
+}  // namespace pa
+
+namespace {
+
+constexpr int VERSION = 100;
+constexpr size_t RING_TARGET_BYTES = 96 * 1024;
+constexpr int DEFAULT_TARGET_PER_SM = 8;
+constexpr int MIN_SPLIT_TOKENS = 512;
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+int dtype_bits(int dt) {
+    switch (dt) {
+        case PA_F16: case PA_BF16: return 16;
+        case PA_E4M3: case PA_INT8: return 8;
+        case PA_INT4: return 4;
+        default: return 0;
+    }
+}
+
+std::atomic<int> g_sms[64];
+
+pa_status device_sms(int *sms) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return PA_ERR_CUDA;
+    if (dev >= 0 && dev < 64) {
+        const int c = g_sms[dev].load(std::memory_order_relaxed);
+        if (c > 0) { *sms = c; return PA_OK; }
+    }
+    int v = 0;
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0)
+        return PA_ERR_CUDA;
+    if (dev >= 0 && dev < 64) g_sms[dev].store(v, std::memory_order_relaxed);
+    *sms = v;
+    return PA_OK;
+}
+
+// Everything derived from a problem on the host.
+struct Derived {
+    int G, R, row_blocks, sms, target, min_pages, T;
+    long long max_units;
+    int D, RB, SW, stage_bytes, stages;
+    size_t k_block, v_block, smem;
+    pa_layout L;
+};
+
+pa_status derive(const pa_problem *p, Derived *d) {
+    if (p == nullptr || d == nullptr) return PA_ERR_INVALID_ARG;
+    if (p->batch < 0 || p->next_n < 1 || p->num_q_heads < 1 || p->num_kv_heads < 1 ||
+        p->num_q_heads % p->num_kv_heads != 0 || p->head_dim_k < 1 || p->head_dim_v < 1 ||
+        p->block_size < 1 || p->num_blocks < 1 || p->max_blocks_per_seq < 1 || p->max_context_len < 0 ||
+        p->num_sms < 0 || p->split_target < 0 || p->split_pages < 0)
+        return PA_ERR_INVALID_ARG;
+    if ((p->q_dtype != PA_F16 && p->q_dtype != PA_BF16) || dtype_bits(p->kv_dtype) == 0 ||
+        (p->out_dtype != PA_F32 && p->out_dtype != PA_F16 && p->out_dtype != PA_BF16))
+        return PA_ERR_INVALID_ARG;
+    if (p->k_scale_mode < PA_SCALE_NONE || p->k_scale_mode > PA_SCALE_TOKEN || p->v_scale_mode < PA_SCALE_NONE ||
+        p->v_scale_mode > PA_SCALE_TOKEN)
+        return PA_ERR_INVALID_ARG;
+    if (!std::isfinite(p->softmax_scale)) return PA_ERR_INVALID_ARG;
+    if (p->causal != 0 && p->causal != 1) return PA_ERR_INVALID_ARG;
+    if (p->v_is_k_prefix != 0 && p->v_is_k_prefix != 1) return PA_ERR_INVALID_ARG;
+    if (p->kv_dtype == PA_INT4 && ((p->head_dim_k & 1) || (p->head_dim_v & 1))) return PA_ERR_INVALID_ARG;
+
+    // kernel coverage of this build
+    if (p->v_is_k_prefix || p->k_scale_mode == PA_SCALE_TOKEN || p->v_scale_mode == PA_SCALE_TOKEN)
+        return PA_ERR_UNSUPPORTED;
+    if (p->head_dim_k != p->head_dim_v) return PA_ERR_UNSUPPORTED;
+    const int D = p->head_dim_k;
+    if (D != 64 && D != 128 && D != 256) return PA_ERR_UNSUPPORTED;
+    if (p->kv_dtype == PA_INT4 && D == 64) return PA_ERR_UNSUPPORTED;
+    if (p->block_size % 16 != 0 || p->block_size > 128) return PA_ERR_UNSUPPORTED;
+    if (p->num_kv_heads > 65535) return PA_ERR_UNSUPPORTED;
+
+    d->D = D;
+    d->G = p->num_q_heads / p->num_kv_heads;
+    const long long R = (long long)d->G * p->next_n;
+    if (R > (1 << 20)) return PA_ERR_UNSUPPORTED;
+    d->R = (int)R;
+    d->row_blocks = (d->R + 15) / 16;
+    if (d->row_blocks > 65535) return PA_ERR_UNSUPPORTED;
+    if (p->num_sms > 0) d->sms = p->num_sms;
+    else {
+        const pa_status st = device_sms(&d->sms);
+        if (st != PA_OK) return st;
+    }
+    d->target = p->split_target > 0 ? p->split_target : DEFAULT_TARGET_PER_SM * d->sms;
+    d->min_pages = std::max(1, MIN_SPLIT_TOKENS / p->block_size);
+    d->T = std::max(1, d->target / (p->num_kv_heads * d->row_blocks));
+
+    const int bs = p->block_size;
+    const long long pages_ctx = ((long long)p->max_context_len + bs - 1) / bs;
+    const long long Pmax = std::min<long long>(p->max_blocks_per_seq, pages_ctx);
+    long long u_req;
+    if (p->split_pages > 0) {
+        const long long per = std::max<long long>(1, (Pmax + p->split_pages - 1) / p->split_pages);
+        if (per > 65535) return PA_ERR_UNSUPPORTED;
+        u_req = (long long)p->batch * per;
+    } else {
+        const long long per = std::max<long long>(1, (Pmax + d->min_pages - 1) / d->min_pages);
+        if (per > 65535) return PA_ERR_UNSUPPORTED;
+        u_req = std::min<long long>((long long)p->batch * per, (long long)p->batch + d->T);
+    }
+    d->max_units = u_req * p->num_kv_heads;
+    if (d->max_units > (1ll << 30)) return PA_ERR_UNSUPPORTED;
+
+    const int bits = dtype_bits(p->kv_dtype);
+    d->RB = D * bits / 8;
+    d->SW = d->RB >= 128 ? 128 : 64;
+    d->k_block = (size_t)p->num_kv_heads * bs * d->RB;
+    d->v_block = d->k_block;
+    d->stage_bytes = 2 * bs * d->RB;
+    d->stages = (int)std::min<size_t>(pa::MAX_STAGES, std::max<size_t>(2, RING_TARGET_BYTES / d->stage_bytes));
+    d->smem = pa::attn_smem_bytes(D, d->stages, d->stage_bytes);
+    if (d->smem > 227 * 1024) return PA_ERR_UNSUPPORTED;
+
+    pa_layout &Lo = d->L;
+    std::memset(&Lo, 0, sizeof(Lo));
+    size_t off = 0;
+    Lo.header_offset = off;
+    off = align_up(off + 64, 256);
+    Lo.requests_offset = off;
+    off = align_up(off + (size_t)p->batch * 16, 256);
+    Lo.units_offset = off;
+    off = align_up(off + (size_t)d->max_units * 16, 256);
+    Lo.partial_o_offset = off;
+    off = align_up(off + (size_t)d->max_units * d->R * p->head_dim_v * 4, 256);
+    Lo.partial_lse_offset = off;
+    off = align_up(off + (size_t)d->max_units * d->R * 4, 256);
+    Lo.total_bytes = off;
+    Lo.max_units = (int32_t)d->max_units;
+    Lo.rows_per_kv_head = d->R;
+    Lo.row_blocks = d->row_blocks;
+    Lo.num_sms = d->sms;
+    Lo.split_target = d->target;
+    Lo.min_split_pages = d->min_pages;
+    return PA_OK;
+}
+
+pa_status check_ws(const Derived &d, void *ws, size_t bytes) {
+    if (ws == nullptr || (reinterpret_cast<uintptr_t>(ws) & 255) != 0 || bytes < d.L.total_bytes)
+        return PA_ERR_WORKSPACE;
+    return PA_OK;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static std::once_flag once;
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    std::call_once(once, [] {
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    });
+    return fn;
+}
+
+// [num_blocks][Hkv][bs][RB] bytes (block stride may exceed Hkv*bs*RB), box
+// [SW bytes][bs][1][1], swizzled by SW.
+pa_status make_tmap(CUtensorMap *tm, const void *base, const Derived &d, const pa_problem *p, size_t block_stride) {
+    auto enc = encode_fn();
+    if (enc == nullptr) return PA_ERR_CUDA;
+    cuuint64_t dims[4] = {(cuuint64_t)d.RB, (cuuint64_t)p->block_size, (cuuint64_t)p->num_kv_heads,
+                          (cuuint64_t)p->num_blocks};
+    cuuint64_t strides[3] = {(cuuint64_t)d.RB, (cuuint64_t)p->block_size * d.RB, (cuuint64_t)block_stride};
+    cuuint32_t box[4] = {(cuuint32_t)d.SW, (cuuint32_t)p->block_size, 1, 1};
+    cuuint32_t es[4] = {1, 1, 1, 1};
+    CUresult r = enc(tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void *>(base), dims, strides, box, es,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE,
+                     d.SW == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? PA_OK : PA_ERR_CUDA;
+}
+
+template <typename T>
+T *at(void *ws, size_t off) {
+    return reinterpret_cast<T *>(static_cast<uint8_t *>(ws) + off);
+}
+
+cudaError_t dispatch_attn(const pa_problem *p, const Derived &d, const CUtensorMap &tk, const CUtensorMap &tv,
+                          const pa::AttnParams &P, cudaStream_t s) {
+    const dim3 grid((unsigned)d.max_units, (unsigned)d.row_blocks);
+    if (d.max_units == 0) return cudaSuccess;
+#define PA_CASE(KVT, DD) \
+    if (p->kv_dtype == KVT && d.D == DD) return pa::launch_attn<KVT, DD>(tk, tv, P, grid, d.smem, s);
+    PA_CASE(PA_F16, 64) PA_CASE(PA_F16, 128) PA_CASE(PA_F16, 256)
+    PA_CASE(PA_BF16, 64) PA_CASE(PA_BF16, 128) PA_CASE(PA_BF16, 256)
+    PA_CASE(PA_E4M3, 64) PA_CASE(PA_E4M3, 128) PA_CASE(PA_E4M3, 256)
+    PA_CASE(PA_INT8, 64) PA_CASE(PA_INT8, 128) PA_CASE(PA_INT8, 256)
+    PA_CASE(PA_INT4, 128) PA_CASE(PA_INT4, 256)
+#undef PA_CASE
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace
+
+extern "C" {
+
+PA_API int pa_version(void) { return VERSION; }
+
+PA_API const char *pa_status_string(pa_status s) {
+    switch (s) {
+        case PA_OK: return "PA_OK";
+        case PA_ERR_INVALID_ARG: return "PA_ERR_INVALID_ARG";
+        case PA_ERR_UNSUPPORTED: return "PA_ERR_UNSUPPORTED";
+        case PA_ERR_WORKSPACE: return "PA_ERR_WORKSPACE";
+        case PA_ERR_CUDA: return "PA_ERR_CUDA";
+        default: return "PA_ERR_UNKNOWN";
+    }
+}
+
+PA_API pa_status pa_workspace_layout(const pa_problem *p, pa_layout *layout) {
+    if (layout == nullptr) return PA_ERR_INVALID_ARG;
+    Derived d;
+    const pa_status st = derive(p, &d);
+    if (st != PA_OK) return st;
+    *layout = d.L;
+    return PA_OK;
+}
+
+PA_API pa_status pa_workspace_size(const pa_problem *p, size_t *bytes) {
+    if (bytes == nullptr) return PA_ERR_INVALID_ARG;
+    Derived d;
+    const pa_status st = derive(p, &d);
+    if (st != PA_OK) return st;
+    *bytes = d.L.total_bytes;
+    return PA_OK;
+}
+
+PA_API pa_status pa_plan(const pa_problem *p, const int32_t *context_lens, const float *k_scale, void *workspace,
+                         size_t workspace_bytes, pa_stream_t stream) {
+    Derived d;
+    pa_status st = derive(p, &d);
+    if (st != PA_OK) return st;
+    if ((st = check_ws(d, workspace, workspace_bytes)) != PA_OK) return st;
+    if (p->batch > 0 && context_lens == nullptr) return PA_ERR_INVALID_ARG;
+    if (p->k_scale_mode == PA_SCALE_CHANNEL && k_scale == nullptr) return PA_ERR_INVALID_ARG;
+    pa::PlanParams P;
+    P.context_lens = context_lens;
+    P.hdr = at<uint32_t>(workspace, d.L.header_offset);
+    P.req = at<int4>(workspace, d.L.requests_offset);
+    P.units = at<int4>(workspace, d.L.units_offset);
+    P.B = p->batch;
+    P.Hkv = p->num_kv_heads;
+    P.bs = p->block_size;
+    P.max_ctx = p->max_context_len;
+    P.mbps = p->max_blocks_per_seq;
+    P.T = d.T;
+    P.min_pages = d.min_pages;
+    P.forced_pages = p->split_pages;
+    P.max_units = (int)d.max_units;
+    const float *ks = (p->k_scale_mode == PA_SCALE_CHANNEL) ? k_scale : nullptr;
+    cudaError_t e = pa::launch_plan(P, ks, p->num_kv_heads * p->head_dim_k, reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+PA_API pa_status pa_run(const pa_problem *p, const void *q, const void *k_pool, const void *v_pool,
+                        const int32_t *block_table, const int32_t *context_lens, const float *k_scale,
+                        const float *v_scale, void *workspace, size_t workspace_bytes, void *out, float *lse,
+                        pa_stream_t stream) {
+    Derived d;
+    pa_status st = derive(p, &d);
+    if (st != PA_OK) return st;
+    if ((st = check_ws(d, workspace, workspace_bytes)) != PA_OK) return st;
+    if (p->batch == 0) return PA_OK;
+    if (q == nullptr || k_pool == nullptr || v_pool == nullptr || block_table == nullptr ||
+        context_lens == nullptr || out == nullptr)
+        return PA_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(k_pool) & 15) || (reinterpret_cast<uintptr_t>(v_pool) & 15) ||
+        (reinterpret_cast<uintptr_t>(q) & 1))
+        return PA_ERR_INVALID_ARG;
+    if ((p->k_scale_mode == PA_SCALE_TENSOR || p->k_scale_mode == PA_SCALE_CHANNEL) && k_scale == nullptr)
+        return PA_ERR_INVALID_ARG;
+    if ((p->v_scale_mode == PA_SCALE_TENSOR || p->v_scale_mode == PA_SCALE_CHANNEL) && v_scale == nullptr)
+        return PA_ERR_INVALID_ARG;
+    CUtensorMap tk, tv;
+    if ((st = make_tmap(&tk, k_pool, d, p, d.k_block)) != PA_OK) return st;
+    if ((st = make_tmap(&tv, v_pool, d, p, d.v_block)) != PA_OK) return st;
+    pa::AttnParams P;
+    P.q = static_cast<const uint8_t *>(q);
+    P.block_table = block_table;
+    P.context_lens = context_lens;
+    P.k_scale = k_scale;
+    P.v_scale = v_scale;
+    P.hdr = at<uint32_t>(workspace, d.L.header_offset);
+    P.req = at<const int4>(workspace, d.L.requests_offset);
+    P.units = at<const int4>(workspace, d.L.units_offset);
+    P.part_o = at<float>(workspace, d.L.partial_o_offset);
+    P.part_lse = at<float>(workspace, d.L.partial_lse_offset);
+    P.out = out;
+    P.lse = lse;
+    P.B = p->batch;
+    P.n = p->next_n;
+    P.Hq = p->num_q_heads;
+    P.Hkv = p->num_kv_heads;
+    P.G = d.G;
+    P.R = d.R;
+    P.bs = p->block_size;
+    P.mbps = p->max_blocks_per_seq;
+    P.max_ctx = p->max_context_len;
+    P.num_blocks = p->num_blocks;
+    P.q_dtype = p->q_dtype;
+    P.out_dtype = p->out_dtype;
+    P.k_mode = p->k_scale_mode;
+    P.v_mode = p->v_scale_mode;
+    P.causal = p->causal;
+    P.stages = d.stages;
+    P.stage_bytes = d.stage_bytes;
+    P.max_units = (int)d.max_units;
+    P.softmax_scale = p->softmax_scale;
+    cudaError_t e = dispatch_attn(p, d, tk, tv, P, reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+PA_API pa_status pa_combine(const pa_problem *p, const float *v_scale, void *workspace, size_t workspace_bytes,
+                            void *out, float *lse, pa_stream_t stream) {
+    Derived d;
+    pa_status st = derive(p, &d);
+    if (st != PA_OK) return st;
+    if ((st = check_ws(d, workspace, workspace_bytes)) != PA_OK) return st;
+    if (p->batch == 0) return PA_OK;
+    if (out == nullptr) return PA_ERR_INVALID_ARG;
+    if ((p->v_scale_mode == PA_SCALE_TENSOR || p->v_scale_mode == PA_SCALE_CHANNEL) && v_scale == nullptr)
+        return PA_ERR_INVALID_ARG;
+    pa::CombineParams P;
+    P.req = at<const int4>(workspace, d.L.requests_offset);
+    P.part_o = at<const float>(workspace, d.L.partial_o_offset);
+    P.part_lse = at<const float>(workspace, d.L.partial_lse_offset);
+    P.v_scale = v_scale;
+    P.out = out;
+    P.lse = lse;
+    P.B = p->batch;
+    P.n = p->next_n;
+    P.Hq = p->num_q_heads;
+    P.Hkv = p->num_kv_heads;
+    P.G = d.G;
+    P.R = d.R;
+    P.Dv = p->head_dim_v;
+    P.out_dtype = p->out_dtype;
+    P.v_mode = p->v_scale_mode;
+    P.max_units = d.max_units;
+    cudaError_t e = pa::launch_combine(P, reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+PA_API pa_status pa_attention(const pa_problem *p, const void *q, const void *k_pool, const void *v_pool,
+                              const int32_t *block_table, const int32_t *context_lens, const float *k_scale,
+                              const float *v_scale, void *workspace, size_t workspace_bytes, void *out, float *lse,
+                              pa_stream_t stream) {
+    pa_status st = pa_plan(p, context_lens, k_scale, workspace, workspace_bytes, stream);
+    if (st != PA_OK) return st;
+    st = pa_run(p, q, k_pool, v_pool, block_table, context_lens, k_scale, v_scale, workspace, workspace_bytes, out,
+                lse, stream);
+    if (st != PA_OK) return st;
+    return pa_combine(p, v_scale, workspace, workspace_bytes, out, lse, stream);
+}
+
+PA_API pa_status pa_get_error(const void *workspace, uint32_t *bits, pa_stream_t stream) {
+    if (workspace == nullptr || bits == nullptr) return PA_ERR_INVALID_ARG;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (cudaMemcpyAsync(bits, workspace, sizeof(uint32_t), cudaMemcpyDeviceToHost, s) != cudaSuccess)
+        return PA_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return PA_ERR_CUDA;
+    return PA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,235 @@
+// Device helpers shared by the paged-attention kernels (sm_103a).
+// Inline PTX for mbarriers, bulk tensor copies (TMA), warp-level MMA and the
+// packed conversions used to dequantize KV codes in registers.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <stdint.h>
+
+#include "pa.h"
+
+namespace pa {
+
+// ------------------------------------------------------------ kernel params
+
+struct AttnParams {
+    const uint8_t *q;
+    const int32_t *block_table;
+    const int32_t *context_lens;
+    const float *k_scale;
+    const float *v_scale;
+    uint32_t *hdr;       // workspace header words
+    const int4 *req;     // per-request plan records
+    const int4 *units;   // unit records
+    float *part_o;       // [max_units][R][Dv]
+    float *part_lse;     // [max_units][R]
+    void *out;
+    float *lse;
+    int B, n, Hq, Hkv, G, R, bs, mbps, max_ctx, num_blocks;
+    int q_dtype, out_dtype, k_mode, v_mode, causal;
+    int stages, stage_bytes;
+    int max_units;
+    float softmax_scale;
+};
+
+struct PlanParams {
+    const int32_t *context_lens;
+    uint32_t *hdr;
+    int4 *req;
+    int4 *units;
+    int B, Hkv, bs, max_ctx, mbps;
+    int T, min_pages, forced_pages, max_units;
+};
+
+struct CombineParams {
+    const int4 *req;
+    const float *part_o;
+    const float *part_lse;
+    const float *v_scale;
+    void *out;
+    float *lse;
+    int B, n, Hq, Hkv, G, R, Dv, out_dtype, v_mode;
+    long long max_units;
+};
+
+// header word indices
+constexpr int HDR_ERR = 0;
+constexpr int HDR_NUM_UNITS = 1;
+constexpr int HDR_CHUNK = 2;
+constexpr int HDR_KMAX = 3;
+
+// bounded waits: give up after this many nanoseconds of %globaltimer
+constexpr unsigned long long WAIT_LIMIT_NS = 2000000000ull;
+
+// ------------------------------------------------------------------ basics
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ unsigned long long globaltimer() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__device__ __forceinline__ float lg2(float x) {
+    float y;
+    asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// ---------------------------------------------------------------- mbarrier
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_fence_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Wait for the phase of `bar` with the given parity.  Gives up (returns
+// false) when *abort becomes non-zero or after WAIT_LIMIT_NS.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity, volatile int *abort) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const unsigned long long t0 = globaltimer();
+    while (true) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (*abort) return false;
+        if (globaltimer() - t0 > WAIT_LIMIT_NS) return false;
+    }
+}
+
+// -------------------------------------------------------------------- TMA
+
+// 4-D tiled bulk tensor copy global -> shared, completion counted on `bar`.
+__device__ __forceinline__ void tma_load_4d(void *dst, const CUtensorMap *tm, uint64_t *bar, int x, int y, int z,
+                                            int w) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(z), "r"(w), "r"(smem_u32(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap *tm) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tm)) : "memory");
+}
+
+// -------------------------------------------------------------------- MMA
+
+// D = A * B + D, m16n8k16, fp32 accumulate.  A row-major (4 regs), B
+// column-major (2 regs), C/D 4 floats.
+template <bool BF16>
+__device__ __forceinline__ void mma16816(float c[4], const uint32_t a[4], uint32_t b0, uint32_t b1) {
+    if constexpr (BF16) {
+        asm volatile(
+            "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+            "{%0,%1,%2,%3};"
+            : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+            : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+    } else {
+        asm volatile(
+            "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+            "{%0,%1,%2,%3};"
+            : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+            : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+    }
+}
+
+// ------------------------------------------------------------- conversions
+
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+    __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&h);
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&h);
+}
+
+template <bool BF16>
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+    if constexpr (BF16) return pack_bf16x2(lo, hi);
+    else return pack_f16x2(lo, hi);
+}
+
+// two E4M3 codes (low byte -> low half) to f16x2, exact
+__device__ __forceinline__ uint32_t e4m3x2_f16x2(uint32_t two_codes) {
+    uint32_t r;
+    const uint16_t v = static_cast<uint16_t>(two_codes & 0xFFFFu);
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(v));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t hsub2_u(uint32_t a, uint32_t b) {
+    __half2 r = __hsub2(*reinterpret_cast<__half2 *>(&a), *reinterpret_cast<__half2 *>(&b));
+    return *reinterpret_cast<uint32_t *>(&r);
+}
+
+__device__ __forceinline__ uint32_t hfma2_u(uint32_t a, uint32_t b, uint32_t c) {
+    __half2 r = __hfma2(*reinterpret_cast<__half2 *>(&a), *reinterpret_cast<__half2 *>(&b),
+                        *reinterpret_cast<__half2 *>(&c));
+    return *reinterpret_cast<uint32_t *>(&r);
+}
+
+// Integer codes to f16 through the exponent trick: the f16 with bits 0x64XX
+// is exactly 1024 + XX, and 0x64XY (nibble form) 1024 + XY.
+constexpr uint32_t F16X2_1152 = 0x64806480u;  // {1152, 1152}: 1024 + 128
+constexpr uint32_t F16X2_1032 = 0x64086408u;  // {1032, 1032}: 1024 + 8
+constexpr uint32_t F16X2_1_16 = 0x2C002C00u;  // {1/16, 1/16}
+constexpr uint32_t F16X2_M72 = 0xD480D480u;   // {-72, -72}
+
+// bytes b0, b1 of an (offset-binary) int8 word -> f16x2 {b0 - 128, b1 - 128}
+__device__ __forceinline__ uint32_t u8pair_f16x2(uint32_t ux, uint32_t sel) {
+    return hsub2_u(__byte_perm(ux, 0x64646464u, sel), F16X2_1152);
+}
+
+// low nibbles of bytes 0 and 2 (offset-binary) -> {n0 - 8, n2 - 8}
+__device__ __forceinline__ uint32_t u4lo_f16x2(uint32_t ux) {
+    return hsub2_u((ux & 0x000F000Fu) | 0x64006400u, F16X2_1032);
+}
+
+// high nibbles of bytes 0 and 2 (offset-binary) -> {n0 - 8, n2 - 8}
+__device__ __forceinline__ uint32_t u4hi_f16x2(uint32_t ux) {
+    return hfma2_u((ux & 0x00F000F0u) | 0x64006400u, F16X2_1_16, F16X2_M72);
+}
+
+// -------------------------------------------------------------- reductions
+
+__device__ __forceinline__ void atomic_or_err(uint32_t *hdr, uint32_t bits) {
+    if (bits) atomicOr(hdr + HDR_ERR, bits);
+}
+
+}  // namespace pa

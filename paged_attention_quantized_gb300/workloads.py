@@ -145,7 +145,7 @@ def _poison_bytes(shape, gen, device) -> torch.Tensor:
 
 
 def _lengths(name: str, B: int, gen_cpu: torch.Generator, lo=None, hi=None) -> torch.Tensor:
-    if name == "tiny":
+    if name == "tiny" and lo is None and hi is None and B <= 2:
         return torch.tensor([37, 70], dtype=torch.int32)[:B]
     if name == "latent":
         # lognormal, median 8192, sigma 1, capped at 131072, at least next_n
@@ -154,7 +154,7 @@ def _lengths(name: str, B: int, gen_cpu: torch.Generator, lo=None, hi=None) -> t
         lo_ = 2 if lo is None else lo
         hi_ = 131072 if hi is None else hi
         return L.round().clamp(lo_, hi_).to(torch.int32)
-    rng = {"bf16": (512, 8192), "e4m3": (1024, 32768), "int8": (2048, 16384), "int4": (2048, 16384)}[name]
+    rng = {"tiny": (1, 100), "bf16": (512, 8192), "e4m3": (1024, 32768), "int8": (2048, 16384), "int4": (2048, 16384)}[name]
     lo_ = rng[0] if lo is None else lo
     hi_ = rng[1] if hi is None else hi
     return torch.randint(lo_, hi_ + 1, (B,), generator=gen_cpu, dtype=torch.int64).to(torch.int32)
@@ -174,7 +174,7 @@ _SHAPES = {
 def make(name: str, device="cpu", seed: Optional[int] = None, *, B: Optional[int] = None,
          L_lo: Optional[int] = None, L_hi: Optional[int] = None, context_lens=None,
          poison: Optional[bool] = None, slack_frac: float = 0.10, n: Optional[int] = None,
-         Hq: Optional[int] = None, Hkv: Optional[int] = None) -> Workload:
+         Hq: Optional[int] = None, Hkv: Optional[int] = None, D: Optional[int] = None) -> Workload:
     """Draw one workload.  `name` picks the recipe; keyword overrides shrink it
     (batch, length range, explicit lengths, heads) for tests.  Everything is a
     deterministic function of (name, seed, overrides, device)."""
@@ -186,6 +186,10 @@ def make(name: str, device="cpu", seed: Optional[int] = None, *, B: Optional[int
     n = n0 if n is None else n
     Hq = Hq0 if Hq is None else Hq
     Hkv = Hkv0 if Hkv is None else Hkv
+    if D is not None:
+        if vprefix:
+            raise ValueError("the latent recipe has fixed head dims")
+        Dk = Dv = D
     poison = (name == "e4m3") if poison is None else poison
     device = torch.device(device)
     gcpu = _gen("cpu", seed)

@@ -71,7 +71,7 @@ def reference(w):
         Kh = Kb.permute(1, 0, 2).repeat_interleave(G, dim=0)   # [Hq, L, Dk]
         Vh = Vb.permute(1, 0, 2).repeat_interleave(G, dim=0)
         qb = q[b].permute(1, 0, 2)     # [Hq, n, Dk]
-        pos = L - w.n + torch.arange(w.n)
+        pos = L - w.n + torch.arange(w.n) if w.causal else torch.full((w.n,), L - 1)
         mask = t[None, :] <= pos[:, None]  # [n, L]
         ok = mask.any(dim=1)
         o = F.scaled_dot_product_attention(qb[None], Kh[None], Vh[None],

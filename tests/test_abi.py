@@ -1,0 +1,129 @@
+"""The C-ABI library builds, loads, exports every symbol include/pa.h declares,
+and rejects bad arguments on the host.  No GPU needed: nothing here launches
+a kernel (every call below fails validation or only sizes the workspace)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from paged_attention_quantized_gb300 import build as pabuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def B():
+    pabuild.build()
+    from paged_attention_quantized_gb300 import _binding
+    return _binding
+
+
+def declared_symbols():
+    hdr = open(os.path.join(ROOT, "include", "pa.h")).read()
+    return sorted(set(re.findall(r"PA_API\s+[\w\s\*]+?\b(pa_\w+)\s*\(", hdr)))
+
+
+def test_header_declares_the_boundary():
+    syms = declared_symbols()
+    for name in ("pa_workspace_size", "pa_plan", "pa_run", "pa_combine", "pa_get_error"):
+        assert name in syms
+
+
+def test_library_exports_every_declared_symbol(B):
+    lib = ctypes.CDLL(B.LIB_PATH)
+    for name in declared_symbols():
+        assert hasattr(lib, name), name
+
+
+def test_exports_nothing_undeclared(B):
+    import subprocess
+    out = subprocess.run(["nm", "-D", "--defined-only", B.LIB_PATH], capture_output=True, text=True).stdout
+    exported = {l.split()[-1] for l in out.splitlines() if " T " in l and l.split()[-1].startswith("pa_")}
+    assert exported == set(declared_symbols())
+
+
+def _prob(B, **kw):
+    base = dict(batch=4, next_n=1, num_q_heads=32, num_kv_heads=8, head_dim_k=128, head_dim_v=128,
+                block_size=16, num_blocks=1000, max_blocks_per_seq=64, max_context_len=1024,
+                q_dtype=B.PA_BF16, kv_dtype=B.PA_BF16, out_dtype=B.PA_BF16, k_scale_mode=0, v_scale_mode=0,
+                causal=0, v_is_k_prefix=0, num_sms=152, split_target=0, split_pages=0, softmax_scale=0.088)
+    base.update(kw)
+    return B.Problem(**base)
+
+
+def test_workspace_size_and_layout(B):
+    p = _prob(B)
+    n = B.pa_workspace_size(p)
+    lo = B.pa_workspace_layout(p)
+    assert n == lo.total_bytes > 0
+    offs = [lo.header_offset, lo.requests_offset, lo.units_offset, lo.partial_o_offset, lo.partial_lse_offset]
+    assert offs == sorted(offs) and all(o % 256 == 0 for o in offs)
+    assert lo.rows_per_kv_head == 4 and lo.row_blocks == 1 and lo.num_sms == 152
+    assert lo.partial_lse_offset - lo.partial_o_offset >= lo.max_units * 4 * 128 * 4
+
+
+@pytest.mark.parametrize("field,value", [
+    ("batch", -1), ("next_n", 0), ("num_q_heads", 30), ("num_kv_heads", 0), ("block_size", 0),
+    ("num_blocks", 0), ("max_blocks_per_seq", 0), ("max_context_len", -5), ("q_dtype", 7),
+    ("q_dtype", 3), ("kv_dtype", 9), ("out_dtype", 4), ("k_scale_mode", 5), ("causal", 2),
+])
+def test_invalid_arguments(B, field, value):
+    st = B.raw_status("pa_workspace_size", ctypes.byref(_prob(B, **{field: value})), ctypes.byref(ctypes.c_size_t()))
+    assert st == B.PA_ERR_INVALID_ARG
+
+
+def test_nan_softmax_scale_rejected(B):
+    st = B.raw_status("pa_workspace_size", ctypes.byref(_prob(B, softmax_scale=float("nan"))),
+                      ctypes.byref(ctypes.c_size_t()))
+    assert st == B.PA_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("kw", [dict(head_dim_k=96, head_dim_v=96), dict(head_dim_v=64),
+                                dict(block_size=24), dict(kv_dtype=5, head_dim_k=64, head_dim_v=64)])
+def test_unsupported_shapes(B, kw):
+    st = B.raw_status("pa_workspace_size", ctypes.byref(_prob(B, **kw)), ctypes.byref(ctypes.c_size_t()))
+    assert st == B.PA_ERR_UNSUPPORTED
+
+
+def test_bad_workspace_rejected_before_any_launch(B):
+    p = _prob(B)
+    need = B.pa_workspace_size(p)
+    # NULL, misaligned and too-small workspaces fail on the host
+    for ws, n in ((None, need), (0x1000 + 8, need), (0x1000, need - 1)):
+        assert B.raw_status("pa_plan", ctypes.byref(p), 0x2000, None, ws, n, None) == B.PA_ERR_WORKSPACE
+        assert B.raw_status("pa_combine", ctypes.byref(p), None, ws, n, 0x3000, None, None) == B.PA_ERR_WORKSPACE
+
+
+def test_missing_pointers_rejected(B):
+    p = _prob(B, k_scale_mode=B.PA_SCALE_CHANNEL, kv_dtype=B.PA_INT8)
+    need = B.pa_workspace_size(p)
+    # per-channel K scales without a k_scale pointer
+    assert B.raw_status("pa_plan", ctypes.byref(p), 0x2000, None, 0x10000, need, None) == B.PA_ERR_INVALID_ARG
+    # misaligned pool pointer
+    p2 = _prob(B)
+    need2 = B.pa_workspace_size(p2)
+    st = B.raw_status("pa_run", ctypes.byref(p2), 0x4000, 0x5008, 0x6000, 0x7000, 0x8000, None, None,
+                      0x10000, need2, 0x9000, None, None)
+    assert st == B.PA_ERR_INVALID_ARG
+
+
+def test_max_units_bound_covers_oracle_plan(B):
+    import numpy as np
+    import oracle
+    rng = np.random.default_rng(3)
+    for _ in range(20):
+        Bsz = int(rng.integers(1, 100))
+        bs = int(rng.choice([16, 32, 64]))
+        maxctx = int(rng.integers(1, 40000))
+        Hkv = int(rng.choice([1, 2, 8]))
+        G = int(rng.choice([1, 4, 16]))
+        n = int(rng.choice([1, 2, 4]))
+        mbps = -(-maxctx // bs)
+        p = _prob(B, batch=Bsz, block_size=bs, max_context_len=maxctx, num_kv_heads=Hkv, num_q_heads=Hkv * G,
+                  next_n=n, max_blocks_per_seq=mbps, num_sms=int(rng.integers(1, 200)))
+        lo = B.pa_workspace_layout(p)
+        L = rng.integers(0, maxctx + 1, Bsz)
+        pl = oracle.plan(L, bs=bs, Hkv=Hkv, max_context_len=maxctx, max_blocks_per_seq=mbps,
+                         target_ctas=lo.split_target, min_pages=lo.min_split_pages, row_blocks=lo.row_blocks)
+        assert pl["num_units"] <= lo.max_units

@@ -1,0 +1,291 @@
+"""GPU parity: the CUDA path (through the C ABI) against the CPU oracle, plus
+the bitwise invariances and device-side error handling.  Needs a GB300."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import paged_attention_quantized_gb300 as pa
+from paged_attention_quantized_gb300 import build as pabuild
+from paged_attention_quantized_gb300 import workloads as W
+from tests.gpu_check import compare, error_bits, run_gpu, sample_rows
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    pabuild.build()
+    pa.binding()
+
+
+def make(name, **kw):
+    return W.make(name, device="cuda", **kw)
+
+
+# ------------------------------------------------------------ small parity
+
+SMALL = [
+    ("tiny", dict(), 0),
+    ("tiny", dict(), 1),
+    ("bf16", dict(B=5, L_lo=1, L_hi=700, Hq=8, Hkv=2), 0),
+    ("bf16", dict(B=5, L_lo=1, L_hi=700, Hq=8, Hkv=2), 3),
+    ("bf16", dict(B=3, L_lo=100, L_hi=300, Hq=64, Hkv=2), 2),   # 32 rows: two row blocks
+    ("bf16", dict(B=4, L_lo=1, L_hi=40, Hq=2, Hkv=2, n=3), 1),  # causal, n=3
+    ("e4m3", dict(B=4, L_lo=4, L_hi=900, Hq=16, Hkv=4), 0),
+    ("e4m3", dict(B=4, L_lo=4, L_hi=900, Hq=16, Hkv=4), 2),
+    ("e4m3", dict(B=3, L_lo=1, L_hi=70, Hq=4, Hkv=1, n=4), 1),
+    ("int8", dict(B=4, L_lo=1, L_hi=600, Hq=16, Hkv=2), 0),
+    ("int8", dict(B=4, L_lo=1, L_hi=600, Hq=16, Hkv=2), 2),
+    ("int4", dict(B=4, L_lo=1, L_hi=600, Hq=16, Hkv=2), 0),
+    ("int4", dict(B=4, L_lo=1, L_hi=600, Hq=16, Hkv=2), 3),
+]
+
+
+@pytest.mark.parametrize("name,kw,split", SMALL, ids=lambda x: str(x))
+def test_small_parity(name, kw, split):
+    w = make(name, **kw)
+    out, lse, ws, _ = run_gpu(w, split_pages=split)
+    assert error_bits(ws) == 0
+    compare(w, out, lse)
+
+
+@pytest.mark.parametrize("name", ["int8", "int4"])
+def test_quantized_channel_scales_soft_softmax(name):
+    # q scaled down (scores of order 1) so the softmax mixes many tokens:
+    # checks the dequant and the fold with the plain relative tolerance
+    w = make(name, B=4, L_lo=20, L_hi=500, Hq=16, Hkv=2)
+    w.q = (w.q.float() / 1e7).to(w.q.dtype)
+    out, lse, ws, _ = run_gpu(w, split_pages=2)
+    compare(w, out, lse)
+
+
+@pytest.mark.parametrize("name,D", [("tiny", 128), ("tiny", 256), ("bf16", 64), ("e4m3", 64), ("e4m3", 128),
+                                    ("int8", 64), ("int8", 256), ("int4", 256)])
+def test_other_head_dims(name, D):
+    w = make(name, B=3, L_lo=1, L_hi=300, Hq=8, Hkv=2, D=D)
+    out, lse, ws, _ = run_gpu(w, split_pages=2)
+    assert error_bits(ws) == 0
+    compare(w, out, lse)
+
+
+def test_steps_separately_equal_fused_call():
+    w = make("bf16", B=6, L_lo=1, L_hi=2000, Hq=8, Hkv=2)
+    o1, l1, _, _ = run_gpu(w, split_pages=5)
+    o2, l2, _, _ = run_gpu(w, split_pages=5, steps="plan+run+combine")
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+# --------------------------------------------------------- bitwise contracts
+
+
+@pytest.mark.parametrize("name", ["bf16", "e4m3", "int8", "int4"])
+def test_relocation_bitwise(name):
+    w = make(name, B=6, L_lo=1, L_hi=1500, Hq=16, Hkv=2)
+    out, lse, _, _ = run_gpu(w)
+    for s in (11, 12):
+        w2 = W.relocate(w, seed=s)
+        o2, l2, _, _ = run_gpu(w2)
+        assert torch.equal(out, o2) and torch.equal(lse, l2)
+
+
+@pytest.mark.parametrize("name", ["bf16", "e4m3", "int8", "int4", "tiny"])
+def test_poisoned_padding_bitwise_and_finite(name):
+    kw = {} if name == "tiny" else dict(B=6, L_lo=1, L_hi=1500, Hq=16, Hkv=2)
+    w = make(name, poison=False, **kw)
+    out, lse, _, _ = run_gpu(w)
+    w2 = W.poison_unreferenced(w, seed=3)
+    o2, l2, ws, _ = run_gpu(w2)
+    assert torch.isfinite(o2).all()
+    assert torch.equal(out, o2) and torch.equal(lse, l2)
+    assert error_bits(ws) == 0
+
+
+def test_repeat_runs_bitwise():
+    w = make("e4m3", B=5, L_lo=1, L_hi=3000, Hq=32, Hkv=8, n=4)
+    o1, l1, _, _ = run_gpu(w)
+    o2, l2, _, _ = run_gpu(w)
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+
+
+def test_split_counts_agree_within_tolerance():
+    w = make("bf16", B=4, L_lo=500, L_hi=3000, Hq=8, Hkv=2)
+    outs = [run_gpu(w, split_pages=s)[0].float() for s in (1, 7, 0, 10000)]
+    for o in outs[1:]:
+        assert (o - outs[0]).abs().max().item() <= 1e-2
+
+
+# -------------------------------------------------------------------- plan
+
+
+@pytest.mark.parametrize("kw", [dict(), dict(split_pages=3), dict(split_target=50), dict(num_sms=7)])
+def test_plan_matches_oracle_plan(kw):
+    w = make("bf16", B=37, L_lo=0, L_hi=5000, Hq=8, Hkv=2)
+    p = pa.problem(w, **kw)
+    out, lse, ws = pa.alloc(w, p)
+    pa.run(w, p, out, ws, lse, steps="plan")
+    torch.cuda.synchronize()
+    lo = pa.binding().pa_workspace_layout(p)
+    pl = oracle.plan(w.context_lens.cpu().numpy(), bs=w.bs, Hkv=w.Hkv, max_context_len=w.max_context_len,
+                     max_blocks_per_seq=w.max_blocks_per_seq, target_ctas=lo.split_target,
+                     min_pages=lo.min_split_pages, row_blocks=lo.row_blocks, forced_pages=kw.get("split_pages", 0))
+    raw = ws.cpu().numpy()
+    hdr = raw[lo.header_offset: lo.header_offset + 16].view(np.uint32)
+    assert hdr[1] == pl["num_units"] and hdr[2] == pl["chunk_pages"] and hdr[0] == 0
+    req = raw[lo.requests_offset: lo.requests_offset + 16 * w.B].view(np.int32).reshape(w.B, 4)
+    assert np.array_equal(req[:, 0], w.context_lens.cpu().numpy())
+    assert np.array_equal(req[:, 1], pl["splits"]) and np.array_equal(req[:, 2], pl["offsets"])
+    assert np.array_equal(req[:, 3], pl["flags"])
+    units = raw[lo.units_offset: lo.units_offset + 16 * pl["num_units"]].view(np.int32).reshape(-1, 4)
+    want = np.array([(b, (h << 16) | s, p0, p1) for (b, h, s, p0, p1) in pl["units"]], dtype=np.int32)
+    assert np.array_equal(units, want)
+
+
+def test_max_abs_scale_kernel():
+    w = make("int8", B=2, L_lo=10, L_hi=50, Hq=16, Hkv=2)
+    for ks in (w.k_scale, torch.zeros_like(w.k_scale), -w.k_scale * 3):
+        w.k_scale = ks.contiguous()
+        p = pa.problem(w)
+        out, lse, ws = pa.alloc(w, p)
+        pa.run(w, p, out, ws, lse, steps="plan")
+        torch.cuda.synchronize()
+        got = ws[12:16].cpu().view(torch.float32).item()
+        assert got == oracle.max_abs_scale(ks.cpu().numpy().astype(np.float32).astype(np.float64))
+
+
+# ---------------------------------------------------------- edge cases
+
+
+def test_zero_length_and_short_requests():
+    w = make("e4m3", Hq=8, Hkv=2, n=4, context_lens=[0, 1, 3, 4, 5, 33])
+    out, lse, ws, _ = run_gpu(w)
+    assert error_bits(ws) == 0
+    compare(w, out, lse)
+    o = out.float().cpu()
+    assert torch.all(o[0] == 0) and torch.all(torch.isneginf(lse[0].cpu()))
+    assert torch.all(o[1, :3] == 0) and torch.all(o[2, :1] == 0)
+
+
+def test_empty_batch_is_a_no_op():
+    w = make("bf16", Hq=8, Hkv=2, context_lens=[5])
+    p = pa.problem(w)
+    p.batch = 0
+    out, lse, ws = pa.alloc(w, p)
+    pa.run(w, p, out, ws, lse)
+    torch.cuda.synchronize()
+    assert torch.isnan(out).all()  # untouched
+
+
+def test_worked_fold_case_on_gpu():
+    # q = 100 and k_scale = 1000 with every K code zero (onnxruntime PR #32520,
+    # worked case): scores are all 0, output = mean of the values, finite
+    for kv in ("int8", "int4"):
+        w = make(kv, B=2, Hq=16, Hkv=2, context_lens=[7, 300])
+        w.q = torch.full_like(w.q, 100.0)
+        w.k_scale = torch.full_like(w.k_scale, 1000.0)
+        w.k_pool = torch.zeros_like(w.k_pool)
+        out, lse, ws, _ = run_gpu(w, split_pages=4)
+        assert torch.isfinite(out).all()
+        compare(w, out, lse)
+        assert np.allclose(lse.cpu().numpy()[:, 0, :], np.log([[7.0], [300.0]]), atol=1e-4)
+
+
+def test_large_bf16_query_into_f16_mma():
+    # bf16 queries far outside the f16 range (E4M3 cache -> f16 MMA): the
+    # per-row power-of-two scaling keeps them exact enough
+    w = make("e4m3", B=3, L_lo=10, L_hi=200, Hq=8, Hkv=2)
+    w.q = (w.q.float() * 1e30).to(torch.bfloat16)
+    w.softmax_scale = 1e-30 / 16
+    out, lse, ws, _ = run_gpu(w)
+    compare(w, out, lse)
+
+
+# ----------------------------------------------------- device-side errors
+
+
+def test_bad_block_id_sets_error_and_nan_fills_only_that_request():
+    w = make("bf16", B=3, Hq=8, Hkv=2, context_lens=[40, 100, 70])
+    w.block_table = w.block_table.clone()
+    w.block_table[1, 2] = w.num_blocks + 3   # out of range, visible position
+    out, lse, ws, _ = run_gpu(w)
+    assert error_bits(ws) & pa.binding().PA_DEV_ERR_BLOCK_ID
+    o = out.float().cpu()
+    assert torch.isnan(o[1]).all()
+    assert torch.isfinite(o[0]).all() and torch.isfinite(o[2]).all()
+    w.block_table[1, 2] = 0                  # the null block is not a real page either
+    out, lse, ws, _ = run_gpu(w)
+    assert error_bits(ws) & pa.binding().PA_DEV_ERR_BLOCK_ID
+
+
+def test_context_len_over_max_sets_error():
+    w = make("bf16", B=3, Hq=8, Hkv=2, context_lens=[40, 100, 70])
+    out, lse, ws, _ = run_gpu(w, max_context_len=80)
+    assert error_bits(ws) & pa.binding().PA_DEV_ERR_CONTEXT_LEN
+    o = out.float().cpu()
+    assert torch.isnan(o[1]).all() and torch.isfinite(o[0]).all() and torch.isfinite(o[2]).all()
+
+
+def test_stale_plan_detected():
+    w = make("bf16", B=3, Hq=8, Hkv=2, context_lens=[40, 100, 70])
+    p = pa.problem(w)
+    out, lse, ws = pa.alloc(w, p)
+    pa.run(w, p, out, ws, lse, steps="plan")
+    w.context_lens[1] = 64                   # lengths change after planning
+    pa.run(w, p, out, ws, lse, steps="run+combine")
+    torch.cuda.synchronize()
+    assert error_bits(ws) & pa.binding().PA_DEV_ERR_STALE_PLAN
+    assert torch.isnan(out[1].float()).all() and torch.isfinite(out[0].float()).all()
+    # a fresh plan clears the error word
+    pa.run(w, p, out, ws, lse)
+    torch.cuda.synchronize()
+    assert error_bits(ws) == 0
+    compare(w, out, lse)
+
+
+# ------------------------------------------------------------ CUDA graphs
+
+
+def test_graph_capture_and_replay_with_new_lengths():
+    w = make("bf16", B=8, L_lo=100, L_hi=3000, Hq=8, Hkv=2)
+    p = pa.problem(w, max_context_len=4000)
+    out, lse, ws = pa.alloc(w, p)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        pa.run(w, p, out, ws, lse, stream=s)   # warm-up outside capture
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        pa.run(w, p, out, ws, lse, stream=s)
+    # new lengths within each request's allocated pages
+    old = w.context_lens.cpu()
+    new = (torch.rand(w.B) * old.float()).floor().to(torch.int32) + 1
+    w.context_lens.copy_(new)
+    out.fill_(math.nan)
+    g.replay()
+    torch.cuda.synchronize()
+    assert error_bits(ws) == 0
+    compare(w, out, lse)
+
+
+# ---------------------------------------------------- full-size workloads
+
+
+@pytest.mark.parametrize("name", ["bf16", "e4m3", "int8", "int4"])
+def test_full_size_sampled_parity(name):
+    """The benchmark's workloads at full size, in the benchmark's launch
+    configuration, checked on sampled rows (including the longest request)."""
+    w = make(name)
+    out, lse, ws, _ = run_gpu(w)
+    assert error_bits(ws) == 0
+    assert torch.isfinite(out.float()).all()
+    rows = sample_rows(w, 160 if name != "e4m3" else 96)
+    host = oracle.HostArrays(w)
+    compare(w, out, lse, rows=rows, host=host)
+    # allocation invariance at full size
+    w2 = W.relocate(w, seed=5)
+    o2, l2, _, _ = run_gpu(w2)
+    assert torch.equal(out, o2) and torch.equal(lse, l2)

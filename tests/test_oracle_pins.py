@@ -121,6 +121,18 @@ def test_oracle_matches_sdpa(kw):
     assert np.max(np.abs(lse[fin] - rlse[fin]), initial=0.0) <= 1e-10 * max(1.0, float(np.abs(rlse[fin]).max(initial=1.0)))
 
 
+def test_non_causal_multi_row_matches_sdpa():
+    w = W.make("e4m3", B=2, L_lo=3, L_hi=50, Hq=4, Hkv=2, n=3)
+    w.causal = False
+    out, lse = _oracle_full(w)
+    rout, rlse = reference(w)
+    assert np.max(np.abs(out - rout)) <= 1e-12 * max(1.0, float(np.abs(rout).max()))
+    # every row of a request sees the same tokens: only q differs
+    w.q = w.q[:, :1].expand(-1, 3, -1, -1).contiguous()
+    out, _ = _oracle_full(w)
+    assert np.array_equal(out[:, 0], out[:, 2])
+
+
 def test_rows_subset_equals_full():
     w = W.make("bf16", B=3, L_lo=5, L_hi=60, Hq=8, Hkv=2)
     out, lse = _oracle_full(w)
