@@ -208,6 +208,28 @@ PA_API pa_status pa_attention(const pa_problem *p, const void *q, const void *k_
                               const float *v_scale, void *workspace, size_t workspace_bytes,
                               void *out, float *lse, pa_stream_t stream);
 
+/* pa_attention without a workspace argument, for callers that cannot
+ * allocate device memory (a host that only passes its plugins input and
+ * output buffers, or code that must not allocate while work is recorded).
+ * The pages have no counterpart of this call; it exists for such callers.
+ *
+ * Its scratch is one static device array of 32 MiB that every GPU loading
+ * this library reserves until the process exits; problems whose
+ * pa_workspace_size exceeds 32 MiB are rejected with PA_ERR_WORKSPACE.  It
+ * allocates nothing and calls no allocating routine.  The first call on a
+ * device looks up the array's device address (once per device, with that
+ * device current): make that first call before any stream capture.  All
+ * calls share the one array, which keeps the last call's contents, so calls
+ * that may overlap on the GPU (other streams, other host threads) race with
+ * each other: order them on one stream.  Device error bits land in the shared
+ * array and cannot be read back separately; a request that broke the contract
+ * still gets NaN rows. */
+PA_API pa_status pa_attention_noalloc(const pa_problem *p, const void *q, const void *k_pool,
+                                      const void *v_pool, const int32_t *block_table,
+                                      const int32_t *context_lens, const float *k_scale,
+                                      const float *v_scale, void *out, float *lse,
+                                      pa_stream_t stream);
+
 /* Copy the device error word to *bits.  Synchronises `stream`. */
 PA_API pa_status pa_get_error(const void *workspace, uint32_t *bits, pa_stream_t stream);
 

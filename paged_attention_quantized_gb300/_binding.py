@@ -72,6 +72,8 @@ _lib.pa_combine.restype = ctypes.c_int
 _lib.pa_combine.argtypes = [_P(Problem), _vp, _vp, ctypes.c_size_t, _vp, _vp, _vp]
 _lib.pa_attention.restype = ctypes.c_int
 _lib.pa_attention.argtypes = [_P(Problem)] + [_vp] * 8 + [ctypes.c_size_t, _vp, _vp, _vp]
+_lib.pa_attention_noalloc.restype = ctypes.c_int
+_lib.pa_attention_noalloc.argtypes = [_P(Problem)] + [_vp] * 10
 _lib.pa_get_error.restype = ctypes.c_int
 _lib.pa_get_error.argtypes = [_vp, _P(ctypes.c_uint32), _vp]
 
@@ -119,6 +121,14 @@ def pa_attention(p: Problem, q, k_pool, v_pool, block_table, context_lens, k_sca
                  workspace_bytes, out, lse, stream) -> None:
     _check(_lib.pa_attention(ctypes.byref(p), q, k_pool, v_pool, block_table, context_lens, k_scale, v_scale,
                              workspace, workspace_bytes, out, lse, stream), "pa_attention")
+
+
+def pa_attention_noalloc(p: Problem, q, k_pool, v_pool, block_table, context_lens, k_scale, v_scale, out, lse,
+                         stream) -> None:
+    """pa_attention with the library's static 32 MiB device scratch instead of a
+    caller workspace (for callers that cannot allocate device memory)."""
+    _check(_lib.pa_attention_noalloc(ctypes.byref(p), q, k_pool, v_pool, block_table, context_lens, k_scale,
+                                     v_scale, out, lse, stream), "pa_attention_noalloc")
 
 
 def pa_get_error(workspace: int, stream) -> int:
