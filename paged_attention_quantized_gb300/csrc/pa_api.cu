@@ -19,7 +19,10 @@ cudaError_t launch_combine(const CombineParams &P, cudaStream_t s);
 namespace {
 
 constexpr int VERSION = 100;
-constexpr size_t RING_TARGET_BYTES = 96 * 1024;
+#ifndef PA_RING_KB
+#define PA_RING_KB 48
+#endif
+constexpr size_t RING_TARGET_BYTES = PA_RING_KB * 1024;
 constexpr int DEFAULT_TARGET_PER_SM = 8;
 constexpr int MIN_SPLIT_TOKENS = 512;
 
@@ -126,7 +129,14 @@ pa_status derive(const pa_problem *p, Derived *d) {
     d->k_block = (size_t)p->num_kv_heads * bs * d->RB;
     d->v_block = d->k_block;
     d->stage_bytes = 2 * bs * d->RB;
-    d->stages = (int)std::min<size_t>(pa::MAX_STAGES, std::max<size_t>(2, RING_TARGET_BYTES / d->stage_bytes));
+    // The ring depth must be a multiple of the consumer warp count: page i and
+    // page i - stages then belong to the same warp, so a warp waiting on a
+    // slot's barrier never sees a phase two behind (its own previous page on
+    // that slot is complete) and parity waits cannot alias.
+    {
+        const size_t fit = RING_TARGET_BYTES / d->stage_bytes / pa::NW * pa::NW;
+        d->stages = (int)std::min<size_t>(pa::MAX_STAGES, std::max<size_t>(pa::NW, fit));
+    }
     d->smem = pa::attn_smem_bytes(D, d->stages, d->stage_bytes);
     if (d->smem > 227 * 1024) return PA_ERR_UNSUPPORTED;
 

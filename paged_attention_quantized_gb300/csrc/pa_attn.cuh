@@ -41,6 +41,15 @@
 namespace pa {
 
 constexpr int NW = 4;                      // consumer warps
+#ifndef PA_MIN_BLOCKS_SMALL_D
+#define PA_MIN_BLOCKS_SMALL_D 3
+#endif
+#ifndef PA_MIN_BLOCKS_LARGE_D
+#define PA_MIN_BLOCKS_LARGE_D 2
+#endif
+// resident CTAs per SM the register allocation is sized for
+template <int D>
+constexpr int min_blocks() { return D <= 128 ? PA_MIN_BLOCKS_SMALL_D : PA_MIN_BLOCKS_LARGE_D; }
 constexpr int ATTN_THREADS = (NW + 1) * 32;
 constexpr int MAX_STAGES = 32;
 constexpr int ROWS = 16;                   // query rows per CTA (mma M)
@@ -218,7 +227,7 @@ __device__ __forceinline__ float load_q(const AttnParams &P, int b, int j, int h
 }
 
 template <int KVT, int D>
-__global__ void __launch_bounds__(ATTN_THREADS, 1)
+__global__ void __launch_bounds__(ATTN_THREADS, min_blocks<D>())
     pa_attn_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv, AttnParams P) {
     using G = Geo<KVT, D>;
     constexpr bool BF = G::BF;
@@ -262,10 +271,13 @@ __global__ void __launch_bounds__(ATTN_THREADS, 1)
         if (!unit_ok) { bad = 1; err |= PA_DEV_ERR_STALE_PLAN; }
         if (Rq.w != 0) { bad = 1; err |= PA_DEV_ERR_CONTEXT_LEN; }
         if (L != Rq.x || (long long)p1 * bs > (long long)L + bs - 1) { bad = 1; err |= PA_DEV_ERR_STALE_PLAN; }
+        // the ring depth must be a positive multiple of the consumer warps
+        // (see the host's stage choice); never run a ring that could alias
+        if (ST < NW || ST > MAX_STAGES || ST % NW != 0) { bad = 1; err |= PA_DEV_ERR_TIMEOUT; }
         ms->bad = bad;
         ms->err = err;
         ms->abort_flag = 0;
-        for (int s = 0; s < ST; ++s) {
+        for (int s = 0; s < min(ST, MAX_STAGES); ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
         }
