@@ -20,7 +20,7 @@ namespace {
 
 constexpr int VERSION = 100;
 #ifndef PA_RING_KB
-#define PA_RING_KB 48
+#define PA_RING_KB 64
 #endif
 constexpr size_t RING_TARGET_BYTES = PA_RING_KB * 1024;
 constexpr int DEFAULT_TARGET_PER_SM = 8;

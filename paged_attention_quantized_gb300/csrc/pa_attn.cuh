@@ -244,8 +244,10 @@ __global__ void __launch_bounds__(ATTN_THREADS, min_blocks<D>())
     // shared-memory carve-up
     uint8_t *ring = smem;
     uint32_t *qs = reinterpret_cast<uint32_t *>(ring + (size_t)ST * P.stage_bytes);  // [KSTEPS][32][4]
-    float *mbuf = reinterpret_cast<float *>(qs + G::KSTEPS * 128);                  // [ROWS][D]
-    SmemMisc *ms = reinterpret_cast<SmemMisc *>(mbuf + ROWS * D);
+    // [ROWS][D] merge buffer: the ring is free once every page has been consumed
+    // (all copies landed and were read); the host sizes the ring to hold it
+    float *mbuf = reinterpret_cast<float *>(ring);
+    SmemMisc *ms = reinterpret_cast<SmemMisc *>(qs + G::KSTEPS * 128);
     uint64_t *full = reinterpret_cast<uint64_t *>(reinterpret_cast<uint8_t *>(ms) + ((sizeof(SmemMisc) + 15) & ~15));
     uint64_t *empty = full + MAX_STAGES;
 
@@ -297,10 +299,12 @@ __global__ void __launch_bounds__(ATTN_THREADS, min_blocks<D>())
             }
             const int32_t *tab = P.block_table + (size_t)b * P.mbps + p0;
             bool stop = false;
+            int id_next = (lane < npages) ? tab[lane] : 0;
             for (int base = 0; base < npages && !stop; base += 32) {
                 const int n_here = min(32, npages - base);
-                int id = 0;
-                if (lane < n_here) id = tab[base + lane];
+                const int id = id_next;
+                // block ids of the next batch, in flight while this one is issued
+                id_next = (base + 32 + lane < npages) ? tab[base + 32 + lane] : 0;
                 const bool ok = (lane >= n_here) || (id >= 1 && id < P.num_blocks);
                 const unsigned okmask = __ballot_sync(0xffffffffu, ok);
                 for (int k = 0; k < n_here; ++k) {

@@ -2,6 +2,8 @@
 // encoding and head dimension, compiled in separate translation units).
 #pragma once
 
+#include <algorithm>
+
 #include "pa_attn.cuh"
 
 namespace pa {
@@ -10,8 +12,9 @@ namespace pa {
 // fragments, the merge buffer, row constants and the stage barriers
 inline size_t attn_smem_bytes(int D, int stages, int stage_bytes) {
     const size_t misc = (sizeof(SmemMisc) + 15) & ~size_t(15);
-    return 1024 + (size_t)stages * stage_bytes + (size_t)(D / 16) * 512 + (size_t)ROWS * D * 4 + misc +
-           2 * MAX_STAGES * sizeof(uint64_t);
+    // the merge buffer [ROWS][D] fp32 lives in the ring after the last page
+    const size_t ring = std::max((size_t)stages * stage_bytes, (size_t)ROWS * D * 4);
+    return 1024 + ring + (size_t)(D / 16) * 512 + misc + 2 * MAX_STAGES * sizeof(uint64_t);
 }
 
 template <int KVT, int D>
