@@ -137,34 +137,40 @@ typedef struct pa_problem {
     int32_t v_scale_mode;       /* pa_scale_mode (ignored when v_is_k_prefix) */
     int32_t causal;             /* 1: row j sees tokens [0, L_b - next_n + j] */
     int32_t v_is_k_prefix;      /* 1: V = first Dv channels of the K plane */
-    int32_t num_sms;            /* planner target width; 0 = current device's SM count */
-    int32_t split_target;       /* CTAs the planner aims for; 0 = library default */
-    int32_t split_pages;        /* > 0: force this many pages per split (tests) */
+    int32_t num_sms;            /* SMs to size the launch for; 0 = current device's SM count */
+    int32_t grid_ctas;          /* persistent CTAs of pa_run; 0 = num_sms x resident CTAs per SM */
     float softmax_scale;        /* e.g. 1/sqrt(Dk) */
 } pa_problem;
 
-/* Byte offsets inside the workspace (all 256-byte aligned) and the effective
- * planner parameters.  Header words (uint32): [0] device error bits,
- * [1] number of work units, [2] pages per split, [3] max|k_scale| (fp32 bits).
- * Request records (int32 x4 per request): {L_b seen by pa_plan, splits S_b,
- * first split index, flags}.  Unit records (int32 x4): {b, kv_head << 16 |
- * split, first page, end page}; unit u = first_split_index(b) * Hkv +
- * kv_head * S_b + split.  Partials: fp32 [max_units][rows_per_kv_head][Dv]
- * normalised outputs and fp32 [max_units][rows_per_kv_head] log-sum-exp, row
+/* Byte offsets inside the workspace (all 256-byte aligned) and the launch
+ * shape.  Header words (uint32): [0] device error bits, [1] total pages
+ * sum_b P_b of the plan, [3] max|k_scale| (fp32 bits).  Request records
+ * (int32 x4 per request): {L_b seen by pa_plan, P_b = ceil(L_b / bs) (0 when
+ * L_b breaks the contract), PS_b = sum of P over earlier requests, flags}.
+ *
+ * pa_run orders every page of the batch by logical position -- request,
+ * kv head, block of 16 query rows ("segment"), page -- and gives warp k of the
+ * persistent launch (W warps) positions [k*N/W, (k+1)*N/W) of the N in total.
+ * A warp's run of pages inside one segment is a "piece"; a piece that is a
+ * whole segment writes `out` directly, other pieces write a partial
+ * (normalised output, log-sum-exp) to slot (segment index + k), which
+ * pa_combine merges in ascending k.  Partials: fp32
+ * [partial_slots][16][Dv] outputs and fp32 [partial_slots][16] log-sum-exps,
+ * row i of a slot = query row 16 * (row block) + i of the kv head, query row
  * r = j * (Hq / Hkv) + (h mod (Hq / Hkv)). */
 typedef struct pa_layout {
     size_t total_bytes;
     size_t header_offset;
     size_t requests_offset;
-    size_t units_offset;
     size_t partial_o_offset;
     size_t partial_lse_offset;
-    int32_t max_units;
-    int32_t rows_per_kv_head;
-    int32_t row_blocks;      /* CTAs per unit along the rows */
-    int32_t num_sms;         /* effective */
-    int32_t split_target;    /* effective */
-    int32_t min_split_pages; /* effective */
+    int64_t partial_slots;       /* B * Hkv * row_blocks + warps */
+    int32_t rows_per_kv_head;    /* (Hq / Hkv) * next_n */
+    int32_t row_blocks;          /* ceil(rows_per_kv_head / 16) */
+    int32_t num_sms;             /* effective */
+    int32_t grid_ctas;           /* effective persistent CTAs of pa_run */
+    int32_t warps;               /* grid_ctas * warps per CTA */
+    int32_t ring_pages_per_warp; /* pages each warp keeps in flight */
 } pa_layout;
 
 /* Library version: major * 10000 + minor * 100 + patch. */
@@ -180,24 +186,28 @@ PA_API pa_status pa_workspace_size(const pa_problem *p, size_t *bytes);
 /* Workspace layout for *p (host only, as pa_workspace_size). */
 PA_API pa_status pa_workspace_layout(const pa_problem *p, pa_layout *layout);
 
-/* Plan the work for the current context_lens (device pointer).  With
+/* Plan the work for the current context_lens (device pointer): pages of
+ * every request and their prefix sums (request records, header word 1).  With
  * PA_SCALE_CHANNEL K scales, also reduces max|k_scale| over every (kv head,
  * channel) on the device (k_scale: device [Hkv][Dk] fp32); otherwise k_scale
  * may be NULL.  Clears the device error word.  Launches 1-2 kernels. */
 PA_API pa_status pa_plan(const pa_problem *p, const int32_t *context_lens, const float *k_scale,
                          void *workspace, size_t workspace_bytes, pa_stream_t stream);
 
-/* The attention itself over the planned units.  Requests with one split write
- * `out` (and `lse` if not NULL) directly; split requests write partials into
- * the workspace for pa_combine.  All pointers are device pointers. */
+/* The attention itself over the planned pages (see pa_layout for how they
+ * are shared out).  Segments handled whole by one warp write `out` (and `lse`
+ * if not NULL) directly; the others leave partials in the workspace for
+ * pa_combine.  All pointers are device pointers. */
 PA_API pa_status pa_run(const pa_problem *p, const void *q, const void *k_pool, const void *v_pool,
                         const int32_t *block_table, const int32_t *context_lens,
                         const float *k_scale, const float *v_scale, void *workspace,
                         size_t workspace_bytes, void *out, float *lse, pa_stream_t stream);
 
-/* Merge the partials of split requests (log-sum-exp, ascending split order),
- * apply the V scale and write `out` / `lse` for them.  Requests with one
- * split are left untouched. */
+/* Merge the partials of every segment that several warps shared (log-sum-exp,
+ * ascending warp order), apply the V scale and write `out` / `lse` for them;
+ * write 0 / -inf for requests without pages (NaN for flagged ones).  Segments
+ * one warp handled whole are left untouched.  Must follow pa_run with the same
+ * problem (its launch shape decides the pieces). */
 PA_API pa_status pa_combine(const pa_problem *p, const float *v_scale, void *workspace,
                             size_t workspace_bytes, void *out, float *lse, pa_stream_t stream);
 

@@ -24,7 +24,7 @@ def binding():
     return _binding
 
 
-def problem(w, *, num_sms: int = 0, split_target: int = 0, split_pages: int = 0,
+def problem(w, *, num_sms: int = 0, grid_ctas: int = 0,
             max_context_len: Optional[int] = None, out_dtype: Optional[str] = None):
     """pa_problem for a workload-shaped batch (see workloads.Workload)."""
     b = binding()
@@ -35,8 +35,8 @@ def problem(w, *, num_sms: int = 0, split_target: int = 0, split_pages: int = 0,
         q_dtype=b.DTYPE[w.q_dtype], kv_dtype=b.DTYPE[w.kv_dtype],
         out_dtype=b.DTYPE[out_dtype or w.out_dtype], k_scale_mode=b.SCALE[w.k_scale_mode],
         v_scale_mode=b.SCALE[w.v_scale_mode], causal=int(bool(w.causal)),
-        v_is_k_prefix=int(bool(w.v_is_k_prefix)), num_sms=num_sms, split_target=split_target,
-        split_pages=split_pages, softmax_scale=float(w.softmax_scale))
+        v_is_k_prefix=int(bool(w.v_is_k_prefix)), num_sms=num_sms, grid_ctas=grid_ctas,
+        softmax_scale=float(w.softmax_scale))
 
 
 def _ptr(t) -> Optional[int]:

@@ -37,15 +37,15 @@ class Problem(ctypes.Structure):
     _fields_ = [(k, ctypes.c_int32) for k in (
         "batch", "next_n", "num_q_heads", "num_kv_heads", "head_dim_k", "head_dim_v", "block_size",
         "num_blocks", "max_blocks_per_seq", "max_context_len", "q_dtype", "kv_dtype", "out_dtype",
-        "k_scale_mode", "v_scale_mode", "causal", "v_is_k_prefix", "num_sms", "split_target",
-        "split_pages")] + [("softmax_scale", ctypes.c_float)]
+        "k_scale_mode", "v_scale_mode", "causal", "v_is_k_prefix", "num_sms", "grid_ctas")] + \
+        [("softmax_scale", ctypes.c_float)]
 
 
 class Layout(ctypes.Structure):
     _fields_ = [(k, ctypes.c_size_t) for k in (
-        "total_bytes", "header_offset", "requests_offset", "units_offset", "partial_o_offset",
-        "partial_lse_offset")] + [(k, ctypes.c_int32) for k in (
-            "max_units", "rows_per_kv_head", "row_blocks", "num_sms", "split_target", "min_split_pages")]
+        "total_bytes", "header_offset", "requests_offset", "partial_o_offset", "partial_lse_offset")] + \
+        [("partial_slots", ctypes.c_int64)] + [(k, ctypes.c_int32) for k in (
+            "rows_per_kv_head", "row_blocks", "num_sms", "grid_ctas", "warps", "ring_pages_per_warp")]
 
 
 if not os.path.exists(LIB_PATH):

@@ -19,12 +19,9 @@ cudaError_t launch_combine(const CombineParams &P, cudaStream_t s);
 namespace {
 
 constexpr int VERSION = 100;
-#ifndef PA_RING_KB
-#define PA_RING_KB 64
-#endif
-constexpr size_t RING_TARGET_BYTES = PA_RING_KB * 1024;
-constexpr int DEFAULT_TARGET_PER_SM = 8;
-constexpr int MIN_SPLIT_TOKENS = 512;
+constexpr size_t SM_SMEM_BYTES = 228 * 1024;     // shared memory per SM
+constexpr size_t CTA_RESERVED_BYTES = 1024;       // reserved by the runtime per resident CTA
+constexpr size_t MAX_DYN_SMEM_BYTES = 227 * 1024; // opt-in limit per CTA
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
@@ -56,9 +53,9 @@ pa_status device_sms(int *sms) {
 
 // Everything derived from a problem on the host.
 struct Derived {
-    int G, R, row_blocks, sms, target, min_pages, T;
-    long long max_units;
-    int D, RB, SW, stage_bytes, stages;
+    int G, R, row_blocks, sms, ctas, minb;
+    long long nwarps, slots_partial;
+    int D, RB, SW, slots, warp_smem;
     size_t k_block, v_block, smem;
     pa_layout L;
 };
@@ -68,7 +65,7 @@ pa_status derive(const pa_problem *p, Derived *d) {
     if (p->batch < 0 || p->next_n < 1 || p->num_q_heads < 1 || p->num_kv_heads < 1 ||
         p->num_q_heads % p->num_kv_heads != 0 || p->head_dim_k < 1 || p->head_dim_v < 1 ||
         p->block_size < 1 || p->num_blocks < 1 || p->max_blocks_per_seq < 1 || p->max_context_len < 0 ||
-        p->num_sms < 0 || p->split_target < 0 || p->split_pages < 0)
+        p->num_sms < 0 || p->grid_ctas < 0 || p->grid_ctas > (1 << 20))
         return PA_ERR_INVALID_ARG;
     if ((p->q_dtype != PA_F16 && p->q_dtype != PA_BF16) || dtype_bits(p->kv_dtype) == 0 ||
         (p->out_dtype != PA_F32 && p->out_dtype != PA_F16 && p->out_dtype != PA_BF16))
@@ -103,42 +100,40 @@ pa_status derive(const pa_problem *p, Derived *d) {
         const pa_status st = device_sms(&d->sms);
         if (st != PA_OK) return st;
     }
-    d->target = p->split_target > 0 ? p->split_target : DEFAULT_TARGET_PER_SM * d->sms;
-    d->min_pages = std::max(1, MIN_SPLIT_TOKENS / p->block_size);
-    d->T = std::max(1, d->target / (p->num_kv_heads * d->row_blocks));
-
     const int bs = p->block_size;
-    const long long pages_ctx = ((long long)p->max_context_len + bs - 1) / bs;
-    const long long Pmax = std::min<long long>(p->max_blocks_per_seq, pages_ctx);
-    long long u_req;
-    if (p->split_pages > 0) {
-        const long long per = std::max<long long>(1, (Pmax + p->split_pages - 1) / p->split_pages);
-        if (per > 65535) return PA_ERR_UNSUPPORTED;
-        u_req = (long long)p->batch * per;
-    } else {
-        const long long per = std::max<long long>(1, (Pmax + d->min_pages - 1) / d->min_pages);
-        if (per > 65535) return PA_ERR_UNSUPPORTED;
-        u_req = std::min<long long>((long long)p->batch * per, (long long)p->batch + d->T);
-    }
-    d->max_units = u_req * p->num_kv_heads;
-    if (d->max_units > (1ll << 30)) return PA_ERR_UNSUPPORTED;
-
     const int bits = dtype_bits(p->kv_dtype);
     d->RB = D * bits / 8;
     d->SW = d->RB >= 128 ? 128 : 64;
     d->k_block = (size_t)p->num_kv_heads * bs * d->RB;
     d->v_block = d->k_block;
-    d->stage_bytes = 2 * bs * d->RB;
-    // The ring depth must be a multiple of the consumer warp count: page i and
-    // page i - stages then belong to the same warp, so a warp waiting on a
-    // slot's barrier never sees a phase two behind (its own previous page on
-    // that slot is complete) and parity waits cannot alias.
-    {
-        const size_t fit = RING_TARGET_BYTES / d->stage_bytes / pa::NW * pa::NW;
-        d->stages = (int)std::min<size_t>(pa::MAX_STAGES, std::max<size_t>(pa::NW, fit));
+    // Ring pages per warp: as many as fit the shared memory of the resident
+    // CTAs per SM the kernel's registers allow (each warp streams its own
+    // pages); with pages too large for two per warp, one CTA per SM, and one
+    // page per warp as the last resort.
+    const int page_bytes = 2 * bs * d->RB;
+    auto wsm = [&](int s) { return D <= 128 ? pa::warp_smem_bytes<128>(s, page_bytes) : pa::warp_smem_bytes<256>(s, page_bytes); };
+    auto fit = [&](int minb) {
+        const size_t budget = std::min(MAX_DYN_SMEM_BYTES, SM_SMEM_BYTES / minb - CTA_RESERVED_BYTES) - 1024;
+        int slots = 0;
+        for (int s = 1; s <= pa::MAX_SLOTS; ++s)
+            if ((size_t)pa::NWK * wsm(s) <= budget) slots = s;
+        return slots;
+    };
+    d->minb = D <= 128 ? PA_MIN_BLOCKS_SMALL_D : PA_MIN_BLOCKS_LARGE_D;
+    d->slots = fit(d->minb);
+    if (d->slots < 2 && d->minb > 1) {
+        d->minb = 1;
+        d->slots = fit(1);
     }
-    d->smem = pa::attn_smem_bytes(D, d->stages, d->stage_bytes);
-    if (d->smem > 227 * 1024) return PA_ERR_UNSUPPORTED;
+    if (d->slots < 1) return PA_ERR_UNSUPPORTED;
+    d->warp_smem = wsm(d->slots);
+    d->smem = 1024 + (size_t)pa::NWK * d->warp_smem;
+    d->ctas = p->grid_ctas > 0 ? p->grid_ctas : d->sms * d->minb;
+    d->nwarps = (long long)d->ctas * pa::NWK;
+
+    const long long X = (long long)p->num_kv_heads * d->row_blocks;
+    d->slots_partial = (long long)p->batch * X + d->nwarps;
+    if (d->slots_partial > (1ll << 31)) return PA_ERR_UNSUPPORTED;
 
     pa_layout &Lo = d->L;
     std::memset(&Lo, 0, sizeof(Lo));
@@ -147,19 +142,18 @@ pa_status derive(const pa_problem *p, Derived *d) {
     off = align_up(off + 64, 256);
     Lo.requests_offset = off;
     off = align_up(off + (size_t)p->batch * 16, 256);
-    Lo.units_offset = off;
-    off = align_up(off + (size_t)d->max_units * 16, 256);
     Lo.partial_o_offset = off;
-    off = align_up(off + (size_t)d->max_units * d->R * p->head_dim_v * 4, 256);
+    off = align_up(off + (size_t)d->slots_partial * 16 * p->head_dim_v * 4, 256);
     Lo.partial_lse_offset = off;
-    off = align_up(off + (size_t)d->max_units * d->R * 4, 256);
+    off = align_up(off + (size_t)d->slots_partial * 16 * 4, 256);
     Lo.total_bytes = off;
-    Lo.max_units = (int32_t)d->max_units;
+    Lo.partial_slots = d->slots_partial;
     Lo.rows_per_kv_head = d->R;
     Lo.row_blocks = d->row_blocks;
     Lo.num_sms = d->sms;
-    Lo.split_target = d->target;
-    Lo.min_split_pages = d->min_pages;
+    Lo.grid_ctas = d->ctas;
+    Lo.warps = (int32_t)d->nwarps;
+    Lo.ring_pages_per_warp = d->slots;
     return PA_OK;
 }
 
@@ -207,8 +201,7 @@ T *at(void *ws, size_t off) {
 
 cudaError_t dispatch_attn(const pa_problem *p, const Derived &d, const CUtensorMap &tk, const CUtensorMap &tv,
                           const pa::AttnParams &P, cudaStream_t s) {
-    const dim3 grid((unsigned)d.max_units, (unsigned)d.row_blocks);
-    if (d.max_units == 0) return cudaSuccess;
+    const dim3 grid((unsigned)d.ctas);
 #define PA_CASE(KVT, DD) \
     if (p->kv_dtype == KVT && d.D == DD) return pa::launch_attn<KVT, DD>(tk, tv, P, grid, d.smem, s);
     PA_CASE(PA_F16, 64) PA_CASE(PA_F16, 128) PA_CASE(PA_F16, 256)
@@ -267,16 +260,10 @@ PA_API pa_status pa_plan(const pa_problem *p, const int32_t *context_lens, const
     P.context_lens = context_lens;
     P.hdr = at<uint32_t>(workspace, d.L.header_offset);
     P.req = at<int4>(workspace, d.L.requests_offset);
-    P.units = at<int4>(workspace, d.L.units_offset);
     P.B = p->batch;
-    P.Hkv = p->num_kv_heads;
     P.bs = p->block_size;
     P.max_ctx = p->max_context_len;
     P.mbps = p->max_blocks_per_seq;
-    P.T = d.T;
-    P.min_pages = d.min_pages;
-    P.forced_pages = p->split_pages;
-    P.max_units = (int)d.max_units;
     const float *ks = (p->k_scale_mode == PA_SCALE_CHANNEL) ? k_scale : nullptr;
     cudaError_t e = pa::launch_plan(P, ks, p->num_kv_heads * p->head_dim_k, reinterpret_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
@@ -312,7 +299,6 @@ PA_API pa_status pa_run(const pa_problem *p, const void *q, const void *k_pool, 
     P.v_scale = v_scale;
     P.hdr = at<uint32_t>(workspace, d.L.header_offset);
     P.req = at<const int4>(workspace, d.L.requests_offset);
-    P.units = at<const int4>(workspace, d.L.units_offset);
     P.part_o = at<float>(workspace, d.L.partial_o_offset);
     P.part_lse = at<float>(workspace, d.L.partial_lse_offset);
     P.out = out;
@@ -323,18 +309,17 @@ PA_API pa_status pa_run(const pa_problem *p, const void *q, const void *k_pool, 
     P.Hkv = p->num_kv_heads;
     P.G = d.G;
     P.R = d.R;
+    P.RBLK = d.row_blocks;
     P.bs = p->block_size;
     P.mbps = p->max_blocks_per_seq;
-    P.max_ctx = p->max_context_len;
     P.num_blocks = p->num_blocks;
     P.q_dtype = p->q_dtype;
     P.out_dtype = p->out_dtype;
     P.k_mode = p->k_scale_mode;
     P.v_mode = p->v_scale_mode;
     P.causal = p->causal;
-    P.stages = d.stages;
-    P.stage_bytes = d.stage_bytes;
-    P.max_units = (int)d.max_units;
+    P.slots = d.slots;
+    P.warp_smem = d.warp_smem;
     P.softmax_scale = p->softmax_scale;
     cudaError_t e = dispatch_attn(p, d, tk, tv, P, reinterpret_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
@@ -352,6 +337,7 @@ PA_API pa_status pa_combine(const pa_problem *p, const float *v_scale, void *wor
         return PA_ERR_INVALID_ARG;
     pa::CombineParams P;
     P.req = at<const int4>(workspace, d.L.requests_offset);
+    P.hdr = at<const uint32_t>(workspace, d.L.header_offset);
     P.part_o = at<const float>(workspace, d.L.partial_o_offset);
     P.part_lse = at<const float>(workspace, d.L.partial_lse_offset);
     P.v_scale = v_scale;
@@ -363,10 +349,11 @@ PA_API pa_status pa_combine(const pa_problem *p, const float *v_scale, void *wor
     P.Hkv = p->num_kv_heads;
     P.G = d.G;
     P.R = d.R;
+    P.RBLK = d.row_blocks;
     P.Dv = p->head_dim_v;
     P.out_dtype = p->out_dtype;
     P.v_mode = p->v_scale_mode;
-    P.max_units = d.max_units;
+    P.nwarps = d.nwarps;
     cudaError_t e = pa::launch_combine(P, reinterpret_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }

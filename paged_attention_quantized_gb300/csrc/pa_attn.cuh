@@ -40,19 +40,22 @@
 
 namespace pa {
 
-constexpr int NW = 4;                      // consumer warps
+constexpr int NWK = 4;                     // warps per CTA, each an independent stream
 #ifndef PA_MIN_BLOCKS_SMALL_D
-#define PA_MIN_BLOCKS_SMALL_D 3
+#define PA_MIN_BLOCKS_SMALL_D 2
 #endif
 #ifndef PA_MIN_BLOCKS_LARGE_D
-#define PA_MIN_BLOCKS_LARGE_D 2
+#define PA_MIN_BLOCKS_LARGE_D 1
 #endif
-// resident CTAs per SM the register allocation is sized for
+// resident CTAs per SM the register and shared-memory budgets are sized for
 template <int D>
-constexpr int min_blocks() { return D <= 128 ? PA_MIN_BLOCKS_SMALL_D : PA_MIN_BLOCKS_LARGE_D; }
-constexpr int ATTN_THREADS = (NW + 1) * 32;
-constexpr int MAX_STAGES = 32;
-constexpr int ROWS = 16;                   // query rows per CTA (mma M)
+__host__ __device__ constexpr int min_blocks() { return D <= 128 ? PA_MIN_BLOCKS_SMALL_D : PA_MIN_BLOCKS_LARGE_D; }
+// q' fragments live in registers for D <= 128, in the warp's shared memory above
+template <int D>
+__host__ __device__ constexpr bool q_in_regs() { return D <= 128; }
+constexpr int ATTN_THREADS = NWK * 32;
+constexpr int MAX_SLOTS = 16;              // ring slots (pages) per warp
+constexpr int ROWS = 16;                   // query rows per segment (mma M)
 constexpr float LOG2E = 1.4426950408889634f;
 constexpr float LN2 = 0.6931471805599453f;
 
@@ -207,16 +210,65 @@ __device__ __forceinline__ void lds_words(uint32_t *w, const uint8_t *p) {
     }
 }
 
-struct SmemMisc {
-    float sc[ROWS];        // score scale per row (log2 domain)
-    int vis[ROWS];         // visible tokens per row
-    float m_w[NW][ROWS];   // per-warp running max (log2 domain)
-    float l_w[NW][ROWS];   // per-warp running sum
-    float rowmax[ROWS];    // max |q'| per row (prologue)
-    int bad;               // unit must be NaN-filled
-    int abort_flag;        // a bounded wait ran out
-    uint32_t err;          // error bits to publish
+// Bytes of one warp's shared memory: its ring of pages, its q' fragments (when
+// they do not live in registers) and the ring barriers, rounded to 1 KB.
+template <int D>
+__host__ __device__ constexpr int warp_smem_bytes(int slots, int page_bytes) {
+    return (slots * page_bytes + (q_in_regs<D>() ? 0 : (D / 16) * 512) + MAX_SLOTS * 8 + 1023) / 1024 * 1024;
+}
+
+// Position of logical page p of segment q (kv head * row blocks + row block)
+// of request b in the global page sequence: PS_b * X + q * P_b + p, where
+// PS_b = sum of P over earlier requests and X = segments per request.
+struct Cursor {
+    int b, q, p;  // request, segment within the request, page
+    int Pb;       // pages of request b
 };
+
+// pages of request b as planned, clamped to the table width so that a
+// workspace planned for another problem cannot send a read out of bounds
+__device__ __forceinline__ int planned_pages(const int4 *req, int b, int mbps) {
+    return min(max(req[b].y, 0), mbps);
+}
+
+__device__ __forceinline__ void cursor_next(Cursor &cu, const int4 *req, int B, int X, int mbps) {
+    if (++cu.p < cu.Pb) return;
+    cu.p = 0;
+    if (++cu.q < X) return;
+    cu.q = 0;
+    do {
+        ++cu.b;
+        cu.Pb = cu.b < B ? planned_pages(req, cu.b, mbps) : 0;
+    } while (cu.b < B && cu.Pb == 0);
+}
+
+// The cursor of global position x (< total pages): the request is the last
+// one whose first position is <= x (it cannot be empty).  Returns b = B if
+// the records do not describe such a request.
+__device__ __forceinline__ Cursor cursor_at(long long x, const int4 *req, int B, int X, int mbps) {
+    int lo = 0, hi = B - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if ((long long)req[mid].z * X <= x) lo = mid;
+        else hi = mid - 1;
+    }
+    Cursor cu;
+    cu.b = lo;
+    cu.Pb = planned_pages(req, lo, mbps);
+    const long long off = x - (long long)req[lo].z * X;
+    if (cu.Pb < 1 || off < 0 || off >= (long long)cu.Pb * X) {
+        cu.b = B;
+        cu.q = cu.p = 0;
+        return cu;
+    }
+    cu.q = (int)(off / cu.Pb);
+    cu.p = (int)(off % cu.Pb);
+    return cu;
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
 
 template <int KVT, int D>
 __device__ __forceinline__ float load_q(const AttnParams &P, int b, int j, int h, int d) {
@@ -231,215 +283,259 @@ __global__ void __launch_bounds__(ATTN_THREADS, min_blocks<D>())
     pa_attn_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv, AttnParams P) {
     using G = Geo<KVT, D>;
     constexpr bool BF = G::BF;
+    constexpr bool QREG = q_in_regs<D>();
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
-    const int unit = blockIdx.x;
-    const int rblk = blockIdx.y;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int ST = P.stages;
+    const int g = lane >> 2, c = lane & 3;
+    const int NS = P.slots;
     const int bs = P.bs;
     const int tile_bytes = bs * G::RB;
+    const int page_bytes = 2 * tile_bytes;  // K tile then V tile
+    const int X = P.Hkv * P.RBLK;           // segments per request
 
-    // shared-memory carve-up
-    uint8_t *ring = smem;
-    uint32_t *qs = reinterpret_cast<uint32_t *>(ring + (size_t)ST * P.stage_bytes);  // [KSTEPS][32][4]
-    // [ROWS][D] merge buffer: the ring is free once every page has been consumed
-    // (all copies landed and were read); the host sizes the ring to hold it
-    float *mbuf = reinterpret_cast<float *>(ring);
-    SmemMisc *ms = reinterpret_cast<SmemMisc *>(qs + G::KSTEPS * 128);
-    uint64_t *full = reinterpret_cast<uint64_t *>(reinterpret_cast<uint8_t *>(ms) + ((sizeof(SmemMisc) + 15) & ~15));
-    uint64_t *empty = full + MAX_STAGES;
+    // this warp's shared memory: ring of NS pages, q' fragments, barriers
+    uint8_t *ring = smem + (size_t)warp * P.warp_smem;
+    uint4 *qs = reinterpret_cast<uint4 *>(ring + (size_t)NS * page_bytes);          // [KSTEPS][32]
+    uint64_t *full = reinterpret_cast<uint64_t *>(reinterpret_cast<uint8_t *>(qs) +
+                                                  (QREG ? 0 : G::KSTEPS * 512));  // [MAX_SLOTS]
+    if (NS < 1 || NS > MAX_SLOTS) return;  // the host never launches this
 
-    const uint32_t num_units = P.hdr[HDR_NUM_UNITS];
-    if (unit >= (int)num_units || unit >= P.max_units) return;
-
-    const int4 U = P.units[unit];
-    // a unit record that does not fit this problem (workspace planned for
-    // another problem) is rejected before anything it names is read
-    const bool unit_ok = U.x >= 0 && U.x < P.B && (U.y >> 16) < P.Hkv && U.z >= 0 && U.z <= U.w &&
-                         U.w <= P.mbps;
-    const int b = unit_ok ? U.x : 0, kvh = unit_ok ? (U.y >> 16) : 0, split = U.y & 0xFFFF;
-    const int p0 = unit_ok ? U.z : 0, p1 = unit_ok ? U.w : 0;
-    const int4 Rq = P.req[b];
-    const int L = P.context_lens[b];
-    const int S_b = Rq.y;
-    const int npages = p1 - p0;
-    const int r0 = rblk * ROWS;
-
-    if (threadIdx.x == 0) {
-        uint32_t err = 0;
-        int bad = 0;
-        if (!unit_ok) { bad = 1; err |= PA_DEV_ERR_STALE_PLAN; }
-        if (Rq.w != 0) { bad = 1; err |= PA_DEV_ERR_CONTEXT_LEN; }
-        if (L != Rq.x || (long long)p1 * bs > (long long)L + bs - 1) { bad = 1; err |= PA_DEV_ERR_STALE_PLAN; }
-        // the ring depth must be a positive multiple of the consumer warps
-        // (see the host's stage choice); never run a ring that could alias
-        if (ST < NW || ST > MAX_STAGES || ST % NW != 0) { bad = 1; err |= PA_DEV_ERR_TIMEOUT; }
-        ms->bad = bad;
-        ms->err = err;
-        ms->abort_flag = 0;
-        for (int s = 0; s < min(ST, MAX_STAGES); ++s) {
-            mbar_init(&full[s], 1);
-            mbar_init(&empty[s], 1);
-        }
-        mbar_fence_init();
-    }
-    __syncthreads();
-
-    const bool bad0 = ms->bad != 0;
-
-    if (warp == NW) {
-        // ------------------------------------------------------- producer
-        int issued = 0;  // pages whose copy was started (in order)
-        if (!bad0) {
-            if (lane == 0) {
-                tma_prefetch_desc(&tmk);
-                tma_prefetch_desc(&tmv);
-            }
-            const int32_t *tab = P.block_table + (size_t)b * P.mbps + p0;
-            bool stop = false;
-            int id_next = (lane < npages) ? tab[lane] : 0;
-            for (int base = 0; base < npages && !stop; base += 32) {
-                const int n_here = min(32, npages - base);
-                const int id = id_next;
-                // block ids of the next batch, in flight while this one is issued
-                id_next = (base + 32 + lane < npages) ? tab[base + 32 + lane] : 0;
-                const bool ok = (lane >= n_here) || (id >= 1 && id < P.num_blocks);
-                const unsigned okmask = __ballot_sync(0xffffffffu, ok);
-                for (int k = 0; k < n_here; ++k) {
-                    const int i = base + k;
-                    const int slot = i % ST;
-                    if (i >= ST && !mbar_wait_bounded(&empty[slot], ((i / ST) - 1) & 1, &ms->abort_flag)) {
-                        if (lane == 0) { ms->abort_flag = 1; atomicOr(&ms->err, PA_DEV_ERR_TIMEOUT); }
-                        stop = true;
-                        break;
-                    }
-                    const int blk = __shfl_sync(0xffffffffu, id, k);
-                    if (lane == 0) {
-                        uint8_t *kt = ring + (size_t)slot * P.stage_bytes;
-                        uint8_t *vt = kt + tile_bytes;
-                        if ((okmask >> k) & 1u) {
-                            mbar_arrive_expect_tx(&full[slot], (uint32_t)(2 * tile_bytes));
-#pragma unroll
-                            for (int sg = 0; sg < G::NSEG; ++sg) {
-                                tma_load_4d(kt + sg * bs * G::SW, &tmk, &full[slot], sg * G::SW, 0, kvh, blk);
-                                tma_load_4d(vt + sg * bs * G::SW, &tmv, &full[slot], sg * G::SW, 0, kvh, blk);
-                            }
-                        } else {
-                            // invalid id: no copy; the unit is NaN-filled
-                            atomicOr(&ms->err, PA_DEV_ERR_BLOCK_ID);
-                            ms->bad = 1;
-                            mbar_arrive(&full[slot]);
-                        }
-                    }
-                    issued = i + 1;
-                    __syncwarp();
-                }
-            }
-        }
-        // wait for the consumers, then make sure no copy is still landing
-        asm volatile("bar.sync 2, %0;" ::"n"(ATTN_THREADS));
-        if (lane == 0 && ms->abort_flag) {
-            volatile int never = 0;
-            for (int i = max(0, issued - ST); i < issued; ++i)
-                mbar_wait_bounded(&full[i % ST], (i / ST) & 1, &never);
-        }
-        if (threadIdx.x == NW * 32) atomic_or_err(P.hdr, ms->err);
+    // the warp's share of the global page sequence
+    const long long total = P.hdr[HDR_TOTAL_PAGES];
+    if (total > (long long)P.B * P.mbps) {  // not a plan of this problem
+        if (threadIdx.x == 0) atomic_or_err(P.hdr, PA_DEV_ERR_STALE_PLAN);
         return;
     }
+    const long long Ntot = total * X;
+    const long long NWt = (long long)gridDim.x * NWK;
+    const long long kw = (long long)blockIdx.x * NWK + warp;
+    const long long x0 = kw * Ntot / NWt, x1 = (kw + 1) * Ntot / NWt;
+    if (x0 >= x1) return;
+    const int npg = (int)(x1 - x0);
 
-    // ------------------------------------------------------------ consumers
-    const int g = lane >> 2, c = lane & 3;
-    const int ctid = threadIdx.x;  // 0 .. NW*32-1
+    if (lane == 0) {
+        for (int s = 0; s < NS; ++s) mbar_init(&full[s], 1);
+        mbar_fence_init();
+        tma_prefetch_desc(&tmk);
+        tma_prefetch_desc(&tmv);
+    }
+    __syncwarp();
 
-    // per-row constants
-    if (ctid < ROWS) {
-        const int r = r0 + ctid;
-        int vis = L;
-        if (r < P.R && P.causal) vis = L - (P.n - 1 - r / P.G);
-        ms->vis[ctid] = vis;
+    uint32_t err = 0;
+    Cursor cc = cursor_at(x0, P.req, P.B, X, P.mbps);  // compute cursor
+    if (cc.b >= P.B) {
+        if (lane == 0) atomic_or_err(P.hdr, PA_DEV_ERR_STALE_PLAN);
+        return;
     }
-    const float kmax = (P.k_mode == PA_SCALE_CHANNEL) ? __uint_as_float(P.hdr[HDR_KMAX]) : 1.0f;
-    const float kscal = (P.k_mode == PA_SCALE_TENSOR) ? P.k_scale[0] : kmax;
-    // fold factor of channel d (per-channel K scale normalised by its max)
-    auto fold = [&](int d) -> float {
-        return (P.k_mode == PA_SCALE_CHANNEL) ? P.k_scale[(size_t)kvh * D + d] / kmax : 1.0f;
-    };
-    // row maxima of |q'| (f16 MMAs only)
-    if constexpr (!BF) {
-        const int row = ctid >> 3, sub = ctid & 7;  // 8 threads per row
-        float mx = 0.f;
-        const int r = r0 + row;
-        if (r < P.R) {
-            const int jq = r / P.G, h = kvh * P.G + (r % P.G);
-            for (int d = sub; d < D; d += 8) mx = fmaxf(mx, fabsf(load_q<KVT, D>(P, b, jq, h, d) * fold(d)));
+    Cursor ci = cc;                             // issue cursor (runs NS pages ahead)
+    int idc_b = -1, idc_w0 = 0, idc = 0;        // block ids of ci.b, pages [idc_w0, idc_w0 + 32)
+    unsigned slot_bad = 0;                      // slots whose page had an invalid id
+
+    auto issue = [&](int j) {
+        const int slot = j % NS;
+        if (ci.b >= P.B) {  // inconsistent records: no copy, the slot still completes
+            if (lane == 0) mbar_arrive(&full[slot]);
+            slot_bad |= 1u << slot;
+            return;
         }
-#pragma unroll
-        for (int o = 4; o >= 1; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-        if (sub == 0) ms->rowmax[row] = mx;
-    }
-    asm volatile("bar.sync 1, %0;" ::"n"(NW * 32));
-    if (ctid < ROWS) {
-        float rho = 1.0f;
-        if constexpr (!BF) {
-            const float mx = ms->rowmax[ctid];
-            if (mx > 0.f && mx < 3.0e38f) {
-                int e;
-                frexpf(mx, &e);  // mx = f * 2^e, f in [0.5, 1)
-                rho = ldexpf(1.0f, e);
-            }
+        if (ci.b != idc_b || ci.p < idc_w0 || ci.p >= idc_w0 + 32) {
+            idc_b = ci.b;
+            idc_w0 = ci.p;
+            const int pg = idc_w0 + lane;
+            idc = (pg < ci.Pb) ? P.block_table[(size_t)ci.b * P.mbps + pg] : 0;
         }
-        ms->rowmax[ctid] = rho;  // reuse: the power-of-two row factor
-        ms->sc[ctid] = P.softmax_scale * kscal * rho * LOG2E;
-    }
-    asm volatile("bar.sync 1, %0;" ::"n"(NW * 32));
-    // q' fragments, shared by all consumer warps: warp w builds k-steps w, w+NW, ...
-    for (int K = warp; K < G::KSTEPS; K += NW) {
-        uint32_t a[4];
+        const int blk = __shfl_sync(0xffffffffu, idc, ci.p - idc_w0);
+        const bool ok = blk >= 1 && blk < P.num_blocks;
+        const int kvh = ci.q / P.RBLK;
+        if (lane == 0) {
+            uint8_t *kt = ring + (size_t)slot * page_bytes;
+            uint8_t *vt = kt + tile_bytes;
+            if (ok) {
+                mbar_arrive_expect_tx(&full[slot], (uint32_t)page_bytes);
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {       // a0a1/a2a3 use e=0,1; a4a5/a6a7 use e=2,3
-#pragma unroll
-            for (int rr = 0; rr < 2; ++rr) {         // row g, row g+8
-                const int row = g + 8 * rr, r = r0 + row;
-                float v0 = 0.f, v1 = 0.f;
-                if (r < P.R) {
-                    const int jq = r / P.G, h = kvh * P.G + (r % P.G);
-                    const float inv = 1.0f / ms->rowmax[row];
-                    const int d0 = phys_ch<KVT, D>(K, c, 2 * half), d1 = phys_ch<KVT, D>(K, c, 2 * half + 1);
-                    v0 = load_q<KVT, D>(P, b, jq, h, d0) * fold(d0) * inv;
-                    v1 = load_q<KVT, D>(P, b, jq, h, d1) * fold(d1) * inv;
+                for (int sg = 0; sg < G::NSEG; ++sg) {
+                    tma_load_4d(kt + sg * bs * G::SW, &tmk, &full[slot], sg * G::SW, 0, kvh, blk);
+                    tma_load_4d(vt + sg * bs * G::SW, &tmv, &full[slot], sg * G::SW, 0, kvh, blk);
                 }
-                a[2 * half + rr] = pack2<BF>(v0, v1);
+            } else {
+                mbar_arrive(&full[slot]);  // no copy: the piece is NaN-filled
             }
         }
-        reinterpret_cast<uint4 *>(qs)[K * 32 + lane] = make_uint4(a[0], a[1], a[2], a[3]);
-    }
-    asm volatile("bar.sync 1, %0;" ::"n"(NW * 32));
+        slot_bad = ok ? (slot_bad & ~(1u << slot)) : (slot_bad | (1u << slot));
+        cursor_next(ci, P.req, P.B, X, P.mbps);
+    };
 
-    const float sc0 = ms->sc[g], sc1 = ms->sc[g + 8];
-    const int vis0 = ms->vis[g], vis1 = ms->vis[g + 8];
-    const int vis_min = min(vis0, vis1);
+    const int npre = min(NS, npg);
+    for (int j = 0; j < npre; ++j) issue(j);
 
+    // ---- per-piece state (a piece = this warp's run of pages of one segment)
     float o[G::NT2][4];
-#pragma unroll
-    for (int t = 0; t < G::NT2; ++t) o[t][0] = o[t][1] = o[t][2] = o[t][3] = 0.f;
     float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
-    bool aborted = false;
+    uint32_t qreg[QREG ? G::KSTEPS : 1][4];
+    float sc0 = 0.f, sc1 = 0.f;
+    int vis0 = 0, vis1 = 0, L = 0, kvh = 0, rblk = 0, piece_b = -1, piece_q = -1, piece_p0 = 0, last_p = 0;
+    bool pbad = false;
 
-    for (int i = warp; i < (bad0 ? 0 : npages); i += NW) {
-        const int slot = i % ST;
-        if (!mbar_wait_bounded(&full[slot], (i / ST) & 1, &ms->abort_flag)) {
-            if (lane == 0) { ms->abort_flag = 1; atomicOr(&ms->err, PA_DEV_ERR_TIMEOUT); }
-            aborted = true;
+    auto start_piece = [&]() {
+        piece_b = cc.b;
+        piece_q = cc.q;
+        piece_p0 = cc.p;
+        kvh = cc.q / P.RBLK;
+        rblk = cc.q % P.RBLK;
+        const int4 Rq = P.req[cc.b];
+        L = P.context_lens[cc.b];
+        pbad = false;
+        if (Rq.w != 0) { pbad = true; err |= PA_DEV_ERR_CONTEXT_LEN; }
+        if (L != Rq.x) { pbad = true; err |= PA_DEV_ERR_STALE_PLAN; }
+        const int r0 = rblk * ROWS;
+        const int rg0 = r0 + g, rg1 = r0 + g + 8;
+        vis0 = (rg0 < P.R && P.causal) ? L - (P.n - 1 - rg0 / P.G) : L;
+        vis1 = (rg1 < P.R && P.causal) ? L - (P.n - 1 - rg1 / P.G) : L;
+        const float kmax = (P.k_mode == PA_SCALE_CHANNEL) ? __uint_as_float(P.hdr[HDR_KMAX]) : 1.0f;
+        const float kscal = (P.k_mode == PA_SCALE_TENSOR) ? P.k_scale[0] : kmax;
+        auto fold = [&](int d) -> float {
+            return (P.k_mode == PA_SCALE_CHANNEL) ? P.k_scale[(size_t)kvh * D + d] / kmax : 1.0f;
+        };
+        // rows g and g+8 of this segment: query position jq, query head h
+        const bool ok0 = rg0 < P.R, ok1 = rg1 < P.R;
+        const int jq0 = ok0 ? rg0 / P.G : 0, h0 = kvh * P.G + (ok0 ? rg0 % P.G : 0);
+        const int jq1 = ok1 ? rg1 / P.G : 0, h1 = kvh * P.G + (ok1 ? rg1 % P.G : 0);
+        // power-of-two row factors so that f16 operands of any bf16 query fit
+        float rho0 = 1.f, rho1 = 1.f;
+        if constexpr (!BF) {
+            float mx0 = 0.f, mx1 = 0.f;
+            for (int K = 0; K < G::KSTEPS; ++K) {
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int d = phys_ch<KVT, D>(K, c, e);
+                    const float f = fold(d);
+                    if (ok0) mx0 = fmaxf(mx0, fabsf(load_q<KVT, D>(P, cc.b, jq0, h0, d) * f));
+                    if (ok1) mx1 = fmaxf(mx1, fabsf(load_q<KVT, D>(P, cc.b, jq1, h1, d) * f));
+                }
+            }
+            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+            mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+            mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+            int e;
+            if (mx0 > 0.f && mx0 < 3.0e38f) { frexpf(mx0, &e); rho0 = ldexpf(1.0f, e); }
+            if (mx1 > 0.f && mx1 < 3.0e38f) { frexpf(mx1, &e); rho1 = ldexpf(1.0f, e); }
+        }
+        sc0 = P.softmax_scale * kscal * rho0 * LOG2E;
+        sc1 = P.softmax_scale * kscal * rho1 * LOG2E;
+        const float inv0 = 1.0f / rho0, inv1 = 1.0f / rho1;
+#pragma unroll
+        for (int K = 0; K < G::KSTEPS; ++K) {
+            uint32_t a[4];
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {  // a0a1/a2a3 use e=0,1; a4a5/a6a7 use e=2,3
+                const int d0 = phys_ch<KVT, D>(K, c, 2 * half), d1 = phys_ch<KVT, D>(K, c, 2 * half + 1);
+                const float f0 = fold(d0), f1 = fold(d1);
+                float u0 = 0.f, u1 = 0.f, w0 = 0.f, w1 = 0.f;
+                if (ok0) {
+                    u0 = load_q<KVT, D>(P, cc.b, jq0, h0, d0) * f0 * inv0;
+                    u1 = load_q<KVT, D>(P, cc.b, jq0, h0, d1) * f1 * inv0;
+                }
+                if (ok1) {
+                    w0 = load_q<KVT, D>(P, cc.b, jq1, h1, d0) * f0 * inv1;
+                    w1 = load_q<KVT, D>(P, cc.b, jq1, h1, d1) * f1 * inv1;
+                }
+                a[2 * half] = pack2<BF>(u0, u1);
+                a[2 * half + 1] = pack2<BF>(w0, w1);
+            }
+            if constexpr (QREG) {
+                qreg[K][0] = a[0]; qreg[K][1] = a[1]; qreg[K][2] = a[2]; qreg[K][3] = a[3];
+            } else {
+                qs[K * 32 + lane] = make_uint4(a[0], a[1], a[2], a[3]);
+            }
+        }
+        __syncwarp();
+#pragma unroll
+        for (int t = 0; t < G::NT2; ++t) o[t][0] = o[t][1] = o[t][2] = o[t][3] = 0.f;
+        m0 = m1 = -INFINITY;
+        l0 = l1 = 0.f;
+    };
+
+    auto finish_piece = [&]() {
+        float la = l0, lb = l1;
+        la += __shfl_xor_sync(0xffffffffu, la, 1);
+        la += __shfl_xor_sync(0xffffffffu, la, 2);
+        lb += __shfl_xor_sync(0xffffffffu, lb, 1);
+        lb += __shfl_xor_sync(0xffffffffu, lb, 2);
+        const int Pb = P.req[piece_b].y;
+        const bool complete = (piece_p0 == 0 && last_p == Pb - 1);
+        const long long slot_id = (long long)piece_b * X + piece_q + kw;  // partial slot of this piece
+        const int r0 = rblk * ROWS;
+        const float NaN = __int_as_float(0x7fc00000);
+#pragma unroll
+        for (int rr = 0; rr < 2; ++rr) {
+            const int row = g + 8 * rr, r = r0 + row;
+            if (r >= P.R) continue;
+            const float l = rr ? lb : la, m = rr ? m1 : m0;
+            const float inv = l > 0.f ? 1.0f / l : 0.f;
+            float lse_v = l > 0.f ? (m + lg2(l)) * LN2 : -INFINITY;
+            if (pbad) lse_v = NaN;
+            const int jq = r / P.G, h = kvh * P.G + (r % P.G);
+#pragma unroll
+            for (int t = 0; t < G::NT2; ++t) {
+                const int sg = t / G::EPL, e = t % G::EPL;
+#pragma unroll
+                for (int cc2 = 0; cc2 < 2; ++cc2) {
+                    const int d = sg * G::EPS + (2 * c + cc2) * G::EPL + e;
+                    float val = o[t][2 * rr + cc2] * inv;
+                    if (pbad) val = NaN;
+                    if (complete) {
+                        float vsc = 1.0f;
+                        if (P.v_mode == PA_SCALE_TENSOR) vsc = P.v_scale[0];
+                        else if (P.v_mode == PA_SCALE_CHANNEL) vsc = P.v_scale[(size_t)kvh * D + d];
+                        const float y = val * vsc;
+                        const size_t oi = (((size_t)piece_b * P.n + jq) * P.Hq + h) * D + d;
+                        if (P.out_dtype == PA_F32) reinterpret_cast<float *>(P.out)[oi] = y;
+                        else if (P.out_dtype == PA_F16) reinterpret_cast<__half *>(P.out)[oi] = __float2half_rn(y);
+                        else reinterpret_cast<__nv_bfloat16 *>(P.out)[oi] = __float2bfloat16_rn(y);
+                    } else {
+                        P.part_o[((size_t)slot_id * ROWS + row) * D + d] = val;
+                    }
+                }
+            }
+            if (c == 0) {
+                if (complete) {
+                    if (P.lse != nullptr) P.lse[((size_t)piece_b * P.n + jq) * P.Hq + h] = lse_v;
+                } else {
+                    P.part_lse[(size_t)slot_id * ROWS + row] = lse_v;
+                }
+            }
+        }
+    };
+
+    int j = 0;
+    for (; j < npg; ++j) {
+        if (cc.b >= P.B) {  // records shorter than the shares: stop, copies drained below
+            err |= PA_DEV_ERR_STALE_PLAN;
             break;
         }
-        if (!*reinterpret_cast<volatile int *>(&ms->bad)) {
-            const uint8_t *kt = ring + (size_t)slot * P.stage_bytes;
+        if (cc.b != piece_b || cc.q != piece_q) {
+            if (piece_b >= 0) finish_piece();
+            start_piece();
+        }
+        const int slot = j % NS;
+        if (!mbar_wait_bounded(&full[slot], (j / NS) & 1, nullptr)) {
+            err |= PA_DEV_ERR_TIMEOUT;
+            pbad = true;
+            break;
+        }
+        if ((slot_bad >> slot) & 1u) {
+            err |= PA_DEV_ERR_BLOCK_ID;
+            pbad = true;
+        }
+        if (!pbad) {
+            const uint8_t *kt = ring + (size_t)slot * page_bytes;
             const uint8_t *vt = kt + tile_bytes;
-            const int page = p0 + i;
-            const int t_page = page * bs;
+            const int t_page = cc.p * bs;
             const int nvalid = min(bs, L - t_page);  // real tokens in this page
+            const int vis_min = min(vis0, vis1);
             for (int ch = 0; ch < bs; ch += 16) {
                 // ---- S = q' K^T for tokens ch .. ch+15 (two n-tiles)
                 float s[2][4];
@@ -447,25 +543,31 @@ __global__ void __launch_bounds__(ATTN_THREADS, min_blocks<D>())
                 for (int t = 0; t < 2; ++t) s[t][0] = s[t][1] = s[t][2] = s[t][3] = 0.f;
 #pragma unroll
                 for (int sg = 0; sg < G::NSEG; ++sg) {
-                    uint32_t kw[2][G::KWORDS];
+                    uint32_t kw2[2][G::KWORDS];
 #pragma unroll
                     for (int t = 0; t < 2; ++t) {
                         const int srow = ch + 8 * t + g;
                         if constexpr (G::SW == 128) {
-                            lds_words<4>(kw[t], kt + tile_off<128>(srow, sg, 2 * c, bs));
-                            lds_words<4>(kw[t] + 4, kt + tile_off<128>(srow, sg, 2 * c + 1, bs));
+                            lds_words<4>(kw2[t], kt + tile_off<128>(srow, sg, 2 * c, bs));
+                            lds_words<4>(kw2[t] + 4, kt + tile_off<128>(srow, sg, 2 * c + 1, bs));
                         } else {
-                            lds_words<4>(kw[t], kt + tile_off<64>(srow, sg, c, bs));
+                            lds_words<4>(kw2[t], kt + tile_off<64>(srow, sg, c, bs));
                         }
                     }
 #pragma unroll
-                    for (int j = 0; j < G::KPS; ++j) {
-                        const uint4 av = reinterpret_cast<const uint4 *>(qs)[(sg * G::KPS + j) * 32 + lane];
-                        const uint32_t a[4] = {av.x, av.y, av.z, av.w};
+                    for (int jj = 0; jj < G::KPS; ++jj) {
+                        uint32_t a[4];
+                        if constexpr (QREG) {
+                            a[0] = qreg[sg * G::KPS + jj][0]; a[1] = qreg[sg * G::KPS + jj][1];
+                            a[2] = qreg[sg * G::KPS + jj][2]; a[3] = qreg[sg * G::KPS + jj][3];
+                        } else {
+                            const uint4 av = qs[(sg * G::KPS + jj) * 32 + lane];
+                            a[0] = av.x; a[1] = av.y; a[2] = av.z; a[3] = av.w;
+                        }
 #pragma unroll
                         for (int t = 0; t < 2; ++t) {
                             uint32_t b0, b1;
-                            k_frag<KVT>(kw[t], j, b0, b1);
+                            k_frag<KVT>(kw2[t], jj, b0, b1);
                             mma16816<BF>(s[t], a, b0, b1);
                         }
                     }
@@ -479,15 +581,15 @@ __global__ void __launch_bounds__(ATTN_THREADS, min_blocks<D>())
 #pragma unroll
                     for (int e = 0; e < 2; ++e) {
                         const int tok = tbase + 8 * t + e;
-                        float x0 = s[t][e] * sc0, x1 = s[t][2 + e] * sc1;
+                        float x0v = s[t][e] * sc0, x1v = s[t][2 + e] * sc1;
                         if (need_mask) {
-                            x0 = (tok < vis0) ? x0 : -INFINITY;
-                            x1 = (tok < vis1) ? x1 : -INFINITY;
+                            x0v = (tok < vis0) ? x0v : -INFINITY;
+                            x1v = (tok < vis1) ? x1v : -INFINITY;
                         }
-                        s[t][e] = x0;
-                        s[t][2 + e] = x1;
-                        mx0 = fmaxf(mx0, x0);
-                        mx1 = fmaxf(mx1, x1);
+                        s[t][e] = x0v;
+                        s[t][2 + e] = x1v;
+                        mx0 = fmaxf(mx0, x0v);
+                        mx1 = fmaxf(mx1, x1v);
                     }
                 }
                 mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
@@ -529,7 +631,9 @@ __global__ void __launch_bounds__(ATTN_THREADS, min_blocks<D>())
                 pa[2] = pack2<BF>(s[1][0], s[1][1]);
                 pa[3] = pack2<BF>(s[1][2], s[1][3]);
                 const int rA = ch + 2 * c, rB = rA + 1, rC = rA + 8, rD = rA + 9;
-                const bool zA = rA >= nvalid, zB = rB >= nvalid, zC = rC >= nvalid, zD = rD >= nvalid;
+                const bool tail = ch + 16 > nvalid;  // padding slots in this chunk: codes -> 0
+                const bool zA = tail && rA >= nvalid, zB = tail && rB >= nvalid;
+                const bool zC = tail && rC >= nvalid, zD = tail && rD >= nvalid;
 #pragma unroll
                 for (int sg = 0; sg < G::NSEG; ++sg) {
                     uint32_t va[G::VWORDS], vb[G::VWORDS], vc[G::VWORDS], vd[G::VWORDS];
@@ -545,12 +649,14 @@ __global__ void __launch_bounds__(ATTN_THREADS, min_blocks<D>())
                         lds_words<2>(vc, vt + tile_off<64>(rC, sg, g >> 1, bs) + hoff);
                         lds_words<2>(vd, vt + tile_off<64>(rD, sg, g >> 1, bs) + hoff);
                     }
+                    if (tail) {
 #pragma unroll
-                    for (int k = 0; k < G::VWORDS; ++k) {  // padding slots: codes -> 0
-                        va[k] = zA ? 0u : va[k];
-                        vb[k] = zB ? 0u : vb[k];
-                        vc[k] = zC ? 0u : vc[k];
-                        vd[k] = zD ? 0u : vd[k];
+                        for (int k = 0; k < G::VWORDS; ++k) {
+                            va[k] = zA ? 0u : va[k];
+                            vb[k] = zB ? 0u : vb[k];
+                            vc[k] = zC ? 0u : vc[k];
+                            vd[k] = zD ? 0u : vd[k];
+                        }
                     }
                     uint32_t bf[G::EPL][2];
                     v_frags<KVT, G::EPL, G::VWORDS>(va, vb, vc, vd, bf);
@@ -559,92 +665,19 @@ __global__ void __launch_bounds__(ATTN_THREADS, min_blocks<D>())
                 }
             }
         }
+        last_p = cc.p;
+        // every lane is done reading the slot before a copy may overwrite it
         __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[slot]);
+        fence_proxy_async_smem();
+        if (j + NS < npg) issue(j + NS);
+        cursor_next(cc, P.req, P.B, X, P.mbps);
     }
-    (void)aborted;
-
-    // ------------------------------------------------------ merge the warps
-    l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
-    l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
-    l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
-    l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
-    if (c == 0) {
-        ms->m_w[warp][g] = m0;
-        ms->m_w[warp][g + 8] = m1;
-        ms->l_w[warp][g] = l0;
-        ms->l_w[warp][g + 8] = l1;
+    if (j < npg) {
+        // a wait ran out: let every copy still in flight land before exiting
+        for (int i = j; i < min(npg, j + NS); ++i) mbar_wait_bounded(&full[i % NS], (i / NS) & 1, nullptr);
     }
-    asm volatile("bar.sync 1, %0;" ::"n"(NW * 32));
-    float f0, f1;
-    {
-        float M0 = -INFINITY, M1 = -INFINITY;
-#pragma unroll
-        for (int w = 0; w < NW; ++w) {
-            M0 = fmaxf(M0, ms->m_w[w][g]);
-            M1 = fmaxf(M1, ms->m_w[w][g + 8]);
-        }
-        f0 = (M0 == -INFINITY) ? 0.f : ex2(m0 - M0);
-        f1 = (M1 == -INFINITY) ? 0.f : ex2(m1 - M1);
-    }
-    for (int w = 0; w < NW; ++w) {
-        if (warp == w) {
-#pragma unroll
-            for (int t = 0; t < G::NT2; ++t) {
-                const int sg = t / G::EPL, e = t % G::EPL;
-#pragma unroll
-                for (int cc = 0; cc < 2; ++cc) {
-                    const int d = sg * G::EPS + (2 * c + cc) * G::EPL + e;
-                    float *p0r = mbuf + g * D + d;
-                    float *p1r = mbuf + (g + 8) * D + d;
-                    if (w == 0) {
-                        *p0r = o[t][cc] * f0;
-                        *p1r = o[t][2 + cc] * f1;
-                    } else {
-                        *p0r += o[t][cc] * f0;
-                        *p1r += o[t][2 + cc] * f1;
-                    }
-                }
-            }
-        }
-        asm volatile("bar.sync 1, %0;" ::"n"(NW * 32));
-    }
-
-    // ---------------------------------------------------------- epilogue
-    const bool bad = ms->bad || ms->abort_flag;
-    const int rows_here = unit_ok ? min(ROWS, P.R - r0) : 0;
-    const bool final_out = (S_b == 1);
-    for (int idx = ctid; idx < rows_here * D; idx += NW * 32) {
-        const int row = idx / D, d = idx % D;
-        float M = -INFINITY, Lsum = 0.f;
-#pragma unroll
-        for (int w = 0; w < NW; ++w) M = fmaxf(M, ms->m_w[w][row]);
-        if (M != -INFINITY) {
-#pragma unroll
-            for (int w = 0; w < NW; ++w) Lsum += ms->l_w[w][row] * ex2(ms->m_w[w][row] - M);
-        }
-        float val = (Lsum > 0.f) ? mbuf[row * D + d] / Lsum : 0.f;
-        float lse_v = (Lsum > 0.f) ? (M + lg2(Lsum)) * LN2 : -INFINITY;
-        if (bad) { val = __int_as_float(0x7fc00000); lse_v = __int_as_float(0x7fc00000); }
-        const int r = r0 + row;
-        const int jq = r / P.G, h = kvh * P.G + (r % P.G);
-        if (final_out) {
-            float vsc = 1.0f;
-            if (P.v_mode == PA_SCALE_TENSOR) vsc = P.v_scale[0];
-            else if (P.v_mode == PA_SCALE_CHANNEL) vsc = P.v_scale[(size_t)kvh * D + d];
-            const float y = val * vsc;
-            const size_t oi = (((size_t)b * P.n + jq) * P.Hq + h) * D + d;
-            if (P.out_dtype == PA_F32) reinterpret_cast<float *>(P.out)[oi] = y;
-            else if (P.out_dtype == PA_F16) reinterpret_cast<__half *>(P.out)[oi] = __float2half_rn(y);
-            else reinterpret_cast<__nv_bfloat16 *>(P.out)[oi] = __float2bfloat16_rn(y);
-            if (P.lse != nullptr && d == 0) P.lse[((size_t)b * P.n + jq) * P.Hq + h] = lse_v;
-        } else {
-            P.part_o[((size_t)unit * P.R + r) * D + d] = val;
-            if (d == 0) P.part_lse[(size_t)unit * P.R + r] = lse_v;
-        }
-    }
-    (void)split;
-    asm volatile("bar.sync 2, %0;" ::"n"(ATTN_THREADS));
+    if (piece_b >= 0) finish_piece();
+    if (lane == 0) atomic_or_err(P.hdr, err);
 }
 
 }  // namespace pa

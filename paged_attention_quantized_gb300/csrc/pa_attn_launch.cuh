@@ -8,15 +8,6 @@
 
 namespace pa {
 
-// dynamic shared memory of one CTA: alignment slack, the stage ring, the q'
-// fragments, the merge buffer, row constants and the stage barriers
-inline size_t attn_smem_bytes(int D, int stages, int stage_bytes) {
-    const size_t misc = (sizeof(SmemMisc) + 15) & ~size_t(15);
-    // the merge buffer [ROWS][D] fp32 lives in the ring after the last page
-    const size_t ring = std::max((size_t)stages * stage_bytes, (size_t)ROWS * D * 4);
-    return 1024 + ring + (size_t)(D / 16) * 512 + misc + 2 * MAX_STAGES * sizeof(uint64_t);
-}
-
 template <int KVT, int D>
 cudaError_t launch_attn(const CUtensorMap &tk, const CUtensorMap &tv, const AttnParams &P, dim3 grid, size_t smem,
                         cudaStream_t s);

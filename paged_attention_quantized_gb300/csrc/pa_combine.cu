@@ -1,8 +1,8 @@
 // Split-KV merge for paged attention (sm_103a).
 //
-// For every request with S_b > 1 splits and every row of one kv head, the
-// normalised partial outputs o_s and log-sum-exps lse_s of the splits are
-// merged in ascending split order:
+// Every segment (request, kv head, block of 16 query rows) whose pages were
+// shared by several warps has one normalised partial output o_s and
+// log-sum-exp lse_s per warp; they are merged in ascending position order:
 //     M = max_s lse_s,  w_s = exp(lse_s - M),
 //     out = (sum_s w_s o_s) / (sum_s w_s) * v_scale,   lse = M + ln(sum_s w_s)
 // (the pages name split "partial" kernels -- 1Cat-vLLM PR #647, Fix -- and
@@ -15,38 +15,69 @@ namespace pa {
 
 constexpr int COMBINE_THREADS = 256;
 
+// first position of warp k's share of the n positions split over nw warps
+__device__ __forceinline__ long long share_start(long long k, long long n, long long nw) { return k * n / nw; }
+
+// the warp whose share holds position x (the last k with share_start <= x)
+__device__ __forceinline__ long long share_owner(long long x, long long n, long long nw) {
+    return ((x + 1) * nw + n - 1) / n - 1;
+}
+
+// One CTA per segment (request, kv head, row block).
 __global__ void __launch_bounds__(COMBINE_THREADS) pa_combine_kernel(CombineParams P) {
-    const int b = blockIdx.x / P.Hkv, kvh = blockIdx.x % P.Hkv;
+    const int X = P.Hkv * P.RBLK;
+    const int seg = blockIdx.x;
+    const int b = seg / X, q = seg % X;
+    const int kvh = q / P.RBLK, rblk = q % P.RBLK;
     const int4 Rq = P.req[b];
-    const int S = Rq.y;
-    if (S <= 1) return;
-    const long long u0 = (long long)Rq.z * P.Hkv + (long long)kvh * S;
-    if (Rq.z < 0 || u0 + S > P.max_units) return;  // not a plan of this problem
+    const int Pb = Rq.y;
+    const int rows_here = min(16, P.R - rblk * 16);
+    const float NaN = __int_as_float(0x7fc00000);
     const float LOG2E_ = 1.4426950408889634f;
-    for (int idx = threadIdx.x; idx < P.R * P.Dv; idx += COMBINE_THREADS) {
-        const int r = idx / P.Dv, d = idx % P.Dv;
-        float M = -INFINITY;
-        bool nan = false;
-        for (int s = 0; s < S; ++s) {
-            const float l = P.part_lse[(u0 + s) * P.R + r];
-            nan |= (l != l);
-            M = fmaxf(M, l);
-        }
+    const long long N = (long long)P.hdr[HDR_TOTAL_PAGES] * X;
+    long long kf = 0, kl = -1;
+    if (Pb > 0) {
+        const long long x0 = (long long)Rq.z * X + (long long)q * Pb;
+        const long long xl = x0 + Pb - 1;
+        if (xl >= N) return;  // not a plan of this problem
+        kf = share_owner(x0, N, P.nwarps);
+        kl = share_owner(xl, N, P.nwarps);
+        if (kf == kl) return;  // one piece: the attention kernel wrote the output
+    }
+    for (int idx = threadIdx.x; idx < rows_here * P.Dv; idx += COMBINE_THREADS) {
+        const int i = idx / P.Dv, d = idx % P.Dv;
+        const int r = rblk * 16 + i;
         float y, lse_v;
-        if (nan) {
-            y = lse_v = __int_as_float(0x7fc00000);
-        } else if (M == -INFINITY) {
-            y = 0.f;
-            lse_v = -INFINITY;
+        if (Pb == 0) {
+            // no visible page: a flagged request is NaN, an empty one is 0
+            y = Rq.w ? NaN : 0.f;
+            lse_v = Rq.w ? NaN : -INFINITY;
         } else {
-            float acc = 0.f, den = 0.f;
-            for (int s = 0; s < S; ++s) {
-                const float w = ex2((P.part_lse[(u0 + s) * P.R + r] - M) * LOG2E_);
-                den += w;
-                acc += w * P.part_o[((u0 + s) * P.R + r) * P.Dv + d];
+            float M = -INFINITY;
+            bool nan = false;
+            for (long long k = kf; k <= kl; ++k) {
+                if (share_start(k, N, P.nwarps) == share_start(k + 1, N, P.nwarps)) continue;  // empty share
+                const float l = P.part_lse[((long long)seg + k) * 16 + i];
+                nan |= (l != l);
+                M = fmaxf(M, l);
             }
-            y = acc / den;
-            lse_v = M + lg2(den) * 0.6931471805599453f;
+            if (nan) {
+                y = lse_v = NaN;
+            } else if (M == -INFINITY) {
+                y = 0.f;
+                lse_v = -INFINITY;
+            } else {
+                float acc = 0.f, den = 0.f;
+                for (long long k = kf; k <= kl; ++k) {
+                    if (share_start(k, N, P.nwarps) == share_start(k + 1, N, P.nwarps)) continue;
+                    const long long slot = (long long)seg + k;
+                    const float w = ex2((P.part_lse[slot * 16 + i] - M) * LOG2E_);
+                    den += w;
+                    acc += w * P.part_o[(slot * 16 + i) * P.Dv + d];
+                }
+                y = acc / den;
+                lse_v = M + lg2(den) * 0.6931471805599453f;
+            }
         }
         float vsc = 1.0f;
         if (P.v_mode == PA_SCALE_TENSOR) vsc = P.v_scale[0];
@@ -63,7 +94,7 @@ __global__ void __launch_bounds__(COMBINE_THREADS) pa_combine_kernel(CombinePara
 
 cudaError_t launch_combine(const CombineParams &P, cudaStream_t s) {
     if (P.B == 0) return cudaSuccess;
-    pa_combine_kernel<<<P.B * P.Hkv, COMBINE_THREADS, 0, s>>>(P);
+    pa_combine_kernel<<<P.B * P.Hkv * P.RBLK, COMBINE_THREADS, 0, s>>>(P);
     return cudaGetLastError();
 }
 

@@ -21,16 +21,15 @@ struct AttnParams {
     const float *k_scale;
     const float *v_scale;
     uint32_t *hdr;       // workspace header words
-    const int4 *req;     // per-request plan records
-    const int4 *units;   // unit records
-    float *part_o;       // [max_units][R][Dv]
-    float *part_lse;     // [max_units][R]
+    const int4 *req;     // per-request plan records {L, pages, pages before, flags}
+    float *part_o;       // [slots][16][Dv] partial outputs of segment pieces
+    float *part_lse;     // [slots][16]
     void *out;
     float *lse;
-    int B, n, Hq, Hkv, G, R, bs, mbps, max_ctx, num_blocks;
+    int B, n, Hq, Hkv, G, R, RBLK, bs, mbps, num_blocks;
     int q_dtype, out_dtype, k_mode, v_mode, causal;
-    int stages, stage_bytes;
-    int max_units;
+    int slots;           // ring pages per warp
+    int warp_smem;       // shared-memory bytes per warp
     float softmax_scale;
 };
 
@@ -38,26 +37,24 @@ struct PlanParams {
     const int32_t *context_lens;
     uint32_t *hdr;
     int4 *req;
-    int4 *units;
-    int B, Hkv, bs, max_ctx, mbps;
-    int T, min_pages, forced_pages, max_units;
+    int B, bs, max_ctx, mbps;
 };
 
 struct CombineParams {
     const int4 *req;
+    const uint32_t *hdr;
     const float *part_o;
     const float *part_lse;
     const float *v_scale;
     void *out;
     float *lse;
-    int B, n, Hq, Hkv, G, R, Dv, out_dtype, v_mode;
-    long long max_units;
+    int B, n, Hq, Hkv, G, R, RBLK, Dv, out_dtype, v_mode;
+    long long nwarps;  // warps of the attention launch
 };
 
 // header word indices
 constexpr int HDR_ERR = 0;
-constexpr int HDR_NUM_UNITS = 1;
-constexpr int HDR_CHUNK = 2;
+constexpr int HDR_TOTAL_PAGES = 1;  // sum over requests of their pages
 constexpr int HDR_KMAX = 3;
 
 // bounded waits: give up after this many nanoseconds of %globaltimer
@@ -119,13 +116,13 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
 }
 
 // Wait for the phase of `bar` with the given parity.  Gives up (returns
-// false) when *abort becomes non-zero or after WAIT_LIMIT_NS.
+// false) when *abort (if given) becomes non-zero or after WAIT_LIMIT_NS.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity, volatile int *abort) {
     if (mbar_try_wait(bar, parity)) return true;
     const unsigned long long t0 = globaltimer();
     while (true) {
         if (mbar_try_wait(bar, parity)) return true;
-        if (*abort) return false;
+        if (abort != nullptr && *abort) return false;
         if (globaltimer() - t0 > WAIT_LIMIT_NS) return false;
     }
 }

@@ -47,7 +47,7 @@ def _prob(B, **kw):
     base = dict(batch=4, next_n=1, num_q_heads=32, num_kv_heads=8, head_dim_k=128, head_dim_v=128,
                 block_size=16, num_blocks=1000, max_blocks_per_seq=64, max_context_len=1024,
                 q_dtype=B.PA_BF16, kv_dtype=B.PA_BF16, out_dtype=B.PA_BF16, k_scale_mode=0, v_scale_mode=0,
-                causal=0, v_is_k_prefix=0, num_sms=152, split_target=0, split_pages=0, softmax_scale=0.088)
+                causal=0, v_is_k_prefix=0, num_sms=152, grid_ctas=0, softmax_scale=0.088)
     base.update(kw)
     return B.Problem(**base)
 
@@ -57,15 +57,17 @@ def test_workspace_size_and_layout(B):
     n = B.pa_workspace_size(p)
     lo = B.pa_workspace_layout(p)
     assert n == lo.total_bytes > 0
-    offs = [lo.header_offset, lo.requests_offset, lo.units_offset, lo.partial_o_offset, lo.partial_lse_offset]
+    offs = [lo.header_offset, lo.requests_offset, lo.partial_o_offset, lo.partial_lse_offset]
     assert offs == sorted(offs) and all(o % 256 == 0 for o in offs)
     assert lo.rows_per_kv_head == 4 and lo.row_blocks == 1 and lo.num_sms == 152
-    assert lo.partial_lse_offset - lo.partial_o_offset >= lo.max_units * 4 * 128 * 4
+    assert lo.grid_ctas == 152 * 2 and lo.warps == lo.grid_ctas * 4 and lo.ring_pages_per_warp >= 2
+    assert lo.partial_slots == 4 * 8 + lo.warps
+    assert lo.partial_lse_offset - lo.partial_o_offset >= lo.partial_slots * 16 * 128 * 4
 
 
 @pytest.mark.parametrize("field,value", [
     ("batch", -1), ("next_n", 0), ("num_q_heads", 30), ("num_kv_heads", 0), ("block_size", 0),
-    ("num_blocks", 0), ("max_blocks_per_seq", 0), ("max_context_len", -5), ("q_dtype", 7),
+    ("num_blocks", 0), ("max_blocks_per_seq", 0), ("max_context_len", -5), ("q_dtype", 7), ("grid_ctas", -1),
     ("q_dtype", 3), ("kv_dtype", 9), ("out_dtype", 4), ("k_scale_mode", 5), ("causal", 2),
 ])
 def test_invalid_arguments(B, field, value):
@@ -108,22 +110,24 @@ def test_missing_pointers_rejected(B):
     assert st == B.PA_ERR_INVALID_ARG
 
 
-def test_max_units_bound_covers_oracle_plan(B):
+def test_partial_slots_cover_oracle_pieces(B):
     import numpy as np
     import oracle
     rng = np.random.default_rng(3)
     for _ in range(20):
-        Bsz = int(rng.integers(1, 100))
+        Bsz = int(rng.integers(1, 60))
         bs = int(rng.choice([16, 32, 64]))
-        maxctx = int(rng.integers(1, 40000))
+        maxctx = int(rng.integers(1, 20000))
         Hkv = int(rng.choice([1, 2, 8]))
         G = int(rng.choice([1, 4, 16]))
         n = int(rng.choice([1, 2, 4]))
         mbps = -(-maxctx // bs)
         p = _prob(B, batch=Bsz, block_size=bs, max_context_len=maxctx, num_kv_heads=Hkv, num_q_heads=Hkv * G,
-                  next_n=n, max_blocks_per_seq=mbps, num_sms=int(rng.integers(1, 200)))
+                  next_n=n, max_blocks_per_seq=mbps, num_sms=int(rng.integers(1, 200)),
+                  grid_ctas=int(rng.integers(0, 50)))
         lo = B.pa_workspace_layout(p)
         L = rng.integers(0, maxctx + 1, Bsz)
         pl = oracle.plan(L, bs=bs, Hkv=Hkv, max_context_len=maxctx, max_blocks_per_seq=mbps,
-                         target_ctas=lo.split_target, min_pages=lo.min_split_pages, row_blocks=lo.row_blocks)
-        assert pl["num_units"] <= lo.max_units
+                         row_blocks=lo.row_blocks, warps=lo.warps)
+        assert pl["slots"] == lo.partial_slots
+        assert all(pc["slot"] < lo.partial_slots for pc in pl["pieces"])

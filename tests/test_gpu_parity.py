@@ -45,10 +45,10 @@ SMALL = [
 ]
 
 
-@pytest.mark.parametrize("name,kw,split", SMALL, ids=lambda x: str(x))
+@pytest.mark.parametrize("name,kw,split", SMALL, ids=lambda x: str(x))  # split: persistent CTAs (0 = default)
 def test_small_parity(name, kw, split):
     w = make(name, **kw)
-    out, lse, ws, _ = run_gpu(w, split_pages=split)
+    out, lse, ws, _ = run_gpu(w, grid_ctas=split)
     assert error_bits(ws) == 0
     compare(w, out, lse)
 
@@ -59,7 +59,7 @@ def test_quantized_channel_scales_soft_softmax(name):
     # checks the dequant and the fold with the plain relative tolerance
     w = make(name, B=4, L_lo=20, L_hi=500, Hq=16, Hkv=2)
     w.q = (w.q.float() / 1e7).to(w.q.dtype)
-    out, lse, ws, _ = run_gpu(w, split_pages=2)
+    out, lse, ws, _ = run_gpu(w, grid_ctas=2)
     compare(w, out, lse)
 
 
@@ -67,15 +67,15 @@ def test_quantized_channel_scales_soft_softmax(name):
                                     ("int8", 64), ("int8", 256), ("int4", 256)])
 def test_other_head_dims(name, D):
     w = make(name, B=3, L_lo=1, L_hi=300, Hq=8, Hkv=2, D=D)
-    out, lse, ws, _ = run_gpu(w, split_pages=2)
+    out, lse, ws, _ = run_gpu(w, grid_ctas=2)
     assert error_bits(ws) == 0
     compare(w, out, lse)
 
 
 def test_steps_separately_equal_fused_call():
     w = make("bf16", B=6, L_lo=1, L_hi=2000, Hq=8, Hkv=2)
-    o1, l1, _, _ = run_gpu(w, split_pages=5)
-    o2, l2, _, _ = run_gpu(w, split_pages=5, steps="plan+run+combine")
+    o1, l1, _, _ = run_gpu(w, grid_ctas=5)
+    o2, l2, _, _ = run_gpu(w, grid_ctas=5, steps="plan+run+combine")
     assert torch.equal(o1, o2) and torch.equal(l1, l2)
 
 
@@ -113,7 +113,7 @@ def test_repeat_runs_bitwise():
 
 def test_split_counts_agree_within_tolerance():
     w = make("bf16", B=4, L_lo=500, L_hi=3000, Hq=8, Hkv=2)
-    outs = [run_gpu(w, split_pages=s)[0].float() for s in (1, 7, 0, 10000)]
+    outs = [run_gpu(w, grid_ctas=s)[0].float() for s in (1, 7, 0, 3000)]
     for o in outs[1:]:
         assert (o - outs[0]).abs().max().item() <= 1e-2
 
@@ -121,7 +121,7 @@ def test_split_counts_agree_within_tolerance():
 # -------------------------------------------------------------------- plan
 
 
-@pytest.mark.parametrize("kw", [dict(), dict(split_pages=3), dict(split_target=50), dict(num_sms=7)])
+@pytest.mark.parametrize("kw", [dict(), dict(grid_ctas=3), dict(grid_ctas=50), dict(num_sms=7)])
 def test_plan_matches_oracle_plan(kw):
     w = make("bf16", B=37, L_lo=0, L_hi=5000, Hq=8, Hkv=2)
     p = pa.problem(w, **kw)
@@ -130,18 +130,38 @@ def test_plan_matches_oracle_plan(kw):
     torch.cuda.synchronize()
     lo = pa.binding().pa_workspace_layout(p)
     pl = oracle.plan(w.context_lens.cpu().numpy(), bs=w.bs, Hkv=w.Hkv, max_context_len=w.max_context_len,
-                     max_blocks_per_seq=w.max_blocks_per_seq, target_ctas=lo.split_target,
-                     min_pages=lo.min_split_pages, row_blocks=lo.row_blocks, forced_pages=kw.get("split_pages", 0))
+                     max_blocks_per_seq=w.max_blocks_per_seq, row_blocks=lo.row_blocks, warps=lo.warps)
     raw = ws.cpu().numpy()
     hdr = raw[lo.header_offset: lo.header_offset + 16].view(np.uint32)
-    assert hdr[1] == pl["num_units"] and hdr[2] == pl["chunk_pages"] and hdr[0] == 0
+    assert hdr[1] == pl["total_pages"] and hdr[0] == 0
     req = raw[lo.requests_offset: lo.requests_offset + 16 * w.B].view(np.int32).reshape(w.B, 4)
     assert np.array_equal(req[:, 0], w.context_lens.cpu().numpy())
-    assert np.array_equal(req[:, 1], pl["splits"]) and np.array_equal(req[:, 2], pl["offsets"])
+    assert np.array_equal(req[:, 1], pl["pages"]) and np.array_equal(req[:, 2], pl["prefix"])
     assert np.array_equal(req[:, 3], pl["flags"])
-    units = raw[lo.units_offset: lo.units_offset + 16 * pl["num_units"]].view(np.int32).reshape(-1, 4)
-    want = np.array([(b, (h << 16) | s, p0, p1) for (b, h, s, p0, p1) in pl["units"]], dtype=np.int32)
-    assert np.array_equal(units, want)
+
+
+def test_partial_pieces_match_oracle_plan():
+    # with many warps every segment is cut into pieces: each piece's partial
+    # lse slot is written, the rest of the slots are not touched
+    w = make("bf16", B=3, L_lo=200, L_hi=900, Hq=8, Hkv=2)
+    p = pa.problem(w, grid_ctas=40)
+    out, lse, ws = pa.alloc(w, p)
+    lo = pa.binding().pa_workspace_layout(p)
+    ws_f = ws.view(torch.float32)
+    ws_f[lo.partial_lse_offset // 4: lo.partial_lse_offset // 4 + lo.partial_slots * 16] = float("nan")
+    pa.run(w, p, out, ws, lse, steps="plan+run")
+    torch.cuda.synchronize()
+    pl = oracle.plan(w.context_lens.cpu().numpy(), bs=w.bs, Hkv=w.Hkv, max_context_len=w.max_context_len,
+                     max_blocks_per_seq=w.max_blocks_per_seq, row_blocks=lo.row_blocks, warps=lo.warps)
+    lse_parts = ws_f[lo.partial_lse_offset // 4:][: lo.partial_slots * 16].view(-1, 16).cpu().numpy()
+    R = lo.rows_per_kv_head
+    written = set()
+    for pc in pl["pieces"]:
+        if not pc["complete"]:
+            written.add(pc["slot"])
+            assert np.isfinite(lse_parts[pc["slot"], :R]).all(), pc
+    untouched = [s for s in range(lo.partial_slots) if s not in written]
+    assert np.isnan(lse_parts[untouched]).all()
 
 
 def test_max_abs_scale_kernel():
@@ -187,7 +207,7 @@ def test_worked_fold_case_on_gpu():
         w.q = torch.full_like(w.q, 100.0)
         w.k_scale = torch.full_like(w.k_scale, 1000.0)
         w.k_pool = torch.zeros_like(w.k_pool)
-        out, lse, ws, _ = run_gpu(w, split_pages=4)
+        out, lse, ws, _ = run_gpu(w, grid_ctas=4)
         assert torch.isfinite(out).all()
         compare(w, out, lse)
         assert np.allclose(lse.cpu().numpy()[:, 0, :], np.log([[7.0], [300.0]]), atol=1e-4)
