@@ -19,6 +19,9 @@ cudaError_t launch_combine(const CombineParams &P, cudaStream_t s);
 namespace {
 
 constexpr int VERSION = 100;
+#ifndef PA_TOKM_MAX_ROWS
+#define PA_TOKM_MAX_ROWS 8  // at most 8: the rows are the MMA N axis then
+#endif
 constexpr size_t SM_SMEM_BYTES = 228 * 1024;     // shared memory per SM
 constexpr size_t CTA_RESERVED_BYTES = 1024;       // reserved by the runtime per resident CTA
 constexpr size_t MAX_DYN_SMEM_BYTES = 227 * 1024; // opt-in limit per CTA
@@ -202,8 +205,9 @@ T *at(void *ws, size_t off) {
 cudaError_t dispatch_attn(const pa_problem *p, const Derived &d, const CUtensorMap &tk, const CUtensorMap &tv,
                           const pa::AttnParams &P, cudaStream_t s) {
     const dim3 grid((unsigned)d.ctas);
+    const bool tokm = d.R <= PA_TOKM_MAX_ROWS;  // few query rows per kv head: tokens on the MMA M axis
 #define PA_CASE(KVT, DD) \
-    if (p->kv_dtype == KVT && d.D == DD) return pa::launch_attn<KVT, DD>(tk, tv, P, grid, d.smem, s);
+    if (p->kv_dtype == KVT && d.D == DD) return pa::launch_attn<KVT, DD>(tk, tv, P, grid, d.smem, tokm, s);
     PA_CASE(PA_F16, 64) PA_CASE(PA_F16, 128) PA_CASE(PA_F16, 256)
     PA_CASE(PA_BF16, 64) PA_CASE(PA_BF16, 128) PA_CASE(PA_BF16, 256)
     PA_CASE(PA_E4M3, 64) PA_CASE(PA_E4M3, 128) PA_CASE(PA_E4M3, 256)

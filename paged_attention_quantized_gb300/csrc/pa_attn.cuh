@@ -266,6 +266,14 @@ __device__ __forceinline__ Cursor cursor_at(long long x, const int4 *req, int B,
     return cu;
 }
 
+// 8x8 transpose of 16-bit elements held in the mma fragment layout (lane t
+// holds row t/4, columns 2(t%4) and 2(t%4)+1)
+__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t a) {
+    uint32_t r;
+    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(r) : "r"(a));
+    return r;
+}
+
 __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
@@ -278,12 +286,17 @@ __device__ __forceinline__ float load_q(const AttnParams &P, int b, int j, int h
     return __half2float(__ushort_as_half(bits));
 }
 
-template <int KVT, int D>
+// TOKM: at most 8 query rows per kv head.  Tokens then form the MMA M axis
+// (S^T = K q'^T and O^T = V^T P^T with the rows as N = 8), which halves the
+// tensor work and the O accumulator against padding 8 rows up to M = 16.
+template <int KVT, int D, bool TOKM>
 __global__ void __launch_bounds__(ATTN_THREADS, min_blocks<D>())
     pa_attn_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv, AttnParams P) {
     using G = Geo<KVT, D>;
     constexpr bool BF = G::BF;
     constexpr bool QREG = q_in_regs<D>();
+    constexpr int NO = TOKM ? D / 16 : G::NT2;  // accumulator tiles of O (O^T with TOKM)
+    constexpr int HEPL = G::EPL / 2;            // TOKM: O^T tiles per V segment
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
@@ -371,7 +384,9 @@ __global__ void __launch_bounds__(ATTN_THREADS, min_blocks<D>())
     for (int j = 0; j < npre; ++j) issue(j);
 
     // ---- per-piece state (a piece = this warp's run of pages of one segment)
-    float o[G::NT2][4];
+    // o: rows g / g+8 x channels (rows-as-M), or channels x rows 2c / 2c+1 (TOKM);
+    // m0/l0 and m1/l1 are the running max / sum of the lane's two rows
+    float o[NO][4];
     float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
     uint32_t qreg[QREG ? G::KSTEPS : 1][4];
     float sc0 = 0.f, sc1 = 0.f;
@@ -425,6 +440,16 @@ __global__ void __launch_bounds__(ATTN_THREADS, min_blocks<D>())
         }
         sc0 = P.softmax_scale * kscal * rho0 * LOG2E;
         sc1 = P.softmax_scale * kscal * rho1 * LOG2E;
+        if constexpr (TOKM) {
+            // this lane's score rows are 2c and 2c+1; their q rows were folded
+            // by the lanes with g = 2c and g = 2c+1
+            const float sA = __shfl_sync(0xffffffffu, sc0, 8 * c), sB = __shfl_sync(0xffffffffu, sc0, 8 * c + 4);
+            const int ra = r0 + 2 * c, rb = ra + 1;
+            vis0 = (ra < P.R && P.causal) ? L - (P.n - 1 - ra / P.G) : L;
+            vis1 = (rb < P.R && P.causal) ? L - (P.n - 1 - rb / P.G) : L;
+            sc0 = sA;
+            sc1 = sB;
+        }
         const float inv0 = 1.0f / rho0, inv1 = 1.0f / rho1;
 #pragma unroll
         for (int K = 0; K < G::KSTEPS; ++K) {
@@ -453,59 +478,94 @@ __global__ void __launch_bounds__(ATTN_THREADS, min_blocks<D>())
         }
         __syncwarp();
 #pragma unroll
-        for (int t = 0; t < G::NT2; ++t) o[t][0] = o[t][1] = o[t][2] = o[t][3] = 0.f;
+        for (int t = 0; t < NO; ++t) o[t][0] = o[t][1] = o[t][2] = o[t][3] = 0.f;
         m0 = m1 = -INFINITY;
         l0 = l1 = 0.f;
     };
 
     auto finish_piece = [&]() {
         float la = l0, lb = l1;
-        la += __shfl_xor_sync(0xffffffffu, la, 1);
-        la += __shfl_xor_sync(0xffffffffu, la, 2);
-        lb += __shfl_xor_sync(0xffffffffu, lb, 1);
-        lb += __shfl_xor_sync(0xffffffffu, lb, 2);
-        const int Pb = P.req[piece_b].y;
+        if constexpr (TOKM) {  // the lane's rows were summed over its tokens g, g+8
+#pragma unroll
+            for (int off = 4; off <= 16; off <<= 1) {
+                la += __shfl_xor_sync(0xffffffffu, la, off);
+                lb += __shfl_xor_sync(0xffffffffu, lb, off);
+            }
+        } else {
+            la += __shfl_xor_sync(0xffffffffu, la, 1);
+            la += __shfl_xor_sync(0xffffffffu, la, 2);
+            lb += __shfl_xor_sync(0xffffffffu, lb, 1);
+            lb += __shfl_xor_sync(0xffffffffu, lb, 2);
+        }
+        const int Pb = planned_pages(P.req, piece_b, P.mbps);
         const bool complete = (piece_p0 == 0 && last_p == Pb - 1);
         const long long slot_id = (long long)piece_b * X + piece_q + kw;  // partial slot of this piece
         const int r0 = rblk * ROWS;
         const float NaN = __int_as_float(0x7fc00000);
-#pragma unroll
-        for (int rr = 0; rr < 2; ++rr) {
-            const int row = g + 8 * rr, r = r0 + row;
-            if (r >= P.R) continue;
-            const float l = rr ? lb : la, m = rr ? m1 : m0;
-            const float inv = l > 0.f ? 1.0f / l : 0.f;
+        // store value `val` of (row index within the segment, channel d)
+        auto put = [&](int row, int d, float val) {
+            const int r = r0 + row;
+            if (pbad) val = NaN;
+            if (complete) {
+                float vsc = 1.0f;
+                if (P.v_mode == PA_SCALE_TENSOR) vsc = P.v_scale[0];
+                else if (P.v_mode == PA_SCALE_CHANNEL) vsc = P.v_scale[(size_t)kvh * D + d];
+                const float y = val * vsc;
+                const int jq = r / P.G, h = kvh * P.G + (r % P.G);
+                const size_t oi = (((size_t)piece_b * P.n + jq) * P.Hq + h) * D + d;
+                if (P.out_dtype == PA_F32) reinterpret_cast<float *>(P.out)[oi] = y;
+                else if (P.out_dtype == PA_F16) reinterpret_cast<__half *>(P.out)[oi] = __float2half_rn(y);
+                else reinterpret_cast<__nv_bfloat16 *>(P.out)[oi] = __float2bfloat16_rn(y);
+            } else {
+                P.part_o[((size_t)slot_id * ROWS + row) * D + d] = val;
+            }
+        };
+        auto put_lse = [&](int row, float l, float m) {
+            const int r = r0 + row;
             float lse_v = l > 0.f ? (m + lg2(l)) * LN2 : -INFINITY;
             if (pbad) lse_v = NaN;
-            const int jq = r / P.G, h = kvh * P.G + (r % P.G);
+            if (complete) {
+                const int jq = r / P.G, h = kvh * P.G + (r % P.G);
+                if (P.lse != nullptr) P.lse[((size_t)piece_b * P.n + jq) * P.Hq + h] = lse_v;
+            } else {
+                P.part_lse[(size_t)slot_id * ROWS + row] = lse_v;
+            }
+        };
+        if constexpr (TOKM) {
+            const int ra = 2 * c, rb = 2 * c + 1;
+            const float ia = la > 0.f ? 1.0f / la : 0.f, ib = lb > 0.f ? 1.0f / lb : 0.f;
 #pragma unroll
-            for (int t = 0; t < G::NT2; ++t) {
-                const int sg = t / G::EPL, e = t % G::EPL;
-#pragma unroll
-                for (int cc2 = 0; cc2 < 2; ++cc2) {
-                    const int d = sg * G::EPS + (2 * c + cc2) * G::EPL + e;
-                    float val = o[t][2 * rr + cc2] * inv;
-                    if (pbad) val = NaN;
-                    if (complete) {
-                        float vsc = 1.0f;
-                        if (P.v_mode == PA_SCALE_TENSOR) vsc = P.v_scale[0];
-                        else if (P.v_mode == PA_SCALE_CHANNEL) vsc = P.v_scale[(size_t)kvh * D + d];
-                        const float y = val * vsc;
-                        const size_t oi = (((size_t)piece_b * P.n + jq) * P.Hq + h) * D + d;
-                        if (P.out_dtype == PA_F32) reinterpret_cast<float *>(P.out)[oi] = y;
-                        else if (P.out_dtype == PA_F16) reinterpret_cast<__half *>(P.out)[oi] = __float2half_rn(y);
-                        else reinterpret_cast<__nv_bfloat16 *>(P.out)[oi] = __float2bfloat16_rn(y);
-                    } else {
-                        P.part_o[((size_t)slot_id * ROWS + row) * D + d] = val;
-                    }
+            for (int t = 0; t < NO; ++t) {
+                const int sg = t / HEPL, mm = t % HEPL;
+                const int dlo = sg * G::EPS + g * G::EPL + 2 * mm;
+                if (r0 + ra < P.R) {
+                    put(ra, dlo, o[t][0] * ia);
+                    put(ra, dlo + 1, o[t][2] * ia);
+                }
+                if (r0 + rb < P.R) {
+                    put(rb, dlo, o[t][1] * ib);
+                    put(rb, dlo + 1, o[t][3] * ib);
                 }
             }
-            if (c == 0) {
-                if (complete) {
-                    if (P.lse != nullptr) P.lse[((size_t)piece_b * P.n + jq) * P.Hq + h] = lse_v;
-                } else {
-                    P.part_lse[(size_t)slot_id * ROWS + row] = lse_v;
+            if (g == 0) {
+                if (r0 + ra < P.R) put_lse(ra, la, m0);
+                if (r0 + rb < P.R) put_lse(rb, lb, m1);
+            }
+        } else {
+#pragma unroll
+            for (int rr = 0; rr < 2; ++rr) {
+                const int row = g + 8 * rr;
+                if (r0 + row >= P.R) continue;
+                const float l = rr ? lb : la;
+                const float inv = l > 0.f ? 1.0f / l : 0.f;
+#pragma unroll
+                for (int t = 0; t < G::NT2; ++t) {
+                    const int sg = t / G::EPL, e = t % G::EPL;
+#pragma unroll
+                    for (int cc2 = 0; cc2 < 2; ++cc2)
+                        put(row, sg * G::EPS + (2 * c + cc2) * G::EPL + e, o[t][2 * rr + cc2] * inv);
                 }
+                if (c == 0) put_lse(row, l, rr ? m1 : m0);
             }
         }
     };
@@ -537,6 +597,121 @@ __global__ void __launch_bounds__(ATTN_THREADS, min_blocks<D>())
             const int nvalid = min(bs, L - t_page);  // real tokens in this page
             const int vis_min = min(vis0, vis1);
             for (int ch = 0; ch < bs; ch += 16) {
+              if constexpr (TOKM) {
+                // ---- S^T = K q'^T for tokens ch .. ch+15 (M) x query rows (N = 8);
+                // two partial accumulators halve the dependent MMA chain
+                float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int sg = 0; sg < G::NSEG; ++sg) {
+                    uint32_t kw2[2][G::KWORDS];
+#pragma unroll
+                    for (int t = 0; t < 2; ++t) {
+                        const int srow = ch + 8 * t + g;
+                        if constexpr (G::SW == 128) {
+                            lds_words<4>(kw2[t], kt + tile_off<128>(srow, sg, 2 * c, bs));
+                            lds_words<4>(kw2[t] + 4, kt + tile_off<128>(srow, sg, 2 * c + 1, bs));
+                        } else {
+                            lds_words<4>(kw2[t], kt + tile_off<64>(srow, sg, c, bs));
+                        }
+                    }
+#pragma unroll
+                    for (int jj = 0; jj < G::KPS; ++jj) {
+                        const int K = sg * G::KPS + jj;
+                        uint32_t q0, q1;
+                        if constexpr (QREG) {
+                            q0 = qreg[K][0];
+                            q1 = qreg[K][2];
+                        } else {
+                            const uint4 av = qs[K * 32 + lane];
+                            q0 = av.x;
+                            q1 = av.z;
+                        }
+                        uint32_t a[4];
+                        k_frag<KVT>(kw2[0], jj, a[0], a[2]);  // token row g
+                        k_frag<KVT>(kw2[1], jj, a[1], a[3]);  // token row g+8
+                        if (K & 1) mma16816<BF>(sb, a, q0, q1);
+                        else mma16816<BF>(sa, a, q0, q1);
+                    }
+                }
+                // ---- scale, mask, online softmax (rows 2c, 2c+1; tokens g, g+8)
+                float x[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) x[e] = (sa[e] + sb[e]) * ((e & 1) ? sc1 : sc0);
+                if (t_page + ch + 16 > vis_min) {
+                    const int tg = t_page + ch + g;
+                    x[0] = (tg < vis0) ? x[0] : -INFINITY;
+                    x[1] = (tg < vis1) ? x[1] : -INFINITY;
+                    x[2] = (tg + 8 < vis0) ? x[2] : -INFINITY;
+                    x[3] = (tg + 8 < vis1) ? x[3] : -INFINITY;
+                }
+                float mx0 = fmaxf(x[0], x[2]), mx1 = fmaxf(x[1], x[3]);
+#pragma unroll
+                for (int off = 4; off <= 16; off <<= 1) {
+                    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+                    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+                }
+                const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+                const float base0 = (mn0 == -INFINITY) ? 0.f : mn0;
+                const float base1 = (mn1 == -INFINITY) ? 0.f : mn1;
+                const float al0 = ex2(m0 - base0), al1 = ex2(m1 - base1);
+                m0 = mn0;
+                m1 = mn1;
+                x[0] = ex2(x[0] - base0);
+                x[2] = ex2(x[2] - base0);
+                x[1] = ex2(x[1] - base1);
+                x[3] = ex2(x[3] - base1);
+                l0 = l0 * al0 + (x[0] + x[2]);
+                l1 = l1 * al1 + (x[1] + x[3]);
+                if (__any_sync(0xffffffffu, al0 != 1.f || al1 != 1.f)) {
+#pragma unroll
+                    for (int t = 0; t < NO; ++t) {
+                        o[t][0] *= al0;
+                        o[t][1] *= al1;
+                        o[t][2] *= al0;
+                        o[t][3] *= al1;
+                    }
+                }
+                // ---- P^T fragments: transpose the [token][row] pairs
+                const uint32_t pb0 = movmatrix_trans(pack2<BF>(x[0], x[1]));  // tokens 2c,2c+1 of row g
+                const uint32_t pb1 = movmatrix_trans(pack2<BF>(x[2], x[3]));  // tokens 2c+8,2c+9
+                // ---- O^T += V^T P^T
+                const int rA = ch + 2 * c, rB = rA + 1, rC = rA + 8, rD = rA + 9;
+                const bool tail = ch + 16 > nvalid;
+                const bool zA = tail && rA >= nvalid, zB = tail && rB >= nvalid;
+                const bool zC = tail && rC >= nvalid, zD = tail && rD >= nvalid;
+#pragma unroll
+                for (int sg = 0; sg < G::NSEG; ++sg) {
+                    uint32_t va[G::VWORDS], vb[G::VWORDS], vc[G::VWORDS], vd[G::VWORDS];
+                    if constexpr (G::SW == 128) {
+                        lds_words<4>(va, vt + tile_off<128>(rA, sg, g, bs));
+                        lds_words<4>(vb, vt + tile_off<128>(rB, sg, g, bs));
+                        lds_words<4>(vc, vt + tile_off<128>(rC, sg, g, bs));
+                        lds_words<4>(vd, vt + tile_off<128>(rD, sg, g, bs));
+                    } else {
+                        const int hoff = 8 * (g & 1);
+                        lds_words<2>(va, vt + tile_off<64>(rA, sg, g >> 1, bs) + hoff);
+                        lds_words<2>(vb, vt + tile_off<64>(rB, sg, g >> 1, bs) + hoff);
+                        lds_words<2>(vc, vt + tile_off<64>(rC, sg, g >> 1, bs) + hoff);
+                        lds_words<2>(vd, vt + tile_off<64>(rD, sg, g >> 1, bs) + hoff);
+                    }
+                    if (tail) {
+#pragma unroll
+                        for (int k = 0; k < G::VWORDS; ++k) {
+                            va[k] = zA ? 0u : va[k];
+                            vb[k] = zB ? 0u : vb[k];
+                            vc[k] = zC ? 0u : vc[k];
+                            vd[k] = zD ? 0u : vd[k];
+                        }
+                    }
+                    uint32_t bf[G::EPL][2];
+                    v_frags<KVT, G::EPL, G::VWORDS>(va, vb, vc, vd, bf);
+#pragma unroll
+                    for (int mm = 0; mm < HEPL; ++mm) {
+                        const uint32_t a[4] = {bf[2 * mm][0], bf[2 * mm + 1][0], bf[2 * mm][1], bf[2 * mm + 1][1]};
+                        mma16816<BF>(o[sg * HEPL + mm], a, pb0, pb1);
+                    }
+                }
+              } else {
                 // ---- S = q' K^T for tokens ch .. ch+15 (two n-tiles)
                 float s[2][4];
 #pragma unroll
@@ -663,6 +838,7 @@ __global__ void __launch_bounds__(ATTN_THREADS, min_blocks<D>())
 #pragma unroll
                     for (int e = 0; e < G::EPL; ++e) mma16816<BF>(o[sg * G::EPL + e], pa, bf[e][0], bf[e][1]);
                 }
+              }
             }
         }
         last_p = cc.p;

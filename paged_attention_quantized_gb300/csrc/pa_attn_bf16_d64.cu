@@ -1,0 +1,6 @@
+// Attention kernel instantiations for BF16 KV codes, head dim 64.
+#include "pa_attn_launch.cuh"
+
+namespace pa {
+PA_DEFINE_ATTN(PA_BF16, 64)
+}  // namespace pa

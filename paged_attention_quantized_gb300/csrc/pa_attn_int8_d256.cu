@@ -1,0 +1,6 @@
+// Attention kernel instantiations for INT8 KV codes, head dim 256.
+#include "pa_attn_launch.cuh"
+
+namespace pa {
+PA_DEFINE_ATTN(PA_INT8, 256)
+}  // namespace pa

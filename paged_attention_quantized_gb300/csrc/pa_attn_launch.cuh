@@ -1,5 +1,6 @@
-// Launch helpers for the split-KV attention kernel (one instantiation per KV
-// encoding and head dimension, compiled in separate translation units).
+// Launch helpers for the split-KV attention kernel (one pair of instantiations
+// -- rows or tokens on the MMA M axis -- per KV encoding and head dimension,
+// compiled in separate translation units).
 #pragma once
 
 #include <algorithm>
@@ -10,23 +11,30 @@ namespace pa {
 
 template <int KVT, int D>
 cudaError_t launch_attn(const CUtensorMap &tk, const CUtensorMap &tv, const AttnParams &P, dim3 grid, size_t smem,
-                        cudaStream_t s);
+                        bool tokens_as_m, cudaStream_t s);
+
+template <int KVT, int D, bool TOKM>
+cudaError_t launch_attn_t(const CUtensorMap &tk, const CUtensorMap &tv, const AttnParams &P, dim3 grid, size_t smem,
+                          cudaStream_t s) {
+    cudaError_t e = cudaFuncSetAttribute(pa_attn_kernel<KVT, D, TOKM>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)smem);
+    if (e != cudaSuccess) return e;
+    pa_attn_kernel<KVT, D, TOKM><<<grid, ATTN_THREADS, smem, s>>>(tk, tv, P);
+    return cudaGetLastError();
+}
 
 #define PA_DEFINE_ATTN(KVT, D)                                                                                  \
     template <>                                                                                                 \
     cudaError_t launch_attn<KVT, D>(const CUtensorMap &tk, const CUtensorMap &tv, const AttnParams &P,          \
-                                    dim3 grid, size_t smem, cudaStream_t s) {                                   \
-        cudaError_t e = cudaFuncSetAttribute(pa_attn_kernel<KVT, D>, cudaFuncAttributeMaxDynamicSharedMemorySize, \
-                                             (int)smem);                                                        \
-        if (e != cudaSuccess) return e;                                                                         \
-        pa_attn_kernel<KVT, D><<<grid, ATTN_THREADS, smem, s>>>(tk, tv, P);                                     \
-        return cudaGetLastError();                                                                              \
+                                    dim3 grid, size_t smem, bool tokens_as_m, cudaStream_t s) {                 \
+        return tokens_as_m ? launch_attn_t<KVT, D, true>(tk, tv, P, grid, smem, s)                              \
+                           : launch_attn_t<KVT, D, false>(tk, tv, P, grid, smem, s);                            \
     }
 
 #define PA_DECLARE_ATTN(KVT, D)                                                                                 \
     template <>                                                                                                 \
     cudaError_t launch_attn<KVT, D>(const CUtensorMap &tk, const CUtensorMap &tv, const AttnParams &P,          \
-                                    dim3 grid, size_t smem, cudaStream_t s);
+                                    dim3 grid, size_t smem, bool tokens_as_m, cudaStream_t s);
 
 PA_DECLARE_ATTN(PA_F16, 64) PA_DECLARE_ATTN(PA_F16, 128) PA_DECLARE_ATTN(PA_F16, 256)
 PA_DECLARE_ATTN(PA_BF16, 64) PA_DECLARE_ATTN(PA_BF16, 128) PA_DECLARE_ATTN(PA_BF16, 256)
