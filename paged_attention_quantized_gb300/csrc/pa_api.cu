@@ -57,6 +57,7 @@ pa_status device_sms(int *sms) {
 // Everything derived from a problem on the host.
 struct Derived {
     int G, R, row_blocks, sms, ctas, minb;
+    bool tokm;
     long long nwarps, slots_partial;
     int D, RB, SW, slots, warp_smem;
     size_t k_block, v_block, smem;
@@ -122,11 +123,14 @@ pa_status derive(const pa_problem *p, Derived *d) {
             if ((size_t)pa::NWK * wsm(s) <= budget) slots = s;
         return slots;
     };
-    d->minb = D <= 128 ? PA_MIN_BLOCKS_SMALL_D : PA_MIN_BLOCKS_LARGE_D;
+    d->tokm = d->R <= PA_TOKM_MAX_ROWS;  // few query rows per kv head: tokens on the MMA M axis
+    d->minb = D <= 128 ? (d->tokm ? PA_MIN_BLOCKS_TOKM : PA_MIN_BLOCKS_SMALL_D) : PA_MIN_BLOCKS_LARGE_D;
+    // fewer resident CTAs until every warp holds two pages (one in flight
+    // while it computes on the other); one page per warp as the last resort
     d->slots = fit(d->minb);
-    if (d->slots < 2 && d->minb > 1) {
-        d->minb = 1;
-        d->slots = fit(1);
+    while (d->slots < 2 && d->minb > 1) {
+        d->minb -= 1;
+        d->slots = fit(d->minb);
     }
     if (d->slots < 1) return PA_ERR_UNSUPPORTED;
     d->warp_smem = wsm(d->slots);
@@ -205,7 +209,7 @@ T *at(void *ws, size_t off) {
 cudaError_t dispatch_attn(const pa_problem *p, const Derived &d, const CUtensorMap &tk, const CUtensorMap &tv,
                           const pa::AttnParams &P, cudaStream_t s) {
     const dim3 grid((unsigned)d.ctas);
-    const bool tokm = d.R <= PA_TOKM_MAX_ROWS;  // few query rows per kv head: tokens on the MMA M axis
+    const bool tokm = d.tokm;
 #define PA_CASE(KVT, DD) \
     if (p->kv_dtype == KVT && d.D == DD) return pa::launch_attn<KVT, DD>(tk, tv, P, grid, d.smem, tokm, s);
     PA_CASE(PA_F16, 64) PA_CASE(PA_F16, 128) PA_CASE(PA_F16, 256)

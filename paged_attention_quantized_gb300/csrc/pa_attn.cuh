@@ -47,9 +47,15 @@ constexpr int NWK = 4;                     // warps per CTA, each an independent
 #ifndef PA_MIN_BLOCKS_LARGE_D
 #define PA_MIN_BLOCKS_LARGE_D 1
 #endif
+#ifndef PA_MIN_BLOCKS_TOKM
+#define PA_MIN_BLOCKS_TOKM 4
+#endif
 // resident CTAs per SM the register and shared-memory budgets are sized for
-template <int D>
-__host__ __device__ constexpr int min_blocks() { return D <= 128 ? PA_MIN_BLOCKS_SMALL_D : PA_MIN_BLOCKS_LARGE_D; }
+// (tokens-as-M kernels need fewer registers)
+template <int D, bool TOKM>
+__host__ __device__ constexpr int min_blocks() {
+    return D <= 128 ? (TOKM ? PA_MIN_BLOCKS_TOKM : PA_MIN_BLOCKS_SMALL_D) : PA_MIN_BLOCKS_LARGE_D;
+}
 // q' fragments live in registers for D <= 128, in the warp's shared memory above
 template <int D>
 __host__ __device__ constexpr bool q_in_regs() { return D <= 128; }
@@ -290,7 +296,7 @@ __device__ __forceinline__ float load_q(const AttnParams &P, int b, int j, int h
 // (S^T = K q'^T and O^T = V^T P^T with the rows as N = 8), which halves the
 // tensor work and the O accumulator against padding 8 rows up to M = 16.
 template <int KVT, int D, bool TOKM>
-__global__ void __launch_bounds__(ATTN_THREADS, min_blocks<D>())
+__global__ void __launch_bounds__(ATTN_THREADS, min_blocks<D, TOKM>())
     pa_attn_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv, AttnParams P) {
     using G = Geo<KVT, D>;
     constexpr bool BF = G::BF;
