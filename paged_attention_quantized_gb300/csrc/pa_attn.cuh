@@ -321,6 +321,8 @@ __global__ void __launch_bounds__(ATTN_THREADS, min_blocks<D, TOKM>())
                                                   (QREG ? 0 : G::KSTEPS * 512));  // [MAX_SLOTS]
     if (NS < 1 || NS > MAX_SLOTS) return;  // the host never launches this
 
+    // the plan (and anything else earlier on the stream) must be complete
+    grid_dependency_wait();
     // the warp's share of the global page sequence
     const long long total = P.hdr[HDR_TOTAL_PAGES];
     if (total > (long long)P.B * P.mbps) {  // not a plan of this problem
@@ -858,6 +860,8 @@ __global__ void __launch_bounds__(ATTN_THREADS, min_blocks<D, TOKM>())
         // a wait ran out: let every copy still in flight land before exiting
         for (int i = j; i < min(npg, j + NS); ++i) mbar_wait_bounded(&full[i % NS], (i / NS) & 1, nullptr);
     }
+    // the combine may start launching while the last pieces are written
+    grid_dependents_launch();
     if (piece_b >= 0) finish_piece();
     if (lane == 0) atomic_or_err(P.hdr, err);
 }

@@ -19,7 +19,8 @@ cudaError_t launch_attn_t(const CUtensorMap &tk, const CUtensorMap &tv, const At
     cudaError_t e = cudaFuncSetAttribute(pa_attn_kernel<KVT, D, TOKM>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem);
     if (e != cudaSuccess) return e;
-    pa_attn_kernel<KVT, D, TOKM><<<grid, ATTN_THREADS, smem, s>>>(tk, tv, P);
+    e = launch_pdl(pa_attn_kernel<KVT, D, TOKM>, grid, dim3(ATTN_THREADS), smem, s, tk, tv, P);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 

@@ -23,8 +23,17 @@ __device__ __forceinline__ long long share_owner(long long x, long long n, long 
     return ((x + 1) * nw + n - 1) / n - 1;
 }
 
-// One CTA per segment (request, kv head, row block).
+constexpr int MAX_CACHED_PIECES = 64;
+
+// One CTA per segment (request, kv head, row block).  The pieces (non-empty
+// warp shares) and the per-row weights w = exp(lse - M) / sum exp(lse - M) are
+// worked out once; every output element is then one weighted sum.
 __global__ void __launch_bounds__(COMBINE_THREADS) pa_combine_kernel(CombineParams P) {
+    __shared__ long long s_piece[MAX_CACHED_PIECES];   // partial slots, ascending warp order
+    __shared__ float s_w[MAX_CACHED_PIECES][16];       // weight of piece k for row i
+    __shared__ float s_M[16], s_den[16];
+    __shared__ int s_np, s_nan[16];
+    grid_dependency_wait();  // the attention's partials are complete
     const int X = P.Hkv * P.RBLK;
     const int seg = blockIdx.x;
     const int b = seg / X, q = seg % X;
@@ -44,6 +53,66 @@ __global__ void __launch_bounds__(COMBINE_THREADS) pa_combine_kernel(CombinePara
         kl = share_owner(xl, N, P.nwarps);
         if (kf == kl) return;  // one piece: the attention kernel wrote the output
     }
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    // 1. the pieces: warps kf..kl with a non-empty share (empty shares only
+    //    exist when there are fewer positions than warps)
+    if (threadIdx.x == 0) {
+        int np = 0;
+        for (long long k = kf; k <= kl; ++k) {
+            if (share_start(k, N, P.nwarps) == share_start(k + 1, N, P.nwarps)) continue;
+            if (np < MAX_CACHED_PIECES) s_piece[np] = (long long)seg + k;
+            ++np;
+        }
+        s_np = np;
+    }
+    __syncthreads();
+    const int np = s_np;
+    const bool cached = np <= MAX_CACHED_PIECES;
+    // slot of the n-th piece (recomputed when there are too many to cache)
+    auto piece_slot = [&](int n) -> long long {
+        if (cached) return s_piece[n];
+        int seen = 0;
+        for (long long k = kf; k <= kl; ++k) {
+            if (share_start(k, N, P.nwarps) == share_start(k + 1, N, P.nwarps)) continue;
+            if (seen++ == n) return (long long)seg + k;
+        }
+        return (long long)seg + kf;
+    };
+    // 2. per row: M = max lse, den = sum exp(lse - M), NaN if any piece is NaN
+    if (Pb > 0) {
+        for (int i = warp; i < rows_here; i += COMBINE_THREADS / 32) {
+            float M = -INFINITY;
+            int nan = 0;
+            for (int n = lane; n < np; n += 32) {
+                const float l = P.part_lse[piece_slot(n) * 16 + i];
+                nan |= (l != l);
+                M = fmaxf(M, l);
+            }
+#pragma unroll
+            for (int o = 16; o >= 1; o >>= 1) {
+                M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+                nan |= __shfl_xor_sync(0xffffffffu, nan, o);
+            }
+            float den = 0.f;
+            if (M != -INFINITY && !nan) {
+                for (int n = lane; n < np; n += 32) {
+                    const float w = ex2((P.part_lse[piece_slot(n) * 16 + i] - M) * LOG2E_);
+                    if (cached) s_w[n][i] = w;
+                    den += w;
+                }
+            }
+            // fixed-order sum of the lane partials (bitwise reproducible)
+#pragma unroll
+            for (int o = 16; o >= 1; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
+            if (lane == 0) {
+                s_M[i] = M;
+                s_den[i] = den;
+                s_nan[i] = nan;
+            }
+        }
+    }
+    __syncthreads();
+    // 3. every output element: one weighted sum in ascending piece order
     for (int idx = threadIdx.x; idx < rows_here * P.Dv; idx += COMBINE_THREADS) {
         const int i = idx / P.Dv, d = idx % P.Dv;
         const int r = rblk * 16 + i;
@@ -52,32 +121,21 @@ __global__ void __launch_bounds__(COMBINE_THREADS) pa_combine_kernel(CombinePara
             // no visible page: a flagged request is NaN, an empty one is 0
             y = Rq.w ? NaN : 0.f;
             lse_v = Rq.w ? NaN : -INFINITY;
+        } else if (s_nan[i]) {
+            y = lse_v = NaN;
+        } else if (s_M[i] == -INFINITY) {
+            y = 0.f;
+            lse_v = -INFINITY;
         } else {
-            float M = -INFINITY;
-            bool nan = false;
-            for (long long k = kf; k <= kl; ++k) {
-                if (share_start(k, N, P.nwarps) == share_start(k + 1, N, P.nwarps)) continue;  // empty share
-                const float l = P.part_lse[((long long)seg + k) * 16 + i];
-                nan |= (l != l);
-                M = fmaxf(M, l);
+            const float M = s_M[i], den = s_den[i];
+            float acc = 0.f;
+            for (int n = 0; n < np; ++n) {
+                const long long slot = piece_slot(n);
+                const float w = cached ? s_w[n][i] : ex2((P.part_lse[slot * 16 + i] - M) * LOG2E_);
+                acc += w * P.part_o[(slot * 16 + i) * P.Dv + d];
             }
-            if (nan) {
-                y = lse_v = NaN;
-            } else if (M == -INFINITY) {
-                y = 0.f;
-                lse_v = -INFINITY;
-            } else {
-                float acc = 0.f, den = 0.f;
-                for (long long k = kf; k <= kl; ++k) {
-                    if (share_start(k, N, P.nwarps) == share_start(k + 1, N, P.nwarps)) continue;
-                    const long long slot = (long long)seg + k;
-                    const float w = ex2((P.part_lse[slot * 16 + i] - M) * LOG2E_);
-                    den += w;
-                    acc += w * P.part_o[(slot * 16 + i) * P.Dv + d];
-                }
-                y = acc / den;
-                lse_v = M + lg2(den) * 0.6931471805599453f;
-            }
+            y = acc / den;
+            lse_v = M + lg2(den) * 0.6931471805599453f;
         }
         float vsc = 1.0f;
         if (P.v_mode == PA_SCALE_TENSOR) vsc = P.v_scale[0];
@@ -94,7 +152,8 @@ __global__ void __launch_bounds__(COMBINE_THREADS) pa_combine_kernel(CombinePara
 
 cudaError_t launch_combine(const CombineParams &P, cudaStream_t s) {
     if (P.B == 0) return cudaSuccess;
-    pa_combine_kernel<<<P.B * P.Hkv * P.RBLK, COMBINE_THREADS, 0, s>>>(P);
+    cudaError_t e = launch_pdl(pa_combine_kernel, dim3(P.B * P.Hkv * P.RBLK), dim3(COMBINE_THREADS), 0, s, P);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 

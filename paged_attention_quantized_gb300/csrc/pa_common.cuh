@@ -223,6 +223,32 @@ __device__ __forceinline__ uint32_t u4hi_f16x2(uint32_t ux) {
     return hfma2_u((ux & 0x00F000F0u) | 0x64006400u, F16X2_1_16, F16X2_M72);
 }
 
+// ------------------------------------------------- programmatic dependent launch
+
+// Block until the grid this launch depends on has finished and its writes are
+// visible (a no-op when the launch had no programmatic dependency).
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Let the next launch on the stream start its prologue early.
+__device__ __forceinline__ void grid_dependents_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+// Launch `kernel` with programmatic stream serialisation: it may begin while
+// the previous kernel on the stream drains, and waits in grid_dependency_wait.
+template <typename... Args>
+cudaError_t launch_pdl(void (*kernel)(Args...), dim3 grid, dim3 block, size_t smem, cudaStream_t s, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 // -------------------------------------------------------------- reductions
 
 __device__ __forceinline__ void atomic_or_err(uint32_t *hdr, uint32_t bits) {

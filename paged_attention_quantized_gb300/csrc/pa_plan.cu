@@ -74,6 +74,8 @@ __device__ __forceinline__ long long block_exclusive_scan(long long v, long long
 }
 
 __global__ void __launch_bounds__(PLAN_THREADS) pa_plan_kernel(PlanParams P) {
+    // the attention launch may queue up behind this single block right away
+    grid_dependents_launch();
     __shared__ long long warp_tot[32];
     __shared__ long long s_total;
     __shared__ uint32_t s_err;
