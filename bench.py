@@ -15,7 +15,9 @@ by the device time of the step.
 
 The default workload is the bf16 GQA decode batch (B=64, L~U[512,8192], 32 q /
 8 kv heads, D=128, bs=16).  The other workloads of the library can be timed
-with --workload (tiny, e4m3, int8, int4).
+with --workload (tiny, e4m3, int8, int4, latent).  The latent workload is a
+dense contraction: its roofline is the tensor rate (flops of S = q K^T and
+O = P V over the visible tokens), with the HBM fraction beside it.
 
 With N > 1 (torchrun, one rank per GPU) every rank times its own replica of
 the batch (requests are independent, nothing is exchanged): weak scaling,
@@ -51,19 +53,22 @@ WORKLOAD_TEXT = {
             "k/v scales log-uniform [1e-2,1e3], q~N(0,100^2) fp16, fp32 out",
     "int4": "INT4 per-channel KV (packed 2/byte): B=128, L~U[2048,16384], next_n=1, 64 q / 8 kv heads, "
             "D=128, bs=16, k/v scales log-uniform [1e-2,1e3], q~N(0,100^2) fp16, fp32 out",
+    "latent": "single-latent-KV MQA decode: B=256, L~lognormal(median 8192, sigma 1, cap 131072), next_n=2 "
+              "causal, 128 q heads / 1 kv head, Dk=576, Dv=512 (first 512 of K), bs=64, E4M3 KV with a "
+              "per-token fp32 scale, q~N(0,1) bf16, bf16 out",
 }
-COMPUTE_DTYPE = {"tiny": "f16", "bf16": "bf16", "e4m3": "f16", "int8": "f16", "int4": "f16"}
+COMPUTE_DTYPE = {"tiny": "f16", "bf16": "bf16", "e4m3": "f16", "int8": "f16", "int4": "f16", "latent": "f16"}
 L2_FLUSH_BYTES = 256 << 20
 
 
-def _peaks():
+def _peaks(key: str = "hbm_gbs"):
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
         with open(path) as f:
             d = json.load(f)
-        return float(d["hbm_gbs"]), "measured"
+        return float(d[key]), "measured"
     except Exception:
-        return 6800.0, "fallback"
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}[key], "fallback"
 
 
 def _kernel_sha() -> str:
@@ -277,6 +282,24 @@ def gpu_arm(args, rank, world, local_rank):
     peak, peak_kind = _peaks()
     achieved = eff_bytes / (attn_avg * 1e-3) / 1e9
     traffic = _traffic(args.workload)
+    roofline = {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
+                "frac": round(achieved / peak, 4), "traffic": traffic,
+                "kernel": "pa_attn_kernel", "peak_source": f"{peak_kind} hbm_gbs",
+                "attn_ms": round(attn_avg, 5)}
+    if w.v_is_k_prefix:
+        # the latent path is a dense contraction: 2 (Dk + Dv) flops per
+        # (query head row, visible token); f16 operands run at the bf16 rate
+        L = w.context_lens.cpu().to(torch.int64)
+        vis = sum(int((L - (w.n - 1 - j)).clamp(min=0).sum()) if w.causal else int(L.sum()) for j in range(w.n))
+        flops = 2.0 * (w.Dk + w.Dv) * (w.Hq // w.Hkv) * vis
+        tpeak, tkind = _peaks("bf16_tflops")
+        tach = flops / (attn_avg * 1e-3) / 1e12
+        roofline = {"bound": "tensor", "achieved": round(tach, 2), "peak": tpeak, "unit": "TFLOP/s",
+                    "frac": round(tach / tpeak, 4), "traffic": traffic, "kernel": "pa_latent_kernel",
+                    "peak_source": f"{tkind} bf16_tflops (f16 MMA, same rate)", "attn_ms": round(attn_avg, 5),
+                    "flops_per_launch": flops,
+                    "hbm": {"achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
+                            "frac": round(achieved / peak, 4)}}
     return {
         "metric": METRIC,
         "value": round(value, 2),
@@ -300,10 +323,7 @@ def gpu_arm(args, rank, world, local_rank):
         "query_rows_per_s": round(world * query_rows / (ms_per_step * 1e-3), 1),
         "head_rows_per_s": round(world * rows / (ms_per_step * 1e-3), 1),
         "pct_of_hbm_peak": round(100.0 * value / world / peak, 2),
-        "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
-                     "frac": round(achieved / peak, 4), "traffic": traffic,
-                     "kernel": "pa_attn_kernel", "peak_source": f"{peak_kind} hbm_gbs",
-                     "attn_ms": round(attn_avg, 5)},
+        "roofline": roofline,
         "e2e": {"value": round(world * eff_bytes / (e2e_avg * 1e-3) / 1e9, 2), "unit": "GB/s",
                 "ms_per_step": round(e2e_avg, 5), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": launches_per_step * args.steps,
@@ -422,8 +442,7 @@ def main():
         dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
     line, w = gpu_arm(args, rank, world, local_rank)
     if rank == 0 and not args.no_cpu_baseline:
-        from paged_attention_quantized_gb300 import workloads as W
-        wc = W.make(args.workload, device="cpu")
+        wc = w  # the timed batch itself; the oracle reads host copies of it
         v, r, n, dt, threads = oracle_rate(wc, budget_s=args.cpu_baseline_s)
         line["cpu_baseline"] = {"value": round(v, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
                                 "sample": f"{n} of {wc.B * wc.n * wc.Hq} (b, j, h) rows, seeded, {dt:.1f} s; "

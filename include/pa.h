@@ -44,7 +44,9 @@
  *               E4M3: the "fn" FP8 format (0x7F / 0xFF are NaN).
  *               Base address 16-byte aligned.
  *  v_pool       the same with Dv, or NULL when v_is_k_prefix (V is then the
- *               first Dv channels of the K plane and uses K's scales).
+ *               first Dv channels of the K plane and uses K's scales; this
+ *               build supports it for the single-latent shape only: E4M3
+ *               codes, PA_SCALE_TOKEN, Dk = 576, Dv = 512, bs = 64).
  *  block_table  [batch][max_blocks_per_seq] int32 physical block ids.  Columns
  *               p < ceil(L_b / bs) must hold ids in [1, num_blocks); block 0 is
  *               the null block.  Other columns are never read.
@@ -149,15 +151,20 @@ typedef struct pa_problem {
  * L_b breaks the contract), PS_b = sum of P over earlier requests, flags}.
  *
  * pa_run orders every page of the batch by logical position -- request,
- * kv head, block of 16 query rows ("segment"), page -- and gives warp k of the
- * persistent launch (W warps) positions [k*N/W, (k+1)*N/W) of the N in total.
- * A warp's run of pages inside one segment is a "piece"; a piece that is a
- * whole segment writes `out` directly, other pieces write a partial
+ * kv head, block of S query rows ("segment"), page -- and gives worker k of
+ * the persistent launch (W workers) positions [k*N/W, (k+1)*N/W) of the N in
+ * total.  A worker's run of pages inside one segment is a "piece"; a piece
+ * that is a whole segment writes `out` directly, other pieces write a partial
  * (normalised output, log-sum-exp) to slot (segment index + k), which
- * pa_combine merges in ascending k.  Partials: fp32
- * [partial_slots][16][Dv] outputs and fp32 [partial_slots][16] log-sum-exps,
- * row i of a slot = query row 16 * (row block) + i of the kv head, query row
- * r = j * (Hq / Hkv) + (h mod (Hq / Hkv)). */
+ * pa_combine merges in ascending k.  Partials: fp32 [partial_slots][S][Dv]
+ * outputs and fp32 [partial_slots][S] log-sum-exps, row i of a slot = query
+ * row S * (row block) + i of the kv head, query row
+ * r = j * (Hq / Hkv) + (h mod (Hq / Hkv)).
+ *
+ * Two kernels: the grouped kernel (separate K and V planes, per-tensor or
+ * per-channel scales) has S = 16 and one worker per warp; the single-latent
+ * kernel (v_is_k_prefix: E4M3, PA_SCALE_TOKEN, Dk = 576, Dv = 512, bs = 64)
+ * has S = 64 and one worker per CTA (one CTA per SM). */
 typedef struct pa_layout {
     size_t total_bytes;
     size_t header_offset;
@@ -166,11 +173,12 @@ typedef struct pa_layout {
     size_t partial_lse_offset;
     int64_t partial_slots;       /* B * Hkv * row_blocks + warps */
     int32_t rows_per_kv_head;    /* (Hq / Hkv) * next_n */
-    int32_t row_blocks;          /* ceil(rows_per_kv_head / 16) */
+    int32_t row_blocks;          /* ceil(rows_per_kv_head / rows_per_segment) */
     int32_t num_sms;             /* effective */
     int32_t grid_ctas;           /* effective persistent CTAs of pa_run */
-    int32_t warps;               /* grid_ctas * warps per CTA */
-    int32_t ring_pages_per_warp; /* pages each warp keeps in flight */
+    int32_t warps;               /* workers W: grid_ctas * 4 (grouped) or grid_ctas (latent) */
+    int32_t ring_pages_per_warp; /* pages each worker keeps in flight */
+    int32_t rows_per_segment;    /* S: 16 (grouped) or 64 (latent) */
 } pa_layout;
 
 /* Library version: major * 10000 + minor * 100 + patch. */

@@ -45,7 +45,8 @@ class Layout(ctypes.Structure):
     _fields_ = [(k, ctypes.c_size_t) for k in (
         "total_bytes", "header_offset", "requests_offset", "partial_o_offset", "partial_lse_offset")] + \
         [("partial_slots", ctypes.c_int64)] + [(k, ctypes.c_int32) for k in (
-            "rows_per_kv_head", "row_blocks", "num_sms", "grid_ctas", "warps", "ring_pages_per_warp")]
+            "rows_per_kv_head", "row_blocks", "num_sms", "grid_ctas", "warps", "ring_pages_per_warp",
+            "rows_per_segment")]
 
 
 if not os.path.exists(LIB_PATH):

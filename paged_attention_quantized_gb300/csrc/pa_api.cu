@@ -14,6 +14,8 @@
 namespace pa {
 cudaError_t launch_plan(const PlanParams &P, const float *k_scale, int k_count, cudaStream_t s);
 cudaError_t launch_combine(const CombineParams &P, cudaStream_t s);
+cudaError_t launch_latent(const CUtensorMap &ta, const CUtensorMap &tb, const LatentParams &P, int ctas,
+                          cudaStream_t s);
 }  // namespace pa
 
 namespace {
@@ -25,6 +27,8 @@ constexpr int VERSION = 100;
 constexpr size_t SM_SMEM_BYTES = 228 * 1024;     // shared memory per SM
 constexpr size_t CTA_RESERVED_BYTES = 1024;       // reserved by the runtime per resident CTA
 constexpr size_t MAX_DYN_SMEM_BYTES = 227 * 1024; // opt-in limit per CTA
+// the single-latent kernel's fixed shape (one CTA of 64 query rows per SM)
+constexpr int LAT_DK = 576, LAT_DV = 512, LAT_BS = 64, LAT_ROWS = 64, LAT_RING = 2;
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
@@ -57,12 +61,15 @@ pa_status device_sms(int *sms) {
 // Everything derived from a problem on the host.
 struct Derived {
     int G, R, row_blocks, sms, ctas, minb;
-    bool tokm;
+    bool tokm, latent;
+    int rows_seg;  // query rows per segment
     long long nwarps, slots_partial;
     int D, RB, SW, slots, warp_smem;
     size_t k_block, v_block, smem;
     pa_layout L;
 };
+
+pa_status derive_grouped(const pa_problem *p, Derived *d);
 
 pa_status derive(const pa_problem *p, Derived *d) {
     if (p == nullptr || d == nullptr) return PA_ERR_INVALID_ARG;
@@ -82,9 +89,76 @@ pa_status derive(const pa_problem *p, Derived *d) {
     if (p->v_is_k_prefix != 0 && p->v_is_k_prefix != 1) return PA_ERR_INVALID_ARG;
     if (p->kv_dtype == PA_INT4 && ((p->head_dim_k & 1) || (p->head_dim_v & 1))) return PA_ERR_INVALID_ARG;
 
-    // kernel coverage of this build
-    if (p->v_is_k_prefix || p->k_scale_mode == PA_SCALE_TOKEN || p->v_scale_mode == PA_SCALE_TOKEN)
-        return PA_ERR_UNSUPPORTED;
+    if (p->v_is_k_prefix && p->head_dim_v > p->head_dim_k) return PA_ERR_INVALID_ARG;
+    d->G = p->num_q_heads / p->num_kv_heads;
+    {
+        const long long R = (long long)d->G * p->next_n;
+        if (R > (1 << 20)) return PA_ERR_UNSUPPORTED;
+        d->R = (int)R;
+    }
+    if (p->num_sms > 0) d->sms = p->num_sms;
+    else {
+        const pa_status st = device_sms(&d->sms);
+        if (st != PA_OK) return st;
+    }
+    d->latent = p->v_is_k_prefix != 0;
+    if (d->latent) {
+        // single-latent MQA: one E4M3 plane, V = its first 512 of 576
+        // channels, a per-token fp32 scale after the codes of each block
+        if (p->kv_dtype != PA_E4M3 || p->k_scale_mode != PA_SCALE_TOKEN || p->head_dim_k != LAT_DK ||
+            p->head_dim_v != LAT_DV || p->block_size != LAT_BS || p->num_kv_heads > 65535)
+            return PA_ERR_UNSUPPORTED;
+        d->D = LAT_DK;
+        d->rows_seg = LAT_ROWS;
+        d->row_blocks = (d->R + LAT_ROWS - 1) / LAT_ROWS;
+        if (d->row_blocks > 65535) return PA_ERR_UNSUPPORTED;
+        d->tokm = false;
+        d->minb = 1;
+        d->RB = LAT_DK;
+        d->SW = 128;
+        d->k_block = (size_t)p->num_kv_heads * LAT_BS * (LAT_DK + 4);
+        d->v_block = d->k_block;
+        d->slots = LAT_RING;
+        d->warp_smem = 0;
+        d->smem = 0;
+        d->ctas = p->grid_ctas > 0 ? p->grid_ctas : d->sms;
+        d->nwarps = d->ctas;  // the workers are CTAs
+    } else {
+        const pa_status st = derive_grouped(p, d);
+        if (st != PA_OK) return st;
+    }
+
+    const long long X = (long long)p->num_kv_heads * d->row_blocks;
+    d->slots_partial = (long long)p->batch * X + d->nwarps;
+    if (d->slots_partial > (1ll << 31)) return PA_ERR_UNSUPPORTED;
+
+    pa_layout &Lo = d->L;
+    std::memset(&Lo, 0, sizeof(Lo));
+    size_t off = 0;
+    Lo.header_offset = off;
+    off = align_up(off + 64, 256);
+    Lo.requests_offset = off;
+    off = align_up(off + (size_t)p->batch * 16, 256);
+    Lo.partial_o_offset = off;
+    off = align_up(off + (size_t)d->slots_partial * d->rows_seg * p->head_dim_v * 4, 256);
+    Lo.partial_lse_offset = off;
+    off = align_up(off + (size_t)d->slots_partial * d->rows_seg * 4, 256);
+    Lo.total_bytes = off;
+    Lo.partial_slots = d->slots_partial;
+    Lo.rows_per_kv_head = d->R;
+    Lo.row_blocks = d->row_blocks;
+    Lo.num_sms = d->sms;
+    Lo.grid_ctas = d->ctas;
+    Lo.warps = (int32_t)d->nwarps;
+    Lo.ring_pages_per_warp = d->slots;
+    Lo.rows_per_segment = d->rows_seg;
+    return PA_OK;
+}
+
+// The grouped kernel (K and V planes of their own, per-tensor / per-channel
+// scales): launch shape and shared-memory budget.
+pa_status derive_grouped(const pa_problem *p, Derived *d) {
+    if (p->k_scale_mode == PA_SCALE_TOKEN || p->v_scale_mode == PA_SCALE_TOKEN) return PA_ERR_UNSUPPORTED;
     if (p->head_dim_k != p->head_dim_v) return PA_ERR_UNSUPPORTED;
     const int D = p->head_dim_k;
     if (D != 64 && D != 128 && D != 256) return PA_ERR_UNSUPPORTED;
@@ -93,17 +167,9 @@ pa_status derive(const pa_problem *p, Derived *d) {
     if (p->num_kv_heads > 65535) return PA_ERR_UNSUPPORTED;
 
     d->D = D;
-    d->G = p->num_q_heads / p->num_kv_heads;
-    const long long R = (long long)d->G * p->next_n;
-    if (R > (1 << 20)) return PA_ERR_UNSUPPORTED;
-    d->R = (int)R;
+    d->rows_seg = 16;
     d->row_blocks = (d->R + 15) / 16;
     if (d->row_blocks > 65535) return PA_ERR_UNSUPPORTED;
-    if (p->num_sms > 0) d->sms = p->num_sms;
-    else {
-        const pa_status st = device_sms(&d->sms);
-        if (st != PA_OK) return st;
-    }
     const int bs = p->block_size;
     const int bits = dtype_bits(p->kv_dtype);
     d->RB = D * bits / 8;
@@ -137,30 +203,6 @@ pa_status derive(const pa_problem *p, Derived *d) {
     d->smem = 1024 + (size_t)pa::NWK * d->warp_smem;
     d->ctas = p->grid_ctas > 0 ? p->grid_ctas : d->sms * d->minb;
     d->nwarps = (long long)d->ctas * pa::NWK;
-
-    const long long X = (long long)p->num_kv_heads * d->row_blocks;
-    d->slots_partial = (long long)p->batch * X + d->nwarps;
-    if (d->slots_partial > (1ll << 31)) return PA_ERR_UNSUPPORTED;
-
-    pa_layout &Lo = d->L;
-    std::memset(&Lo, 0, sizeof(Lo));
-    size_t off = 0;
-    Lo.header_offset = off;
-    off = align_up(off + 64, 256);
-    Lo.requests_offset = off;
-    off = align_up(off + (size_t)p->batch * 16, 256);
-    Lo.partial_o_offset = off;
-    off = align_up(off + (size_t)d->slots_partial * 16 * p->head_dim_v * 4, 256);
-    Lo.partial_lse_offset = off;
-    off = align_up(off + (size_t)d->slots_partial * 16 * 4, 256);
-    Lo.total_bytes = off;
-    Lo.partial_slots = d->slots_partial;
-    Lo.rows_per_kv_head = d->R;
-    Lo.row_blocks = d->row_blocks;
-    Lo.num_sms = d->sms;
-    Lo.grid_ctas = d->ctas;
-    Lo.warps = (int32_t)d->nwarps;
-    Lo.ring_pages_per_warp = d->slots;
     return PA_OK;
 }
 
@@ -186,17 +228,19 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 
 // [num_blocks][Hkv][bs][RB] bytes (block stride may exceed Hkv*bs*RB), box
 // [SW bytes][bs][1][1], swizzled by SW.
-pa_status make_tmap(CUtensorMap *tm, const void *base, const Derived &d, const pa_problem *p, size_t block_stride) {
+pa_status make_tmap(CUtensorMap *tm, const void *base, const Derived &d, const pa_problem *p, size_t block_stride,
+                    int box_bytes = 0) {
     auto enc = encode_fn();
     if (enc == nullptr) return PA_ERR_CUDA;
+    const int bx = box_bytes > 0 ? box_bytes : d.SW;
     cuuint64_t dims[4] = {(cuuint64_t)d.RB, (cuuint64_t)p->block_size, (cuuint64_t)p->num_kv_heads,
                           (cuuint64_t)p->num_blocks};
     cuuint64_t strides[3] = {(cuuint64_t)d.RB, (cuuint64_t)p->block_size * d.RB, (cuuint64_t)block_stride};
-    cuuint32_t box[4] = {(cuuint32_t)d.SW, (cuuint32_t)p->block_size, 1, 1};
+    cuuint32_t box[4] = {(cuuint32_t)bx, (cuuint32_t)p->block_size, 1, 1};
     cuuint32_t es[4] = {1, 1, 1, 1};
     CUresult r = enc(tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void *>(base), dims, strides, box, es,
                      CU_TENSOR_MAP_INTERLEAVE_NONE,
-                     d.SW == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+                     bx == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? PA_OK : PA_ERR_CUDA;
 }
@@ -286,9 +330,47 @@ PA_API pa_status pa_run(const pa_problem *p, const void *q, const void *k_pool, 
     if (st != PA_OK) return st;
     if ((st = check_ws(d, workspace, workspace_bytes)) != PA_OK) return st;
     if (p->batch == 0) return PA_OK;
-    if (q == nullptr || k_pool == nullptr || v_pool == nullptr || block_table == nullptr ||
+    if (q == nullptr || k_pool == nullptr || (v_pool == nullptr && !d.latent) || block_table == nullptr ||
         context_lens == nullptr || out == nullptr)
         return PA_ERR_INVALID_ARG;
+    if (d.latent) {
+        // outputs are stored as channel pairs
+        const uintptr_t out_align = p->out_dtype == PA_F32 ? 7 : 3;
+        if ((reinterpret_cast<uintptr_t>(k_pool) & 15) || (reinterpret_cast<uintptr_t>(q) & 1) ||
+            (reinterpret_cast<uintptr_t>(out) & out_align))
+            return PA_ERR_INVALID_ARG;
+        CUtensorMap ta, tb;
+        if ((st = make_tmap(&ta, k_pool, d, p, d.k_block, 128)) != PA_OK) return st;
+        if ((st = make_tmap(&tb, k_pool, d, p, d.k_block, 64)) != PA_OK) return st;
+        pa::LatentParams P;
+        P.q = static_cast<const uint8_t *>(q);
+        P.k_pool = static_cast<const uint8_t *>(k_pool);
+        P.block_table = block_table;
+        P.context_lens = context_lens;
+        P.hdr = at<uint32_t>(workspace, d.L.header_offset);
+        P.req = at<const int4>(workspace, d.L.requests_offset);
+        P.part_o = at<float>(workspace, d.L.partial_o_offset);
+        P.part_lse = at<float>(workspace, d.L.partial_lse_offset);
+        P.out = out;
+        P.lse = lse;
+        P.block_stride = (long long)d.k_block;
+        P.codes_bytes = p->num_kv_heads * LAT_BS * LAT_DK;
+        P.B = p->batch;
+        P.n = p->next_n;
+        P.Hq = p->num_q_heads;
+        P.Hkv = p->num_kv_heads;
+        P.G = d.G;
+        P.R = d.R;
+        P.RBLK = d.row_blocks;
+        P.mbps = p->max_blocks_per_seq;
+        P.num_blocks = p->num_blocks;
+        P.q_dtype = p->q_dtype;
+        P.out_dtype = p->out_dtype;
+        P.causal = p->causal;
+        P.softmax_scale = p->softmax_scale;
+        cudaError_t e = pa::launch_latent(ta, tb, P, d.ctas, reinterpret_cast<cudaStream_t>(stream));
+        return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+    }
     if ((reinterpret_cast<uintptr_t>(k_pool) & 15) || (reinterpret_cast<uintptr_t>(v_pool) & 15) ||
         (reinterpret_cast<uintptr_t>(q) & 1))
         return PA_ERR_INVALID_ARG;
@@ -341,7 +423,8 @@ PA_API pa_status pa_combine(const pa_problem *p, const float *v_scale, void *wor
     if ((st = check_ws(d, workspace, workspace_bytes)) != PA_OK) return st;
     if (p->batch == 0) return PA_OK;
     if (out == nullptr) return PA_ERR_INVALID_ARG;
-    if ((p->v_scale_mode == PA_SCALE_TENSOR || p->v_scale_mode == PA_SCALE_CHANNEL) && v_scale == nullptr)
+    const int v_mode = d.latent ? PA_SCALE_TOKEN : p->v_scale_mode;  // latent: V shares K's token scales
+    if ((v_mode == PA_SCALE_TENSOR || v_mode == PA_SCALE_CHANNEL) && v_scale == nullptr)
         return PA_ERR_INVALID_ARG;
     pa::CombineParams P;
     P.req = at<const int4>(workspace, d.L.requests_offset);
@@ -360,7 +443,8 @@ PA_API pa_status pa_combine(const pa_problem *p, const float *v_scale, void *wor
     P.RBLK = d.row_blocks;
     P.Dv = p->head_dim_v;
     P.out_dtype = p->out_dtype;
-    P.v_mode = p->v_scale_mode;
+    P.v_mode = v_mode;
+    P.rows_seg = d.rows_seg;
     P.nwarps = d.nwarps;
     cudaError_t e = pa::launch_combine(P, reinterpret_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;

@@ -1,8 +1,9 @@
 // Split-KV merge for paged attention (sm_103a).
 //
-// Every segment (request, kv head, block of 16 query rows) whose pages were
-// shared by several warps has one normalised partial output o_s and
-// log-sum-exp lse_s per warp; they are merged in ascending position order:
+// Every segment (request, kv head, block of 16 -- or, for the latent kernel,
+// 64 -- query rows) whose pages were shared by several workers (warps, or
+// CTAs of the latent kernel) has one normalised partial output o_s and
+// log-sum-exp lse_s per worker; they are merged in ascending position order:
 //     M = max_s lse_s,  w_s = exp(lse_s - M),
 //     out = (sum_s w_s o_s) / (sum_s w_s) * v_scale,   lse = M + ln(sum_s w_s)
 // (the pages name split "partial" kernels -- 1Cat-vLLM PR #647, Fix -- and
@@ -24,15 +25,16 @@ __device__ __forceinline__ long long share_owner(long long x, long long n, long 
 }
 
 constexpr int MAX_CACHED_PIECES = 64;
+constexpr int MAX_ROWS_SEG = 64;
 
 // One CTA per segment (request, kv head, row block).  The pieces (non-empty
 // warp shares) and the per-row weights w = exp(lse - M) / sum exp(lse - M) are
 // worked out once; every output element is then one weighted sum.
 __global__ void __launch_bounds__(COMBINE_THREADS) pa_combine_kernel(CombineParams P) {
     __shared__ long long s_piece[MAX_CACHED_PIECES];   // partial slots, ascending warp order
-    __shared__ float s_w[MAX_CACHED_PIECES][16];       // weight of piece k for row i
-    __shared__ float s_M[16], s_den[16];
-    __shared__ int s_np, s_nan[16];
+    __shared__ float s_w[MAX_CACHED_PIECES][MAX_ROWS_SEG];  // weight of piece k for row i
+    __shared__ float s_M[MAX_ROWS_SEG], s_den[MAX_ROWS_SEG];
+    __shared__ int s_np, s_nan[MAX_ROWS_SEG];
     grid_dependency_wait();  // the attention's partials are complete
     const int X = P.Hkv * P.RBLK;
     const int seg = blockIdx.x;
@@ -40,7 +42,8 @@ __global__ void __launch_bounds__(COMBINE_THREADS) pa_combine_kernel(CombinePara
     const int kvh = q / P.RBLK, rblk = q % P.RBLK;
     const int4 Rq = P.req[b];
     const int Pb = Rq.y;
-    const int rows_here = min(16, P.R - rblk * 16);
+    const int RS = P.rows_seg;
+    const int rows_here = min(RS, P.R - rblk * RS);
     const float NaN = __int_as_float(0x7fc00000);
     const float LOG2E_ = 1.4426950408889634f;
     const long long N = (long long)P.hdr[HDR_TOTAL_PAGES] * X;
@@ -84,7 +87,7 @@ __global__ void __launch_bounds__(COMBINE_THREADS) pa_combine_kernel(CombinePara
             float M = -INFINITY;
             int nan = 0;
             for (int n = lane; n < np; n += 32) {
-                const float l = P.part_lse[piece_slot(n) * 16 + i];
+                const float l = P.part_lse[piece_slot(n) * RS + i];
                 nan |= (l != l);
                 M = fmaxf(M, l);
             }
@@ -96,7 +99,7 @@ __global__ void __launch_bounds__(COMBINE_THREADS) pa_combine_kernel(CombinePara
             float den = 0.f;
             if (M != -INFINITY && !nan) {
                 for (int n = lane; n < np; n += 32) {
-                    const float w = ex2((P.part_lse[piece_slot(n) * 16 + i] - M) * LOG2E_);
+                    const float w = ex2((P.part_lse[piece_slot(n) * RS + i] - M) * LOG2E_);
                     if (cached) s_w[n][i] = w;
                     den += w;
                 }
@@ -115,7 +118,7 @@ __global__ void __launch_bounds__(COMBINE_THREADS) pa_combine_kernel(CombinePara
     // 3. every output element: one weighted sum in ascending piece order
     for (int idx = threadIdx.x; idx < rows_here * P.Dv; idx += COMBINE_THREADS) {
         const int i = idx / P.Dv, d = idx % P.Dv;
-        const int r = rblk * 16 + i;
+        const int r = rblk * RS + i;
         float y, lse_v;
         if (Pb == 0) {
             // no visible page: a flagged request is NaN, an empty one is 0
@@ -131,8 +134,8 @@ __global__ void __launch_bounds__(COMBINE_THREADS) pa_combine_kernel(CombinePara
             float acc = 0.f;
             for (int n = 0; n < np; ++n) {
                 const long long slot = piece_slot(n);
-                const float w = cached ? s_w[n][i] : ex2((P.part_lse[slot * 16 + i] - M) * LOG2E_);
-                acc += w * P.part_o[(slot * 16 + i) * P.Dv + d];
+                const float w = cached ? s_w[n][i] : ex2((P.part_lse[slot * RS + i] - M) * LOG2E_);
+                acc += w * P.part_o[(slot * RS + i) * P.Dv + d];
             }
             y = acc / den;
             lse_v = M + lg2(den) * 0.6931471805599453f;
@@ -152,6 +155,7 @@ __global__ void __launch_bounds__(COMBINE_THREADS) pa_combine_kernel(CombinePara
 
 cudaError_t launch_combine(const CombineParams &P, cudaStream_t s) {
     if (P.B == 0) return cudaSuccess;
+    if (P.rows_seg < 1 || P.rows_seg > MAX_ROWS_SEG) return cudaErrorInvalidValue;
     cudaError_t e = launch_pdl(pa_combine_kernel, dim3(P.B * P.Hkv * P.RBLK), dim3(COMBINE_THREADS), 0, s, P);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();

@@ -33,6 +33,27 @@ struct AttnParams {
     float softmax_scale;
 };
 
+// The single-latent kernel: K and V share one E4M3 plane per kv head (V is
+// the first 512 of 576 channels) with a per-token fp32 scale after the codes
+// of every block.
+struct LatentParams {
+    const uint8_t *q;
+    const uint8_t *k_pool;     // block b starts at k_pool + b * block_stride
+    const int32_t *block_table;
+    const int32_t *context_lens;
+    uint32_t *hdr;
+    const int4 *req;
+    float *part_o;             // [slots][64][512]
+    float *part_lse;           // [slots][64]
+    void *out;
+    float *lse;
+    long long block_stride;    // bytes per pool block (codes + scales)
+    int codes_bytes;           // Hkv * bs * 576: offset of the scales in a block
+    int B, n, Hq, Hkv, G, R, RBLK, mbps, num_blocks;
+    int q_dtype, out_dtype, causal;
+    float softmax_scale;
+};
+
 struct PlanParams {
     const int32_t *context_lens;
     uint32_t *hdr;
@@ -49,7 +70,8 @@ struct CombineParams {
     void *out;
     float *lse;
     int B, n, Hq, Hkv, G, R, RBLK, Dv, out_dtype, v_mode;
-    long long nwarps;  // warps of the attention launch
+    int rows_seg;      // query rows per segment (16, or 64 for the latent kernel)
+    long long nwarps;  // workers of the attention launch (warps, or CTAs for the latent kernel)
 };
 
 // header word indices
@@ -139,6 +161,14 @@ __device__ __forceinline__ void tma_load_4d(void *dst, const CUtensorMap *tm, ui
         : "memory");
 }
 
+// 1-D bulk copy global -> shared (16-byte aligned addresses, size a multiple of 16)
+__device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap *tm) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tm)) : "memory");
 }
@@ -162,6 +192,25 @@ __device__ __forceinline__ void mma16816(float c[4], const uint32_t a[4], uint32
             : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
             : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
     }
+}
+
+// four 8x8 b16 matrices from shared memory (lane i supplies the row address
+// of matrix i / 8); .trans delivers the transposed matrices
+__device__ __forceinline__ void ldsm_x4(uint32_t r[4], uint32_t addr) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr));
+}
+
+__device__ __forceinline__ void ldsm_x4_t(uint32_t r[4], uint32_t addr) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr));
+}
+
+// barrier `id` (1..15) over `count` threads (a multiple of 32)
+__device__ __forceinline__ void named_barrier(int id, int count) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
 // ------------------------------------------------------------- conversions

@@ -174,10 +174,16 @@ _SHAPES = {
 def make(name: str, device="cpu", seed: Optional[int] = None, *, B: Optional[int] = None,
          L_lo: Optional[int] = None, L_hi: Optional[int] = None, context_lens=None,
          poison: Optional[bool] = None, slack_frac: float = 0.10, n: Optional[int] = None,
-         Hq: Optional[int] = None, Hkv: Optional[int] = None, D: Optional[int] = None) -> Workload:
+         Hq: Optional[int] = None, Hkv: Optional[int] = None, D: Optional[int] = None,
+         token_scale_spread: int = 0) -> Workload:
     """Draw one workload.  `name` picks the recipe; keyword overrides shrink it
     (batch, length range, explicit lengths, heads) for tests.  Everything is a
-    deterministic function of (name, seed, overrides, device)."""
+    deterministic function of (name, seed, overrides, device).
+
+    token_scale_spread = k > 0 (per-token E4M3 scales only): every block's
+    scales are multiplied by 2^u, u uniform in {0..k} per block, and its codes
+    encoded against them, so the scales of neighbouring pages differ by up
+    to 2^k while the dequantized values keep their distribution."""
     if name not in _SHAPES:
         raise ValueError(f"unknown workload {name!r}")
     (B0, n0, Hq0, Hkv0, Dk, Dv, bs, qd, kvd, outd, kmode, vmode, causal, vprefix) = _SHAPES[name]
@@ -263,6 +269,9 @@ def make(name: str, device="cpu", seed: Optional[int] = None, *, B: Optional[int
                     x = torch.randn(shape, generator=gdev, device=device)
                     s = x.abs().amax(dim=-1) / 448.0
                     s = torch.where(s > 0, s, torch.ones_like(s))
+                    if token_scale_spread > 0:
+                        u = torch.randint(0, token_scale_spread + 1, (m, 1, 1), generator=gdev, device=device)
+                        s = s * torch.pow(2.0, u.to(s.dtype))
                     data = e4m3_codes(x / s[..., None]).reshape(m, codes_bytes)
                     sc = s.to(torch.float32).reshape(m, Hkv * bs)
                 elif kvd in ("int8", "int4"):

@@ -61,8 +61,50 @@ def test_workspace_size_and_layout(B):
     assert offs == sorted(offs) and all(o % 256 == 0 for o in offs)
     assert lo.rows_per_kv_head == 4 and lo.row_blocks == 1 and lo.num_sms == 152
     assert lo.grid_ctas % 152 == 0 and lo.warps == lo.grid_ctas * 4 and lo.ring_pages_per_warp >= 2
-    assert lo.partial_slots == 4 * 8 + lo.warps
+    assert lo.partial_slots == 4 * 8 + lo.warps and lo.rows_per_segment == 16
     assert lo.partial_lse_offset - lo.partial_o_offset >= lo.partial_slots * 16 * 128 * 4
+
+
+def _latent(B, **kw):
+    base = dict(batch=8, next_n=2, num_q_heads=128, num_kv_heads=1, head_dim_k=576, head_dim_v=512,
+                block_size=64, num_blocks=2000, max_blocks_per_seq=200, max_context_len=12800,
+                q_dtype=B.PA_BF16, kv_dtype=B.PA_E4M3, out_dtype=B.PA_BF16, k_scale_mode=B.PA_SCALE_TOKEN,
+                v_scale_mode=B.PA_SCALE_TOKEN, causal=1, v_is_k_prefix=1, num_sms=152, softmax_scale=1 / 24)
+    base.update(kw)
+    return _prob(B, **base)
+
+
+def test_latent_layout(B):
+    lo = B.pa_workspace_layout(_latent(B))
+    assert lo.rows_per_kv_head == 256 and lo.rows_per_segment == 64 and lo.row_blocks == 4
+    assert lo.grid_ctas == 152 and lo.warps == 152 and lo.ring_pages_per_warp == 2
+    assert lo.partial_slots == 8 * 4 + 152
+    assert lo.partial_lse_offset - lo.partial_o_offset >= lo.partial_slots * 64 * 512 * 4
+    assert lo.total_bytes - lo.partial_lse_offset >= lo.partial_slots * 64 * 4
+
+
+@pytest.mark.parametrize("kw", [dict(block_size=32), dict(head_dim_k=512), dict(head_dim_v=256),
+                                dict(kv_dtype=5, head_dim_k=576), dict(k_scale_mode=1), dict(kv_dtype=1)])
+def test_latent_unsupported_variants(B, kw):
+    st = B.raw_status("pa_workspace_size", ctypes.byref(_latent(B, **kw)), ctypes.byref(ctypes.c_size_t()))
+    assert st == B.PA_ERR_UNSUPPORTED
+
+
+def test_latent_v_wider_than_k_rejected(B):
+    st = B.raw_status("pa_workspace_size", ctypes.byref(_latent(B, head_dim_v=640)), ctypes.byref(ctypes.c_size_t()))
+    assert st == B.PA_ERR_INVALID_ARG
+
+
+def test_latent_run_needs_no_v_pool_but_checks_the_rest(B):
+    p = _latent(B)
+    need = B.pa_workspace_size(p)
+    # q misaligned (odd address): rejected before any launch
+    st = B.raw_status("pa_run", ctypes.byref(p), 0x4001, 0x5000, None, 0x7000, 0x8000, None, None,
+                      0x10000, need, 0x9000, None, None)
+    assert st == B.PA_ERR_INVALID_ARG
+    st = B.raw_status("pa_run", ctypes.byref(p), 0x4000, 0x5008, None, 0x7000, 0x8000, None, None,
+                      0x10000, need, 0x9000, None, None)
+    assert st == B.PA_ERR_INVALID_ARG
 
 
 @pytest.mark.parametrize("field,value", [
@@ -110,7 +152,8 @@ def test_missing_pointers_rejected(B):
     assert st == B.PA_ERR_INVALID_ARG
 
 
-def test_partial_slots_cover_oracle_pieces(B):
+@pytest.mark.parametrize("latent", [False, True])
+def test_partial_slots_cover_oracle_pieces(B, latent):
     import numpy as np
     import oracle
     rng = np.random.default_rng(3)
@@ -122,9 +165,16 @@ def test_partial_slots_cover_oracle_pieces(B):
         G = int(rng.choice([1, 4, 16]))
         n = int(rng.choice([1, 2, 4]))
         mbps = -(-maxctx // bs)
-        p = _prob(B, batch=Bsz, block_size=bs, max_context_len=maxctx, num_kv_heads=Hkv, num_q_heads=Hkv * G,
-                  next_n=n, max_blocks_per_seq=mbps, num_sms=int(rng.integers(1, 200)),
-                  grid_ctas=int(rng.integers(0, 50)))
+        if latent:
+            bs = 64
+            mbps = -(-maxctx // bs)
+            p = _latent(B, batch=Bsz, max_context_len=maxctx, num_kv_heads=Hkv, num_q_heads=Hkv * G * 8,
+                        next_n=n, max_blocks_per_seq=mbps, num_sms=int(rng.integers(1, 200)),
+                        grid_ctas=int(rng.integers(0, 50)))
+        else:
+            p = _prob(B, batch=Bsz, block_size=bs, max_context_len=maxctx, num_kv_heads=Hkv, num_q_heads=Hkv * G,
+                      next_n=n, max_blocks_per_seq=mbps, num_sms=int(rng.integers(1, 200)),
+                      grid_ctas=int(rng.integers(0, 50)))
         lo = B.pa_workspace_layout(p)
         L = rng.integers(0, maxctx + 1, Bsz)
         pl = oracle.plan(L, bs=bs, Hkv=Hkv, max_context_len=maxctx, max_blocks_per_seq=mbps,
