@@ -35,7 +35,8 @@
  *    padding and unused slots never reach P.V (0 * NaN = NaN).
  *
  * ------------------------------------------------------------------ layouts
- *  q            [batch][next_n][Hq][Dk]   fp16 or bf16, contiguous.
+ *  q            [batch][next_n][Hq][Dk]   fp16 or bf16, contiguous (16-byte
+ *               aligned for the single-latent shape, 2-byte otherwise).
  *  k_pool       [num_blocks] blocks; each block is [Hkv][bs][row bytes] codes,
  *               followed -- only with PA_SCALE_TOKEN -- by [Hkv][bs] fp32
  *               per-token scales.  Row bytes = Dk * bits / 8 (fp16/bf16 16,
@@ -164,14 +165,20 @@ typedef struct pa_problem {
  * Two kernels: the grouped kernel (separate K and V planes, per-tensor or
  * per-channel scales) has S = 16 and one worker per warp; the single-latent
  * kernel (v_is_k_prefix: E4M3, PA_SCALE_TOKEN, Dk = 576, Dv = 512, bs = 64)
- * has S = 64 and one worker per CTA (one CTA per SM). */
+ * has S = 64 and one worker per CTA (one CTA per SM), and its workers come
+ * in groups of G = row_blocks: positions then run over (request, kv head,
+ * page), the W / G groups share them as above, and worker g*G + i takes row
+ * block i of every page of group g's share (the G workers read the same
+ * pages at about the same time, so all but the first read hit L2).  The
+ * piece of segment (b, kv head u, row block i) in group g has slot
+ * (b*Hkv + u + g)*G + i. */
 typedef struct pa_layout {
     size_t total_bytes;
     size_t header_offset;
     size_t requests_offset;
     size_t partial_o_offset;
     size_t partial_lse_offset;
-    int64_t partial_slots;       /* B * Hkv * row_blocks + warps */
+    int64_t partial_slots;       /* B * Hkv * row_blocks + warps (grouped: (B*Hkv + W/G)*G) */
     int32_t rows_per_kv_head;    /* (Hq / Hkv) * next_n */
     int32_t row_blocks;          /* ceil(rows_per_kv_head / rows_per_segment) */
     int32_t num_sms;             /* effective */
@@ -179,6 +186,7 @@ typedef struct pa_layout {
     int32_t warps;               /* workers W: grid_ctas * 4 (grouped) or grid_ctas (latent) */
     int32_t ring_pages_per_warp; /* pages each worker keeps in flight */
     int32_t rows_per_segment;    /* S: 16 (grouped) or 64 (latent) */
+    int32_t group_size;          /* G: workers sharing one run of pages (1, or row_blocks for latent) */
 } pa_layout;
 
 /* Library version: major * 10000 + minor * 100 + patch. */

@@ -20,6 +20,14 @@ Rule
   warp k of W takes positions [k N / W, (k + 1) N / W)   (integer division)
   piece = a warp's positions inside one segment; its partial slot is s + k;
   a piece that is a whole segment is "complete" (written as the output).
+
+Grouped workers (group_size G > 1, the single-latent kernel: one worker per
+row block of a kv head): positions run over (request, kv head, page) only --
+U = X / G units per request, unit u = segments u*G .. u*G + G-1 --, the
+W / G worker groups share them as above, and worker g*G + i of group g takes
+row block i of every unit in the group's share.  The piece of segment
+s = b*X + u*G + i in group g has partial slot (b*U + u + g)*G + i; slots in
+all: (B*U + W/G)*G.  G = 1 is the rule above.
 """
 from __future__ import annotations
 
@@ -27,7 +35,7 @@ import numpy as np
 
 
 def plan(context_lens, *, bs: int, Hkv: int, max_context_len: int, max_blocks_per_seq: int,
-         row_blocks: int = 1, warps: int = 1):
+         row_blocks: int = 1, warps: int = 1, group_size: int = 1):
     L = np.asarray(context_lens, dtype=np.int64).reshape(-1)
     B = L.size
     P = np.zeros(B, dtype=np.int64)
@@ -40,20 +48,25 @@ def plan(context_lens, *, bs: int, Hkv: int, max_context_len: int, max_blocks_pe
         P[b] = pb
     PS = np.concatenate([[0], np.cumsum(P)[:-1]]).astype(np.int64) if B else np.zeros(0, dtype=np.int64)
     X = Hkv * row_blocks
-    N = int(P.sum()) * X
-    starts = [k * N // warps for k in range(warps + 1)]
+    G = group_size
+    assert X % G == 0 and warps % G == 0
+    U = X // G
+    NG = warps // G
+    N = int(P.sum()) * U
+    starts = [g * N // NG for g in range(NG + 1)]
     pieces = []
     for b in range(B):
-        for q in range(X):
+        for u in range(U):
             if P[b] == 0:
                 continue
-            s = b * X + q
-            o0 = int(PS[b]) * X + q * int(P[b])
+            o0 = int(PS[b]) * U + u * int(P[b])
             o1 = o0 + int(P[b])
-            for k in range(warps):
-                lo, hi = max(o0, starts[k]), min(o1, starts[k + 1])
+            for g in range(NG):
+                lo, hi = max(o0, starts[g]), min(o1, starts[g + 1])
                 if lo < hi:
-                    pieces.append({"segment": s, "warp": k, "slot": s + k, "pages": (lo - o0, hi - o0),
-                                   "complete": lo == o0 and hi == o1})
+                    for i in range(G):
+                        s = b * X + u * G + i
+                        pieces.append({"segment": s, "warp": g * G + i, "slot": (b * U + u + g) * G + i,
+                                       "pages": (lo - o0, hi - o0), "complete": lo == o0 and hi == o1})
     return {"pages": P, "prefix": PS, "flags": flags, "total_pages": int(P.sum()), "positions": N,
-            "warp_starts": starts, "pieces": pieces, "slots": B * X + warps}
+            "warp_starts": starts, "pieces": pieces, "slots": (B * U + NG) * G}

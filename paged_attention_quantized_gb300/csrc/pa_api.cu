@@ -63,6 +63,7 @@ struct Derived {
     int G, R, row_blocks, sms, ctas, minb;
     bool tokm, latent;
     int rows_seg;  // query rows per segment
+    int gs;        // workers per group (they share one run of pages, one row block each)
     long long nwarps, slots_partial;
     int D, RB, SW, slots, warp_smem;
     size_t k_block, v_block, smem;
@@ -121,15 +122,18 @@ pa_status derive(const pa_problem *p, Derived *d) {
         d->slots = LAT_RING;
         d->warp_smem = 0;
         d->smem = 0;
-        d->ctas = p->grid_ctas > 0 ? p->grid_ctas : d->sms;
-        d->nwarps = d->ctas;  // the workers are CTAs
+        // the workers are CTAs, in groups of one per row block
+        d->gs = d->row_blocks;
+        const int want = p->grid_ctas > 0 ? p->grid_ctas : d->sms;
+        d->ctas = std::max(d->gs, want / d->gs * d->gs);
+        d->nwarps = d->ctas;
     } else {
         const pa_status st = derive_grouped(p, d);
         if (st != PA_OK) return st;
     }
 
     const long long X = (long long)p->num_kv_heads * d->row_blocks;
-    d->slots_partial = (long long)p->batch * X + d->nwarps;
+    d->slots_partial = ((long long)p->batch * (X / d->gs) + d->nwarps / d->gs) * d->gs;
     if (d->slots_partial > (1ll << 31)) return PA_ERR_UNSUPPORTED;
 
     pa_layout &Lo = d->L;
@@ -152,6 +156,7 @@ pa_status derive(const pa_problem *p, Derived *d) {
     Lo.warps = (int32_t)d->nwarps;
     Lo.ring_pages_per_warp = d->slots;
     Lo.rows_per_segment = d->rows_seg;
+    Lo.group_size = d->gs;
     return PA_OK;
 }
 
@@ -168,6 +173,7 @@ pa_status derive_grouped(const pa_problem *p, Derived *d) {
 
     d->D = D;
     d->rows_seg = 16;
+    d->gs = 1;
     d->row_blocks = (d->R + 15) / 16;
     if (d->row_blocks > 65535) return PA_ERR_UNSUPPORTED;
     const int bs = p->block_size;
@@ -334,9 +340,9 @@ PA_API pa_status pa_run(const pa_problem *p, const void *q, const void *k_pool, 
         context_lens == nullptr || out == nullptr)
         return PA_ERR_INVALID_ARG;
     if (d.latent) {
-        // outputs are stored as channel pairs
+        // q rows are read in 16-byte pieces, outputs as channel pairs
         const uintptr_t out_align = p->out_dtype == PA_F32 ? 7 : 3;
-        if ((reinterpret_cast<uintptr_t>(k_pool) & 15) || (reinterpret_cast<uintptr_t>(q) & 1) ||
+        if ((reinterpret_cast<uintptr_t>(k_pool) & 15) || (reinterpret_cast<uintptr_t>(q) & 15) ||
             (reinterpret_cast<uintptr_t>(out) & out_align))
             return PA_ERR_INVALID_ARG;
         CUtensorMap ta, tb;
@@ -445,6 +451,7 @@ PA_API pa_status pa_combine(const pa_problem *p, const float *v_scale, void *wor
     P.out_dtype = p->out_dtype;
     P.v_mode = v_mode;
     P.rows_seg = d.rows_seg;
+    P.gs = d.gs;
     P.nwarps = d.nwarps;
     cudaError_t e = pa::launch_combine(P, reinterpret_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;

@@ -40,30 +40,34 @@ __global__ void __launch_bounds__(COMBINE_THREADS) pa_combine_kernel(CombinePara
     const int seg = blockIdx.x;
     const int b = seg / X, q = seg % X;
     const int kvh = q / P.RBLK, rblk = q % P.RBLK;
+    // positions run over units of gs segments; worker groups share them
+    const int GS = P.gs, U = X / GS, u = q / GS, gi = q % GS;
+    const long long NG = P.nwarps / GS;
     const int4 Rq = P.req[b];
     const int Pb = Rq.y;
     const int RS = P.rows_seg;
     const int rows_here = min(RS, P.R - rblk * RS);
     const float NaN = __int_as_float(0x7fc00000);
     const float LOG2E_ = 1.4426950408889634f;
-    const long long N = (long long)P.hdr[HDR_TOTAL_PAGES] * X;
+    const long long N = (long long)P.hdr[HDR_TOTAL_PAGES] * U;
     long long kf = 0, kl = -1;
     if (Pb > 0) {
-        const long long x0 = (long long)Rq.z * X + (long long)q * Pb;
+        const long long x0 = (long long)Rq.z * U + (long long)u * Pb;
         const long long xl = x0 + Pb - 1;
         if (xl >= N) return;  // not a plan of this problem
-        kf = share_owner(x0, N, P.nwarps);
-        kl = share_owner(xl, N, P.nwarps);
+        kf = share_owner(x0, N, NG);
+        kl = share_owner(xl, N, NG);
         if (kf == kl) return;  // one piece: the attention kernel wrote the output
     }
+    const long long slot0 = ((long long)b * U + u) * GS + gi;  // slot of group g: slot0 + g * GS
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    // 1. the pieces: warps kf..kl with a non-empty share (empty shares only
-    //    exist when there are fewer positions than warps)
+    // 1. the pieces: worker groups kf..kl with a non-empty share (empty shares
+    //    only exist when there are fewer positions than groups)
     if (threadIdx.x == 0) {
         int np = 0;
         for (long long k = kf; k <= kl; ++k) {
-            if (share_start(k, N, P.nwarps) == share_start(k + 1, N, P.nwarps)) continue;
-            if (np < MAX_CACHED_PIECES) s_piece[np] = (long long)seg + k;
+            if (share_start(k, N, NG) == share_start(k + 1, N, NG)) continue;
+            if (np < MAX_CACHED_PIECES) s_piece[np] = slot0 + k * GS;
             ++np;
         }
         s_np = np;
@@ -76,10 +80,10 @@ __global__ void __launch_bounds__(COMBINE_THREADS) pa_combine_kernel(CombinePara
         if (cached) return s_piece[n];
         int seen = 0;
         for (long long k = kf; k <= kl; ++k) {
-            if (share_start(k, N, P.nwarps) == share_start(k + 1, N, P.nwarps)) continue;
-            if (seen++ == n) return (long long)seg + k;
+            if (share_start(k, N, NG) == share_start(k + 1, N, NG)) continue;
+            if (seen++ == n) return slot0 + k * GS;
         }
-        return (long long)seg + kf;
+        return slot0 + kf * GS;
     };
     // 2. per row: M = max lse, den = sum exp(lse - M), NaN if any piece is NaN
     if (Pb > 0) {
@@ -155,7 +159,9 @@ __global__ void __launch_bounds__(COMBINE_THREADS) pa_combine_kernel(CombinePara
 
 cudaError_t launch_combine(const CombineParams &P, cudaStream_t s) {
     if (P.B == 0) return cudaSuccess;
-    if (P.rows_seg < 1 || P.rows_seg > MAX_ROWS_SEG) return cudaErrorInvalidValue;
+    if (P.rows_seg < 1 || P.rows_seg > MAX_ROWS_SEG || P.gs < 1 || (P.Hkv * P.RBLK) % P.gs != 0 ||
+        P.nwarps % P.gs != 0)
+        return cudaErrorInvalidValue;
     cudaError_t e = launch_pdl(pa_combine_kernel, dim3(P.B * P.Hkv * P.RBLK), dim3(COMBINE_THREADS), 0, s, P);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();

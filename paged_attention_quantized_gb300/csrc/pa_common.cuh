@@ -71,6 +71,7 @@ struct CombineParams {
     float *lse;
     int B, n, Hq, Hkv, G, R, RBLK, Dv, out_dtype, v_mode;
     int rows_seg;      // query rows per segment (16, or 64 for the latent kernel)
+    int gs;            // workers per group (1, or the row blocks for the latent kernel)
     long long nwarps;  // workers of the attention launch (warps, or CTAs for the latent kernel)
 };
 

@@ -1,82 +1,212 @@
-// Single-latent-KV MQA decode / verify attention for sm_103a.
+// Single-latent-KV MQA decode / verify attention for sm_103a, on the fifth-
+// generation tensor cores (tcgen05: operands in shared memory, accumulators in
+// tensor memory).
 //
 // K and V live in one E4M3 plane per kv head: a token row holds 576 channels,
 // V is its first 512, and every block ends with one fp32 scale per token
 // (the layout of a "data region then scale region" block, FlashInfer docs,
 // "flashinfer.fp4_paged_mqa_logits", Parameters).  With 128 query heads on
 // one kv head and two query rows per request there are 256 query rows per
-// request, so both S = q K^T (576 deep) and O = P V (512 wide) are dense
-// contractions; the MMA tiles are the point of this kernel.
+// request, so S = q K^T (576 deep) and O = P V (512 wide) are dense
+// contractions.
 //
-// Work split: the same global page order as the grouped kernel -- (request,
-// kv head, block of 64 query rows = "segment", page), logical positions only
-// (1Cat-vLLM PR #494, "Stabilize QSA page4 order under KV relocation",
-// Summary) -- shared evenly over the CTAs of a persistent launch, one CTA
-// per SM.  A CTA's run of pages inside one segment is a piece; a piece that
-// is a whole segment writes `out`, the others write a normalised partial and
-// its log-sum-exp to slot (segment + CTA index) for the combine kernel.
+// Work split: pages in logical order -- (request, kv head, page), never by
+// physical id (1Cat-vLLM PR #494, "Stabilize QSA page4 order under KV
+// relocation", Summary) -- shared evenly over groups of R/64 CTAs of a
+// persistent launch, one CTA per SM; CTA i of a group computes query rows
+// 64i..64i+63 (row block i) of every page of the group's share, so the group
+// reads each page at about the same time and all but the first read hit L2.
+// A CTA's run of pages inside one (request, kv head) is a piece; a piece that
+// covers all of them writes `out`, the others write a normalised partial and
+// its log-sum-exp to slot ((b*Hkv + kv head) + group)*G + i for the combine.
 //
-// Per page (64 tokens), the CTA's eight warps:
-//  1. wait for the page's bulk tensor copies (codes as four 128-byte and one
-//     64-byte swizzled column boxes, scales as a 256-byte bulk copy) and
-//     dequantize the codes once into an f16 tile [token][576] in shared
-//     memory (E4M3 -> f16 is exact).  Token slots past L_b become zero codes
-//     and zero scales, so neither a NaN code nor a NaN scale in the padding
-//     reaches P.V (1Cat-vLLM PR #647, "Stop grouped-page4 null-block padding
-//     from leaking E4M3 NaN", Fix);
-//  2. S = q' K^T with m16n8k16 MMAs (warp w: rows 16(w%4).., tokens
-//     32(w/4)..), scores scaled in fp32 by softmax_scale, the query row's
-//     power-of-two factor and the token's scale, then masked (t >= vis);
-//  3. online softmax in the exp2 domain; the two warps of a row tile trade
-//     their row maxima through shared memory.  P' = p * scale_t * 2^-E (E
-//     the exponent of the page's largest token scale, so P' fits f16 with
-//     full precision) is stored as f16; the row sum keeps p alone;
-//  4. O += P' V with m16n8k16 MMAs (warp w: rows 32(w%2).., channels
-//     128(w/2)..); the factor exp2(m_old - m_new) * 2^(E_old - E) rescales O
-//     first, so O always carries the current page's 2^-E.
-// The query rows of a segment are staged once per piece as f16, each row
-// scaled by a power of two into [-1, 1) (exact), the factor joining the score
-// scale.
+// Roles (10 warps), hand-offs through mbarriers whose waits are all bounded:
+//  * warp 0 (producer): block ids (32 per load, range-checked) and the bulk
+//    tensor copies of each page -- the codes as four 128-byte and one 64-byte
+//    swizzled column boxes, exactly the K-major operand layout the MMA reads
+//    -- plus the 256-byte scale tail, into a 2-slot ring;
+//  * warp 1 (MMA): S = q' K^T as E4M3 x E4M3 MMAs (M = 64 query rows, N = 64
+//    tokens, K = 32 channels per step) straight from the ring, q' given as
+//    two E4M3 terms hi + lo that add up to the bf16 query exactly (a bf16
+//    significand has 8 bits, each E4M3 term carries 4), into one of two S
+//    buffers in tensor memory; then O^T += V^T P'^T as f16 MMAs (M = 128
+//    channels, N = 64 query rows, K = 16 tokens) for four channel tiles, V^T
+//    read MN-major from the dequantized V tile.  S(j+1) is issued before
+//    O(j), so the tensor pipe works while page j's softmax runs;
+//  * warps 2-5 (softmax, one query row per lane 0-15 of each warp -- the
+//    M = 64 accumulator layout): scores scaled in fp32 by softmax_scale, the
+//    row's power-of-two factor and the token scale, masked (t >= vis), online
+//    softmax in the exp2 domain with a lazy maximum (O is rescaled only when
+//    a row maximum grows by more than 2^6, or when the page-scale exponent E
+//    leaves its band); P' = p * scale_t * 2^-E stored as f16 for the MMA, the
+//    row sum keeps p; at the end of a piece they read O^T back, normalise
+//    and write `out` or the partial.  They also stage q' for each piece;
+//  * warps 6-9 (dequant): V codes of each page -> f16 tile (exact), token
+//    slots past L_b zeroed, so neither NaN codes nor NaN scales in padding
+//    reach P.V (1Cat-vLLM PR #647, "Stop grouped-page4 null-block padding
+//    from leaking E4M3 NaN", Fix).
 #include "pa_attn.cuh"
 
 namespace pa {
 namespace lat {
 
-constexpr int DK = 576, DV = 512, BS = 64, LROWS = 64, THREADS = 256, NSLOT = 2;
-constexpr int KB = DK / 64;                          // column blocks of 64 channels (128 B of f16)
-constexpr int BLK = LROWS * 128;                      // bytes of one column block (64 rows)
-constexpr int QS_OFF = 0;                            // q' [KB][64 rows][128 B], swizzled
-constexpr int KS_OFF = QS_OFF + KB * BLK;            // f16 page [KB][64 tokens][128 B], swizzled
-constexpr int RING_OFF = KS_OFF + KB * BLK;          // E4M3 pages as copied
-constexpr int SLOT_BYTES = 4 * BS * 128 + BS * 64;   // four 128-B column boxes + one 64-B box
-constexpr int PS_OFF = RING_OFF + NSLOT * SLOT_BYTES;  // P' [64 rows][64 tokens] f16, swizzled
-constexpr int TSRAW_OFF = PS_OFF + LROWS * 128;       // [NSLOT][64] token scales as copied
-constexpr int TSN_OFF = TSRAW_OFF + NSLOT * BS * 4;  // [64] scale_t * 2^-E (0 past L_b)
-constexpr int RMAX_OFF = TSN_OFF + BS * 4;           // [2][64] row maxima of the two token halves
-constexpr int LPART_OFF = RMAX_OFF;                  //   (at the end of a piece: row sums)
-constexpr int ALPHA_OFF = RMAX_OFF + 2 * LROWS * 4;   // [64] O rescale factors
-constexpr int MROW_OFF = ALPHA_OFF;                  //   (at the end of a piece: row maxima)
-constexpr int ROWSC_OFF = ALPHA_OFF + LROWS * 4;      // [64] score factor of each query row
-constexpr int BAR_OFF = ROWSC_OFF + LROWS * 4;        // [NSLOT] mbarriers
-constexpr int FLAG_OFF = BAR_OFF + NSLOT * 8;        // [0] wait ok, [1] E of the page, [2 + s] slot s bad, [4] errors
-constexpr int SMEM_USED = FLAG_OFF + 32;
-constexpr int SMEM_BYTES = SMEM_USED + 1024;         // + alignment of the base to 1 KB
-constexpr uint32_t PAGE_TX = SLOT_BYTES + BS * 4;    // bytes one page's copies deliver
+constexpr int DK = 576, DV = 512, BS = 64, LROWS = 64, NSLOT = 2;
+constexpr int NWARPS = 10, THREADS = NWARPS * 32;
+constexpr int W_PROD = 0, W_MMA = 1, W_SM = 2, W_DQ = 6;
+// shared memory (offsets from a 1 KB aligned base)
+constexpr int QH_OFF = 0;                              // q' hi, E4M3 [64 rows]: 4 x SW128 [64][128 B] + SW64 [64][64 B]
+constexpr int QL_OFF = 36864;                          // q' lo, same layout
+constexpr int RING_OFF = 73728;                        // NSLOT pages as copied, same layout
+constexpr int SLOT_BYTES = 36864;
+constexpr int V_OFF = RING_OFF + NSLOT * SLOT_BYTES;   // V f16 [8 x 64 channels][64 tokens][128 B], SW128
+constexpr int P_OFF = V_OFF + 65536;                   // P' f16 [2][64 rows][64 tokens], SW128
+constexpr int TSRAW_OFF = P_OFF + 2 * 8192;            // [NSLOT][64] token scales as copied
+constexpr int ALPHA_OFF = TSRAW_OFF + NSLOT * 256;     // [2][64] O rescale factors
+constexpr int STAT_OFF = ALPHA_OFF + 2 * 256;          // [64] 2^E / l, [64] lse
+constexpr int NEED_OFF = STAT_OFF + 512;               // [2][4] rescale votes of the softmax warps
+constexpr int BAR_OFF = NEED_OFF + 32;
+enum {
+    B_FULL = 0,                     // [NSLOT] page copied (tx bytes)
+    B_SLOTFREE = B_FULL + NSLOT,    // [NSLOT] S MMAs done + dequant and softmax done reading
+    B_SFULL = B_SLOTFREE + NSLOT,   // [2] S(j) complete
+    B_SFREE = B_SFULL + 2,          // [2] S(j) read out
+    B_PFULL = B_SFREE + 2,          // [2] P'(j) written (and O^T rescaled)
+    B_PVDONE = B_PFULL + 2,         // [2] O^T += V^T P'(j)^T complete
+    B_VFULL = B_PVDONE + 2,         // V tile of page j written
+    B_QFULL = B_VFULL + 1,          // q' of the piece staged
+    B_OFREE = B_QFULL + 1,          // O^T of the previous piece read out
+    B_WG = B_OFREE + 1,             // the four softmax warps
+    B_MDONE = B_WG + 1,             // every MMA of the CTA complete
+    NBARS = B_MDONE + 1
+};
+constexpr int MISC_OFF = BAR_OFF + NBARS * 8;          // [0] tmem base, [1] abort, [2 + s] slot s bad, [4] errors
+constexpr int SMEM_USED = MISC_OFF + 64;
+constexpr int SMEM_BYTES = SMEM_USED + 1024;           // + alignment of the base to 1 KB
+constexpr uint32_t PAGE_TX = SLOT_BYTES + BS * 4;
+constexpr uint32_t TM_S = 0, TM_O = 256;               // tensor-memory columns: S[2] x 64, O^T[4] x 64
+constexpr float ROW_SLACK = 6.0f;                      // lazy maximum: rescale when a row max grows by > 2^6
 static_assert(SMEM_BYTES <= 227 * 1024, "latent kernel exceeds the shared memory of one CTA");
+static_assert(NSLOT == 2, "barrier counts below assume two ring slots");
 
-// byte offset of the 16-byte chunk holding channels 8c..8c+7 (c < 72) of row
-// r in a [KB][64][128 B] tile: chunk index XOR (r mod 8) inside each 128 B
-__device__ __forceinline__ uint32_t sw_off(int r, int c) {
-    return (uint32_t)((c >> 3) * BLK + r * 128 + (((c & 7) ^ (r & 7)) << 4));
+// ---------------------------------------------------------- tcgen05 helpers
+
+// shared-memory matrix descriptor: start, leading / stride byte offsets,
+// descriptor version 1, swizzle (2 = 128 B, 4 = 64 B)
+__device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t sbo, uint32_t swz) {
+    return (uint64_t)((saddr >> 4) & 0x3FFF) | ((uint64_t)((lbo >> 4) & 0x3FFF) << 16) |
+           ((uint64_t)((sbo >> 4) & 0x3FFF) << 32) | ((uint64_t)1 << 46) | ((uint64_t)swz << 61);
 }
 
-__device__ __forceinline__ float load_qv(const LatentParams &P, size_t idx) {
-    const uint16_t bits = reinterpret_cast<const uint16_t *>(P.q)[idx];
-    if (P.q_dtype == PA_BF16) return __uint_as_float((uint32_t)bits << 16);
-    return __half2float(__ushort_as_half(bits));
+// instruction descriptor: fp32 accumulator, A/B formats 0 (f16 for kind::f16,
+// E4M3 for kind::f8f6f4), A MN-major flag, N >> 3, M >> 4
+__host__ __device__ constexpr uint32_t idesc(int M, int N, int a_mn) {
+    return (1u << 4) | ((uint32_t)a_mn << 15) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+__device__ __forceinline__ void mma_f8(uint32_t d, uint64_t a, uint64_t b, uint32_t id, uint32_t acc) {
+    asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+                 "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
+                 "l"(a), "l"(b), "r"(id), "r"(acc));
+}
+
+__device__ __forceinline__ void mma_f16(uint32_t d, uint64_t a, uint64_t b, uint32_t id, uint32_t acc) {
+    asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+                 "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
+                 "l"(a), "l"(b), "r"(id), "r"(acc));
+}
+
+__device__ __forceinline__ void mma_commit(uint64_t *bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+                 : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// 32 lanes x 32 columns of 32 bits: lane i of the warp's quarter -> thread i
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float *v) {
+    uint32_t r[32];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const float *v) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+        "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+        "f"(v[0]), "f"(v[1]), "f"(v[2]), "f"(v[3]), "f"(v[4]), "f"(v[5]), "f"(v[6]), "f"(v[7]), "f"(v[8]),
+        "f"(v[9]), "f"(v[10]), "f"(v[11]), "f"(v[12]), "f"(v[13]), "f"(v[14]), "f"(v[15]), "f"(v[16]),
+        "f"(v[17]), "f"(v[18]), "f"(v[19]), "f"(v[20]), "f"(v[21]), "f"(v[22]), "f"(v[23]), "f"(v[24]),
+        "f"(v[25]), "f"(v[26]), "f"(v[27]), "f"(v[28]), "f"(v[29]), "f"(v[30]), "f"(v[31])
+        : "memory");
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// two fp32 -> two E4M3 codes (RNE, saturating), lo in the low byte
+__device__ __forceinline__ uint32_t f32x2_e4m3x2(float lo, float hi) {
+    uint16_t r;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+__device__ __forceinline__ float2 e4m3x2_f32x2(uint32_t two_codes) {
+    const uint32_t h = e4m3x2_f16x2(two_codes);
+    __half2 hh;
+    memcpy(&hh, &h, 4);
+    return __half22float2(hh);
 }
 
 __device__ __forceinline__ float pow2f(int e) { return __int_as_float((min(max(e, -126), 127) + 127) << 23); }
+
+// byte offset of the 16-byte chunk c (0..35, 16 E4M3 channels each) of row r
+// in a [4 x SW128 [64][128 B] | SW64 [64][64 B]] tile (the copied page layout)
+__device__ __forceinline__ uint32_t e4_off(int r, int c) {
+    if (c < 32) return (uint32_t)((c >> 3) * (64 * 128) + r * 128 + (((c & 7) ^ (r & 7)) << 4));
+    return (uint32_t)(4 * 64 * 128 + r * 64 + ((((c - 32) & 3) ^ ((r >> 1) & 3)) << 4));
+}
+
+// byte offset of the 16-byte chunk c (0..63, 8 f16 channels each) of token t
+// in the V tile [8][64 tokens][128 B]
+__device__ __forceinline__ uint32_t v_off(int t, int c) {
+    return (uint32_t)((c >> 3) * (64 * 128) + t * 128 + (((c & 7) ^ (t & 7)) << 4));
+}
+
+// Bounded wait by lane 0, outcome shared with the warp; on a timeout the
+// CTA's abort word is raised so every role leaves its loop.
+__device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, volatile int *abort, uint32_t &err) {
+    int ok = 1;
+    if ((threadIdx.x & 31) == 0) {
+        ok = mbar_wait_bounded(bar, parity, abort) ? 1 : 0;
+        if (!ok && *abort == 0) {
+            *abort = 1;
+            err |= PA_DEV_ERR_TIMEOUT;
+        }
+    }
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    if (ok) (void)mbar_try_wait(bar, parity);  // acquire in every lane
+    return ok != 0;
+}
+
+__device__ __forceinline__ void warp_arrive(uint64_t *bar) {
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
+}
+
+// two consecutive q values of a packed word (low half first)
+__device__ __forceinline__ float2 q_pair(uint32_t u, int q_dtype) {
+    if (q_dtype == PA_BF16) return make_float2(__uint_as_float(u << 16), __uint_as_float(u & 0xFFFF0000u));
+    return make_float2(__half2float(__ushort_as_half((uint16_t)(u & 0xFFFFu))),
+                       __half2float(__ushort_as_half((uint16_t)(u >> 16))));
+}
 
 }  // namespace lat
 
@@ -86,21 +216,20 @@ __global__ void __launch_bounds__(lat::THREADS, 1)
     using namespace lat;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    const uint32_t sbase = smem_u32(smem);
-    const uint32_t qs = sbase + QS_OFF, ks = sbase + KS_OFF, ps = sbase + PS_OFF;
-    float *tsraw = reinterpret_cast<float *>(smem + TSRAW_OFF);
-    float *tsn = reinterpret_cast<float *>(smem + TSN_OFF);
-    float *rmax = reinterpret_cast<float *>(smem + RMAX_OFF);
-    float *lpart = reinterpret_cast<float *>(smem + LPART_OFF);
+    const uint32_t sb = smem_u32(smem);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + BAR_OFF);
+    int *misc = reinterpret_cast<int *>(smem + MISC_OFF);
+    volatile int *abort = misc + 1;
+    const float *tsraw = reinterpret_cast<const float *>(smem + TSRAW_OFF);
     float *alpha = reinterpret_cast<float *>(smem + ALPHA_OFF);
-    float *mrow = reinterpret_cast<float *>(smem + MROW_OFF);
-    float *rowsc = reinterpret_cast<float *>(smem + ROWSC_OFF);
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem + BAR_OFF);
-    int *flags = reinterpret_cast<int *>(smem + FLAG_OFF);
+    float *stat_f = reinterpret_cast<float *>(smem + STAT_OFF);
+    float *stat_lse = stat_f + 64;
+    volatile int *need = reinterpret_cast<volatile int *>(smem + NEED_OFF);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int g = lane >> 2, c = lane & 3;
-    const int X = P.Hkv * P.RBLK;
+    const int GS = P.RBLK;                 // CTAs per group: one per row block
+    const int rb = (int)(blockIdx.x % GS);  // this CTA's row block
+    const int U = P.Hkv;                   // units (kv heads) per request
 
     grid_dependency_wait();
     const long long total = P.hdr[HDR_TOTAL_PAGES];
@@ -108,416 +237,504 @@ __global__ void __launch_bounds__(lat::THREADS, 1)
         if (tid == 0) atomic_or_err(P.hdr, PA_DEV_ERR_STALE_PLAN);
         return;
     }
-    const long long Ntot = total * X;
-    const long long NW = gridDim.x;
-    const long long kw = blockIdx.x;
-    const long long x0 = kw * Ntot / NW, x1 = (kw + 1) * Ntot / NW;
+    const long long Ntot = total * U;
+    const long long NG = gridDim.x / GS;
+    const long long kg = blockIdx.x / GS;  // this CTA's group
+    if (kg >= NG) return;                  // the host launches whole groups
+    const long long x0 = kg * Ntot / NG, x1 = (kg + 1) * Ntot / NG;
     if (x0 >= x1) return;
     const int npg = (int)(x1 - x0);
+    const Cursor c0 = cursor_at(x0, P.req, P.B, U, P.mbps);
+    if (c0.b >= P.B) {  // uniform: every thread computed the same cursor
+        if (tid == 0) atomic_or_err(P.hdr, PA_DEV_ERR_STALE_PLAN);
+        return;
+    }
 
+    // ---- setup: barriers, tensor memory (512 columns, one CTA per SM)
     if (tid == 0) {
-        for (int s = 0; s < NSLOT; ++s) mbar_init(&full[s], 1);
+        const uint32_t counts[NBARS] = {1, 1, 9, 9, 1, 1, 4, 4, 4, 4, 1, 1, 4, 4, 4, 4, 1};
+        for (int i = 0; i < NBARS; ++i) mbar_init(&bars[i], counts[i]);
+        misc[1] = 0;
+        misc[4] = 0;
         mbar_fence_init();
         tma_prefetch_desc(&tma);
         tma_prefetch_desc(&tmb);
     }
+    if (warp == W_PROD) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 512;" ::"r"(sb + MISC_OFF)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
     __syncthreads();
-
-    Cursor cc = cursor_at(x0, P.req, P.B, X, P.mbps);
-    if (cc.b >= P.B) {  // uniform: every thread computed the same cursor
-        if (tid == 0) atomic_or_err(P.hdr, PA_DEV_ERR_STALE_PLAN);
-        return;
-    }
-    // ---- producer state (warp 0): issue cursor and a cache of 32 block ids
-    Cursor ci = cc;
-    int idc_b = -1, idc_w0 = 0, idc = 0;
-    auto issue = [&](int j) {  // warp 0 only
-        const int slot = j % NSLOT;
-        bool ok = false;
-        int blk = 0;
-        if (ci.b < P.B) {
-            if (ci.b != idc_b || ci.p < idc_w0 || ci.p >= idc_w0 + 32) {
-                idc_b = ci.b;
-                idc_w0 = ci.p;
-                const int pg = idc_w0 + lane;
-                idc = (pg < ci.Pb) ? P.block_table[(size_t)ci.b * P.mbps + pg] : 0;
-            }
-            blk = __shfl_sync(0xffffffffu, idc, ci.p - idc_w0);
-            ok = blk >= 1 && blk < P.num_blocks;
-        }
-        if (lane == 0) {
-            flags[2 + slot] = ok ? 0 : 1;
-            if (ok) {
-                const int kvh = ci.q / P.RBLK;
-                uint8_t *dst = smem + RING_OFF + slot * SLOT_BYTES;
-                mbar_arrive_expect_tx(&full[slot], PAGE_TX);
-#pragma unroll
-                for (int sg = 0; sg < 4; ++sg) tma_load_4d(dst + sg * BS * 128, &tma, &full[slot], sg * 128, 0, kvh, blk);
-                tma_load_4d(dst + 4 * BS * 128, &tmb, &full[slot], 512, 0, kvh, blk);
-                const uint8_t *src = P.k_pool + (size_t)blk * P.block_stride + P.codes_bytes + (size_t)kvh * BS * 4;
-                bulk_load(smem + TSRAW_OFF + slot * BS * 4, src, BS * 4, &full[slot]);
-            } else {
-                mbar_arrive(&full[slot]);  // no copy: the piece is NaN-filled
-            }
-        }
-        if (ci.b < P.B) cursor_next(ci, P.req, P.B, X, P.mbps);
-    };
-    if (warp == 0) {
-        for (int j = 0; j < min(NSLOT, npg); ++j) issue(j);
-    }
-
-    // ---- roles: QK warp (rows 16*mt.., tokens 32*th..), PV warp (rows 32*mr.., channels 128*dq..)
-    const int mt = warp & 3, th = warp >> 2;
-    const int mr = warp & 1, dq = warp >> 1;
-    const int ra = 16 * mt + g, rb = ra + 8;  // the thread's two score rows within the segment
-
-    float o[2][16][4];       // O rows 32mr + 16i + g (+8), channels 128dq + 8t + 2c (+1)
-    float m_a = -INFINITY, m_b = -INFINITY, l_a = 0.f, l_b = 0.f;
-    int vis_a = 0, vis_b = 0, L = 0, kvh = 0, rblk = 0;
-    int piece_b = -1, piece_q = -1, piece_p0 = 0, last_p = 0;
-    int E_run = 0;
-    bool pbad = false;
+    tc_fence_after();
+    const uint32_t tmem = (uint32_t)misc[0];
     uint32_t err = 0;
 
-    auto start_piece = [&]() {
-        piece_b = cc.b;
-        piece_q = cc.q;
-        piece_p0 = cc.p;
-        kvh = cc.q / P.RBLK;
-        rblk = cc.q % P.RBLK;
-        const int4 Rq = P.req[cc.b];
-        L = P.context_lens[cc.b];
-        pbad = false;
-        if (Rq.w != 0) { pbad = true; err |= PA_DEV_ERR_CONTEXT_LEN; }
-        if (L != Rq.x) { pbad = true; err |= PA_DEV_ERR_STALE_PLAN; }
-        const int r0 = rblk * LROWS;
-        auto vis_of = [&](int r) { return (r0 + r < P.R && P.causal) ? L - (P.n - 1 - (r0 + r) / P.G) : L; };
-        vis_a = vis_of(ra);
-        vis_b = vis_of(rb);
-        // q rows: 4 threads per row, 18 chunks of 8 channels each
-        const int qr = tid >> 2, part = tid & 3;
-        const int r = r0 + qr;
-        const bool rok = r < P.R;
-        size_t qbase = 0;
-        if (rok) {
-            const int jq = r / P.G, h = kvh * P.G + r % P.G;
-            qbase = (((size_t)cc.b * P.n + jq) * P.Hq + h) * DK;
-        }
-        float mx = 0.f;
-        if (rok) {
-#pragma unroll 1
-            for (int k = 0; k < 18; ++k) {
-                const int ch = part + 4 * k;
-#pragma unroll
-                for (int e = 0; e < 8; ++e) mx = fmaxf(mx, fabsf(load_qv(P, qbase + ch * 8 + e)));
-            }
-        }
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-        float rho = 1.f;
-        if (mx > 0.f && mx < 3.0e38f) {
-            int e;
-            frexpf(mx, &e);
-            rho = ldexpf(1.0f, e);
-        }
-        const float inv = 1.0f / rho;
-#pragma unroll 1
-        for (int k = 0; k < 18; ++k) {
-            const int ch = part + 4 * k;
-            uint32_t w[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                float u0 = 0.f, u1 = 0.f;
-                if (rok) {
-                    u0 = load_qv(P, qbase + ch * 8 + 2 * e) * inv;
-                    u1 = load_qv(P, qbase + ch * 8 + 2 * e + 1) * inv;
+    if (warp == W_PROD) {
+        // ================================================== producer
+        Cursor ci = c0;
+        int idc_b = -1, idc_w0 = 0, idc = 0, issued = 0;
+        for (int j = 0; j < npg; ++j) {
+            const int slot = j % NSLOT;
+            if (j >= NSLOT && !warp_wait(&bars[B_SLOTFREE + slot], ((j / NSLOT) - 1) & 1, abort, err)) break;
+            bool ok = false;
+            int blk = 0;
+            if (ci.b < P.B) {
+                if (ci.b != idc_b || ci.p < idc_w0 || ci.p >= idc_w0 + 32) {
+                    idc_b = ci.b;
+                    idc_w0 = ci.p;
+                    const int pg = idc_w0 + lane;
+                    idc = (pg < ci.Pb) ? P.block_table[(size_t)ci.b * P.mbps + pg] : 0;
                 }
-                w[e] = pack_f16x2(u0, u1);
+                blk = __shfl_sync(0xffffffffu, idc, ci.p - idc_w0);
+                ok = blk >= 1 && blk < P.num_blocks;
             }
-            *reinterpret_cast<uint4 *>(smem + QS_OFF + sw_off(qr, ch)) = make_uint4(w[0], w[1], w[2], w[3]);
+            if (lane == 0) {
+                misc[2 + slot] = ok ? 0 : 1;
+                uint64_t *bar = &bars[B_FULL + slot];
+                if (ok) {
+                    const int kvh = ci.q;
+                    uint8_t *dst = smem + RING_OFF + slot * SLOT_BYTES;
+                    mbar_arrive_expect_tx(bar, PAGE_TX);
+#pragma unroll
+                    for (int sg = 0; sg < 4; ++sg) tma_load_4d(dst + sg * BS * 128, &tma, bar, sg * 128, 0, kvh, blk);
+                    tma_load_4d(dst + 4 * BS * 128, &tmb, bar, 512, 0, kvh, blk);
+                    const uint8_t *src = P.k_pool + (size_t)blk * P.block_stride + P.codes_bytes + (size_t)kvh * BS * 4;
+                    bulk_load(smem + TSRAW_OFF + slot * BS * 4, src, BS * 4, bar);
+                } else {
+                    mbar_arrive(bar);  // no copy: the piece is NaN-filled
+                }
+            }
+            __syncwarp();
+            ++issued;
+            if (ci.b < P.B) cursor_next(ci, P.req, P.B, U, P.mbps);
         }
-        if (part == 0) rowsc[qr] = rok ? P.softmax_scale * rho * LOG2E : 0.f;
+        if (*abort && lane == 0) {
+            // let every copy still in flight land before the CTA exits
+            for (int i = max(0, issued - NSLOT); i < issued; ++i)
+                (void)mbar_wait_bounded(&bars[B_FULL + i % NSLOT], (i / NSLOT) & 1, nullptr);
+        }
+        __syncwarp();
+    } else if (warp == W_MMA) {
+        // ================================================== MMA issue
+        constexpr uint32_t ID_QK = idesc(64, 64, 0), ID_PV = idesc(128, 64, 1);
+        Cursor cq = c0, cp = c0;
+        int q_piece = -1, q_pb = -1, q_pq = -1;  // pieces seen by the S stream
+        int p_piece = -1, p_pb = -1, p_pq = -1;  // pieces seen by the O stream
+        auto issue_s = [&](int j) -> bool {
+            if (cq.b >= P.B) { err |= PA_DEV_ERR_STALE_PLAN; return false; }
+            const int slot = j % NSLOT, sbuf = j & 1;
+            if (cq.b != q_pb || cq.q != q_pq) {
+                ++q_piece;
+                q_pb = cq.b;
+                q_pq = cq.q;
+                if (!warp_wait(&bars[B_QFULL], q_piece & 1, abort, err)) return false;
+            }
+            if (!warp_wait(&bars[B_FULL + slot], (j / NSLOT) & 1, abort, err)) return false;
+            if (j >= 2 && !warp_wait(&bars[B_SFREE + sbuf], ((j >> 1) - 1) & 1, abort, err)) return false;
+            tc_fence_after();
+            if (lane == 0) {
+                const uint32_t ring = sb + RING_OFF + slot * SLOT_BYTES;
+                const uint32_t dS = tmem + TM_S + 64u * sbuf;
+                uint32_t acc = 0;
 #pragma unroll
-        for (int i = 0; i < 2; ++i)
+                for (int cb = 0; cb < 5; ++cb) {
+                    const uint32_t swz = cb < 4 ? 2u : 4u, sbo = cb < 4 ? 1024u : 512u;
+                    const uint32_t boff = (uint32_t)cb * (64 * 128);
 #pragma unroll
-            for (int t = 0; t < 16; ++t) o[i][t][0] = o[i][t][1] = o[i][t][2] = o[i][t][3] = 0.f;
-        m_a = m_b = -INFINITY;
-        l_a = l_b = 0.f;
-        E_run = 0;
-    };
-
-    auto finish_piece = [&]() {
-        __syncthreads();  // every warp is past its last P.V (alpha is reused below)
-        float la = l_a, lb = l_b;
-        la += __shfl_xor_sync(0xffffffffu, la, 1);
-        la += __shfl_xor_sync(0xffffffffu, la, 2);
-        lb += __shfl_xor_sync(0xffffffffu, lb, 1);
-        lb += __shfl_xor_sync(0xffffffffu, lb, 2);
-        if (c == 0) {
-            lpart[th * LROWS + ra] = la;
-            lpart[th * LROWS + rb] = lb;
-            if (th == 0) {
-                mrow[ra] = m_a;
-                mrow[rb] = m_b;
+                    for (int ks = 0; ks < (cb < 4 ? 4 : 2); ++ks) {
+                        const uint64_t bdesc = sdesc(ring + boff + 32 * ks, 16, sbo, swz);
+                        mma_f8(dS, sdesc(sb + QH_OFF + boff + 32 * ks, 16, sbo, swz), bdesc, ID_QK, acc);
+                        acc = 1;
+                        mma_f8(dS, sdesc(sb + QL_OFF + boff + 32 * ks, 16, sbo, swz), bdesc, ID_QK, 1);
+                    }
+                }
+                mma_commit(&bars[B_SFULL + sbuf]);
+                mma_commit(&bars[B_SLOTFREE + slot]);
+            }
+            __syncwarp();
+            cursor_next(cq, P.req, P.B, U, P.mbps);
+            return true;
+        };
+        auto issue_o = [&](int j) -> bool {
+            const int pbuf = j & 1;
+            bool first = false;
+            if (cp.b != p_pb || cp.q != p_pq) {
+                ++p_piece;
+                p_pb = cp.b;
+                p_pq = cp.q;
+                first = true;
+                if (p_piece > 0 && !warp_wait(&bars[B_OFREE], (p_piece - 1) & 1, abort, err)) return false;
+            }
+            if (!warp_wait(&bars[B_PFULL + pbuf], (j >> 1) & 1, abort, err)) return false;
+            if (!warp_wait(&bars[B_VFULL], j & 1, abort, err)) return false;
+            tc_fence_after();
+            if (lane == 0) {
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const uint32_t dO = tmem + TM_O + 64u * i;
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const uint64_t adesc = sdesc(sb + V_OFF + (2 * i) * (64 * 128) + 2048 * k, 8192, 1024, 2);
+                        const uint64_t bdesc = sdesc(sb + P_OFF + pbuf * 8192 + 32 * k, 16, 1024, 2);
+                        mma_f16(dO, adesc, bdesc, ID_PV, (first && k == 0) ? 0u : 1u);
+                    }
+                }
+                mma_commit(&bars[B_PVDONE + pbuf]);
+            }
+            __syncwarp();
+            cursor_next(cp, P.req, P.B, U, P.mbps);
+            return true;
+        };
+        if (issue_s(0)) {
+            for (int j = 0; j < npg; ++j) {
+                if (j + 1 < npg && !issue_s(j + 1)) break;
+                if (!issue_o(j)) break;
             }
         }
-        __syncthreads();
-        const int Pb = planned_pages(P.req, piece_b, P.mbps);
-        const bool complete = (piece_p0 == 0 && last_p == Pb - 1);
-        const long long slot_id = (long long)piece_b * X + piece_q + kw;
-        const int r0 = rblk * LROWS;
+        // every MMA issued so far is complete before tensor memory is released
+        if (lane == 0) {
+            mma_commit(&bars[B_MDONE]);
+            (void)mbar_wait_bounded(&bars[B_MDONE], 0, nullptr);
+        }
+        __syncwarp();
+    } else if (warp >= W_SM && warp < W_SM + 4) {
+        // ================================================== softmax, q staging, epilogue
+        const int qd = warp & 3;                 // tensor-memory lane quarter
+        const bool owner = lane < 16;            // lanes whose TMEM lane holds the row of S
+        const int half = lane >> 4;              // tokens 32 * half .. of the row
+        const int row = 16 * qd + (lane & 15);   // this lane's row
+        const uint32_t tl = tmem + ((uint32_t)(32 * qd) << 16);
+        Cursor cs = c0;
+        int piece = -1, pb = -1, pq = -1, p0 = 0, last_p = 0, kvh = 0, rblk = 0, L = 0;
+        int wg_phase = 0;
+        float m = -INFINITY, lsum = 0.f, rowsc = 0.f;
+        int vis = 0, E_run = 0;
+        bool E_set = false, pbad = false;
         const float NaN = __int_as_float(0x7fc00000);
-        const float escale = pow2f(E_run);
+
+        // q' of segment (cs.b, kvh_n, rblk_n): row `row`, channel half (lane >> 4)
+        auto stage_q = [&](int kvh_n, int rblk_n) -> float {
+            const int r = rblk_n * LROWS + row;
+            const bool rok = r < P.R;
+            size_t qbase = 0;
+            if (rok) {
+                const int jq = r / P.G, h = kvh_n * P.G + r % P.G;
+                qbase = (((size_t)cs.b * P.n + jq) * P.Hq + h) * DK;
+            }
+            const uint8_t *qrow = P.q + 2 * qbase;
+            float mx = 0.f;
+            if (rok) {
+#pragma unroll 1
+                for (int c = 18 * half; c < 18 * half + 18; ++c) {
+                    const uint4 v = *reinterpret_cast<const uint4 *>(qrow + 32 * c);
+                    const uint4 w = *reinterpret_cast<const uint4 *>(qrow + 32 * c + 16);
+                    const uint32_t u[8] = {v.x, v.y, v.z, v.w, w.x, w.y, w.z, w.w};
 #pragma unroll
-        for (int i = 0; i < 2; ++i) {
-#pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
-                const int row = 32 * mr + 16 * i + g + 8 * hh;
-                const int r = r0 + row;
-                if (r >= P.R) continue;
-                const float l = lpart[row] + lpart[LROWS + row];
-                const float m = mrow[row];
-                const float f = l > 0.f ? escale / l : 0.f;
-                const int jq = r / P.G, h = kvh * P.G + r % P.G;
-                const size_t obase = (((size_t)piece_b * P.n + jq) * P.Hq + h) * DV;
-#pragma unroll
-                for (int t = 0; t < 16; ++t) {
-                    const int d = 128 * dq + 8 * t + 2 * c;
-                    float v0 = o[i][t][2 * hh] * f, v1 = o[i][t][2 * hh + 1] * f;
-                    if (pbad) v0 = v1 = NaN;
-                    if (complete) {
-                        if (P.out_dtype == PA_F32) {
-                            *reinterpret_cast<float2 *>(reinterpret_cast<float *>(P.out) + obase + d) = make_float2(v0, v1);
-                        } else if (P.out_dtype == PA_F16) {
-                            *reinterpret_cast<uint32_t *>(reinterpret_cast<__half *>(P.out) + obase + d) = pack_f16x2(v0, v1);
-                        } else {
-                            *reinterpret_cast<uint32_t *>(reinterpret_cast<__nv_bfloat16 *>(P.out) + obase + d) =
-                                pack_bf16x2(v0, v1);
-                        }
-                    } else {
-                        *reinterpret_cast<float2 *>(P.part_o + ((size_t)slot_id * LROWS + row) * DV + d) = make_float2(v0, v1);
-                    }
-                }
-                if (dq == 0 && c == 0) {
-                    float lse_v = l > 0.f ? (m + lg2(l)) * LN2 : -INFINITY;
-                    if (pbad) lse_v = NaN;
-                    if (complete) {
-                        if (P.lse != nullptr) P.lse[((size_t)piece_b * P.n + jq) * P.Hq + h] = lse_v;
-                    } else {
-                        P.part_lse[(size_t)slot_id * LROWS + row] = lse_v;
+                    for (int e = 0; e < 8; ++e) {
+                        const float2 f = q_pair(u[e], P.q_dtype);
+                        mx = fmaxf(mx, fmaxf(fabsf(f.x), fabsf(f.y)));
                     }
                 }
             }
-        }
-    };
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+            // q * 2^s has its largest magnitude in [128, 256): both E4M3 terms stay finite
+            int ex = 0;
+            const bool fin = mx > 0.f && mx < 3.0e38f;
+            if (fin) frexpf(mx, &ex);
+            const int s = fin ? 8 - ex : 0;
+            const float up = pow2f(s);
+#pragma unroll 1
+            for (int c = 18 * half; c < 18 * half + 18; ++c) {
+                uint32_t hw[4] = {0u, 0u, 0u, 0u}, lw[4] = {0u, 0u, 0u, 0u};
+                if (rok) {
+                    const uint4 v = *reinterpret_cast<const uint4 *>(qrow + 32 * c);
+                    const uint4 w = *reinterpret_cast<const uint4 *>(qrow + 32 * c + 16);
+                    const uint32_t u[8] = {v.x, v.y, v.z, v.w, w.x, w.y, w.z, w.w};
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        const float2 f = q_pair(u[e], P.q_dtype);
+                        const float a = f.x * up, b = f.y * up;
+                        const uint32_t h2 = f32x2_e4m3x2(a, b);
+                        const float2 hf = e4m3x2_f32x2(h2);
+                        const uint32_t l2 = f32x2_e4m3x2(a - hf.x, b - hf.y);
+                        hw[e >> 1] |= h2 << (16 * (e & 1));
+                        lw[e >> 1] |= l2 << (16 * (e & 1));
+                    }
+                }
+                *reinterpret_cast<uint4 *>(smem + QH_OFF + e4_off(row, c)) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+                *reinterpret_cast<uint4 *>(smem + QL_OFF + e4_off(row, c)) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+            }
+            return rok ? P.softmax_scale * LOG2E * pow2f(-s) : 0.f;
+        };
 
-    int j = 0;
-    for (; j < npg; ++j) {
-        if (cc.b >= P.B) {  // records shorter than the shares (uniform)
-            err |= PA_DEV_ERR_STALE_PLAN;
-            break;
-        }
-        if (cc.b != piece_b || cc.q != piece_q) {
-            if (piece_b >= 0) finish_piece();
-            start_piece();
-        }
-        const int slot = j % NSLOT;
-        // ---- wait for the page (one thread waits; the outcome is shared)
-        if (tid == 0) flags[0] = mbar_wait_bounded(&full[slot], (j / NSLOT) & 1, nullptr) ? 1 : 0;
-        __syncthreads();
-        if (!flags[0]) {
-            err |= PA_DEV_ERR_TIMEOUT;
-            pbad = true;
-            break;
-        }
-        (void)mbar_try_wait(&full[slot], (j / NSLOT) & 1);  // acquire the copies' writes in every thread
-        if (flags[2 + slot]) {
-            err |= PA_DEV_ERR_BLOCK_ID;
-            pbad = true;
-        }
-        const int nvalid = min(BS, L - cc.p * BS);  // real tokens of this page
-        const uint8_t *pg8 = smem + RING_OFF + slot * SLOT_BYTES;
-        // ---- token scales: zero past L_b, normalised by the page's largest power of two
-        if (warp == 0) {
-            const float s0 = lane < nvalid ? tsraw[slot * BS + lane] : 0.f;
-            const float s1 = lane + 32 < nvalid ? tsraw[slot * BS + lane + 32] : 0.f;
-            float mx = fmaxf(fabsf(s0), fabsf(s1));
-#pragma unroll
-            for (int off = 16; off >= 1; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-            int E = E_run;
-            if (mx > 0.f && mx < 3.0e38f) {
-                frexpf(mx, &E);
-                E = min(max(E, -120), 120);
+        // read O^T of the finished piece (last page jl), normalise, write out / partial
+        auto epilogue = [&](int jl) -> bool {
+            const int Pb = planned_pages(P.req, pb, P.mbps);
+            const bool complete = (p0 == 0 && last_p == Pb - 1);
+            const long long slot_id = ((long long)pb * U + pq + kg) * GS + rb;
+            const int r0 = rblk * LROWS;
+            const float lrow = lsum + __shfl_xor_sync(0xffffffffu, lsum, 16);
+            if (owner) {
+                const bool lok = lrow > 0.f;
+                stat_f[row] = pbad ? NaN : (lok ? pow2f(E_run) / lrow : 0.f);
+                float lse_v = lok ? (m + lg2(lrow)) * LN2 : -INFINITY;
+                if (pbad) lse_v = NaN;
+                stat_lse[row] = lse_v;
             }
-            const float ne = pow2f(-E);
-            tsn[lane] = s0 * ne;
-            tsn[lane + 32] = s1 * ne;
-            if (lane == 0) flags[1] = E;
-        }
-        // ---- dequantize the codes into the f16 tile (zero rows past L_b)
-#pragma unroll 3
-        for (int it = 0; it < 9; ++it) {
-            const int item = it * THREADS + tid;  // 64 tokens x 36 chunks of 16 codes
-            const int t = item / 36, c16 = item % 36;
-            uint4 v = make_uint4(0u, 0u, 0u, 0u);
-            if (t < nvalid) {
-                const uint8_t *src;
-                if (c16 < 32) src = pg8 + (c16 >> 3) * (BS * 128) + t * 128 + (((c16 & 7) ^ (t & 7)) << 4);
-                else src = pg8 + 4 * BS * 128 + t * 64 + ((((c16 - 32) & 3) ^ ((t >> 1) & 3)) << 4);
-                v = *reinterpret_cast<const uint4 *>(src);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars[B_WG]);
+            if (!warp_wait(&bars[B_WG], wg_phase & 1, abort, err)) return false;
+            ++wg_phase;
+            if (!warp_wait(&bars[B_PVDONE + (jl & 1)], (jl >> 1) & 1, abort, err)) return false;
+            tc_fence_after();
+            if (owner && r0 + row < P.R) {
+                const int r = r0 + row, jq = r / P.G, h = kvh * P.G + r % P.G;
+                if (complete) {
+                    if (P.lse != nullptr) P.lse[((size_t)pb * P.n + jq) * P.Hq + h] = stat_lse[row];
+                } else {
+                    P.part_lse[(size_t)slot_id * LROWS + row] = stat_lse[row];
+                }
             }
-            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-            uint32_t h[8];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                h[2 * e] = e4m3x2_f16x2(w[e]);
-                h[2 * e + 1] = e4m3x2_f16x2(w[e] >> 16);
-            }
-            *reinterpret_cast<uint4 *>(smem + KS_OFF + sw_off(t, 2 * c16)) = make_uint4(h[0], h[1], h[2], h[3]);
-            *reinterpret_cast<uint4 *>(smem + KS_OFF + sw_off(t, 2 * c16 + 1)) = make_uint4(h[4], h[5], h[6], h[7]);
-        }
-        __syncthreads();  // f16 tile, scales and E ready; the ring slot is free
-        const int E_page = flags[1];
-        if (warp == 0) {
-            fence_proxy_async_smem();
-            if (j + NSLOT < npg) issue(j + NSLOT);
-        }
-
-        // ---- S = q' K^T: rows 16mt.., tokens 32th..
-        float s[4][4];
-#pragma unroll
-        for (int t = 0; t < 4; ++t) s[t][0] = s[t][1] = s[t][2] = s[t][3] = 0.f;
-        {
-            const int arow = 16 * mt + (lane & 15);
-            const int brow0 = 32 * th + (lane & 7) + 8 * (lane >> 4);
+#pragma unroll 1
+            for (int i = 0; i < 4; ++i) {
+                const int d = 128 * i + 32 * qd + lane;
+#pragma unroll 1
+                for (int half = 0; half < 2; ++half) {
+                    float o[32];
+                    tmem_ld32(tl + TM_O + 64u * i + 32u * half, o);
 #pragma unroll 4
-            for (int kst = 0; kst < DK / 16; ++kst) {
-                uint32_t a[4], b0[4], b1[4];
-                ldsm_x4(a, qs + sw_off(arow, 2 * kst + (lane >> 4)));
-                ldsm_x4(b0, ks + sw_off(brow0, 2 * kst + ((lane >> 3) & 1)));
-                ldsm_x4(b1, ks + sw_off(brow0 + 16, 2 * kst + ((lane >> 3) & 1)));
-                mma16816<false>(s[0], a, b0[0], b0[1]);
-                mma16816<false>(s[1], a, b0[2], b0[3]);
-                mma16816<false>(s[2], a, b1[0], b1[1]);
-                mma16816<false>(s[3], a, b1[2], b1[3]);
-            }
-        }
-        // ---- scale, mask, row maxima
-        const float fe = pow2f(E_page);
-        const float fa = rowsc[ra] * fe, fb = rowsc[rb] * fe;
-        const int tpage = cc.p * BS;
-        float mxa = -INFINITY, mxb = -INFINITY;
-#pragma unroll
-        for (int t = 0; t < 4; ++t) {
-            const int tl = 32 * th + 8 * t + 2 * c;
-            const float2 sn = *reinterpret_cast<const float2 *>(tsn + tl);
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-                const float sne = e ? sn.y : sn.x;
-                float xa = s[t][e] * fa * sne, xb = s[t][2 + e] * fb * sne;
-                xa = (tpage + tl + e < vis_a) ? xa : -INFINITY;
-                xb = (tpage + tl + e < vis_b) ? xb : -INFINITY;
-                s[t][e] = xa;
-                s[t][2 + e] = xb;
-                mxa = fmaxf(mxa, xa);
-                mxb = fmaxf(mxb, xb);
-            }
-        }
-        mxa = fmaxf(mxa, __shfl_xor_sync(0xffffffffu, mxa, 1));
-        mxa = fmaxf(mxa, __shfl_xor_sync(0xffffffffu, mxa, 2));
-        mxb = fmaxf(mxb, __shfl_xor_sync(0xffffffffu, mxb, 1));
-        mxb = fmaxf(mxb, __shfl_xor_sync(0xffffffffu, mxb, 2));
-        if (c == 0) {
-            rmax[th * LROWS + ra] = mxa;
-            rmax[th * LROWS + rb] = mxb;
-        }
-        named_barrier(1 + mt, 64);  // the two warps of row tile mt
-        mxa = fmaxf(mxa, rmax[(1 - th) * LROWS + ra]);
-        mxb = fmaxf(mxb, rmax[(1 - th) * LROWS + rb]);
-        const float mna = fmaxf(m_a, mxa), mnb = fmaxf(m_b, mxb);
-        const float basea = (mna == -INFINITY) ? 0.f : mna;
-        const float baseb = (mnb == -INFINITY) ? 0.f : mnb;
-        const float ala = ex2(m_a - basea), alb = ex2(m_b - baseb);
-        m_a = mna;
-        m_b = mnb;
-        float psa = 0.f, psb = 0.f;
-#pragma unroll
-        for (int t = 0; t < 4; ++t) {
-            const int tl = 32 * th + 8 * t + 2 * c;
-            const float2 sn = *reinterpret_cast<const float2 *>(tsn + tl);
-            const float pa0 = ex2(s[t][0] - basea), pa1 = ex2(s[t][1] - basea);
-            const float pb0 = ex2(s[t][2] - baseb), pb1 = ex2(s[t][3] - baseb);
-            psa += pa0 + pa1;
-            psb += pb0 + pb1;
-            const int chunk = 4 * th + t;  // tokens 8*chunk .. 8*chunk+7
-            *reinterpret_cast<uint32_t *>(smem + PS_OFF + ra * 128 + ((chunk ^ (ra & 7)) << 4) + 4 * c) =
-                pack_f16x2(pa0 * sn.x, pa1 * sn.y);
-            *reinterpret_cast<uint32_t *>(smem + PS_OFF + rb * 128 + ((chunk ^ (rb & 7)) << 4) + 4 * c) =
-                pack_f16x2(pb0 * sn.x, pb1 * sn.y);
-        }
-        l_a = l_a * ala + psa;
-        l_b = l_b * alb + psb;
-        if (th == 0 && c == 0) {
-            const float fE = pow2f(E_run - E_page);
-            alpha[ra] = ala * fE;
-            alpha[rb] = alb * fE;
-        }
-        E_run = E_page;
-        __syncthreads();  // P', alpha ready
-
-        // ---- O = alpha O + P' V: rows 32mr.., channels 128dq..
-        {
-            float al[2][2];
-#pragma unroll
-            for (int i = 0; i < 2; ++i)
-#pragma unroll
-                for (int hh = 0; hh < 2; ++hh) al[i][hh] = alpha[32 * mr + 16 * i + g + 8 * hh];
-            if (__any_sync(0xffffffffu, al[0][0] != 1.f || al[0][1] != 1.f || al[1][0] != 1.f || al[1][1] != 1.f)) {
-#pragma unroll
-                for (int i = 0; i < 2; ++i)
-#pragma unroll
-                    for (int t = 0; t < 16; ++t) {
-                        o[i][t][0] *= al[i][0];
-                        o[i][t][1] *= al[i][0];
-                        o[i][t][2] *= al[i][1];
-                        o[i][t][3] *= al[i][1];
+                    for (int k = 0; k < 32; ++k) {
+                        const int rr = 32 * half + k;
+                        const int r = r0 + rr;
+                        if (r >= P.R) break;
+                        const float y = o[k] * stat_f[rr];
+                        if (complete) {
+                            const int jq = r / P.G, h = kvh * P.G + r % P.G;
+                            const size_t oi = (((size_t)pb * P.n + jq) * P.Hq + h) * DV + d;
+                            if (P.out_dtype == PA_F32) reinterpret_cast<float *>(P.out)[oi] = y;
+                            else if (P.out_dtype == PA_F16) reinterpret_cast<__half *>(P.out)[oi] = __float2half_rn(y);
+                            else reinterpret_cast<__nv_bfloat16 *>(P.out)[oi] = __float2bfloat16_rn(y);
+                        } else {
+                            P.part_o[((size_t)slot_id * LROWS + rr) * DV + d] = y;
+                        }
                     }
-            }
-            const int prow = 32 * mr + (lane & 15);
-            const int vtok = (lane & 7) + 8 * ((lane >> 3) & 1);
-#pragma unroll
-            for (int kst = 0; kst < BS / 16; ++kst) {
-                uint32_t a0[4], a1[4];
-                ldsm_x4(a0, ps + prow * 128 + (((2 * kst + (lane >> 4)) ^ (prow & 7)) << 4));
-                ldsm_x4(a1, ps + (prow + 16) * 128 + (((2 * kst + (lane >> 4)) ^ ((prow + 16) & 7)) << 4));
-                const int tok = 16 * kst + vtok;
-#pragma unroll
-                for (int pr = 0; pr < 8; ++pr) {
-                    uint32_t b[4];
-                    ldsm_x4_t(b, ks + sw_off(tok, 16 * dq + 2 * pr + (lane >> 4)));
-                    mma16816<false>(o[0][2 * pr], a0, b[0], b[1]);
-                    mma16816<false>(o[1][2 * pr], a1, b[0], b[1]);
-                    mma16816<false>(o[0][2 * pr + 1], a0, b[2], b[3]);
-                    mma16816<false>(o[1][2 * pr + 1], a1, b[2], b[3]);
                 }
             }
+            tc_fence_before();
+            warp_arrive(&bars[B_OFREE]);
+            return true;
+        };
+
+        bool alive = true;
+        int j = 0;
+        for (; j < npg; ++j) {
+            if (cs.b >= P.B) { err |= PA_DEV_ERR_STALE_PLAN; alive = false; break; }
+            const int slot = j % NSLOT, sbuf = j & 1;
+            const bool first = (cs.b != pb || cs.q != pq);
+            if (first) {
+                // stage q' of the new piece first (its S MMAs wait for it), then
+                // finish the previous piece (whose last O MMAs are already queued)
+                const float rowsc_new = stage_q(cs.q, rb);
+                fence_proxy_async_smem();
+                warp_arrive(&bars[B_QFULL]);
+                if (piece >= 0 && !epilogue(j - 1)) { alive = false; break; }
+                ++piece;
+                pb = cs.b;
+                pq = cs.q;
+                p0 = cs.p;
+                kvh = cs.q;
+                rblk = rb;
+                const int4 Rq = P.req[cs.b];
+                L = P.context_lens[cs.b];
+                pbad = false;
+                if (Rq.w != 0) { pbad = true; err |= PA_DEV_ERR_CONTEXT_LEN; }
+                if (L != Rq.x) { pbad = true; err |= PA_DEV_ERR_STALE_PLAN; }
+                const int r = rblk * LROWS + row;
+                vis = (r < P.R && P.causal) ? L - (P.n - 1 - r / P.G) : L;
+                rowsc = rowsc_new;
+                m = -INFINITY;
+                lsum = 0.f;
+                E_set = false;
+            }
+            // ---- scores of page j: lane l < 16 takes tokens 0..31 of row 16qd + l,
+            // lane l + 16 tokens 32..63 of the same row
+            if (!warp_wait(&bars[B_SFULL + sbuf], (j >> 1) & 1, abort, err)) { alive = false; break; }
+            if (!warp_wait(&bars[B_FULL + slot], (j / NSLOT) & 1, abort, err)) { alive = false; break; }
+            tc_fence_after();
+            float x[32];
+            {
+                float xa[32], xb[32];
+                tmem_ld32(tl + TM_S + 64u * sbuf, xa);
+                tmem_ld32(tl + TM_S + 64u * sbuf + 32u, xb);
+                tc_fence_before();
+                warp_arrive(&bars[B_SFREE + sbuf]);
+#pragma unroll
+                for (int k = 0; k < 32; ++k) {
+                    const float up = __shfl_up_sync(0xffffffffu, xb[k], 16);
+                    x[k] = half ? up : xa[k];
+                }
+            }
+            if (misc[2 + slot]) { pbad = true; err |= PA_DEV_ERR_BLOCK_ID; }
+            const int nvalid = min(BS, max(0, L - cs.p * BS));
+            float ts[32];
+            {
+                const float4 *tq = reinterpret_cast<const float4 *>(tsraw + slot * BS + 32 * half);
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    const float4 v = tq[k];
+                    ts[4 * k] = v.x; ts[4 * k + 1] = v.y; ts[4 * k + 2] = v.z; ts[4 * k + 3] = v.w;
+                }
+            }
+            warp_arrive(&bars[B_SLOTFREE + slot]);  // the ring slot is no longer read here
+            const int t0 = 32 * half;
+            float sm4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int k = 0; k < 32; ++k) {
+                ts[k] = (t0 + k < nvalid) ? ts[k] : 0.f;
+                sm4[k & 3] = fmaxf(sm4[k & 3], fabsf(ts[k]));
+            }
+            // the page's scale exponent (the same in every thread)
+            float smax = fmaxf(fmaxf(sm4[0], sm4[1]), fmaxf(sm4[2], sm4[3]));
+            smax = fmaxf(smax, __shfl_xor_sync(0xffffffffu, smax, 16));
+            float aE = 1.f;
+            if (smax > 0.f && smax < 3.0e38f) {
+                int e;
+                frexpf(smax, &e);
+                e = min(max(e, -120), 120);
+                if (!E_set) {
+                    E_run = e;
+                    E_set = true;
+                } else if (e > E_run + 4 || e < E_run - 8) {
+                    aE = pow2f(E_run - e);
+                    E_run = e;
+                }
+            }
+            const float nE = pow2f(-E_run);
+            const int tv = vis - cs.p * BS - t0;  // tokens of this half that are visible: k < tv
+            float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+            for (int k = 0; k < 32; ++k) {
+                x[k] = (k < tv) ? x[k] * rowsc * ts[k] : -INFINITY;
+                mx4[k & 3] = fmaxf(mx4[k & 3], x[k]);
+            }
+            float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+            // alm rescales the row sum (p carries no token scale); O^T also takes aE
+            float alm = 1.f;
+            if (mx > m + ROW_SLACK) {  // also true for m = -inf and a finite maximum
+                if (m != -INFINITY) alm = ex2(m - mx);
+                m = mx;
+            }
+            const float base = (m == -INFINITY) ? 0.f : m;
+            float al = alm * aE;
+            if (first) al = 1.f;  // O^T is overwritten by the piece's first P.V
+            const bool resc = (al != 1.f);
+            float ps4[4] = {0.f, 0.f, 0.f, 0.f};
+            uint32_t pw[16];
+#pragma unroll
+            for (int k = 0; k < 32; k += 2) {
+                const float a = ex2(x[k] - base), b = ex2(x[k + 1] - base);
+                ps4[(k >> 1) & 3] += a + b;
+                pw[k >> 1] = pack_f16x2(a * ts[k] * nE, b * ts[k + 1] * nE);
+            }
+            lsum = lsum * alm + ((ps4[0] + ps4[1]) + (ps4[2] + ps4[3]));  // this half's share of the row sum
+            // P'(j) goes into buffer sbuf: the O MMAs of page j-2 must be done with it
+            if (j >= 2 && !warp_wait(&bars[B_PVDONE + sbuf], ((j >> 1) - 1) & 1, abort, err)) { alive = false; break; }
+            {
+                uint8_t *prow = smem + P_OFF + sbuf * 8192 + row * 128;
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+                    *reinterpret_cast<uint4 *>(prow + (((4 * half + c) ^ (row & 7)) << 4)) =
+                        make_uint4(pw[4 * c], pw[4 * c + 1], pw[4 * c + 2], pw[4 * c + 3]);
+                if (owner) alpha[sbuf * 64 + row] = al;
+            }
+            const int vote = __any_sync(0xffffffffu, resc) ? 1 : 0;
+            if (lane == 0) need[sbuf * 4 + qd] = vote;
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars[B_WG]);
+            if (!warp_wait(&bars[B_WG], wg_phase & 1, abort, err)) { alive = false; break; }
+            ++wg_phase;
+            if (need[sbuf * 4] | need[sbuf * 4 + 1] | need[sbuf * 4 + 2] | need[sbuf * 4 + 3]) {
+                // rescale the O^T columns (query rows) of this lane quarter once page j-1's O is in
+                if (!warp_wait(&bars[B_PVDONE + (sbuf ^ 1)], ((j - 1) >> 1) & 1, abort, err)) { alive = false; break; }
+                tc_fence_after();
+#pragma unroll 1
+                for (int i = 0; i < 4; ++i) {
+#pragma unroll 1
+                    for (int half = 0; half < 2; ++half) {
+                        float o[32];
+                        const uint32_t ta = tl + TM_O + 64u * i + 32u * half;
+                        tmem_ld32(ta, o);
+#pragma unroll
+                        for (int k = 0; k < 32; ++k) o[k] *= alpha[sbuf * 64 + 32 * half + k];
+                        tmem_st32(ta, o);
+                    }
+                }
+                tc_fence_before();
+            }
+            warp_arrive(&bars[B_PFULL + sbuf]);
+            last_p = cs.p;
+            cursor_next(cs, P.req, P.B, U, P.mbps);
         }
-        last_p = cc.p;
-        cursor_next(cc, P.req, P.B, X, P.mbps);
+        if (alive && piece >= 0) (void)epilogue(npg - 1);
+    } else {
+        // ================================================== V dequant
+        const int dt = tid - 32 * W_DQ;  // 0..127
+        Cursor cd = c0;
+        int pb = -1, pq = -1, L = 0;
+        for (int j = 0; j < npg; ++j) {
+            if (cd.b >= P.B) break;
+            const int slot = j % NSLOT;
+            if (cd.b != pb || cd.q != pq) {
+                pb = cd.b;
+                pq = cd.q;
+                L = P.context_lens[cd.b];
+            }
+            if (!warp_wait(&bars[B_FULL + slot], (j / NSLOT) & 1, abort, err)) break;
+            const int nvalid = min(BS, max(0, L - cd.p * BS));
+            const uint8_t *pg8 = smem + RING_OFF + slot * SLOT_BYTES;
+            // the codes go to registers first, so the ring slot is released at once
+            uint4 cv[16];
+#pragma unroll
+            for (int it = 0; it < 16; ++it) {
+                const int item = it * 128 + dt;  // 64 tokens x 32 chunks of 16 channels
+                const int t = item >> 5, c16 = item & 31;
+                cv[it] = (t < nvalid) ? *reinterpret_cast<const uint4 *>(pg8 + e4_off(t, c16)) : make_uint4(0u, 0u, 0u, 0u);
+            }
+            warp_arrive(&bars[B_SLOTFREE + slot]);
+            if (j >= 1 && !warp_wait(&bars[B_PVDONE + ((j - 1) & 1)], ((j - 1) >> 1) & 1, abort, err)) break;
+#pragma unroll
+            for (int it = 0; it < 16; ++it) {
+                const int item = it * 128 + dt;
+                const int t = item >> 5, c16 = item & 31;
+                const uint32_t w[4] = {cv[it].x, cv[it].y, cv[it].z, cv[it].w};
+                uint32_t h[8];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    h[2 * e] = e4m3x2_f16x2(w[e]);
+                    h[2 * e + 1] = e4m3x2_f16x2(w[e] >> 16);
+                }
+                *reinterpret_cast<uint4 *>(smem + V_OFF + v_off(t, 2 * c16)) = make_uint4(h[0], h[1], h[2], h[3]);
+                *reinterpret_cast<uint4 *>(smem + V_OFF + v_off(t, 2 * c16 + 1)) = make_uint4(h[4], h[5], h[6], h[7]);
+            }
+            fence_proxy_async_smem();
+            warp_arrive(&bars[B_VFULL]);
+            cursor_next(cd, P.req, P.B, U, P.mbps);
+        }
     }
-    if (j < npg && tid == 0) {
-        // a wait ran out: let every copy still in flight land before exiting
-        for (int i = j; i < min(npg, j + NSLOT); ++i) mbar_wait_bounded(&full[i % NSLOT], (i / NSLOT) & 1, nullptr);
-    }
+
+    // ---- teardown: one error word per CTA, tensor memory released
     grid_dependents_launch();
-    if (piece_b >= 0) finish_piece();
-    // one word per CTA
-    unsigned *s_err = reinterpret_cast<unsigned *>(flags + 4);
-    if (tid == 0) *s_err = 0u;
+    if (err) atomicOr(reinterpret_cast<unsigned *>(misc + 4), err);
+    tc_fence_before();
     __syncthreads();
-    if (err) atomicOr(s_err, err);
-    __syncthreads();
-    if (tid == 0) atomic_or_err(P.hdr, *s_err);
+    tc_fence_after();
+    if (warp == W_PROD)
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 512;" ::"r"(tmem) : "memory");
+    if (tid == 0) atomic_or_err(P.hdr, (uint32_t)misc[4]);
 }
 
 cudaError_t launch_latent(const CUtensorMap &ta, const CUtensorMap &tb, const LatentParams &P, int ctas,

@@ -61,7 +61,7 @@ def test_workspace_size_and_layout(B):
     assert offs == sorted(offs) and all(o % 256 == 0 for o in offs)
     assert lo.rows_per_kv_head == 4 and lo.row_blocks == 1 and lo.num_sms == 152
     assert lo.grid_ctas % 152 == 0 and lo.warps == lo.grid_ctas * 4 and lo.ring_pages_per_warp >= 2
-    assert lo.partial_slots == 4 * 8 + lo.warps and lo.rows_per_segment == 16
+    assert lo.partial_slots == 4 * 8 + lo.warps and lo.rows_per_segment == 16 and lo.group_size == 1
     assert lo.partial_lse_offset - lo.partial_o_offset >= lo.partial_slots * 16 * 128 * 4
 
 
@@ -77,8 +77,11 @@ def _latent(B, **kw):
 def test_latent_layout(B):
     lo = B.pa_workspace_layout(_latent(B))
     assert lo.rows_per_kv_head == 256 and lo.rows_per_segment == 64 and lo.row_blocks == 4
-    assert lo.grid_ctas == 152 and lo.warps == 152 and lo.ring_pages_per_warp == 2
-    assert lo.partial_slots == 8 * 4 + 152
+    assert lo.grid_ctas == 152 and lo.warps == 152 and lo.ring_pages_per_warp == 2 and lo.group_size == 4
+    assert lo.partial_slots == (8 * 1 + 152 // 4) * 4
+    # the launch is whole groups of one CTA per row block
+    for want, got in ((1, 4), (5, 4), (11, 8), (150, 148)):
+        assert B.pa_workspace_layout(_latent(B, grid_ctas=want)).grid_ctas == got
     assert lo.partial_lse_offset - lo.partial_o_offset >= lo.partial_slots * 64 * 512 * 4
     assert lo.total_bytes - lo.partial_lse_offset >= lo.partial_slots * 64 * 4
 
@@ -98,8 +101,8 @@ def test_latent_v_wider_than_k_rejected(B):
 def test_latent_run_needs_no_v_pool_but_checks_the_rest(B):
     p = _latent(B)
     need = B.pa_workspace_size(p)
-    # q misaligned (odd address): rejected before any launch
-    st = B.raw_status("pa_run", ctypes.byref(p), 0x4001, 0x5000, None, 0x7000, 0x8000, None, None,
+    # q not 16-byte aligned: rejected before any launch
+    st = B.raw_status("pa_run", ctypes.byref(p), 0x4008, 0x5000, None, 0x7000, 0x8000, None, None,
                       0x10000, need, 0x9000, None, None)
     assert st == B.PA_ERR_INVALID_ARG
     st = B.raw_status("pa_run", ctypes.byref(p), 0x4000, 0x5008, None, 0x7000, 0x8000, None, None,
@@ -178,6 +181,6 @@ def test_partial_slots_cover_oracle_pieces(B, latent):
         lo = B.pa_workspace_layout(p)
         L = rng.integers(0, maxctx + 1, Bsz)
         pl = oracle.plan(L, bs=bs, Hkv=Hkv, max_context_len=maxctx, max_blocks_per_seq=mbps,
-                         row_blocks=lo.row_blocks, warps=lo.warps)
+                         row_blocks=lo.row_blocks, warps=lo.warps, group_size=lo.group_size)
         assert pl["slots"] == lo.partial_slots
         assert all(pc["slot"] < lo.partial_slots for pc in pl["pieces"])

@@ -115,19 +115,22 @@ def test_split_counts_agree_within_tolerance():
         assert (o - outs[0]).abs().max().item() <= 1e-2
 
 
-def test_partial_pieces_match_oracle_plan():
-    w = make(B=3, L_lo=200, L_hi=900, Hq=16)
-    p = pa.problem(w, grid_ctas=11)
+@pytest.mark.parametrize("Hq,ctas", [(16, 11), (128, 22)])
+def test_partial_pieces_match_oracle_plan(Hq, ctas):
+    # 32 rows: one row block, groups of one CTA; 256 rows: groups of four
+    w = make(B=3, L_lo=200, L_hi=900, Hq=Hq)
+    p = pa.problem(w, grid_ctas=ctas)
     out, lse, ws = pa.alloc(w, p)
     lo = pa.binding().pa_workspace_layout(p)
-    assert lo.rows_per_segment == 64 and lo.warps == lo.grid_ctas == 11
+    assert lo.rows_per_segment == 64 and lo.warps == lo.grid_ctas == ctas // lo.group_size * lo.group_size
     RS = lo.rows_per_segment
     ws_f = ws.view(torch.float32)
     ws_f[lo.partial_lse_offset // 4: lo.partial_lse_offset // 4 + lo.partial_slots * RS] = float("nan")
     pa.run(w, p, out, ws, lse, steps="plan+run")
     torch.cuda.synchronize()
     pl = oracle.plan(w.context_lens.cpu().numpy(), bs=w.bs, Hkv=w.Hkv, max_context_len=w.max_context_len,
-                     max_blocks_per_seq=w.max_blocks_per_seq, row_blocks=lo.row_blocks, warps=lo.warps)
+                     max_blocks_per_seq=w.max_blocks_per_seq, row_blocks=lo.row_blocks, warps=lo.warps,
+                     group_size=lo.group_size)
     parts = ws_f[lo.partial_lse_offset // 4:][: lo.partial_slots * RS].view(-1, RS).cpu().numpy()
     R = lo.rows_per_kv_head
     written = set()

@@ -5,20 +5,21 @@ import pytest
 import oracle
 
 
-@pytest.mark.parametrize("seed", range(8))
-def test_pieces_partition_every_page_in_logical_order(seed):
+@pytest.mark.parametrize("seed,grouped", [(s, g) for s in range(8) for g in (False, True)])
+def test_pieces_partition_every_page_in_logical_order(seed, grouped):
     rng = np.random.default_rng(seed)
     B = int(rng.integers(1, 40))
     bs = int(rng.choice([16, 32, 64]))
     L = rng.integers(0, 3000, B)
     Hkv = int(rng.integers(1, 5))
-    RB = int(rng.integers(1, 3))
-    W = int(rng.integers(1, 400))
+    RB = int(rng.integers(1, 5))
+    G = RB if grouped else 1
+    W = int(rng.integers(1, 400)) * G
     mbps = int(-(-L.max() // bs)) + 1
     pl = oracle.plan(L, bs=bs, Hkv=Hkv, max_context_len=int(L.max()), max_blocks_per_seq=mbps,
-                     row_blocks=RB, warps=W)
+                     row_blocks=RB, warps=W, group_size=G)
     X = Hkv * RB
-    assert pl["positions"] == X * int(pl["pages"].sum())
+    assert pl["positions"] == X // G * int(pl["pages"].sum())
     # warp shares are contiguous, cover [0, N) and differ in size by at most one
     st = pl["warp_starts"]
     assert st[0] == 0 and st[-1] == pl["positions"]
@@ -43,8 +44,23 @@ def test_pieces_partition_every_page_in_logical_order(seed):
                 pos = p["pages"][1]
             assert pos == pl["pages"][b]
             assert (len(got) == 1) == got[0]["complete"]
+            # a grouped worker g*G + i only ever takes row block i
+            assert all(p["warp"] % G == q % G for p in got)
     slots = [p["slot"] for p in pl["pieces"]]
     assert len(set(slots)) == len(slots) and max(slots, default=0) < pl["slots"]
+
+
+def test_grouped_workers_of_a_group_share_their_pages():
+    # the G workers of a group take the same page runs, one row block each
+    pl = oracle.plan([300, 5, 900], bs=64, Hkv=1, max_context_len=900, max_blocks_per_seq=15,
+                     row_blocks=4, warps=12, group_size=4)
+    runs = {}
+    for p in pl["pieces"]:
+        runs.setdefault((p["warp"] // 4, p["segment"] // 4), set()).add((p["pages"], p["segment"] % 4))
+    for key, v in runs.items():
+        assert {rb for _, rb in v} == {0, 1, 2, 3}
+        assert len({pg for pg, _ in v}) == 1
+    assert pl["slots"] == (3 * 1 + 3) * 4
 
 
 def test_plan_flags_invalid_requests():
