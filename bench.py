@@ -71,10 +71,22 @@ def _peaks(key: str = "hbm_gbs"):
         return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}[key], "fallback"
 
 
-def _kernel_sha() -> str:
+# sources that decide each workload's attention kernel (traffic counters are
+# only reported while these are unchanged)
+KERNEL_SOURCES = {
+    "latent": ("pa_latent.cu", "pa_attn.cuh", "pa_common.cuh"),
+    "tiny": ("pa_attn.cuh", "pa_common.cuh", "pa_attn_launch.cuh", "pa_attn_f16_d64.cu"),
+    "bf16": ("pa_attn.cuh", "pa_common.cuh", "pa_attn_launch.cuh", "pa_attn_bf16_d128.cu"),
+    "e4m3": ("pa_attn.cuh", "pa_common.cuh", "pa_attn_launch.cuh", "pa_attn_e4m3_d256.cu"),
+    "int8": ("pa_attn.cuh", "pa_common.cuh", "pa_attn_launch.cuh", "pa_attn_int8_d128.cu"),
+    "int4": ("pa_attn.cuh", "pa_common.cuh", "pa_attn_launch.cuh", "pa_attn_int4_d128.cu"),
+}
+
+
+def _kernel_sha(workload: str) -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "paged_attention_quantized_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
+    for name in sorted(KERNEL_SOURCES[workload]):
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(name.encode() + f.read())
     return h.hexdigest()[:16]
@@ -87,7 +99,7 @@ def _traffic(workload: str):
     try:
         with open(path) as f:
             d = json.load(f)[workload]
-        if d.get("kernel_sha") == _kernel_sha():
+        if d.get("kernel_sha") == _kernel_sha(workload):
             return d.get("dram_bytes_per_launch")
     except Exception:
         pass
@@ -159,7 +171,7 @@ def gpu_arm(args, rank, world, local_rank):
     pabuild.build()
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
-    w = W.make(args.workload, device=dev)
+    w = W.make(args.workload, device=dev, B=args.batch)
     p = pa.problem(w)
     out, lse, ws = pa.alloc(w, p, device=dev)
     B = pa.binding()
@@ -314,7 +326,8 @@ def gpu_arm(args, rank, world, local_rank):
         "vs_baseline": None,
         "dtype": COMPUTE_DTYPE[args.workload],
         "data": "synthetic",
-        "config": {"workload": WORKLOAD_TEXT[args.workload], "name": args.workload, "batch": w.B,
+        "config": {"workload": WORKLOAD_TEXT[args.workload] + ("" if args.batch is None else f" (batch {w.B})"),
+                   "name": args.workload, "batch": w.B,
                    "next_n": w.n, "total_tokens": int(w.context_lens.sum().item()),
                    "effective_kv_bytes": eff_bytes,
                    "l2": "inputs larger than L2; a 256 MiB buffer is read before every step to evict the "
@@ -371,7 +384,7 @@ def cpu_model() -> str:
 
 def reference_arm(args):
     from paged_attention_quantized_gb300 import workloads as W
-    w = W.make(args.workload, device="cpu")
+    w = W.make(args.workload, device="cpu", B=args.batch)
     for _ in range(args.warmup):
         oracle_rate(w, budget_s=0.5)
     vals, rows_s, secs = [], [], []
@@ -422,6 +435,8 @@ def main():
     ap.add_argument("--ref-step-s", type=float, default=2.0, help="oracle seconds per reference step")
     ap.add_argument("--cpu-baseline-s", type=float, default=12.0, help="oracle seconds for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--batch", type=int, default=None,
+                    help="requests of the workload (default: its recipe); a smaller batch is for profiling only")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
 
