@@ -183,7 +183,8 @@ typedef struct pa_layout {
     int32_t row_blocks;          /* ceil(rows_per_kv_head / rows_per_segment) */
     int32_t num_sms;             /* effective */
     int32_t grid_ctas;           /* effective persistent CTAs of pa_run */
-    int32_t warps;               /* workers W: grid_ctas * 4 (grouped) or grid_ctas (latent) */
+    int32_t warps;               /* workers W: grid_ctas * 4 (grouped; * 2 with paired warps at D = 256
+                                    and more than 8 query rows per kv head) or grid_ctas (latent) */
     int32_t ring_pages_per_warp; /* pages each worker keeps in flight */
     int32_t rows_per_segment;    /* S: 16 (grouped) or 64 (latent) */
     int32_t group_size;          /* G: workers sharing one run of pages (1, or row_blocks for latent) */

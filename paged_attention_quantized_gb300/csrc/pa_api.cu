@@ -21,6 +21,12 @@ cudaError_t launch_latent(const CUtensorMap &ta, const CUtensorMap &tb, const La
 namespace {
 
 constexpr int VERSION = 100;
+#ifndef PA_MIN_RING_PAGES
+#define PA_MIN_RING_PAGES 2  // pages per worker before the resident CTAs per SM are stepped down
+#endif
+#ifndef PA_MIN_RING_PAGES_PAIR
+#define PA_MIN_RING_PAGES_PAIR 1  // paired warps: more resident workers beat a deeper ring
+#endif
 #ifndef PA_TOKM_MAX_ROWS
 #define PA_TOKM_MAX_ROWS 8  // at most 8: the rows are the MMA N axis then
 #endif
@@ -182,33 +188,40 @@ pa_status derive_grouped(const pa_problem *p, Derived *d) {
     d->SW = d->RB >= 128 ? 128 : 64;
     d->k_block = (size_t)p->num_kv_heads * bs * d->RB;
     d->v_block = d->k_block;
-    // Ring pages per warp: as many as fit the shared memory of the resident
-    // CTAs per SM the kernel's registers allow (each warp streams its own
-    // pages); with pages too large for two per warp, one CTA per SM, and one
-    // page per warp as the last resort.
+    // Ring pages per worker (a warp, or a pair of warps sharing one ring for
+    // D = 256 with rows on the MMA M axis): as many as fit the shared memory of
+    // the resident CTAs per SM the kernel's registers allow; with pages too
+    // large for two per worker, fewer CTAs per SM, and one page per worker as
+    // the last resort.
     const int page_bytes = 2 * bs * d->RB;
-    auto wsm = [&](int s) { return D <= 128 ? pa::warp_smem_bytes<128>(s, page_bytes) : pa::warp_smem_bytes<256>(s, page_bytes); };
+    d->tokm = d->R <= PA_TOKM_MAX_ROWS;  // few query rows per kv head: tokens on the MMA M axis
+    const bool pair = pa::pair_mode(D, d->tokm, d->RB / d->SW);
+    const int workers = pa::NWK / (pair ? 2 : 1);  // per CTA
+    auto wsm = [&](int s) {
+        return D <= 128 ? pa::warp_smem_bytes<128>(s, page_bytes, pair) : pa::warp_smem_bytes<256>(s, page_bytes, pair);
+    };
     auto fit = [&](int minb) {
         const size_t budget = std::min(MAX_DYN_SMEM_BYTES, SM_SMEM_BYTES / minb - CTA_RESERVED_BYTES) - 1024;
         int slots = 0;
         for (int s = 1; s <= pa::MAX_SLOTS; ++s)
-            if ((size_t)pa::NWK * wsm(s) <= budget) slots = s;
+            if ((size_t)workers * wsm(s) <= budget) slots = s;
         return slots;
     };
-    d->tokm = d->R <= PA_TOKM_MAX_ROWS;  // few query rows per kv head: tokens on the MMA M axis
-    d->minb = D <= 128 ? (d->tokm ? PA_MIN_BLOCKS_TOKM : PA_MIN_BLOCKS_SMALL_D) : PA_MIN_BLOCKS_LARGE_D;
-    // fewer resident CTAs until every warp holds two pages (one in flight
-    // while it computes on the other); one page per warp as the last resort
+    d->minb = D <= 128 ? pa::min_blocks<128, false>() : pa::min_blocks<256, false>(pair);
+    if (D <= 128 && d->tokm) d->minb = pa::min_blocks<128, true>();
+    // fewer resident CTAs until every worker holds two pages (one in flight
+    // while it computes on the other); one page per worker as the last resort
     d->slots = fit(d->minb);
-    while (d->slots < 2 && d->minb > 1) {
+    const int min_pages = pair ? PA_MIN_RING_PAGES_PAIR : PA_MIN_RING_PAGES;
+    while (d->slots < min_pages && d->minb > 1) {
         d->minb -= 1;
         d->slots = fit(d->minb);
     }
     if (d->slots < 1) return PA_ERR_UNSUPPORTED;
     d->warp_smem = wsm(d->slots);
-    d->smem = 1024 + (size_t)pa::NWK * d->warp_smem;
+    d->smem = 1024 + (size_t)workers * d->warp_smem;
     d->ctas = p->grid_ctas > 0 ? p->grid_ctas : d->sms * d->minb;
-    d->nwarps = (long long)d->ctas * pa::NWK;
+    d->nwarps = (long long)d->ctas * workers;
     return PA_OK;
 }
 

@@ -1,22 +1,23 @@
 // Split-KV paged decode / verify attention for sm_103a.
 //
-// One CTA computes one work unit (request b, kv head, a run of logical pages)
-// for up to 16 query rows of that kv head (the GQA group times next_n).
+// Persistent CTAs of 4 warps; each warp (or, for D = 256 with query rows on
+// the MMA M axis, each pair of warps sharing one ring and splitting the
+// channel segments between them) is an independent worker that streams its
+// share of the logical page sequence for up to 16 query rows of a kv head.
 //
-//  * warp NW (the producer) reads the unit's block ids 32 at a time, checks
-//    each against [1, num_blocks) and copies the K and V tiles of page p --
-//    [bs][row bytes] for this kv head, contiguous in the head-major pool -- into
-//    a ring of shared-memory stages with 4-D bulk tensor copies (TMA), 128- or
-//    64-byte swizzled so the consumers' 16-byte loads hit distinct banks;
-//  * warps 0..NW-1 (consumers) take pages round-robin in logical order; for
-//    every 16-token chunk they dequantize K codes in registers into mma B
-//    fragments, compute S = q' K^T with m16n8k16 tensor-core MMAs (rows are the
-//    16 query rows, fp32 accumulate), run the online softmax (exp2 domain,
-//    warp-shuffle row maxima), and accumulate O += P V with V dequantized the
-//    same way;
-//  * at the end the consumer warps' (m, l, O) are merged in warp order, and
-//    the unit writes either the final output (one split) or a normalised
-//    partial and its log-sum-exp for the combine kernel.
+//  * the worker's lane 0 reads block ids 32 at a time, checks each against
+//    [1, num_blocks) and copies the K and V tiles of its next pages -- [bs][row
+//    bytes] for one kv head, contiguous in the head-major pool -- into its ring
+//    of shared-memory slots with 4-D bulk tensor copies (TMA), 128- or 64-byte
+//    swizzled so the 16-byte loads of the lanes hit distinct banks;
+//  * for every 16-token chunk of a page the worker dequantizes K codes in
+//    registers into mma fragments, computes S = q' K^T with m16n8k16 tensor-
+//    core MMAs (query rows on M, or, with at most 8 rows per kv head, tokens
+//    on M: S^T = K q'^T), runs the online softmax (exp2 domain, warp-shuffle
+//    row maxima) and accumulates O += P V with V dequantized the same way;
+//  * its run of pages inside one segment (request, kv head, block of query
+//    rows) is a piece: a whole segment writes the output, a cut one a
+//    normalised partial and its log-sum-exp for the combine kernel.
 //
 // Pages are ordered by logical position only (1Cat-vLLM PR #494, "Stabilize
 // QSA page4 order under KV relocation": physical addresses are payload), so
@@ -50,15 +51,25 @@ constexpr int NWK = 4;                     // warps per CTA, each an independent
 #ifndef PA_MIN_BLOCKS_TOKM
 #define PA_MIN_BLOCKS_TOKM 4
 #endif
+#ifndef PA_MIN_BLOCKS_PAIR
+#define PA_MIN_BLOCKS_PAIR 3
+#endif
 // resident CTAs per SM the register and shared-memory budgets are sized for
 // (tokens-as-M kernels need fewer registers)
 template <int D, bool TOKM>
-__host__ __device__ constexpr int min_blocks() {
-    return D <= 128 ? (TOKM ? PA_MIN_BLOCKS_TOKM : PA_MIN_BLOCKS_SMALL_D) : PA_MIN_BLOCKS_LARGE_D;
+__host__ __device__ constexpr int min_blocks(bool pair = false) {
+    return D <= 128 ? (TOKM ? PA_MIN_BLOCKS_TOKM : PA_MIN_BLOCKS_SMALL_D)
+                    : (pair ? PA_MIN_BLOCKS_PAIR : PA_MIN_BLOCKS_LARGE_D);
 }
 // q' fragments live in registers for D <= 128, in the warp's shared memory above
 template <int D>
 __host__ __device__ constexpr bool q_in_regs() { return D <= 128; }
+// Paired warps (D = 256, query rows on the MMA M axis, an even number of
+// 128-byte channel segments): two warps share one worker's ring and each takes
+// half of the channel segments -- half of the q.K contraction (the partial
+// scores are summed through shared memory) and half of the output channels --
+// so the O accumulator is 64 registers instead of 128.
+__host__ __device__ constexpr bool pair_mode(int D, bool tokm, int nseg) { return !tokm && D == 256 && nseg % 2 == 0; }
 constexpr int ATTN_THREADS = NWK * 32;
 constexpr int MAX_SLOTS = 16;              // ring slots (pages) per warp
 constexpr int ROWS = 16;                   // query rows per segment (mma M)
@@ -216,11 +227,15 @@ __device__ __forceinline__ void lds_words(uint32_t *w, const uint8_t *p) {
     }
 }
 
-// Bytes of one warp's shared memory: its ring of pages, its q' fragments (when
-// they do not live in registers) and the ring barriers, rounded to 1 KB.
+// Bytes of one worker's shared memory: its ring of pages, its q' fragments
+// (when they do not live in registers), for paired warps the score exchange
+// (2 buffers x 2 warps x 32 lanes x 8 floats) and per-slot flags, and the ring
+// barriers, rounded to 1 KB.
+constexpr int XCHG_BYTES = 2 * 2 * 32 * 8 * 4;
 template <int D>
-__host__ __device__ constexpr int warp_smem_bytes(int slots, int page_bytes) {
-    return (slots * page_bytes + (q_in_regs<D>() ? 0 : (D / 16) * 512) + MAX_SLOTS * 8 + 1023) / 1024 * 1024;
+__host__ __device__ constexpr int warp_smem_bytes(int slots, int page_bytes, bool pair = false) {
+    return (slots * page_bytes + (q_in_regs<D>() ? 0 : (D / 16) * 512) + (pair ? XCHG_BYTES + MAX_SLOTS * 4 + 16 : 0) +
+            MAX_SLOTS * 8 + 1023) / 1024 * 1024;
 }
 
 // Position of logical page p of segment q (kv head * row blocks + row block)
@@ -296,12 +311,16 @@ __device__ __forceinline__ float load_q(const AttnParams &P, int b, int j, int h
 // (S^T = K q'^T and O^T = V^T P^T with the rows as N = 8), which halves the
 // tensor work and the O accumulator against padding 8 rows up to M = 16.
 template <int KVT, int D, bool TOKM>
-__global__ void __launch_bounds__(ATTN_THREADS, min_blocks<D, TOKM>())
+__global__ void __launch_bounds__(ATTN_THREADS, min_blocks<D, TOKM>(pair_mode(D, TOKM, Geo<KVT, D>::NSEG)))
     pa_attn_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv, AttnParams P) {
     using G = Geo<KVT, D>;
     constexpr bool BF = G::BF;
     constexpr bool QREG = q_in_regs<D>();
-    constexpr int NO = TOKM ? D / 16 : G::NT2;  // accumulator tiles of O (O^T with TOKM)
+    constexpr bool PAIR = pair_mode(D, TOKM, G::NSEG);
+    constexpr int WPW = PAIR ? 2 : 1;               // warps per worker
+    constexpr int NSEGW = G::NSEG / WPW;            // channel segments of this warp
+    constexpr int KSW = G::KSTEPS / WPW;            // k-steps of S = q K^T of this warp
+    constexpr int NO = TOKM ? D / 16 : G::NT2 / WPW;  // accumulator tiles of O (O^T with TOKM)
     constexpr int HEPL = G::EPL / 2;            // TOKM: O^T tiles per V segment
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -314,12 +333,22 @@ __global__ void __launch_bounds__(ATTN_THREADS, min_blocks<D, TOKM>())
     const int page_bytes = 2 * tile_bytes;  // K tile then V tile
     const int X = P.Hkv * P.RBLK;           // segments per request
 
-    // this warp's shared memory: ring of NS pages, q' fragments, barriers
-    uint8_t *ring = smem + (size_t)warp * P.warp_smem;
-    uint4 *qs = reinterpret_cast<uint4 *>(ring + (size_t)NS * page_bytes);          // [KSTEPS][32]
-    uint64_t *full = reinterpret_cast<uint64_t *>(reinterpret_cast<uint8_t *>(qs) +
-                                                  (QREG ? 0 : G::KSTEPS * 512));  // [MAX_SLOTS]
+    // this worker's shared memory: ring of NS pages, q' fragments (each warp of
+    // a pair its half), the pair's score exchange and slot flags, barriers
+    const int wk = warp / WPW;                 // worker within the CTA
+    const int hf = PAIR ? (warp & 1) : 0;      // half of the channel segments (paired warps)
+    const int sg0 = hf * NSEGW;                // first channel segment of this warp
+    uint8_t *ring = smem + (size_t)wk * P.warp_smem;
+    uint8_t *qbase = ring + (size_t)NS * page_bytes;
+    uint4 *qs = reinterpret_cast<uint4 *>(qbase) + (size_t)hf * KSW * 32;             // [KSW][32]
+    float *xchg = reinterpret_cast<float *>(qbase + (QREG ? 0 : G::KSTEPS * 512));   // [2][2][32][8]
+    volatile int *sflags = reinterpret_cast<volatile int *>(reinterpret_cast<uint8_t *>(xchg) + XCHG_BYTES);
+    uint64_t *full = reinterpret_cast<uint64_t *>(reinterpret_cast<uint8_t *>(xchg) +
+                                                  (PAIR ? XCHG_BYTES + MAX_SLOTS * 4 + 16 : 0));  // [MAX_SLOTS]
     if (NS < 1 || NS > MAX_SLOTS) return;  // the host never launches this
+    auto pair_sync = [&]() {
+        if constexpr (PAIR) named_barrier(1 + wk, 64);
+    };
 
     // the plan (and anything else earlier on the stream) must be complete
     grid_dependency_wait();
@@ -330,19 +359,20 @@ __global__ void __launch_bounds__(ATTN_THREADS, min_blocks<D, TOKM>())
         return;
     }
     const long long Ntot = total * X;
-    const long long NWt = (long long)gridDim.x * NWK;
-    const long long kw = (long long)blockIdx.x * NWK + warp;
+    const long long NWt = (long long)gridDim.x * (NWK / WPW);
+    const long long kw = (long long)blockIdx.x * (NWK / WPW) + wk;
     const long long x0 = kw * Ntot / NWt, x1 = (kw + 1) * Ntot / NWt;
     if (x0 >= x1) return;
     const int npg = (int)(x1 - x0);
 
-    if (lane == 0) {
+    if (lane == 0 && hf == 0) {
         for (int s = 0; s < NS; ++s) mbar_init(&full[s], 1);
         mbar_fence_init();
         tma_prefetch_desc(&tmk);
         tma_prefetch_desc(&tmv);
     }
     __syncwarp();
+    pair_sync();  // the barriers are initialised before the partner waits on them
 
     uint32_t err = 0;
     Cursor cc = cursor_at(x0, P.req, P.B, X, P.mbps);  // compute cursor
@@ -357,6 +387,9 @@ __global__ void __launch_bounds__(ATTN_THREADS, min_blocks<D, TOKM>())
     auto issue = [&](int j) {
         const int slot = j % NS;
         if (ci.b >= P.B) {  // inconsistent records: no copy, the slot still completes
+            if constexpr (PAIR) {
+                if (lane == 0) sflags[slot] = 1;
+            }
             if (lane == 0) mbar_arrive(&full[slot]);
             slot_bad |= 1u << slot;
             return;
@@ -370,6 +403,9 @@ __global__ void __launch_bounds__(ATTN_THREADS, min_blocks<D, TOKM>())
         const int blk = __shfl_sync(0xffffffffu, idc, ci.p - idc_w0);
         const bool ok = blk >= 1 && blk < P.num_blocks;
         const int kvh = ci.q / P.RBLK;
+        if constexpr (PAIR) {
+            if (lane == 0) sflags[slot] = ok ? 0 : 1;  // published with the barrier's phase
+        }
         if (lane == 0) {
             uint8_t *kt = ring + (size_t)slot * page_bytes;
             uint8_t *vt = kt + tile_bytes;
@@ -389,7 +425,8 @@ __global__ void __launch_bounds__(ATTN_THREADS, min_blocks<D, TOKM>())
     };
 
     const int npre = min(NS, npg);
-    for (int j = 0; j < npre; ++j) issue(j);
+    if (hf == 0)
+        for (int j = 0; j < npre; ++j) issue(j);
 
     // ---- per-piece state (a piece = this warp's run of pages of one segment)
     // o: rows g / g+8 x channels (rows-as-M), or channels x rows 2c / 2c+1 (TOKM);
@@ -460,11 +497,12 @@ __global__ void __launch_bounds__(ATTN_THREADS, min_blocks<D, TOKM>())
         }
         const float inv0 = 1.0f / rho0, inv1 = 1.0f / rho1;
 #pragma unroll
-        for (int K = 0; K < G::KSTEPS; ++K) {
+        for (int K = 0; K < KSW; ++K) {
+            const int Kg = hf * KSW + K;  // k-step of the whole row (paired warps: this half)
             uint32_t a[4];
 #pragma unroll
             for (int half = 0; half < 2; ++half) {  // a0a1/a2a3 use e=0,1; a4a5/a6a7 use e=2,3
-                const int d0 = phys_ch<KVT, D>(K, c, 2 * half), d1 = phys_ch<KVT, D>(K, c, 2 * half + 1);
+                const int d0 = phys_ch<KVT, D>(Kg, c, 2 * half), d1 = phys_ch<KVT, D>(Kg, c, 2 * half + 1);
                 const float f0 = fold(d0), f1 = fold(d1);
                 float u0 = 0.f, u1 = 0.f, w0 = 0.f, w1 = 0.f;
                 if (ok0) {
@@ -567,17 +605,18 @@ __global__ void __launch_bounds__(ATTN_THREADS, min_blocks<D, TOKM>())
                 const float l = rr ? lb : la;
                 const float inv = l > 0.f ? 1.0f / l : 0.f;
 #pragma unroll
-                for (int t = 0; t < G::NT2; ++t) {
-                    const int sg = t / G::EPL, e = t % G::EPL;
+                for (int t = 0; t < NO; ++t) {
+                    const int sg = sg0 + t / G::EPL, e = t % G::EPL;
 #pragma unroll
                     for (int cc2 = 0; cc2 < 2; ++cc2)
                         put(row, sg * G::EPS + (2 * c + cc2) * G::EPL + e, o[t][2 * rr + cc2] * inv);
                 }
-                if (c == 0) put_lse(row, l, rr ? m1 : m0);
+                if (c == 0 && hf == 0) put_lse(row, l, rr ? m1 : m0);
             }
         }
     };
 
+    int xb = 0;  // paired warps: exchange buffer parity
     int j = 0;
     for (; j < npg; ++j) {
         if (cc.b >= P.B) {  // records shorter than the shares: stop, copies drained below
@@ -589,12 +628,23 @@ __global__ void __launch_bounds__(ATTN_THREADS, min_blocks<D, TOKM>())
             start_piece();
         }
         const int slot = j % NS;
-        if (!mbar_wait_bounded(&full[slot], (j / NS) & 1, nullptr)) {
+        bool ok_wait = mbar_wait_bounded(&full[slot], (j / NS) & 1, nullptr);
+        if constexpr (PAIR) {
+            // both warps of the pair leave together: each publishes its outcome
+            const int okw = __all_sync(0xffffffffu, ok_wait) ? 1 : 0;
+            if (lane == 0) sflags[MAX_SLOTS + hf] = okw;
+            pair_sync();
+            ok_wait = sflags[MAX_SLOTS] && sflags[MAX_SLOTS + 1];
+            pair_sync();  // both have read the votes before the next page's
+            if (ok_wait) (void)mbar_try_wait(&full[slot], (j / NS) & 1);
+        }
+        if (!ok_wait) {
             err |= PA_DEV_ERR_TIMEOUT;
             pbad = true;
             break;
         }
-        if ((slot_bad >> slot) & 1u) {
+        const bool bad_slot = PAIR ? (sflags[slot] != 0) : (((slot_bad >> slot) & 1u) != 0);
+        if (bad_slot) {
             err |= PA_DEV_ERR_BLOCK_ID;
             pbad = true;
         }
@@ -720,12 +770,14 @@ __global__ void __launch_bounds__(ATTN_THREADS, min_blocks<D, TOKM>())
                     }
                 }
               } else {
-                // ---- S = q' K^T for tokens ch .. ch+15 (two n-tiles)
+                // ---- S = q' K^T for tokens ch .. ch+15 (two n-tiles); paired
+                // warps each take their half of the channel segments
                 float s[2][4];
 #pragma unroll
                 for (int t = 0; t < 2; ++t) s[t][0] = s[t][1] = s[t][2] = s[t][3] = 0.f;
 #pragma unroll
-                for (int sg = 0; sg < G::NSEG; ++sg) {
+                for (int sgl = 0; sgl < NSEGW; ++sgl) {
+                    const int sg = sg0 + sgl;
                     uint32_t kw2[2][G::KWORDS];
 #pragma unroll
                     for (int t = 0; t < 2; ++t) {
@@ -744,7 +796,7 @@ __global__ void __launch_bounds__(ATTN_THREADS, min_blocks<D, TOKM>())
                             a[0] = qreg[sg * G::KPS + jj][0]; a[1] = qreg[sg * G::KPS + jj][1];
                             a[2] = qreg[sg * G::KPS + jj][2]; a[3] = qreg[sg * G::KPS + jj][3];
                         } else {
-                            const uint4 av = qs[(sg * G::KPS + jj) * 32 + lane];
+                            const uint4 av = qs[(sgl * G::KPS + jj) * 32 + lane];
                             a[0] = av.x; a[1] = av.y; a[2] = av.z; a[3] = av.w;
                         }
 #pragma unroll
@@ -754,6 +806,24 @@ __global__ void __launch_bounds__(ATTN_THREADS, min_blocks<D, TOKM>())
                             mma16816<BF>(s[t], a, b0, b1);
                         }
                     }
+                }
+                if constexpr (PAIR) {
+                    // the partner's partial scores; both warps add them in the same order
+                    float *mine = xchg + (((xb & 1) * 2 + hf) * 32 + lane) * 8;
+                    const float *theirs = xchg + (((xb & 1) * 2 + (hf ^ 1)) * 32 + lane) * 8;
+#pragma unroll
+                    for (int t = 0; t < 2; ++t)
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) mine[4 * t + e] = s[t][e];
+                    pair_sync();
+#pragma unroll
+                    for (int t = 0; t < 2; ++t)
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const float o2 = theirs[4 * t + e];
+                            s[t][e] = hf == 0 ? s[t][e] + o2 : o2 + s[t][e];
+                        }
+                    ++xb;
                 }
                 // ---- scale, mask, online softmax
                 const int tbase = t_page + ch + 2 * c;
@@ -800,7 +870,7 @@ __global__ void __launch_bounds__(ATTN_THREADS, min_blocks<D, TOKM>())
                 l1 = l1 * al1 + ps1;
                 if (__any_sync(0xffffffffu, al0 != 1.f || al1 != 1.f)) {
 #pragma unroll
-                    for (int t = 0; t < G::NT2; ++t) {
+                    for (int t = 0; t < NO; ++t) {
                         o[t][0] *= al0;
                         o[t][1] *= al0;
                         o[t][2] *= al1;
@@ -818,7 +888,8 @@ __global__ void __launch_bounds__(ATTN_THREADS, min_blocks<D, TOKM>())
                 const bool zA = tail && rA >= nvalid, zB = tail && rB >= nvalid;
                 const bool zC = tail && rC >= nvalid, zD = tail && rD >= nvalid;
 #pragma unroll
-                for (int sg = 0; sg < G::NSEG; ++sg) {
+                for (int sgl = 0; sgl < NSEGW; ++sgl) {
+                    const int sg = sg0 + sgl;
                     uint32_t va[G::VWORDS], vb[G::VWORDS], vc[G::VWORDS], vd[G::VWORDS];
                     if constexpr (G::SW == 128) {
                         lds_words<4>(va, vt + tile_off<128>(rA, sg, g, bs));
@@ -844,19 +915,21 @@ __global__ void __launch_bounds__(ATTN_THREADS, min_blocks<D, TOKM>())
                     uint32_t bf[G::EPL][2];
                     v_frags<KVT, G::EPL, G::VWORDS>(va, vb, vc, vd, bf);
 #pragma unroll
-                    for (int e = 0; e < G::EPL; ++e) mma16816<BF>(o[sg * G::EPL + e], pa, bf[e][0], bf[e][1]);
+                    for (int e = 0; e < G::EPL; ++e) mma16816<BF>(o[sgl * G::EPL + e], pa, bf[e][0], bf[e][1]);
                 }
               }
             }
         }
         last_p = cc.p;
-        // every lane is done reading the slot before a copy may overwrite it
+        // every lane (of both warps of a pair) is done reading the slot before
+        // a copy may overwrite it
         __syncwarp();
+        pair_sync();
         fence_proxy_async_smem();
-        if (j + NS < npg) issue(j + NS);
+        if (j + NS < npg && hf == 0) issue(j + NS);
         cursor_next(cc, P.req, P.B, X, P.mbps);
     }
-    if (j < npg) {
+    if (j < npg && hf == 0) {
         // a wait ran out: let every copy still in flight land before exiting
         for (int i = j; i < min(npg, j + NS); ++i) mbar_wait_bounded(&full[i % NS], (i / NS) & 1, nullptr);
     }
