@@ -72,6 +72,28 @@ def test_other_head_dims(name, D):
     compare(w, out, lse)
 
 
+@pytest.mark.parametrize("name,kw", [
+    ("bf16", dict(D=256)),                 # 4 channel segments, 2 per warp
+    ("int8", dict(D=256)),                 # 2 segments, 1 per warp
+    ("e4m3", dict()),                      # the verify recipe's shape
+    ("f16", dict(D=256)),
+])
+@pytest.mark.parametrize("split", [0, 3])
+def test_paired_warps_d256(name, kw, split):
+    # D = 256 with 16 query rows per kv head: two warps share a ring and split
+    # the channel segments (scores summed through shared memory)
+    base = "tiny" if name == "f16" else name
+    w = make(base, B=4, L_lo=1, L_hi=600, Hq=8, Hkv=2, n=4, **kw)
+    p = pa.problem(w, grid_ctas=split)
+    lo = pa.binding().pa_workspace_layout(p)
+    assert lo.warps == lo.grid_ctas * 2  # two warps per worker
+    out, lse, ws, _ = run_gpu(w, grid_ctas=split)
+    assert error_bits(ws) == 0
+    compare(w, out, lse)
+    o2, l2, _, _ = run_gpu(W.relocate(w, seed=2), grid_ctas=split)
+    assert torch.equal(out, o2) and torch.equal(lse, l2)
+
+
 def test_steps_separately_equal_fused_call():
     w = make("bf16", B=6, L_lo=1, L_hi=2000, Hq=8, Hkv=2)
     o1, l1, _, _ = run_gpu(w, grid_ctas=5)
