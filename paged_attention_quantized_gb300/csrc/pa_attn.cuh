@@ -341,7 +341,7 @@ __global__ void __launch_bounds__(ATTN_THREADS, min_blocks<D, TOKM>(pair_mode(D,
     uint8_t *ring = smem + (size_t)wk * P.warp_smem;
     uint8_t *qbase = ring + (size_t)NS * page_bytes;
     uint4 *qs = reinterpret_cast<uint4 *>(qbase) + (size_t)hf * KSW * 32;             // [KSW][32]
-    float *xchg = reinterpret_cast<float *>(qbase + (QREG ? 0 : G::KSTEPS * 512));   // [2][2][32][8]
+    float *xchg = reinterpret_cast<float *>(qbase + (QREG ? 0 : G::KSTEPS * 512));   // [2][2][8][32]
     volatile int *sflags = reinterpret_cast<volatile int *>(reinterpret_cast<uint8_t *>(xchg) + XCHG_BYTES);
     uint64_t *full = reinterpret_cast<uint64_t *>(reinterpret_cast<uint8_t *>(xchg) +
                                                   (PAIR ? XCHG_BYTES + MAX_SLOTS * 4 + 16 : 0));  // [MAX_SLOTS]
@@ -809,18 +809,19 @@ __global__ void __launch_bounds__(ATTN_THREADS, min_blocks<D, TOKM>(pair_mode(D,
                 }
                 if constexpr (PAIR) {
                     // the partner's partial scores; both warps add them in the same order
-                    float *mine = xchg + (((xb & 1) * 2 + hf) * 32 + lane) * 8;
-                    const float *theirs = xchg + (((xb & 1) * 2 + (hf ^ 1)) * 32 + lane) * 8;
+                    // [buffer][warp][value][lane]: consecutive lanes, consecutive banks
+                    float *mine = xchg + ((xb & 1) * 2 + hf) * 256 + lane;
+                    const float *theirs = xchg + ((xb & 1) * 2 + (hf ^ 1)) * 256 + lane;
 #pragma unroll
                     for (int t = 0; t < 2; ++t)
 #pragma unroll
-                        for (int e = 0; e < 4; ++e) mine[4 * t + e] = s[t][e];
+                        for (int e = 0; e < 4; ++e) mine[(4 * t + e) * 32] = s[t][e];
                     pair_sync();
 #pragma unroll
                     for (int t = 0; t < 2; ++t)
 #pragma unroll
                         for (int e = 0; e < 4; ++e) {
-                            const float o2 = theirs[4 * t + e];
+                            const float o2 = theirs[(4 * t + e) * 32];
                             s[t][e] = hf == 0 ? s[t][e] + o2 : o2 + s[t][e];
                         }
                     ++xb;
