@@ -696,20 +696,29 @@ __global__ void __launch_bounds__(lat::THREADS, 1)
             if (!warp_wait(&bars[B_FULL + slot], (j / NSLOT) & 1, abort, err)) break;
             const int nvalid = min(BS, max(0, L - cd.p * BS));
             const uint8_t *pg8 = smem + RING_OFF + slot * SLOT_BYTES;
-            // the codes go to registers first, so the ring slot is released at once
+            // the codes go to registers first, so the ring slot is released at once.
+            // A warp instruction covers tokens t and t^5 (4 lanes each per 8-lane
+            // phase): under the XOR swizzle their loads fall in different halves
+            // and their stores in even / odd chunk slots, so neither conflicts.
+            const int w4 = dt >> 5, ln = dt & 31;
+            const int ph = ln >> 3, sub = (ln >> 2) & 1, q4 = ln & 3;
             uint4 cv[16];
 #pragma unroll
             for (int it = 0; it < 16; ++it) {
-                const int item = it * 128 + dt;  // 64 tokens x 32 chunks of 16 channels
-                const int t = item >> 5, c16 = item & 31;
+                const int combo = it * 4 + w4;            // 32 token pairs x 2 channel halves
+                const int pair = combo >> 1, hh = combo & 1;
+                const int t = (8 * (pair >> 2) + (pair & 3)) ^ (sub ? 5 : 0);
+                const int c16 = 16 * hh + 4 * ph + q4;
                 cv[it] = (t < nvalid) ? *reinterpret_cast<const uint4 *>(pg8 + e4_off(t, c16)) : make_uint4(0u, 0u, 0u, 0u);
             }
             warp_arrive(&bars[B_SLOTFREE + slot]);
             if (j >= 1 && !warp_wait(&bars[B_PVDONE + ((j - 1) & 1)], ((j - 1) >> 1) & 1, abort, err)) break;
 #pragma unroll
             for (int it = 0; it < 16; ++it) {
-                const int item = it * 128 + dt;
-                const int t = item >> 5, c16 = item & 31;
+                const int combo = it * 4 + w4;
+                const int pair = combo >> 1, hh = combo & 1;
+                const int t = (8 * (pair >> 2) + (pair & 3)) ^ (sub ? 5 : 0);
+                const int c16 = 16 * hh + 4 * ph + q4;
                 const uint32_t w[4] = {cv[it].x, cv[it].y, cv[it].z, cv[it].w};
                 uint32_t h[8];
 #pragma unroll
