@@ -152,10 +152,10 @@ __device__ __forceinline__ void k_frag(const uint32_t *w, int j, uint32_t &b0, u
         b0 = u8pair_f16x2(u, 0x4140);
         b1 = u8pair_f16x2(u, 0x4342);
     } else {  // INT4
-        uint32_t u = w[j >> 1] ^ 0x88888888u;
+        uint32_t u = w[j >> 1];
         if (j & 1) u >>= 8;
-        b0 = u4lo_f16x2(u);
-        b1 = u4hi_f16x2(u);
+        b0 = s4lo_f16x2(u);
+        b1 = s4hi_f16x2(u);
     }
 }
 
@@ -196,21 +196,20 @@ __device__ __forceinline__ void v_frags(const uint32_t *ra, const uint32_t *rb, 
             bf[4 * k + 2][1] = u8pair_f16x2(u1, 0x4140);
             bf[4 * k + 3][1] = u8pair_f16x2(u1, 0x4342);
         } else {  // INT4: 8 channels per word
-            const uint32_t xa = ra[k] ^ 0x88888888u, xb = rb[k] ^ 0x88888888u;
-            const uint32_t xc = rc[k] ^ 0x88888888u, xd = rd[k] ^ 0x88888888u;
+            const uint32_t xa = ra[k], xb = rb[k], xc = rc[k], xd = rd[k];
 #pragma unroll
             for (int half = 0; half < 2; ++half) {
                 const uint32_t sel = half ? 0x7632 : 0x5410;
                 const uint32_t t = __byte_perm(xa, xb, sel), u = __byte_perm(xc, xd, sel);
                 const int e = 8 * k + 4 * half;
-                bf[e][0] = u4lo_f16x2(t);
-                bf[e + 1][0] = u4hi_f16x2(t);
-                bf[e + 2][0] = u4lo_f16x2(t >> 8);
-                bf[e + 3][0] = u4hi_f16x2(t >> 8);
-                bf[e][1] = u4lo_f16x2(u);
-                bf[e + 1][1] = u4hi_f16x2(u);
-                bf[e + 2][1] = u4lo_f16x2(u >> 8);
-                bf[e + 3][1] = u4hi_f16x2(u >> 8);
+                bf[e][0] = s4lo_f16x2(t);
+                bf[e + 1][0] = s4hi_f16x2(t);
+                bf[e + 2][0] = s4lo_f16x2(t >> 8);
+                bf[e + 3][0] = s4hi_f16x2(t >> 8);
+                bf[e][1] = s4lo_f16x2(u);
+                bf[e + 1][1] = s4hi_f16x2(u);
+                bf[e + 2][1] = s4lo_f16x2(u >> 8);
+                bf[e + 3][1] = s4hi_f16x2(u >> 8);
             }
         }
     }

@@ -273,6 +273,25 @@ __device__ __forceinline__ uint32_t u4hi_f16x2(uint32_t ux) {
     return hfma2_u((ux & 0x00F000F0u) | 0x64006400u, F16X2_1_16, F16X2_M72);
 }
 
+// (a & b) ^ c in one instruction
+__device__ __forceinline__ uint32_t and_xor(uint32_t a, uint32_t b, uint32_t c) {
+    uint32_t r;
+    asm("lop3.b32 %0, %1, %2, %3, 0x6A;" : "=r"(r) : "r"(a), "r"(b), "r"(c));
+    return r;
+}
+
+// Two's-complement nibbles straight from the stored word (no offset-binary
+// XOR first): ((w ^ 8) & 0xF) | 0x6400 equals (w & 0xF) ^ 0x6408, one LOP3.
+// low nibbles of bytes 0 and 2 -> {n0, n2}
+__device__ __forceinline__ uint32_t s4lo_f16x2(uint32_t w) {
+    return hsub2_u(and_xor(w, 0x000F000Fu, 0x64086408u), F16X2_1032);
+}
+
+// high nibbles of bytes 0 and 2 -> {n0, n2}
+__device__ __forceinline__ uint32_t s4hi_f16x2(uint32_t w) {
+    return hfma2_u(and_xor(w, 0x00F000F0u, 0x64806480u), F16X2_1_16, F16X2_M72);
+}
+
 // ------------------------------------------------- programmatic dependent launch
 
 // Block until the grid this launch depends on has finished and its writes are
