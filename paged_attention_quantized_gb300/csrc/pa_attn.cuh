@@ -13,8 +13,10 @@
 //  * for every 16-token chunk of a page the worker dequantizes K codes in
 //    registers into mma fragments, computes S = q' K^T with m16n8k16 tensor-
 //    core MMAs (query rows on M, or, with at most 8 rows per kv head, tokens
-//    on M: S^T = K q'^T), runs the online softmax (exp2 domain, warp-shuffle
-//    row maxima) and accumulates O += P V with V dequantized the same way;
+//    on M: S^T = K q'^T), runs the online softmax (exp2 domain; the row
+//    maximum is lazy: it is reduced across lanes, and O and the row sum
+//    rescaled, only when some score passes it by more than 2^8, so P stays
+//    below 256) and accumulates O += P V with V dequantized the same way;
 //  * its run of pages inside one segment (request, kv head, block of query
 //    rows) is a piece: a whole segment writes the output, a cut one a
 //    normalised partial and its log-sum-exp for the combine kernel.
@@ -75,6 +77,7 @@ constexpr int MAX_SLOTS = 16;              // ring slots (pages) per warp
 constexpr int ROWS = 16;                   // query rows per segment (mma M)
 constexpr float LOG2E = 1.4426950408889634f;
 constexpr float LN2 = 0.6931471805599453f;
+constexpr float LAZY_SLACK = 8.0f;         // lazy row maximum (exp2 domain): reduce and rescale only when a score exceeds m + 8
 
 template <int KVT>
 struct KvTraits;
@@ -383,8 +386,10 @@ __global__ void __launch_bounds__(ATTN_THREADS, min_blocks<D, TOKM>(pair_mode(D,
     int idc_b = -1, idc_w0 = 0, idc = 0;        // block ids of ci.b, pages [idc_w0, idc_w0 + 32)
     unsigned slot_bad = 0;                      // slots whose page had an invalid id
 
-    auto issue = [&](int j) {
-        const int slot = j % NS;
+    int islot = 0;  // ring slot of the next copy
+    auto issue = [&]() {
+        const int slot = islot;
+        islot = (islot + 1 == NS) ? 0 : islot + 1;
         if (ci.b >= P.B) {  // inconsistent records: no copy, the slot still completes
             if constexpr (PAIR) {
                 if (lane == 0) sflags[slot] = 1;
@@ -401,7 +406,7 @@ __global__ void __launch_bounds__(ATTN_THREADS, min_blocks<D, TOKM>(pair_mode(D,
         }
         const int blk = __shfl_sync(0xffffffffu, idc, ci.p - idc_w0);
         const bool ok = blk >= 1 && blk < P.num_blocks;
-        const int kvh = ci.q / P.RBLK;
+        const int kvh = (P.RBLK == 1) ? ci.q : ci.q / P.RBLK;
         if constexpr (PAIR) {
             if (lane == 0) sflags[slot] = ok ? 0 : 1;  // published with the barrier's phase
         }
@@ -425,7 +430,7 @@ __global__ void __launch_bounds__(ATTN_THREADS, min_blocks<D, TOKM>(pair_mode(D,
 
     const int npre = min(NS, npg);
     if (hf == 0)
-        for (int j = 0; j < npre; ++j) issue(j);
+        for (int j = 0; j < npre; ++j) issue();
 
     // ---- per-piece state (a piece = this warp's run of pages of one segment)
     // o: rows g / g+8 x channels (rows-as-M), or channels x rows 2c / 2c+1 (TOKM);
@@ -616,6 +621,8 @@ __global__ void __launch_bounds__(ATTN_THREADS, min_blocks<D, TOKM>(pair_mode(D,
     };
 
     int xb = 0;  // paired warps: exchange buffer parity
+    int cslot = 0;       // ring slot of page j
+    uint32_t cpar = 0;   // its barrier phase parity
     int j = 0;
     for (; j < npg; ++j) {
         if (cc.b >= P.B) {  // records shorter than the shares: stop, copies drained below
@@ -626,8 +633,10 @@ __global__ void __launch_bounds__(ATTN_THREADS, min_blocks<D, TOKM>(pair_mode(D,
             if (piece_b >= 0) finish_piece();
             start_piece();
         }
-        const int slot = j % NS;
-        bool ok_wait = mbar_wait_bounded(&full[slot], (j / NS) & 1, nullptr);
+        const int slot = cslot;
+        const uint32_t par = cpar;
+        if (++cslot == NS) { cslot = 0; cpar ^= 1u; }
+        bool ok_wait = mbar_wait_bounded(&full[slot], par, nullptr);
         if constexpr (PAIR) {
             // both warps of the pair leave together: each publishes its outcome
             const int okw = __all_sync(0xffffffffu, ok_wait) ? 1 : 0;
@@ -635,7 +644,7 @@ __global__ void __launch_bounds__(ATTN_THREADS, min_blocks<D, TOKM>(pair_mode(D,
             pair_sync();
             ok_wait = sflags[MAX_SLOTS] && sflags[MAX_SLOTS + 1];
             pair_sync();  // both have read the votes before the next page's
-            if (ok_wait) (void)mbar_try_wait(&full[slot], (j / NS) & 1);
+            if (ok_wait) (void)mbar_try_wait(&full[slot], par);
         }
         if (!ok_wait) {
             err |= PA_DEV_ERR_TIMEOUT;
@@ -702,24 +711,19 @@ __global__ void __launch_bounds__(ATTN_THREADS, min_blocks<D, TOKM>(pair_mode(D,
                     x[3] = (tg + 8 < vis1) ? x[3] : -INFINITY;
                 }
                 float mx0 = fmaxf(x[0], x[2]), mx1 = fmaxf(x[1], x[3]);
+                if (__any_sync(0xffffffffu, mx0 > m0 + LAZY_SLACK || mx1 > m1 + LAZY_SLACK)) {
 #pragma unroll
-                for (int off = 4; off <= 16; off <<= 1) {
-                    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
-                    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
-                }
-                const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-                const float base0 = (mn0 == -INFINITY) ? 0.f : mn0;
-                const float base1 = (mn1 == -INFINITY) ? 0.f : mn1;
-                const float al0 = ex2(m0 - base0), al1 = ex2(m1 - base1);
-                m0 = mn0;
-                m1 = mn1;
-                x[0] = ex2(x[0] - base0);
-                x[2] = ex2(x[2] - base0);
-                x[1] = ex2(x[1] - base1);
-                x[3] = ex2(x[3] - base1);
-                l0 = l0 * al0 + (x[0] + x[2]);
-                l1 = l1 * al1 + (x[1] + x[3]);
-                if (__any_sync(0xffffffffu, al0 != 1.f || al1 != 1.f)) {
+                    for (int off = 4; off <= 16; off <<= 1) {
+                        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+                        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+                    }
+                    const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+                    const float al0 = ex2(m0 - ((mn0 == -INFINITY) ? 0.f : mn0));
+                    const float al1 = ex2(m1 - ((mn1 == -INFINITY) ? 0.f : mn1));
+                    m0 = mn0;
+                    m1 = mn1;
+                    l0 *= al0;
+                    l1 *= al1;
 #pragma unroll
                     for (int t = 0; t < NO; ++t) {
                         o[t][0] *= al0;
@@ -728,6 +732,14 @@ __global__ void __launch_bounds__(ATTN_THREADS, min_blocks<D, TOKM>(pair_mode(D,
                         o[t][3] *= al1;
                     }
                 }
+                const float base0 = (m0 == -INFINITY) ? 0.f : m0;
+                const float base1 = (m1 == -INFINITY) ? 0.f : m1;
+                x[0] = ex2(x[0] - base0);
+                x[2] = ex2(x[2] - base0);
+                x[1] = ex2(x[1] - base1);
+                x[3] = ex2(x[3] - base1);
+                l0 += x[0] + x[2];
+                l1 += x[1] + x[3];
                 // ---- P^T fragments: transpose the [token][row] pairs
                 const uint32_t pb0 = movmatrix_trans(pack2<BF>(x[0], x[1]));  // tokens 2c,2c+1 of row g
                 const uint32_t pb1 = movmatrix_trans(pack2<BF>(x[2], x[3]));  // tokens 2c+8,2c+9
@@ -845,16 +857,28 @@ __global__ void __launch_bounds__(ATTN_THREADS, min_blocks<D, TOKM>(pair_mode(D,
                         mx1 = fmaxf(mx1, x1v);
                     }
                 }
-                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
-                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
-                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
-                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
-                const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-                const float base0 = (mn0 == -INFINITY) ? 0.f : mn0;
-                const float base1 = (mn1 == -INFINITY) ? 0.f : mn1;
-                const float al0 = ex2(m0 - base0), al1 = ex2(m1 - base1);  // m = -inf -> 0
-                m0 = mn0;
-                m1 = mn1;
+                if (__any_sync(0xffffffffu, mx0 > m0 + LAZY_SLACK || mx1 > m1 + LAZY_SLACK)) {
+                    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+                    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+                    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+                    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+                    const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+                    const float al0 = ex2(m0 - ((mn0 == -INFINITY) ? 0.f : mn0));  // m = -inf -> 0
+                    const float al1 = ex2(m1 - ((mn1 == -INFINITY) ? 0.f : mn1));
+                    m0 = mn0;
+                    m1 = mn1;
+                    l0 *= al0;
+                    l1 *= al1;
+#pragma unroll
+                    for (int t = 0; t < NO; ++t) {
+                        o[t][0] *= al0;
+                        o[t][1] *= al0;
+                        o[t][2] *= al1;
+                        o[t][3] *= al1;
+                    }
+                }
+                const float base0 = (m0 == -INFINITY) ? 0.f : m0;
+                const float base1 = (m1 == -INFINITY) ? 0.f : m1;
                 float ps0 = 0.f, ps1 = 0.f;
 #pragma unroll
                 for (int t = 0; t < 2; ++t) {
@@ -866,17 +890,8 @@ __global__ void __launch_bounds__(ATTN_THREADS, min_blocks<D, TOKM>(pair_mode(D,
                         ps1 += s[t][2 + e];
                     }
                 }
-                l0 = l0 * al0 + ps0;
-                l1 = l1 * al1 + ps1;
-                if (__any_sync(0xffffffffu, al0 != 1.f || al1 != 1.f)) {
-#pragma unroll
-                    for (int t = 0; t < NO; ++t) {
-                        o[t][0] *= al0;
-                        o[t][1] *= al0;
-                        o[t][2] *= al1;
-                        o[t][3] *= al1;
-                    }
-                }
+                l0 += ps0;
+                l1 += ps1;
                 // ---- O += P V
                 uint32_t pa[4];
                 pa[0] = pack2<BF>(s[0][0], s[0][1]);
@@ -926,7 +941,7 @@ __global__ void __launch_bounds__(ATTN_THREADS, min_blocks<D, TOKM>(pair_mode(D,
         __syncwarp();
         pair_sync();
         fence_proxy_async_smem();
-        if (j + NS < npg && hf == 0) issue(j + NS);
+        if (j + NS < npg && hf == 0) issue();
         cursor_next(cc, P.req, P.B, X, P.mbps);
     }
     if (j < npg && hf == 0) {
