@@ -269,6 +269,28 @@ T *at(void *ws, size_t off) {
     return reinterpret_cast<T *>(static_cast<uint8_t *>(ws) + off);
 }
 
+// One tile of the grouped kernel -- all segments of [bs][RB] for one kv head of
+// one block -- as a single 5-D box {SW bytes, bs rows, NSEG segments, 1, 1}:
+// the segment dimension (stride SW) is placed outside the rows, so the box
+// lands as [segment][row][SW bytes], each SW-byte line swizzled by its row.
+pa_status make_tmap_tile(CUtensorMap *tm, const void *base, const Derived &d, const pa_problem *p,
+                         size_t block_stride) {
+    auto enc = encode_fn();
+    if (enc == nullptr) return PA_ERR_CUDA;
+    const int nseg = d.RB / d.SW;
+    cuuint64_t dims[5] = {(cuuint64_t)d.SW, (cuuint64_t)p->block_size, (cuuint64_t)nseg,
+                          (cuuint64_t)p->num_kv_heads, (cuuint64_t)p->num_blocks};
+    cuuint64_t strides[4] = {(cuuint64_t)d.RB, (cuuint64_t)d.SW, (cuuint64_t)p->block_size * d.RB,
+                             (cuuint64_t)block_stride};
+    cuuint32_t box[5] = {(cuuint32_t)d.SW, (cuuint32_t)p->block_size, (cuuint32_t)nseg, 1, 1};
+    cuuint32_t es[5] = {1, 1, 1, 1, 1};
+    CUresult r = enc(tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, 5, const_cast<void *>(base), dims, strides, box, es,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE,
+                     d.SW == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? PA_OK : PA_ERR_CUDA;
+}
+
 cudaError_t dispatch_attn(const pa_problem *p, const Derived &d, const CUtensorMap &tk, const CUtensorMap &tv,
                           const pa::AttnParams &P, cudaStream_t s) {
     const dim3 grid((unsigned)d.ctas);
@@ -398,8 +420,8 @@ PA_API pa_status pa_run(const pa_problem *p, const void *q, const void *k_pool, 
     if ((p->v_scale_mode == PA_SCALE_TENSOR || p->v_scale_mode == PA_SCALE_CHANNEL) && v_scale == nullptr)
         return PA_ERR_INVALID_ARG;
     CUtensorMap tk, tv;
-    if ((st = make_tmap(&tk, k_pool, d, p, d.k_block)) != PA_OK) return st;
-    if ((st = make_tmap(&tv, v_pool, d, p, d.v_block)) != PA_OK) return st;
+    if ((st = make_tmap_tile(&tk, k_pool, d, p, d.k_block)) != PA_OK) return st;
+    if ((st = make_tmap_tile(&tv, v_pool, d, p, d.v_block)) != PA_OK) return st;
     pa::AttnParams P;
     P.q = static_cast<const uint8_t *>(q);
     P.block_table = block_table;

@@ -8,8 +8,11 @@
 //  * the worker's lane 0 reads block ids 32 at a time, checks each against
 //    [1, num_blocks) and copies the K and V tiles of its next pages -- [bs][row
 //    bytes] for one kv head, contiguous in the head-major pool -- into its ring
-//    of shared-memory slots with 4-D bulk tensor copies (TMA), 128- or 64-byte
-//    swizzled so the 16-byte loads of the lanes hit distinct banks;
+//    of shared-memory slots, one 5-D bulk tensor copy (TMA) per tile: rows of
+//    more than 128 bytes are cut into 128-byte segments, the segment dimension
+//    placed outside the rows, and each line 128- or 64-byte swizzled so the
+//    16-byte loads of the lanes hit distinct banks (the copy instruction, not
+//    the bytes, is what costs the issuing warp);
 //  * for every 16-token chunk of a page the worker dequantizes K codes in
 //    registers into mma fragments, computes S = q' K^T with m16n8k16 tensor-
 //    core MMAs (query rows on M, or, with at most 8 rows per kv head, tokens
@@ -415,11 +418,8 @@ __global__ void __launch_bounds__(ATTN_THREADS, min_blocks<D, TOKM>(pair_mode(D,
             uint8_t *vt = kt + tile_bytes;
             if (ok) {
                 mbar_arrive_expect_tx(&full[slot], (uint32_t)page_bytes);
-#pragma unroll
-                for (int sg = 0; sg < G::NSEG; ++sg) {
-                    tma_load_4d(kt + sg * bs * G::SW, &tmk, &full[slot], sg * G::SW, 0, kvh, blk);
-                    tma_load_4d(vt + sg * bs * G::SW, &tmv, &full[slot], sg * G::SW, 0, kvh, blk);
-                }
+                tma_load_5d(kt, &tmk, &full[slot], 0, 0, 0, kvh, blk);  // all segments of the K tile
+                tma_load_5d(vt, &tmv, &full[slot], 0, 0, 0, kvh, blk);
             } else {
                 mbar_arrive(&full[slot]);  // no copy: the piece is NaN-filled
             }
