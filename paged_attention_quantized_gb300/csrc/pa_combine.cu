@@ -15,6 +15,7 @@
 namespace pa {
 
 constexpr int COMBINE_THREADS = 256;
+constexpr int COMBINE_ROWS = 16;  // query rows of a segment handled by one CTA
 
 // first position of warp k's share of the n positions split over nw warps
 __device__ __forceinline__ long long share_start(long long k, long long n, long long nw) { return k * n / nw; }
@@ -27,14 +28,40 @@ __device__ __forceinline__ long long share_owner(long long x, long long n, long 
 constexpr int MAX_CACHED_PIECES = 64;
 constexpr int MAX_ROWS_SEG = 64;
 
-// One CTA per segment (request, kv head, row block).  The pieces (non-empty
-// warp shares) and the per-row weights w = exp(lse - M) / sum exp(lse - M) are
-// worked out once; every output element is then one weighted sum.
+__device__ __forceinline__ void store4(const CombineParams &P, size_t oi, float4 y, bool vec) {
+    if (P.out_dtype == PA_F32) {
+        float *o = reinterpret_cast<float *>(P.out) + oi;
+        if (vec) *reinterpret_cast<float4 *>(o) = y;
+        else { o[0] = y.x; o[1] = y.y; o[2] = y.z; o[3] = y.w; }
+    } else if (P.out_dtype == PA_F16) {
+        __half *o = reinterpret_cast<__half *>(P.out) + oi;
+        const __half2 a = __floats2half2_rn(y.x, y.y), b = __floats2half2_rn(y.z, y.w);
+        if (vec) {
+            uint2 u;
+            memcpy(&u.x, &a, 4);
+            memcpy(&u.y, &b, 4);
+            *reinterpret_cast<uint2 *>(o) = u;
+        } else { o[0] = a.x; o[1] = a.y; o[2] = b.x; o[3] = b.y; }
+    } else {
+        __nv_bfloat16 *o = reinterpret_cast<__nv_bfloat16 *>(P.out) + oi;
+        const __nv_bfloat162 a = __floats2bfloat162_rn(y.x, y.y), b = __floats2bfloat162_rn(y.z, y.w);
+        if (vec) {
+            uint2 u;
+            memcpy(&u.x, &a, 4);
+            memcpy(&u.y, &b, 4);
+            *reinterpret_cast<uint2 *>(o) = u;
+        } else { o[0] = a.x; o[1] = a.y; o[2] = b.x; o[3] = b.y; }
+    }
+}
+
+// One CTA per (segment, block of 16 query rows of it).  The pieces (non-empty
+// worker shares) and the per-row weights w = exp(lse - M) are worked out once;
+// every 4 output channels are then one weighted sum of float4 partials.
 __global__ void __launch_bounds__(COMBINE_THREADS) pa_combine_kernel(CombineParams P) {
-    __shared__ long long s_piece[MAX_CACHED_PIECES];   // partial slots, ascending warp order
-    __shared__ float s_w[MAX_CACHED_PIECES][MAX_ROWS_SEG];  // weight of piece k for row i
-    __shared__ float s_M[MAX_ROWS_SEG], s_den[MAX_ROWS_SEG];
-    __shared__ int s_np, s_nan[MAX_ROWS_SEG];
+    __shared__ long long s_piece[MAX_CACHED_PIECES];          // partial slots, ascending worker order
+    __shared__ float s_w[MAX_CACHED_PIECES][COMBINE_ROWS];    // weight of piece n for row i
+    __shared__ float s_M[COMBINE_ROWS], s_den[COMBINE_ROWS];
+    __shared__ int s_np, s_nan[COMBINE_ROWS];
     grid_dependency_wait();  // the attention's partials are complete
     const int X = P.Hkv * P.RBLK;
     const int seg = blockIdx.x;
@@ -46,7 +73,9 @@ __global__ void __launch_bounds__(COMBINE_THREADS) pa_combine_kernel(CombinePara
     const int4 Rq = P.req[b];
     const int Pb = Rq.y;
     const int RS = P.rows_seg;
-    const int rows_here = min(RS, P.R - rblk * RS);
+    const int i0 = blockIdx.y * COMBINE_ROWS;             // first row of this CTA within the segment
+    const int rows_here = min(min(COMBINE_ROWS, RS - i0), P.R - rblk * RS - i0);
+    if (rows_here <= 0) return;
     const float NaN = __int_as_float(0x7fc00000);
     const float LOG2E_ = 1.4426950408889634f;
     const long long N = (long long)P.hdr[HDR_TOTAL_PAGES] * U;
@@ -61,14 +90,19 @@ __global__ void __launch_bounds__(COMBINE_THREADS) pa_combine_kernel(CombinePara
     }
     const long long slot0 = ((long long)b * U + u) * GS + gi;  // slot of group g: slot0 + g * GS
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    // 1. the pieces: worker groups kf..kl with a non-empty share (empty shares
-    //    only exist when there are fewer positions than groups)
+    // 1. the pieces: worker groups kf..kl with a non-empty share.  With at
+    //    least as many positions as groups every share is non-empty.
     if (threadIdx.x == 0) {
         int np = 0;
-        for (long long k = kf; k <= kl; ++k) {
-            if (share_start(k, N, NG) == share_start(k + 1, N, NG)) continue;
-            if (np < MAX_CACHED_PIECES) s_piece[np] = slot0 + k * GS;
-            ++np;
+        if (N >= NG) {
+            np = (int)min(kl - kf + 1, 0x7fffffffll);
+            for (int n = 0; n < min(np, MAX_CACHED_PIECES); ++n) s_piece[n] = slot0 + (kf + n) * GS;
+        } else {
+            for (long long k = kf; k <= kl; ++k) {
+                if (share_start(k, N, NG) == share_start(k + 1, N, NG)) continue;
+                if (np < MAX_CACHED_PIECES) s_piece[np] = slot0 + k * GS;
+                ++np;
+            }
         }
         s_np = np;
     }
@@ -78,6 +112,7 @@ __global__ void __launch_bounds__(COMBINE_THREADS) pa_combine_kernel(CombinePara
     // slot of the n-th piece (recomputed when there are too many to cache)
     auto piece_slot = [&](int n) -> long long {
         if (cached) return s_piece[n];
+        if (N >= NG) return slot0 + (kf + n) * GS;
         int seen = 0;
         for (long long k = kf; k <= kl; ++k) {
             if (share_start(k, N, NG) == share_start(k + 1, N, NG)) continue;
@@ -87,11 +122,13 @@ __global__ void __launch_bounds__(COMBINE_THREADS) pa_combine_kernel(CombinePara
     };
     // 2. per row: M = max lse, den = sum exp(lse - M), NaN if any piece is NaN
     if (Pb > 0) {
-        for (int i = warp; i < rows_here; i += COMBINE_THREADS / 32) {
+        for (int ii = warp; ii < rows_here; ii += COMBINE_THREADS / 32) {
+            const int i = i0 + ii;
             float M = -INFINITY;
             int nan = 0;
             for (int n = lane; n < np; n += 32) {
                 const float l = P.part_lse[piece_slot(n) * RS + i];
+                if (cached) s_w[n][ii] = l;
                 nan |= (l != l);
                 M = fmaxf(M, l);
             }
@@ -103,8 +140,9 @@ __global__ void __launch_bounds__(COMBINE_THREADS) pa_combine_kernel(CombinePara
             float den = 0.f;
             if (M != -INFINITY && !nan) {
                 for (int n = lane; n < np; n += 32) {
-                    const float w = ex2((P.part_lse[piece_slot(n) * RS + i] - M) * LOG2E_);
-                    if (cached) s_w[n][i] = w;
+                    const float l = cached ? s_w[n][ii] : P.part_lse[piece_slot(n) * RS + i];
+                    const float w = ex2((l - M) * LOG2E_);
+                    if (cached) s_w[n][ii] = w;
                     den += w;
                 }
             }
@@ -112,47 +150,78 @@ __global__ void __launch_bounds__(COMBINE_THREADS) pa_combine_kernel(CombinePara
 #pragma unroll
             for (int o = 16; o >= 1; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
             if (lane == 0) {
-                s_M[i] = M;
-                s_den[i] = den;
-                s_nan[i] = nan;
+                s_M[ii] = M;
+                s_den[ii] = den;
+                s_nan[ii] = nan;
             }
         }
     }
     __syncthreads();
-    // 3. every output element: one weighted sum in ascending piece order
-    for (int idx = threadIdx.x; idx < rows_here * P.Dv; idx += COMBINE_THREADS) {
-        const int i = idx / P.Dv, d = idx % P.Dv;
+    // 3. every 4 output channels: one weighted float4 sum in ascending piece order
+    const int DV4 = P.Dv >> 2;
+    const float4 *po = reinterpret_cast<const float4 *>(P.part_o);
+    const bool vec = (reinterpret_cast<uintptr_t>(P.out) & 15) == 0;
+    for (int idx = threadIdx.x; idx < rows_here * DV4; idx += COMBINE_THREADS) {
+        const int ii = idx / DV4, d = (idx - ii * DV4) * 4;
+        const int i = i0 + ii;
         const int r = rblk * RS + i;
-        float y, lse_v;
+        float4 y;
+        float lse_v;
         if (Pb == 0) {
             // no visible page: a flagged request is NaN, an empty one is 0
-            y = Rq.w ? NaN : 0.f;
+            const float z = Rq.w ? NaN : 0.f;
+            y = make_float4(z, z, z, z);
             lse_v = Rq.w ? NaN : -INFINITY;
-        } else if (s_nan[i]) {
-            y = lse_v = NaN;
-        } else if (s_M[i] == -INFINITY) {
-            y = 0.f;
+        } else if (s_nan[ii]) {
+            y = make_float4(NaN, NaN, NaN, NaN);
+            lse_v = NaN;
+        } else if (s_M[ii] == -INFINITY) {
+            y = make_float4(0.f, 0.f, 0.f, 0.f);
             lse_v = -INFINITY;
         } else {
-            const float M = s_M[i], den = s_den[i];
-            float acc = 0.f;
-            for (int n = 0; n < np; ++n) {
-                const long long slot = piece_slot(n);
-                const float w = cached ? s_w[n][i] : ex2((P.part_lse[slot * RS + i] - M) * LOG2E_);
-                acc += w * P.part_o[(slot * RS + i) * P.Dv + d];
+            const float M = s_M[ii], den = s_den[ii];
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+            int n = 0;
+            for (; n + 4 <= np; n += 4) {  // four loads in flight
+                float4 v[4];
+                float w[4];
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const long long slot = piece_slot(n + k);
+                    w[k] = cached ? s_w[n + k][ii] : ex2((P.part_lse[slot * RS + i] - M) * LOG2E_);
+                    v[k] = po[(slot * RS + i) * DV4 + (d >> 2)];
+                }
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    acc.x += w[k] * v[k].x;
+                    acc.y += w[k] * v[k].y;
+                    acc.z += w[k] * v[k].z;
+                    acc.w += w[k] * v[k].w;
+                }
             }
-            y = acc / den;
+            for (; n < np; ++n) {
+                const long long slot = piece_slot(n);
+                const float w = cached ? s_w[n][ii] : ex2((P.part_lse[slot * RS + i] - M) * LOG2E_);
+                const float4 v = po[(slot * RS + i) * DV4 + (d >> 2)];
+                acc.x += w * v.x;
+                acc.y += w * v.y;
+                acc.z += w * v.z;
+                acc.w += w * v.w;
+            }
+            const float inv = 1.0f / den;
+            y = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
             lse_v = M + lg2(den) * 0.6931471805599453f;
         }
-        float vsc = 1.0f;
-        if (P.v_mode == PA_SCALE_TENSOR) vsc = P.v_scale[0];
-        else if (P.v_mode == PA_SCALE_CHANNEL) vsc = P.v_scale[(size_t)kvh * P.Dv + d];
-        y *= vsc;
+        if (P.v_mode == PA_SCALE_TENSOR) {
+            const float s = P.v_scale[0];
+            y.x *= s; y.y *= s; y.z *= s; y.w *= s;
+        } else if (P.v_mode == PA_SCALE_CHANNEL) {
+            const float *vs = P.v_scale + (size_t)kvh * P.Dv + d;
+            y.x *= vs[0]; y.y *= vs[1]; y.z *= vs[2]; y.w *= vs[3];
+        }
         const int jq = r / P.G, h = kvh * P.G + (r % P.G);
         const size_t oi = (((size_t)b * P.n + jq) * P.Hq + h) * P.Dv + d;
-        if (P.out_dtype == PA_F32) reinterpret_cast<float *>(P.out)[oi] = y;
-        else if (P.out_dtype == PA_F16) reinterpret_cast<__half *>(P.out)[oi] = __float2half_rn(y);
-        else reinterpret_cast<__nv_bfloat16 *>(P.out)[oi] = __float2bfloat16_rn(y);
+        store4(P, oi, y, vec);
         if (P.lse != nullptr && d == 0) P.lse[((size_t)b * P.n + jq) * P.Hq + h] = lse_v;
     }
 }
@@ -160,9 +229,10 @@ __global__ void __launch_bounds__(COMBINE_THREADS) pa_combine_kernel(CombinePara
 cudaError_t launch_combine(const CombineParams &P, cudaStream_t s) {
     if (P.B == 0) return cudaSuccess;
     if (P.rows_seg < 1 || P.rows_seg > MAX_ROWS_SEG || P.gs < 1 || (P.Hkv * P.RBLK) % P.gs != 0 ||
-        P.nwarps % P.gs != 0)
+        P.nwarps % P.gs != 0 || (P.Dv & 3) != 0)
         return cudaErrorInvalidValue;
-    cudaError_t e = launch_pdl(pa_combine_kernel, dim3(P.B * P.Hkv * P.RBLK), dim3(COMBINE_THREADS), 0, s, P);
+    const dim3 grid((unsigned)(P.B * P.Hkv * P.RBLK), (unsigned)((P.rows_seg + COMBINE_ROWS - 1) / COMBINE_ROWS));
+    cudaError_t e = launch_pdl(pa_combine_kernel, grid, dim3(COMBINE_THREADS), 0, s, P);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
