@@ -207,8 +207,7 @@ pa_status derive_grouped(const pa_problem *p, Derived *d) {
             if ((size_t)workers * wsm(s) <= budget) slots = s;
         return slots;
     };
-    d->minb = D <= 128 ? pa::min_blocks<128, false>() : pa::min_blocks<256, false>(pair);
-    if (D <= 128 && d->tokm) d->minb = pa::min_blocks<128, true>();
+    d->minb = pa::min_blocks(bits, D, d->tokm, pair);
     // fewer resident CTAs until every worker holds two pages (one in flight
     // while it computes on the other); one page per worker as the last resort
     d->slots = fit(d->minb);

@@ -59,11 +59,16 @@ constexpr int NWK = 4;                     // warps per CTA, each an independent
 #ifndef PA_MIN_BLOCKS_PAIR
 #define PA_MIN_BLOCKS_PAIR 3
 #endif
+#ifndef PA_MIN_BLOCKS_TOKM_16BIT
+#define PA_MIN_BLOCKS_TOKM_16BIT 3
+#endif
 // resident CTAs per SM the register and shared-memory budgets are sized for
-// (tokens-as-M kernels need fewer registers)
-template <int D, bool TOKM>
-__host__ __device__ constexpr int min_blocks(bool pair = false) {
-    return D <= 128 ? (TOKM ? PA_MIN_BLOCKS_TOKM : PA_MIN_BLOCKS_SMALL_D)
+// (tokens-as-M kernels need fewer registers; with 16-bit codes two ring pages
+// per warp only fit 3 CTAs per SM at D = 128, so those are given the registers
+// of 3)
+__host__ __device__ constexpr int min_blocks(int bits, int D, bool tokm, bool pair) {
+    return D <= 128 ? (tokm ? (bits == 16 && D == 128 ? PA_MIN_BLOCKS_TOKM_16BIT : PA_MIN_BLOCKS_TOKM)
+                            : PA_MIN_BLOCKS_SMALL_D)
                     : (pair ? PA_MIN_BLOCKS_PAIR : PA_MIN_BLOCKS_LARGE_D);
 }
 // q' fragments live in registers for D <= 128, in the warp's shared memory above
@@ -316,7 +321,7 @@ __device__ __forceinline__ float load_q(const AttnParams &P, int b, int j, int h
 // (S^T = K q'^T and O^T = V^T P^T with the rows as N = 8), which halves the
 // tensor work and the O accumulator against padding 8 rows up to M = 16.
 template <int KVT, int D, bool TOKM>
-__global__ void __launch_bounds__(ATTN_THREADS, min_blocks<D, TOKM>(pair_mode(D, TOKM, Geo<KVT, D>::NSEG)))
+__global__ void __launch_bounds__(ATTN_THREADS, min_blocks(Geo<KVT, D>::BITS, D, TOKM, pair_mode(D, TOKM, Geo<KVT, D>::NSEG)))
     pa_attn_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv, AttnParams P) {
     using G = Geo<KVT, D>;
     constexpr bool BF = G::BF;
