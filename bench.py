@@ -106,6 +106,24 @@ def _traffic(workload: str):
     return None
 
 
+def max_over_ranks(values, world: int, device):
+    """Element-wise maximum of per-rank timings over all ranks (the slowest
+    rank sets the step time); identity for one rank."""
+    if world <= 1:
+        return list(values)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor(list(values), dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
+def job_value(world: int, bytes_per_rank: int, ms_per_step: float) -> float:
+    """Whole-job effective GB/s: every rank processes its own replica of the
+    workload in the (max-over-ranks) step time."""
+    return world * bytes_per_rank / (ms_per_step * 1e-3) / 1e9
+
+
 class ClockSampler:
     """nvidia-smi clock / throttle samples while the timed region runs."""
 
@@ -284,13 +302,9 @@ def gpu_arm(args, rank, world, local_rank):
     total_ms = sum(step_ms)
     attn_avg = sum(attn_ms) / len(attn_ms)
     e2e_avg = sum(e2e_ms) / len(e2e_ms)
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([total_ms, attn_avg, e2e_avg], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms, attn_avg, e2e_avg = t.tolist()
+    total_ms, attn_avg, e2e_avg = max_over_ranks([total_ms, attn_avg, e2e_avg], world, dev)
     ms_per_step = total_ms / args.steps
-    value = world * eff_bytes / (ms_per_step * 1e-3) / 1e9
+    value = job_value(world, eff_bytes, ms_per_step)
     peak, peak_kind = _peaks()
     achieved = eff_bytes / (attn_avg * 1e-3) / 1e9
     traffic = _traffic(args.workload)
