@@ -129,7 +129,7 @@ typedef struct pa_problem {
     int32_t num_kv_heads;       /* Hkv, divides Hq */
     int32_t head_dim_k;         /* Dk */
     int32_t head_dim_v;         /* Dv */
-    int32_t block_size;         /* bs, tokens per block */
+    int32_t block_size;         /* bs, tokens per block (grouped kernel: a multiple of 16, <= 128; latent: 64) */
     int32_t num_blocks;         /* blocks in the pool (block 0 = null block) */
     int32_t max_blocks_per_seq; /* block_table columns */
     int32_t max_context_len;    /* bound on every context_lens entry */
@@ -148,8 +148,11 @@ typedef struct pa_problem {
 /* Byte offsets inside the workspace (all 256-byte aligned) and the launch
  * shape.  Header words (uint32): [0] device error bits, [1] total pages
  * sum_b P_b of the plan, [3] max|k_scale| (fp32 bits).  Request records
- * (int32 x4 per request): {L_b seen by pa_plan, P_b = ceil(L_b / bs) (0 when
- * L_b breaks the contract), PS_b = sum of P over earlier requests, flags}.
+ * (int32 x4 per request): {L_b seen by pa_plan, P_b = ceil(L_b / wp) (0 when
+ * L_b breaks the contract), PS_b = sum of P over earlier requests, flags},
+ * with wp = work_page_tokens: bs, or an equal part of a block when a block
+ * is too large for the kernel's shared-memory ring (a "page" below is a work
+ * page; the parts of a block are consecutive positions).
  *
  * pa_run orders every page of the batch by logical position -- request,
  * kv head, block of S query rows ("segment"), page -- and gives worker k of
@@ -188,6 +191,8 @@ typedef struct pa_layout {
     int32_t ring_pages_per_warp; /* pages each worker keeps in flight */
     int32_t rows_per_segment;    /* S: 16 (grouped) or 64 (latent) */
     int32_t group_size;          /* G: workers sharing one run of pages (1, or row_blocks for latent) */
+    int32_t work_page_tokens;    /* tokens the attention handles as one page: block_size, or an equal
+                                    part of a block (>= 16) when two whole blocks per worker do not fit */
 } pa_layout;
 
 /* Library version: major * 10000 + minor * 100 + patch. */

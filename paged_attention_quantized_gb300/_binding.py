@@ -46,7 +46,7 @@ class Layout(ctypes.Structure):
         "total_bytes", "header_offset", "requests_offset", "partial_o_offset", "partial_lse_offset")] + \
         [("partial_slots", ctypes.c_int64)] + [(k, ctypes.c_int32) for k in (
             "rows_per_kv_head", "row_blocks", "num_sms", "grid_ctas", "warps", "ring_pages_per_warp",
-            "rows_per_segment", "group_size")]
+            "rows_per_segment", "group_size", "work_page_tokens")]
 
 
 if not os.path.exists(LIB_PATH):

@@ -72,6 +72,7 @@ struct Derived {
     int gs;        // workers per group (they share one run of pages, one row block each)
     long long nwarps, slots_partial;
     int D, RB, SW, slots, warp_smem;
+    int wp, wpb;   // work page: tokens the kernel handles as one page (a block, or an equal part of one), parts per block
     size_t k_block, v_block, smem;
     pa_layout L;
 };
@@ -126,6 +127,8 @@ pa_status derive(const pa_problem *p, Derived *d) {
         d->k_block = (size_t)p->num_kv_heads * LAT_BS * (LAT_DK + 4);
         d->v_block = d->k_block;
         d->slots = LAT_RING;
+        d->wp = LAT_BS;
+        d->wpb = 1;
         d->warp_smem = 0;
         d->smem = 0;
         // the workers are CTAs, in groups of one per row block
@@ -163,6 +166,7 @@ pa_status derive(const pa_problem *p, Derived *d) {
     Lo.ring_pages_per_warp = d->slots;
     Lo.rows_per_segment = d->rows_seg;
     Lo.group_size = d->gs;
+    Lo.work_page_tokens = d->wp;
     return PA_OK;
 }
 
@@ -192,32 +196,50 @@ pa_status derive_grouped(const pa_problem *p, Derived *d) {
     // D = 256 with rows on the MMA M axis): as many as fit the shared memory of
     // the resident CTAs per SM the kernel's registers allow; with pages too
     // large for two per worker, fewer CTAs per SM, and one page per worker as
-    // the last resort.
-    const int page_bytes = 2 * bs * d->RB;
+    // the last resort.  A block too large for that is handled as 2, 3, ...
+    // equal work pages of at least 16 tokens (logical order is unchanged: the
+    // parts of a block are consecutive positions), whichever split keeps the
+    // most CTAs per SM with the minimum ring, the larger page on a tie.
     d->tokm = d->R <= PA_TOKM_MAX_ROWS;  // few query rows per kv head: tokens on the MMA M axis
     const bool pair = pa::pair_mode(D, d->tokm, d->RB / d->SW);
     const int workers = pa::NWK / (pair ? 2 : 1);  // per CTA
-    auto wsm = [&](int s) {
+    const int min_pages = pair ? PA_MIN_RING_PAGES_PAIR : PA_MIN_RING_PAGES;
+    auto wsm = [&](int s, int wp) {
+        const int page_bytes = 2 * wp * d->RB;
         return D <= 128 ? pa::warp_smem_bytes<128>(s, page_bytes, pair) : pa::warp_smem_bytes<256>(s, page_bytes, pair);
     };
-    auto fit = [&](int minb) {
+    auto fit = [&](int minb, int wp) {
         const size_t budget = std::min(MAX_DYN_SMEM_BYTES, SM_SMEM_BYTES / minb - CTA_RESERVED_BYTES) - 1024;
         int slots = 0;
         for (int s = 1; s <= pa::MAX_SLOTS; ++s)
-            if ((size_t)workers * wsm(s) <= budget) slots = s;
+            if ((size_t)workers * wsm(s, wp) <= budget) slots = s;
         return slots;
     };
-    d->minb = pa::min_blocks(bits, D, d->tokm, pair);
-    // fewer resident CTAs until every worker holds two pages (one in flight
-    // while it computes on the other); one page per worker as the last resort
-    d->slots = fit(d->minb);
-    const int min_pages = pair ? PA_MIN_RING_PAGES_PAIR : PA_MIN_RING_PAGES;
-    while (d->slots < min_pages && d->minb > 1) {
-        d->minb -= 1;
-        d->slots = fit(d->minb);
+    bool found = false;
+    int best_ok = 0;
+    for (int wp = bs; wp >= 16; wp -= 16) {
+        if (bs % wp != 0) continue;  // work pages: equal parts of a block, multiples of 16 tokens
+        // fewer resident CTAs until every worker holds two pages (one in flight
+        // while it computes on the other); one page per worker as the last resort
+        int minb = pa::min_blocks(bits, D, d->tokm, pair);
+        int slots = fit(minb, wp);
+        while (slots < min_pages && minb > 1) {
+            minb -= 1;
+            slots = fit(minb, wp);
+        }
+        if (slots < 1) continue;
+        const int ok = slots >= min_pages ? 1 : 0;
+        if (!found || ok > best_ok || (ok == best_ok && minb > d->minb)) {
+            found = true;
+            best_ok = ok;
+            d->minb = minb;
+            d->slots = slots;
+            d->wp = wp;
+        }
     }
-    if (d->slots < 1) return PA_ERR_UNSUPPORTED;
-    d->warp_smem = wsm(d->slots);
+    if (!found) return PA_ERR_UNSUPPORTED;
+    d->wpb = bs / d->wp;
+    d->warp_smem = wsm(d->slots, d->wp);
     d->smem = 1024 + (size_t)workers * d->warp_smem;
     d->ctas = p->grid_ctas > 0 ? p->grid_ctas : d->sms * d->minb;
     d->nwarps = (long long)d->ctas * workers;
@@ -268,8 +290,8 @@ T *at(void *ws, size_t off) {
     return reinterpret_cast<T *>(static_cast<uint8_t *>(ws) + off);
 }
 
-// One tile of the grouped kernel -- all segments of [bs][RB] for one kv head of
-// one block -- as a single 5-D box {SW bytes, bs rows, NSEG segments, 1, 1}:
+// One tile of the grouped kernel -- all segments of [wp][RB] for one kv head of
+// one work page of a block -- as a single 5-D box {SW bytes, wp rows, NSEG segments, 1, 1}:
 // the segment dimension (stride SW) is placed outside the rows, so the box
 // lands as [segment][row][SW bytes], each SW-byte line swizzled by its row.
 pa_status make_tmap_tile(CUtensorMap *tm, const void *base, const Derived &d, const pa_problem *p,
@@ -281,7 +303,7 @@ pa_status make_tmap_tile(CUtensorMap *tm, const void *base, const Derived &d, co
                           (cuuint64_t)p->num_kv_heads, (cuuint64_t)p->num_blocks};
     cuuint64_t strides[4] = {(cuuint64_t)d.RB, (cuuint64_t)d.SW, (cuuint64_t)p->block_size * d.RB,
                              (cuuint64_t)block_stride};
-    cuuint32_t box[5] = {(cuuint32_t)d.SW, (cuuint32_t)p->block_size, (cuuint32_t)nseg, 1, 1};
+    cuuint32_t box[5] = {(cuuint32_t)d.SW, (cuuint32_t)d.wp, (cuuint32_t)nseg, 1, 1};  // one work page
     cuuint32_t es[5] = {1, 1, 1, 1, 1};
     CUresult r = enc(tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, 5, const_cast<void *>(base), dims, strides, box, es,
                      CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -294,8 +316,10 @@ cudaError_t dispatch_attn(const pa_problem *p, const Derived &d, const CUtensorM
                           const pa::AttnParams &P, cudaStream_t s) {
     const dim3 grid((unsigned)d.ctas);
     const bool tokm = d.tokm;
-#define PA_CASE(KVT, DD) \
-    if (p->kv_dtype == KVT && d.D == DD) return pa::launch_attn<KVT, DD>(tk, tv, P, grid, d.smem, tokm, s);
+#define PA_CASE(KVT, DD)                                                                               \
+    if (p->kv_dtype == KVT && d.D == DD)                                                               \
+        return d.wpb > 1 ? pa::launch_attn_split<KVT, DD>(tk, tv, P, grid, d.smem, tokm, s)             \
+                         : pa::launch_attn<KVT, DD>(tk, tv, P, grid, d.smem, tokm, s);
     PA_CASE(PA_F16, 64) PA_CASE(PA_F16, 128) PA_CASE(PA_F16, 256)
     PA_CASE(PA_BF16, 64) PA_CASE(PA_BF16, 128) PA_CASE(PA_BF16, 256)
     PA_CASE(PA_E4M3, 64) PA_CASE(PA_E4M3, 128) PA_CASE(PA_E4M3, 256)
@@ -353,9 +377,9 @@ PA_API pa_status pa_plan(const pa_problem *p, const int32_t *context_lens, const
     P.hdr = at<uint32_t>(workspace, d.L.header_offset);
     P.req = at<int4>(workspace, d.L.requests_offset);
     P.B = p->batch;
-    P.bs = p->block_size;
+    P.bs = d.wp;                                        // work pages (a block, or an equal part of one)
     P.max_ctx = p->max_context_len;
-    P.mbps = p->max_blocks_per_seq;
+    P.mbps = p->max_blocks_per_seq * d.wpb;
     const float *ks = (p->k_scale_mode == PA_SCALE_CHANNEL) ? k_scale : nullptr;
     cudaError_t e = pa::launch_plan(P, ks, p->num_kv_heads * p->head_dim_k, reinterpret_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
@@ -440,8 +464,10 @@ PA_API pa_status pa_run(const pa_problem *p, const void *q, const void *k_pool, 
     P.G = d.G;
     P.R = d.R;
     P.RBLK = d.row_blocks;
-    P.bs = p->block_size;
-    P.mbps = p->max_blocks_per_seq;
+    P.bs = d.wp;                                    // work pages (a block, or an equal part of one)
+    P.mbps = p->max_blocks_per_seq * d.wpb;
+    P.wpb = d.wpb;
+    P.tbl_stride = p->max_blocks_per_seq;
     P.num_blocks = p->num_blocks;
     P.q_dtype = p->q_dtype;
     P.out_dtype = p->out_dtype;

@@ -320,7 +320,9 @@ __device__ __forceinline__ float load_q(const AttnParams &P, int b, int j, int h
 // TOKM: at most 8 query rows per kv head.  Tokens then form the MMA M axis
 // (S^T = K q'^T and O^T = V^T P^T with the rows as N = 8), which halves the
 // tensor work and the O accumulator against padding 8 rows up to M = 16.
-template <int KVT, int D, bool TOKM>
+// SPLIT: a block is handled as P.wpb equal work pages of P.bs tokens (blocks
+// too large for the shared-memory ring); the plan counts work pages.
+template <int KVT, int D, bool TOKM, bool SPLIT>
 __global__ void __launch_bounds__(ATTN_THREADS, min_blocks(Geo<KVT, D>::BITS, D, TOKM, pair_mode(D, TOKM, Geo<KVT, D>::NSEG)))
     pa_attn_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv, AttnParams P) {
     using G = Geo<KVT, D>;
@@ -406,13 +408,20 @@ __global__ void __launch_bounds__(ATTN_THREADS, min_blocks(Geo<KVT, D>::BITS, D,
             slot_bad |= 1u << slot;
             return;
         }
-        if (ci.b != idc_b || ci.p < idc_w0 || ci.p >= idc_w0 + 32) {
-            idc_b = ci.b;
-            idc_w0 = ci.p;
-            const int pg = idc_w0 + lane;
-            idc = (pg < ci.Pb) ? P.block_table[(size_t)ci.b * P.mbps + pg] : 0;
+        // work page ci.p: rows [y0, y0 + bs) of block bi of the request
+        int bi = ci.p, y0 = 0, nblk = ci.Pb;
+        if constexpr (SPLIT) {
+            bi = ci.p / P.wpb;
+            y0 = (ci.p - bi * P.wpb) * bs;
+            nblk = (ci.Pb + P.wpb - 1) / P.wpb;
         }
-        const int blk = __shfl_sync(0xffffffffu, idc, ci.p - idc_w0);
+        if (ci.b != idc_b || bi < idc_w0 || bi >= idc_w0 + 32) {
+            idc_b = ci.b;
+            idc_w0 = bi;
+            const int pg = idc_w0 + lane;
+            idc = (pg < nblk) ? P.block_table[(size_t)ci.b * P.tbl_stride + pg] : 0;
+        }
+        const int blk = __shfl_sync(0xffffffffu, idc, bi - idc_w0);
         const bool ok = blk >= 1 && blk < P.num_blocks;
         const int kvh = (P.RBLK == 1) ? ci.q : ci.q / P.RBLK;
         if constexpr (PAIR) {
@@ -423,8 +432,8 @@ __global__ void __launch_bounds__(ATTN_THREADS, min_blocks(Geo<KVT, D>::BITS, D,
             uint8_t *vt = kt + tile_bytes;
             if (ok) {
                 mbar_arrive_expect_tx(&full[slot], (uint32_t)page_bytes);
-                tma_load_5d(kt, &tmk, &full[slot], 0, 0, 0, kvh, blk);  // all segments of the K tile
-                tma_load_5d(vt, &tmv, &full[slot], 0, 0, 0, kvh, blk);
+                tma_load_5d(kt, &tmk, &full[slot], 0, y0, 0, kvh, blk);  // all segments of the K tile
+                tma_load_5d(vt, &tmv, &full[slot], 0, y0, 0, kvh, blk);
             } else {
                 mbar_arrive(&full[slot]);  // no copy: the piece is NaN-filled
             }

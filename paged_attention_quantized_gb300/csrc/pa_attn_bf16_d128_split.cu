@@ -1,0 +1,7 @@
+// Attention kernel instantiations for BF16 KV codes, head dim 128, blocks handled as
+// several work pages.
+#include "pa_attn_launch.cuh"
+
+namespace pa {
+PA_DEFINE_ATTN_SPLIT(PA_BF16, 128)
+}  // namespace pa

@@ -1,0 +1,7 @@
+// Attention kernel instantiations for F16 KV codes, head dim 64, blocks handled as
+// several work pages.
+#include "pa_attn_launch.cuh"
+
+namespace pa {
+PA_DEFINE_ATTN_SPLIT(PA_F16, 64)
+}  // namespace pa

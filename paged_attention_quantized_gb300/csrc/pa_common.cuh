@@ -26,7 +26,11 @@ struct AttnParams {
     float *part_lse;     // [slots][16]
     void *out;
     float *lse;
-    int B, n, Hq, Hkv, G, R, RBLK, bs, mbps, num_blocks;
+    int B, n, Hq, Hkv, G, R, RBLK, num_blocks;
+    int bs;              // tokens of a work page: a block, or an equal part of one
+    int mbps;            // work pages per request at most (table width x wpb)
+    int wpb;             // work pages per block
+    int tbl_stride;      // block_table row stride (blocks per request)
     int q_dtype, out_dtype, k_mode, v_mode, causal;
     int slots;           // ring pages per warp
     int warp_smem;       // shared-memory bytes per warp

@@ -175,9 +175,10 @@ def make(name: str, device="cpu", seed: Optional[int] = None, *, B: Optional[int
          L_lo: Optional[int] = None, L_hi: Optional[int] = None, context_lens=None,
          poison: Optional[bool] = None, slack_frac: float = 0.10, n: Optional[int] = None,
          Hq: Optional[int] = None, Hkv: Optional[int] = None, D: Optional[int] = None,
-         token_scale_spread: int = 0) -> Workload:
+         token_scale_spread: int = 0, bs: Optional[int] = None) -> Workload:
     """Draw one workload.  `name` picks the recipe; keyword overrides shrink it
-    (batch, length range, explicit lengths, heads) for tests.  Everything is a
+    (batch, length range, explicit lengths, heads, head dim, block size) for
+    tests.  Everything is a
     deterministic function of (name, seed, overrides, device).
 
     token_scale_spread = k > 0 (per-token E4M3 scales only): every block's
@@ -186,7 +187,7 @@ def make(name: str, device="cpu", seed: Optional[int] = None, *, B: Optional[int
     to 2^k while the dequantized values keep their distribution."""
     if name not in _SHAPES:
         raise ValueError(f"unknown workload {name!r}")
-    (B0, n0, Hq0, Hkv0, Dk, Dv, bs, qd, kvd, outd, kmode, vmode, causal, vprefix) = _SHAPES[name]
+    (B0, n0, Hq0, Hkv0, Dk, Dv, bs0, qd, kvd, outd, kmode, vmode, causal, vprefix) = _SHAPES[name]
     seed = CONFIG_SEED[name] if seed is None else seed
     B = B0 if B is None else B
     n = n0 if n is None else n
@@ -196,6 +197,12 @@ def make(name: str, device="cpu", seed: Optional[int] = None, *, B: Optional[int
         if vprefix:
             raise ValueError("the latent recipe has fixed head dims")
         Dk = Dv = D
+    if bs is not None:
+        if vprefix:
+            raise ValueError("the latent recipe has a fixed block size")
+        bs = int(bs)
+    else:
+        bs = bs0
     poison = (name == "e4m3") if poison is None else poison
     device = torch.device(device)
     gcpu = _gen("cpu", seed)

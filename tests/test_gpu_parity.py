@@ -331,3 +331,43 @@ def test_full_size_sampled_parity(name):
     w2 = W.relocate(w, seed=5)
     o2, l2, _, _ = run_gpu(w2)
     assert torch.equal(out, o2) and torch.equal(lse, l2)
+
+
+# ------------------------------------------------------- blocks as work pages
+
+LARGE_BLOCKS = [
+    ("bf16", dict(D=128, bs=128, Hq=8, Hkv=2)),           # tokens on M, 16-token work pages
+    ("bf16", dict(D=256, bs=64, Hq=8, Hkv=2, n=4)),       # paired warps
+    ("tiny", dict(D=256, bs=48, Hq=4, Hkv=2)),            # f16, a block in three parts
+    ("e4m3", dict(bs=128, Hq=8, Hkv=2)),                  # the verify shape (n=4, D=256)
+    ("int8", dict(D=256, bs=96, Hq=16, Hkv=2)),
+    ("int4", dict(bs=64, Hq=64, Hkv=2)),                  # 32 rows per kv head: two row blocks
+]
+
+
+@pytest.mark.parametrize("name,kw", LARGE_BLOCKS, ids=lambda x: str(x))
+@pytest.mark.parametrize("split", [0, 5])
+def test_large_blocks_as_work_pages(name, kw, split):
+    """Blocks whose K and V tiles do not fit twice per worker are handled as
+    equal parts of at least 16 tokens: same results as the oracle, the plan
+    in those work pages, bitwise stable under relocation."""
+    w = make(name, B=3, L_lo=1, L_hi=700, **kw)
+    p = pa.problem(w, grid_ctas=split)
+    lo = pa.binding().pa_workspace_layout(p)
+    wp = lo.work_page_tokens
+    assert 16 <= wp <= w.bs and w.bs % wp == 0 and wp % 16 == 0
+    if name in ("bf16", "tiny"):
+        assert wp < w.bs  # these shapes only fit as parts of a block
+    out, lse, ws, _ = run_gpu(w, grid_ctas=split)
+    assert error_bits(ws) == 0
+    compare(w, out, lse)
+    raw = ws.cpu().numpy()
+    pl = oracle.plan(w.context_lens.cpu().numpy(), bs=wp, Hkv=w.Hkv, max_context_len=w.max_context_len,
+                     max_blocks_per_seq=w.max_blocks_per_seq * (w.bs // wp), row_blocks=lo.row_blocks,
+                     warps=lo.warps)
+    req = raw[lo.requests_offset: lo.requests_offset + 16 * w.B].view(np.int32).reshape(w.B, 4)
+    assert np.array_equal(req[:, 1], pl["pages"]) and np.array_equal(req[:, 2], pl["prefix"])
+    o2, l2, _, _ = run_gpu(W.relocate(w, seed=3), grid_ctas=split)
+    assert torch.equal(out, o2) and torch.equal(lse, l2)
+    o3, l3, ws3, _ = run_gpu(W.poison_unreferenced(w, seed=4), grid_ctas=split)
+    assert error_bits(ws3) == 0 and torch.equal(out, o3) and torch.equal(lse, l3)
