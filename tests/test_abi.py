@@ -184,3 +184,21 @@ def test_partial_slots_cover_oracle_pieces(B, latent):
                          row_blocks=lo.row_blocks, warps=lo.warps, group_size=lo.group_size)
         assert pl["slots"] == lo.partial_slots
         assert all(pc["slot"] < lo.partial_slots for pc in pl["pieces"])
+
+
+def test_every_block_size_has_a_launch(B):
+    """Every KV encoding x head dim x block size (multiples of 16 up to 128) x
+    rows per kv head gets a launch: whole blocks when two per worker fit,
+    else equal work pages of >= 16 tokens; the recipe shapes keep whole blocks."""
+    for kv in (B.PA_F16, B.PA_BF16, B.PA_E4M3, B.PA_INT8, B.PA_INT4):
+        for D in (64, 128, 256):
+            if kv == B.PA_INT4 and D == 64:
+                continue
+            for bs in range(16, 129, 16):
+                for hq, n in ((8, 1), (32, 1), (64, 1), (32, 4), (128, 2)):
+                    p = _prob(B, kv_dtype=kv, head_dim_k=D, head_dim_v=D, block_size=bs, num_q_heads=hq, next_n=n)
+                    lo = B.pa_workspace_layout(p)
+                    wp = lo.work_page_tokens
+                    assert wp % 16 == 0 and bs % wp == 0 and lo.ring_pages_per_warp >= 1, (kv, D, bs, hq, n)
+                    if bs == 16:
+                        assert wp == 16
