@@ -371,3 +371,18 @@ def test_large_blocks_as_work_pages(name, kw, split):
     assert torch.equal(out, o2) and torch.equal(lse, l2)
     o3, l3, ws3, _ = run_gpu(W.poison_unreferenced(w, seed=4), grid_ctas=split)
     assert error_bits(ws3) == 0 and torch.equal(out, o3) and torch.equal(lse, l3)
+
+
+@pytest.mark.parametrize("name,kw", [
+    ("bf16", dict(Hq=128, Hkv=2, n=4)),    # 256 query rows per kv head: 16 row blocks
+    ("int8", dict(Hq=64, Hkv=1, n=8)),     # 512 rows, one kv head
+    ("e4m3", dict(Hq=32, Hkv=4, n=16)),    # causal verify with 16 new tokens per request
+])
+def test_many_query_rows_per_kv_head(name, kw):
+    w = make(name, B=3, L_lo=16, L_hi=400, **kw)
+    lo = pa.binding().pa_workspace_layout(pa.problem(w))
+    assert lo.row_blocks == lo.rows_per_kv_head // 16
+    for split in (0, 7):
+        out, lse, ws, _ = run_gpu(w, grid_ctas=split)
+        assert error_bits(ws) == 0
+        compare(w, out, lse)
