@@ -54,14 +54,15 @@ __device__ __forceinline__ void store4(const CombineParams &P, size_t oi, float4
     }
 }
 
-// One CTA per (segment, block of 16 query rows of it).  The pieces (non-empty
-// worker shares) and the per-row weights w = exp(lse - M) are worked out once;
-// every 4 output channels are then one weighted sum of float4 partials.
+// One CTA per (segment, block of 16 query rows of it).  Every thread owns 4
+// output channels of a row at a time and merges them on its own: the row's
+// lse values (the same for the 32 threads of a row, so they come from L1),
+// their maximum, the weights and their sum in ascending piece order, and the
+// weighted float4 sum of the partials -- one round of memory latency and no
+// block barrier (except for listing the pieces when some shares are empty).
 __global__ void __launch_bounds__(COMBINE_THREADS) pa_combine_kernel(CombineParams P) {
-    __shared__ long long s_piece[MAX_CACHED_PIECES];          // partial slots, ascending worker order
-    __shared__ float s_w[MAX_CACHED_PIECES][COMBINE_ROWS];    // weight of piece n for row i
-    __shared__ float s_M[COMBINE_ROWS], s_den[COMBINE_ROWS];
-    __shared__ int s_np, s_nan[COMBINE_ROWS];
+    __shared__ long long s_piece[MAX_CACHED_PIECES];  // partial slots, ascending worker order (some shares empty)
+    __shared__ int s_np;
     grid_dependency_wait();  // the attention's partials are complete
     const int X = P.Hkv * P.RBLK;
     const int seg = blockIdx.x;
@@ -89,30 +90,25 @@ __global__ void __launch_bounds__(COMBINE_THREADS) pa_combine_kernel(CombinePara
         if (kf == kl) return;  // one piece: the attention kernel wrote the output
     }
     const long long slot0 = ((long long)b * U + u) * GS + gi;  // slot of group g: slot0 + g * GS
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     // 1. the pieces: worker groups kf..kl with a non-empty share.  With at
-    //    least as many positions as groups every share is non-empty.
-    if (threadIdx.x == 0) {
+    //    least as many positions as groups every share is non-empty and the
+    //    n-th piece is group kf + n; otherwise thread 0 lists them.
+    if (threadIdx.x == 0 && N < NG) {
         int np = 0;
-        if (N >= NG) {
-            np = (int)min(kl - kf + 1, 0x7fffffffll);
-            for (int n = 0; n < min(np, MAX_CACHED_PIECES); ++n) s_piece[n] = slot0 + (kf + n) * GS;
-        } else {
-            for (long long k = kf; k <= kl; ++k) {
-                if (share_start(k, N, NG) == share_start(k + 1, N, NG)) continue;
-                if (np < MAX_CACHED_PIECES) s_piece[np] = slot0 + k * GS;
-                ++np;
-            }
+        for (long long k = kf; k <= kl; ++k) {
+            if (share_start(k, N, NG) == share_start(k + 1, N, NG)) continue;
+            if (np < MAX_CACHED_PIECES) s_piece[np] = slot0 + k * GS;
+            ++np;
         }
         s_np = np;
     }
-    __syncthreads();
-    const int np = s_np;
+    if (N < NG) __syncthreads();  // uniform: the same N and NG in every thread
+    const int np = (N >= NG) ? (int)min(kl - kf + 1, 0x7fffffffll) : s_np;
     const bool cached = np <= MAX_CACHED_PIECES;
     // slot of the n-th piece (recomputed when there are too many to cache)
     auto piece_slot = [&](int n) -> long long {
-        if (cached) return s_piece[n];
         if (N >= NG) return slot0 + (kf + n) * GS;
+        if (cached) return s_piece[n];
         int seen = 0;
         for (long long k = kf; k <= kl; ++k) {
             if (share_start(k, N, NG) == share_start(k + 1, N, NG)) continue;
@@ -120,44 +116,10 @@ __global__ void __launch_bounds__(COMBINE_THREADS) pa_combine_kernel(CombinePara
         }
         return slot0 + kf * GS;
     };
-    // 2. per row: M = max lse, den = sum exp(lse - M), NaN if any piece is NaN
-    if (Pb > 0) {
-        for (int ii = warp; ii < rows_here; ii += COMBINE_THREADS / 32) {
-            const int i = i0 + ii;
-            float M = -INFINITY;
-            int nan = 0;
-            for (int n = lane; n < np; n += 32) {
-                const float l = P.part_lse[piece_slot(n) * RS + i];
-                if (cached) s_w[n][ii] = l;
-                nan |= (l != l);
-                M = fmaxf(M, l);
-            }
-#pragma unroll
-            for (int o = 16; o >= 1; o >>= 1) {
-                M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-                nan |= __shfl_xor_sync(0xffffffffu, nan, o);
-            }
-            float den = 0.f;
-            if (M != -INFINITY && !nan) {
-                for (int n = lane; n < np; n += 32) {
-                    const float l = cached ? s_w[n][ii] : P.part_lse[piece_slot(n) * RS + i];
-                    const float w = ex2((l - M) * LOG2E_);
-                    if (cached) s_w[n][ii] = w;
-                    den += w;
-                }
-            }
-            // fixed-order sum of the lane partials (bitwise reproducible)
-#pragma unroll
-            for (int o = 16; o >= 1; o >>= 1) den += __shfl_xor_sync(0xffffffffu, den, o);
-            if (lane == 0) {
-                s_M[ii] = M;
-                s_den[ii] = den;
-                s_nan[ii] = nan;
-            }
-        }
-    }
-    __syncthreads();
-    // 3. every 4 output channels: one weighted float4 sum in ascending piece order
+    // 2. every 4 output channels of a row: the row's M = max lse, the weights
+    //    exp(lse - M) and their sum in ascending piece order, then one weighted
+    //    float4 sum; the loads of a row's lse values and partials are all
+    //    independent (one round of memory latency, no block barrier)
     const int DV4 = P.Dv >> 2;
     const float4 *po = reinterpret_cast<const float4 *>(P.part_o);
     const bool vec = (reinterpret_cast<uintptr_t>(P.out) & 15) == 0;
@@ -172,49 +134,61 @@ __global__ void __launch_bounds__(COMBINE_THREADS) pa_combine_kernel(CombinePara
             const float z = Rq.w ? NaN : 0.f;
             y = make_float4(z, z, z, z);
             lse_v = Rq.w ? NaN : -INFINITY;
-        } else if (s_nan[ii]) {
-            y = make_float4(NaN, NaN, NaN, NaN);
-            lse_v = NaN;
-        } else if (s_M[ii] == -INFINITY) {
-            y = make_float4(0.f, 0.f, 0.f, 0.f);
-            lse_v = -INFINITY;
         } else {
-            const float M = s_M[ii], den = s_den[ii];
-            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-            int n = 0;
-            for (; n + 4 <= np; n += 4) {  // four loads in flight
-                float4 v[4];
-                float w[4];
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const long long slot = piece_slot(n + k);
-                    w[k] = cached ? s_w[n + k][ii] : ex2((P.part_lse[slot * RS + i] - M) * LOG2E_);
-                    v[k] = po[(slot * RS + i) * DV4 + (d >> 2)];
-                }
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    acc.x += w[k] * v[k].x;
-                    acc.y += w[k] * v[k].y;
-                    acc.z += w[k] * v[k].z;
-                    acc.w += w[k] * v[k].w;
-                }
+            float M = -INFINITY;
+            bool nan = false;
+            for (int n = 0; n < np; ++n) {
+                const float l = P.part_lse[piece_slot(n) * RS + i];
+                nan |= (l != l);
+                M = fmaxf(M, l);
             }
-            for (; n < np; ++n) {
-                const long long slot = piece_slot(n);
-                const float w = cached ? s_w[n][ii] : ex2((P.part_lse[slot * RS + i] - M) * LOG2E_);
-                const float4 v = po[(slot * RS + i) * DV4 + (d >> 2)];
-                acc.x += w * v.x;
-                acc.y += w * v.y;
-                acc.z += w * v.z;
-                acc.w += w * v.w;
+            if (nan) {
+                y = make_float4(NaN, NaN, NaN, NaN);
+                lse_v = NaN;
+            } else if (M == -INFINITY) {
+                y = make_float4(0.f, 0.f, 0.f, 0.f);
+                lse_v = -INFINITY;
+            } else {
+                float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+                float den = 0.f;
+                int n = 0;
+                for (; n + 4 <= np; n += 4) {  // four pieces' loads in flight
+                    float4 v[4];
+                    float w[4];
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const long long slot = piece_slot(n + k);
+                        w[k] = P.part_lse[slot * RS + i];
+                        v[k] = po[(slot * RS + i) * DV4 + (d >> 2)];
+                    }
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        w[k] = ex2((w[k] - M) * LOG2E_);
+                        den += w[k];
+                        acc.x += w[k] * v[k].x;
+                        acc.y += w[k] * v[k].y;
+                        acc.z += w[k] * v[k].z;
+                        acc.w += w[k] * v[k].w;
+                    }
+                }
+                for (; n < np; ++n) {
+                    const long long slot = piece_slot(n);
+                    const float w = ex2((P.part_lse[slot * RS + i] - M) * LOG2E_);
+                    const float4 v = po[(slot * RS + i) * DV4 + (d >> 2)];
+                    den += w;
+                    acc.x += w * v.x;
+                    acc.y += w * v.y;
+                    acc.z += w * v.z;
+                    acc.w += w * v.w;
+                }
+                const float inv = 1.0f / den;
+                y = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+                lse_v = M + lg2(den) * 0.6931471805599453f;
             }
-            const float inv = 1.0f / den;
-            y = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
-            lse_v = M + lg2(den) * 0.6931471805599453f;
         }
         if (P.v_mode == PA_SCALE_TENSOR) {
-            const float s = P.v_scale[0];
-            y.x *= s; y.y *= s; y.z *= s; y.w *= s;
+            const float sc = P.v_scale[0];
+            y.x *= sc; y.y *= sc; y.z *= sc; y.w *= sc;
         } else if (P.v_mode == PA_SCALE_CHANNEL) {
             const float *vs = P.v_scale + (size_t)kvh * P.Dv + d;
             y.x *= vs[0]; y.y *= vs[1]; y.z *= vs[2]; y.w *= vs[3];
