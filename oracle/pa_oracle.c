@@ -41,7 +41,7 @@
  *    method.  The oracle's summation order is the logical token order, so its
  *    result is bitwise independent of the physical block ids.
  *
- * Readings where the pages are silent (each is listed in the design doc):
+ * Readings where the pages are silent:
  *  - pool layout: head-major [num_blocks][Hkv][bs][row_bytes]; with per-token
  *    scales every block is [Hkv][bs][row_bytes] codes followed by [Hkv][bs] fp32
  *    scales (the FlashInfer page's "data region, then scale-factor region");

@@ -58,7 +58,7 @@ __device__ __forceinline__ void store4(const CombineParams &P, size_t oi, float4
 // output channels of a row at a time and merges them on its own: the row's
 // lse values (the same for the 32 threads of a row, so they come from L1),
 // their maximum, the weights and their sum in ascending piece order, and the
-// weighted float4 sum of the partials -- one round of memory latency and no
+// weighted float4 sum of the partials -- a single memory latency and no
 // block barrier (except for listing the pieces when some shares are empty).
 __global__ void __launch_bounds__(COMBINE_THREADS) pa_combine_kernel(CombineParams P) {
     __shared__ long long s_piece[MAX_CACHED_PIECES];  // partial slots, ascending worker order (some shares empty)
@@ -119,7 +119,7 @@ __global__ void __launch_bounds__(COMBINE_THREADS) pa_combine_kernel(CombinePara
     // 2. every 4 output channels of a row: the row's M = max lse, the weights
     //    exp(lse - M) and their sum in ascending piece order, then one weighted
     //    float4 sum; the loads of a row's lse values and partials are all
-    //    independent (one round of memory latency, no block barrier)
+    //    independent (a single memory latency, no block barrier)
     const int DV4 = P.Dv >> 2;
     const float4 *po = reinterpret_cast<const float4 *>(P.part_o);
     const bool vec = (reinterpret_cast<uintptr_t>(P.out) & 15) == 0;

@@ -32,7 +32,7 @@ struct AttnParams {
     int wpb;             // work pages per block
     int tbl_stride;      // block_table row stride (blocks per request)
     int q_dtype, out_dtype, k_mode, v_mode, causal;
-    int slots;           // ring pages per warp
+    int slots;           // ring pages per worker (a warp, or a pair of warps)
     int warp_smem;       // shared-memory bytes per warp
     float softmax_scale;
 };
