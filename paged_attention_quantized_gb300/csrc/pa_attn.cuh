@@ -309,12 +309,36 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// The 4 q values of row (b, j, h) that lane-quad index c uses in k-step K, in
+// the element order e = 0..3 of phys_ch: with 8- or 16-bit codes they are 4
+// consecutive channels (one 8-byte load when q is 8-byte aligned), with INT4
+// two pairs of consecutive channels (two 4-byte loads when 4-byte aligned).
 template <int KVT, int D>
-__device__ __forceinline__ float load_q(const AttnParams &P, int b, int j, int h, int d) {
-    const size_t idx = (((size_t)b * P.n + j) * P.Hq + h) * D + d;
-    const uint16_t bits = reinterpret_cast<const uint16_t *>(P.q)[idx];
-    if (P.q_dtype == PA_BF16) return __uint_as_float((uint32_t)bits << 16);
-    return __half2float(__ushort_as_half(bits));
+__device__ __forceinline__ void load_q4(const AttnParams &P, int b, int j, int h, int K, int c, float *v) {
+    using G = Geo<KVT, D>;
+    const uint16_t *row = reinterpret_cast<const uint16_t *>(P.q) + (((size_t)b * P.n + j) * P.Hq + h) * D;
+    auto f = [&](uint32_t bits) -> float {
+        return (P.q_dtype == PA_BF16) ? __uint_as_float(bits << 16) : __half2float(__ushort_as_half((uint16_t)bits));
+    };
+    const int d0 = phys_ch<KVT, D>(K, c, 0);
+    if constexpr (G::BITS == 4) {
+        const int d1 = phys_ch<KVT, D>(K, c, 1);  // d0 + 4; e = 2, 3 are d0 + 1, d1 + 1
+        if ((reinterpret_cast<uintptr_t>(P.q) & 3) == 0) {
+            const uint32_t a = *reinterpret_cast<const uint32_t *>(row + d0);
+            const uint32_t bb = *reinterpret_cast<const uint32_t *>(row + d1);
+            v[0] = f(a & 0xFFFFu); v[2] = f(a >> 16); v[1] = f(bb & 0xFFFFu); v[3] = f(bb >> 16);
+        } else {
+            v[0] = f(row[d0]); v[2] = f(row[d0 + 1]); v[1] = f(row[d1]); v[3] = f(row[d1 + 1]);
+        }
+    } else {
+        if ((reinterpret_cast<uintptr_t>(P.q) & 7) == 0) {
+            const uint2 w = *reinterpret_cast<const uint2 *>(row + d0);
+            v[0] = f(w.x & 0xFFFFu); v[1] = f(w.x >> 16); v[2] = f(w.y & 0xFFFFu); v[3] = f(w.y >> 16);
+        } else {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) v[e] = f(row[d0 + e]);
+        }
+    }
 }
 
 // TOKM: at most 8 query rows per kv head.  Tokens then form the MMA M axis
@@ -484,13 +508,16 @@ __global__ void __launch_bounds__(ATTN_THREADS, min_blocks(Geo<KVT, D>::BITS, D,
         float rho0 = 1.f, rho1 = 1.f;
         if constexpr (!BF) {
             float mx0 = 0.f, mx1 = 0.f;
+#pragma unroll 4
             for (int K = 0; K < G::KSTEPS; ++K) {
+                float v0[4] = {0.f, 0.f, 0.f, 0.f}, v1[4] = {0.f, 0.f, 0.f, 0.f};
+                if (ok0) load_q4<KVT, D>(P, cc.b, jq0, h0, K, c, v0);
+                if (ok1) load_q4<KVT, D>(P, cc.b, jq1, h1, K, c, v1);
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
-                    const int d = phys_ch<KVT, D>(K, c, e);
-                    const float f = fold(d);
-                    if (ok0) mx0 = fmaxf(mx0, fabsf(load_q<KVT, D>(P, cc.b, jq0, h0, d) * f));
-                    if (ok1) mx1 = fmaxf(mx1, fabsf(load_q<KVT, D>(P, cc.b, jq1, h1, d) * f));
+                    const float f = fold(phys_ch<KVT, D>(K, c, e));
+                    mx0 = fmaxf(mx0, fabsf(v0[e] * f));
+                    mx1 = fmaxf(mx1, fabsf(v1[e] * f));
                 }
             }
             mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
@@ -518,19 +545,14 @@ __global__ void __launch_bounds__(ATTN_THREADS, min_blocks(Geo<KVT, D>::BITS, D,
         for (int K = 0; K < KSW; ++K) {
             const int Kg = hf * KSW + K;  // k-step of the whole row (paired warps: this half)
             uint32_t a[4];
+            float v0[4] = {0.f, 0.f, 0.f, 0.f}, v1[4] = {0.f, 0.f, 0.f, 0.f};
+            if (ok0) load_q4<KVT, D>(P, cc.b, jq0, h0, Kg, c, v0);
+            if (ok1) load_q4<KVT, D>(P, cc.b, jq1, h1, Kg, c, v1);
 #pragma unroll
             for (int half = 0; half < 2; ++half) {  // a0a1/a2a3 use e=0,1; a4a5/a6a7 use e=2,3
-                const int d0 = phys_ch<KVT, D>(Kg, c, 2 * half), d1 = phys_ch<KVT, D>(Kg, c, 2 * half + 1);
-                const float f0 = fold(d0), f1 = fold(d1);
-                float u0 = 0.f, u1 = 0.f, w0 = 0.f, w1 = 0.f;
-                if (ok0) {
-                    u0 = load_q<KVT, D>(P, cc.b, jq0, h0, d0) * f0 * inv0;
-                    u1 = load_q<KVT, D>(P, cc.b, jq0, h0, d1) * f1 * inv0;
-                }
-                if (ok1) {
-                    w0 = load_q<KVT, D>(P, cc.b, jq1, h1, d0) * f0 * inv1;
-                    w1 = load_q<KVT, D>(P, cc.b, jq1, h1, d1) * f1 * inv1;
-                }
+                const float f0 = fold(phys_ch<KVT, D>(Kg, c, 2 * half)), f1 = fold(phys_ch<KVT, D>(Kg, c, 2 * half + 1));
+                const float u0 = v0[2 * half] * f0 * inv0, u1 = v0[2 * half + 1] * f1 * inv0;
+                const float w0 = v1[2 * half] * f0 * inv1, w1 = v1[2 * half + 1] * f1 * inv1;
                 a[2 * half] = pack2<BF>(u0, u1);
                 a[2 * half + 1] = pack2<BF>(w0, w1);
             }
