@@ -79,7 +79,7 @@ KERNEL_SOURCES = {
     "bf16": ("pa_attn.cuh", "pa_common.cuh", "pa_attn_launch.cuh", "pa_attn_bf16_d128.cu"),
     "e4m3": ("pa_attn.cuh", "pa_common.cuh", "pa_attn_launch.cuh", "pa_attn_e4m3_d256.cu"),
     "int8": ("pa_attn.cuh", "pa_common.cuh", "pa_attn_launch.cuh", "pa_attn_int8_d128.cu"),
-    "int4": ("pa_attn.cuh", "pa_common.cuh", "pa_attn_launch.cuh", "pa_attn_int4_d128.cu"),
+    "int4": ("pa_attn.cuh", "pa_common.cuh", "pa_attn_launch.cuh", "pa_attn_int4_d128_merged.cu"),
 }
 
 

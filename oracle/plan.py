@@ -10,8 +10,9 @@ physical addresses are only payload).
 
 Rule
 ----
-  P_b   = ceil(L_b / bs) pages of request b; a request with L_b < 0,
-          L_b > max_context_len or P_b > max_blocks_per_seq is invalid:
+  P_b   = ceil(L_b / bs) pages of request b (bs: tokens of a work page); a
+          request with L_b < 0, L_b > max_context_len or more blocks of
+          block_size tokens (default bs) than max_blocks_per_seq is invalid:
           flagged, and planned with P_b = 0.
   PS_b  = sum_{b' < b} P_b'                       (request record)
   X     = Hkv * row_blocks                        (segments per request)
@@ -35,14 +36,16 @@ import numpy as np
 
 
 def plan(context_lens, *, bs: int, Hkv: int, max_context_len: int, max_blocks_per_seq: int,
-         row_blocks: int = 1, warps: int = 1, group_size: int = 1):
+         row_blocks: int = 1, warps: int = 1, group_size: int = 1, block_size: int | None = None):
     L = np.asarray(context_lens, dtype=np.int64).reshape(-1)
     B = L.size
     P = np.zeros(B, dtype=np.int64)
     flags = np.zeros(B, dtype=np.int64)
+    tb = bs if block_size is None else block_size
     for b in range(B):
         pb = -(-L[b] // bs) if L[b] > 0 else 0
-        if L[b] < 0 or L[b] > max_context_len or pb > max_blocks_per_seq:
+        nblocks = -(-L[b] // tb) if L[b] > 0 else 0
+        if L[b] < 0 or L[b] > max_context_len or nblocks > max_blocks_per_seq:
             flags[b] = 1
             pb = 0
         P[b] = pb

@@ -72,7 +72,9 @@ struct Derived {
     int gs;        // workers per group (they share one run of pages, one row block each)
     long long nwarps, slots_partial;
     int D, RB, SW, slots, warp_smem;
-    int wp, wpb;   // work page: tokens the kernel handles as one page (a block, or an equal part of one), parts per block
+    int wp;        // work page: tokens the kernel handles as one page (a block, an equal part of one, or merged blocks)
+    int wpb, mpb;  // parts per block (split blocks), blocks per work page (merged blocks); at least one is 1
+    int box_rows;  // rows of one tile copy: the work page, or one block of a merged page
     size_t k_block, v_block, smem;
     pa_layout L;
 };
@@ -129,6 +131,8 @@ pa_status derive(const pa_problem *p, Derived *d) {
         d->slots = LAT_RING;
         d->wp = LAT_BS;
         d->wpb = 1;
+        d->mpb = 1;
+        d->box_rows = LAT_BS;
         d->warp_smem = 0;
         d->smem = 0;
         // the workers are CTAs, in groups of one per row block
@@ -239,11 +243,29 @@ pa_status derive_grouped(const pa_problem *p, Derived *d) {
     }
     if (!found) return PA_ERR_UNSUPPORTED;
     d->wpb = bs / d->wp;
+    d->mpb = 1;
+    d->box_rows = d->wp;
+    // 16-token blocks of short rows (2 KB pages): MERGE_BLOCKS consecutive blocks
+    // per work page, when the ring still holds two of them at the same residency
+    if (d->wpb == 1 && bs == 16 && pa::merge_rows(d->RB)) {
+        const int wp2 = pa::MERGE_BLOCKS * bs;
+        const int s2 = fit(d->minb, wp2);
+        if (s2 >= min_pages) {
+            d->mpb = pa::MERGE_BLOCKS;
+            d->wp = wp2;
+            d->slots = s2;
+        }
+    }
     d->warp_smem = wsm(d->slots, d->wp);
     d->smem = 1024 + (size_t)workers * d->warp_smem;
     d->ctas = p->grid_ctas > 0 ? p->grid_ctas : d->sms * d->minb;
     d->nwarps = (long long)d->ctas * workers;
     return PA_OK;
+}
+
+// work pages per request at most: the table width in work pages
+int work_pages_per_seq(const pa_problem *p, const Derived &d) {
+    return d.mpb > 1 ? (p->max_blocks_per_seq + d.mpb - 1) / d.mpb : p->max_blocks_per_seq * d.wpb;
 }
 
 pa_status check_ws(const Derived &d, void *ws, size_t bytes) {
@@ -290,8 +312,9 @@ T *at(void *ws, size_t off) {
     return reinterpret_cast<T *>(static_cast<uint8_t *>(ws) + off);
 }
 
-// One tile of the grouped kernel -- all segments of [wp][RB] for one kv head of
-// one work page of a block -- as a single 5-D box {SW bytes, wp rows, NSEG segments, 1, 1}:
+// One tile of the grouped kernel -- all segments of [rows][RB] for one kv head of
+// a whole block, a part of one, or one block of a merged work page -- as a single
+// 5-D box {SW bytes, rows, NSEG segments, 1, 1}:
 // the segment dimension (stride SW) is placed outside the rows, so the box
 // lands as [segment][row][SW bytes], each SW-byte line swizzled by its row.
 pa_status make_tmap_tile(CUtensorMap *tm, const void *base, const Derived &d, const pa_problem *p,
@@ -303,7 +326,7 @@ pa_status make_tmap_tile(CUtensorMap *tm, const void *base, const Derived &d, co
                           (cuuint64_t)p->num_kv_heads, (cuuint64_t)p->num_blocks};
     cuuint64_t strides[4] = {(cuuint64_t)d.RB, (cuuint64_t)d.SW, (cuuint64_t)p->block_size * d.RB,
                              (cuuint64_t)block_stride};
-    cuuint32_t box[5] = {(cuuint32_t)d.SW, (cuuint32_t)d.wp, (cuuint32_t)nseg, 1, 1};  // one work page
+    cuuint32_t box[5] = {(cuuint32_t)d.SW, (cuuint32_t)d.box_rows, (cuuint32_t)nseg, 1, 1};
     cuuint32_t es[5] = {1, 1, 1, 1, 1};
     CUresult r = enc(tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, 5, const_cast<void *>(base), dims, strides, box, es,
                      CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -318,8 +341,9 @@ cudaError_t dispatch_attn(const pa_problem *p, const Derived &d, const CUtensorM
     const bool tokm = d.tokm;
 #define PA_CASE(KVT, DD)                                                                               \
     if (p->kv_dtype == KVT && d.D == DD)                                                               \
-        return d.wpb > 1 ? pa::launch_attn_split<KVT, DD>(tk, tv, P, grid, d.smem, tokm, s)             \
-                         : pa::launch_attn<KVT, DD>(tk, tv, P, grid, d.smem, tokm, s);
+        return d.wpb > 1   ? pa::launch_attn_split<KVT, DD>(tk, tv, P, grid, d.smem, tokm, s)           \
+               : d.mpb > 1 ? pa::launch_attn_merged<KVT, DD>(tk, tv, P, grid, d.smem, tokm, s)          \
+                           : pa::launch_attn<KVT, DD>(tk, tv, P, grid, d.smem, tokm, s);
     PA_CASE(PA_F16, 64) PA_CASE(PA_F16, 128) PA_CASE(PA_F16, 256)
     PA_CASE(PA_BF16, 64) PA_CASE(PA_BF16, 128) PA_CASE(PA_BF16, 256)
     PA_CASE(PA_E4M3, 64) PA_CASE(PA_E4M3, 128) PA_CASE(PA_E4M3, 256)
@@ -377,9 +401,11 @@ PA_API pa_status pa_plan(const pa_problem *p, const int32_t *context_lens, const
     P.hdr = at<uint32_t>(workspace, d.L.header_offset);
     P.req = at<int4>(workspace, d.L.requests_offset);
     P.B = p->batch;
-    P.bs = d.wp;                                        // work pages (a block, or an equal part of one)
+    P.bs = d.wp;                                        // work pages (a block, a part of one, or merged blocks)
     P.max_ctx = p->max_context_len;
-    P.mbps = p->max_blocks_per_seq * d.wpb;
+    P.mbps = work_pages_per_seq(p, d);
+    P.bsb = p->block_size;
+    P.tbl = p->max_blocks_per_seq;
     const float *ks = (p->k_scale_mode == PA_SCALE_CHANNEL) ? k_scale : nullptr;
     cudaError_t e = pa::launch_plan(P, ks, p->num_kv_heads * p->head_dim_k, reinterpret_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
@@ -464,9 +490,10 @@ PA_API pa_status pa_run(const pa_problem *p, const void *q, const void *k_pool, 
     P.G = d.G;
     P.R = d.R;
     P.RBLK = d.row_blocks;
-    P.bs = d.wp;                                    // work pages (a block, or an equal part of one)
-    P.mbps = p->max_blocks_per_seq * d.wpb;
+    P.bs = d.wp;                                    // work pages (a block, a part of one, or merged blocks)
+    P.mbps = work_pages_per_seq(p, d);
     P.wpb = d.wpb;
+    P.bsb = p->block_size;
     P.tbl_stride = p->max_blocks_per_seq;
     P.num_blocks = p->num_blocks;
     P.q_dtype = p->q_dtype;

@@ -47,6 +47,8 @@
 namespace pa {
 
 constexpr int NWK = 4;                     // warps per CTA, each an independent stream
+enum : int { WP_WHOLE = 0, WP_PART = 1, WP_MERGED = 2 };  // what a work page is (see pa_attn_kernel)
+constexpr int MERGE_BLOCKS = 2;            // blocks per merged work page
 #ifndef PA_MIN_BLOCKS_SMALL_D
 #define PA_MIN_BLOCKS_SMALL_D 2
 #endif
@@ -254,6 +256,7 @@ __host__ __device__ constexpr int warp_smem_bytes(int slots, int page_bytes, boo
 struct Cursor {
     int b, q, p;  // request, segment within the request, page
     int Pb;       // pages of request b
+    int L;        // its planned length (kept only by cursors that need it: WL)
 };
 
 // pages of request b as planned, clamped to the table width so that a
@@ -262,6 +265,7 @@ __device__ __forceinline__ int planned_pages(const int4 *req, int b, int mbps) {
     return min(max(req[b].y, 0), mbps);
 }
 
+template <bool WL = false>
 __device__ __forceinline__ void cursor_next(Cursor &cu, const int4 *req, int B, int X, int mbps) {
     if (++cu.p < cu.Pb) return;
     cu.p = 0;
@@ -270,6 +274,7 @@ __device__ __forceinline__ void cursor_next(Cursor &cu, const int4 *req, int B, 
     do {
         ++cu.b;
         cu.Pb = cu.b < B ? planned_pages(req, cu.b, mbps) : 0;
+        if constexpr (WL) cu.L = cu.b < B ? req[cu.b].x : 0;
     } while (cu.b < B && cu.Pb == 0);
 }
 
@@ -286,6 +291,7 @@ __device__ __forceinline__ Cursor cursor_at(long long x, const int4 *req, int B,
     Cursor cu;
     cu.b = lo;
     cu.Pb = planned_pages(req, lo, mbps);
+    cu.L = req[lo].x;
     const long long off = x - (long long)req[lo].z * X;
     if (cu.Pb < 1 || off < 0 || off >= (long long)cu.Pb * X) {
         cu.b = B;
@@ -344,9 +350,16 @@ __device__ __forceinline__ void load_q4(const AttnParams &P, int b, int j, int h
 // TOKM: at most 8 query rows per kv head.  Tokens then form the MMA M axis
 // (S^T = K q'^T and O^T = V^T P^T with the rows as N = 8), which halves the
 // tensor work and the O accumulator against padding 8 rows up to M = 16.
-// SPLIT: a block is handled as P.wpb equal work pages of P.bs tokens (blocks
-// too large for the shared-memory ring); the plan counts work pages.
-template <int KVT, int D, bool TOKM, bool SPLIT>
+// WM, what a work page is (the plan counts work pages of P.bs tokens):
+//  WP_WHOLE   one block;
+//  WP_PART    one of P.wpb equal parts of a block (blocks too large for the ring);
+//  WP_MERGED  MERGE_BLOCKS consecutive blocks of the request, for small blocks
+//             whose row fits one swizzle line: each block's tile is its own copy,
+//             landing below the previous one as further rows of the same tile,
+//             and the per-page work (wait, copy issue, cursors) is paid once for
+//             all of them.  Blocks past the request's length are not copied; their
+//             rows are masked like any padding slot.
+template <int KVT, int D, bool TOKM, int WM>
 __global__ void __launch_bounds__(ATTN_THREADS, min_blocks(Geo<KVT, D>::BITS, D, TOKM, pair_mode(D, TOKM, Geo<KVT, D>::NSEG)))
     pa_attn_kernel(const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv, AttnParams P) {
     using G = Geo<KVT, D>;
@@ -418,6 +431,7 @@ __global__ void __launch_bounds__(ATTN_THREADS, min_blocks(Geo<KVT, D>::BITS, D,
     }
     Cursor ci = cc;                             // issue cursor (runs NS pages ahead)
     int idc_b = -1, idc_w0 = 0, idc = 0;        // block ids of ci.b, pages [idc_w0, idc_w0 + 32)
+    int idc_nb = 0;                             // merged work pages: blocks of request ci.b
     unsigned slot_bad = 0;                      // slots whose page had an invalid id
 
     int islot = 0;  // ring slot of the next copy
@@ -432,9 +446,52 @@ __global__ void __launch_bounds__(ATTN_THREADS, min_blocks(Geo<KVT, D>::BITS, D,
             slot_bad |= 1u << slot;
             return;
         }
+        if constexpr (WM == WP_MERGED) {
+            // work page ci.p: blocks [bi0, bi0 + nbp) of the request, all rows
+            const int bi0 = ci.p * MERGE_BLOCKS;
+            if (ci.b != idc_b || bi0 < idc_w0 || bi0 + MERGE_BLOCKS > idc_w0 + 32) {
+                idc_b = ci.b;
+                idc_w0 = bi0;
+                idc_nb = min((ci.L - 1) / P.bsb + 1, P.tbl_stride);  // blocks of the request (L >= 1)
+                const int pg = idc_w0 + lane;
+                idc = (pg < idc_nb) ? P.block_table[(size_t)ci.b * P.tbl_stride + pg] : 0;
+            }
+            const int nbp = min(MERGE_BLOCKS, idc_nb - bi0);
+            int blk[MERGE_BLOCKS];
+            bool ok = nbp >= 1;
+#pragma unroll
+            for (int i = 0; i < MERGE_BLOCKS; ++i) {
+                blk[i] = __shfl_sync(0xffffffffu, idc, bi0 - idc_w0 + i);
+                if (i < nbp) ok = ok && blk[i] >= 1 && blk[i] < P.num_blocks;
+            }
+            const int kvh = (P.RBLK == 1) ? ci.q : ci.q / P.RBLK;
+            if constexpr (PAIR) {
+                if (lane == 0) sflags[slot] = ok ? 0 : 1;
+            }
+            if (lane == 0) {
+                uint8_t *kt = ring + (size_t)slot * page_bytes;
+                uint8_t *vt = kt + tile_bytes;
+                const int sub = P.bsb * G::RB;  // bytes of one block's tile
+                if (ok) {
+                    mbar_arrive_expect_tx(&full[slot], (uint32_t)(2 * nbp * sub));
+#pragma unroll
+                    for (int i = 0; i < MERGE_BLOCKS; ++i) {
+                        if (i < nbp) {
+                            tma_load_5d(kt + i * sub, &tmk, &full[slot], 0, 0, 0, kvh, blk[i]);
+                            tma_load_5d(vt + i * sub, &tmv, &full[slot], 0, 0, 0, kvh, blk[i]);
+                        }
+                    }
+                } else {
+                    mbar_arrive(&full[slot]);
+                }
+            }
+            slot_bad = ok ? (slot_bad & ~(1u << slot)) : (slot_bad | (1u << slot));
+            cursor_next<true>(ci, P.req, P.B, X, P.mbps);
+            return;
+        }
         // work page ci.p: rows [y0, y0 + bs) of block bi of the request
         int bi = ci.p, y0 = 0, nblk = ci.Pb;
-        if constexpr (SPLIT) {
+        if constexpr (WM == WP_PART) {
             bi = ci.p / P.wpb;
             y0 = (ci.p - bi * P.wpb) * bs;
             nblk = (ci.Pb + P.wpb - 1) / P.wpb;

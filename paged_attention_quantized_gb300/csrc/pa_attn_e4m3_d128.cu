@@ -3,4 +3,5 @@
 
 namespace pa {
 PA_DEFINE_ATTN(PA_E4M3, 128)
+PA_DEFINE_ATTN_MERGED(PA_E4M3, 128)  // rows too long to merge: reports cudaErrorNotSupported
 }  // namespace pa

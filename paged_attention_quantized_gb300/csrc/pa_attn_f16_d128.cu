@@ -3,4 +3,5 @@
 
 namespace pa {
 PA_DEFINE_ATTN(PA_F16, 128)
+PA_DEFINE_ATTN_MERGED(PA_F16, 128)  // rows too long to merge: reports cudaErrorNotSupported
 }  // namespace pa

@@ -3,4 +3,5 @@
 
 namespace pa {
 PA_DEFINE_ATTN(PA_INT8, 256)
+PA_DEFINE_ATTN_MERGED(PA_INT8, 256)  // rows too long to merge: reports cudaErrorNotSupported
 }  // namespace pa

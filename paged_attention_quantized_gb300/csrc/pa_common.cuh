@@ -27,9 +27,10 @@ struct AttnParams {
     void *out;
     float *lse;
     int B, n, Hq, Hkv, G, R, RBLK, num_blocks;
-    int bs;              // tokens of a work page: a block, or an equal part of one
-    int mbps;            // work pages per request at most (table width x wpb)
-    int wpb;             // work pages per block
+    int bs;              // tokens of a work page: a block, an equal part of one, or merged blocks
+    int mbps;            // work pages per request at most (table width x wpb, or / blocks merged)
+    int wpb;             // work pages per block (parts of a block)
+    int bsb;             // tokens of a block
     int tbl_stride;      // block_table row stride (blocks per request)
     int q_dtype, out_dtype, k_mode, v_mode, causal;
     int slots;           // ring pages per worker (a warp, or a pair of warps)
@@ -62,7 +63,8 @@ struct PlanParams {
     const int32_t *context_lens;
     uint32_t *hdr;
     int4 *req;
-    int B, bs, max_ctx, mbps;
+    int B, bs, max_ctx, mbps;  // bs: tokens of a work page; mbps: work pages per request at most
+    int bsb, tbl;              // tokens of a block, blocks per request at most (the table width)
 };
 
 struct CombineParams {

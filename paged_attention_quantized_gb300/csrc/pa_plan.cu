@@ -6,8 +6,9 @@
 //    of host synchronisation (onnxruntime PR #32520, "Normalize the
 //    PER_CHANNEL K scale folded into Q for paged XQA", Approach and Cost).
 //  * pa_plan_kernel: one block turns context_lens into the work plan: pages
-//    P_b = ceil(L_b / bs) of every request (0 for a request whose length breaks
-//    the contract, which is flagged) and their exclusive prefix sums PS_b.  The
+//    P_b = ceil(L_b / bs) of every request, bs the tokens of a work page (0 for
+//    a request whose length breaks the contract, which is flagged) and their
+//    exclusive prefix sums PS_b.  The
 //    attention launch orders all pages as (request, kv head, row block, page)
 //    -- logical positions only, never block ids -- and gives every warp an equal
 //    contiguous share, so every reduction order is independent of where pages
@@ -39,9 +40,10 @@ __global__ void __launch_bounds__(256) pa_max_abs_scale_kernel(const float *k_sc
     }
 }
 
-// pages of request b, or -1 when its length breaks the contract
+// pages of request b, or -1 when its length breaks the contract (longer than
+// max_context_len, or than the blocks its table row can name)
 __device__ __forceinline__ int req_pages(const PlanParams &P, int L) {
-    if (L < 0 || L > P.max_ctx) return -1;
+    if (L < 0 || L > P.max_ctx || (long long)L > (long long)P.tbl * P.bsb) return -1;
     const int pb = (L + P.bs - 1) / P.bs;
     return pb > P.mbps ? -1 : pb;
 }

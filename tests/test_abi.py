@@ -189,7 +189,8 @@ def test_partial_slots_cover_oracle_pieces(B, latent):
 def test_every_block_size_has_a_launch(B):
     """Every KV encoding x head dim x block size (multiples of 16 up to 128) x
     rows per kv head gets a launch: whole blocks when two per worker fit,
-    else equal work pages of >= 16 tokens; the recipe shapes keep whole blocks."""
+    else equal work pages of >= 16 tokens; 16-token blocks of rows of at most
+    64 bytes are merged two to a work page when two merged pages fit."""
     for kv in (B.PA_F16, B.PA_BF16, B.PA_E4M3, B.PA_INT8, B.PA_INT4):
         for D in (64, 128, 256):
             if kv == B.PA_INT4 and D == 64:
@@ -199,6 +200,11 @@ def test_every_block_size_has_a_launch(B):
                     p = _prob(B, kv_dtype=kv, head_dim_k=D, head_dim_v=D, block_size=bs, num_q_heads=hq, next_n=n)
                     lo = B.pa_workspace_layout(p)
                     wp = lo.work_page_tokens
-                    assert wp % 16 == 0 and bs % wp == 0 and lo.ring_pages_per_warp >= 1, (kv, D, bs, hq, n)
-                    if bs == 16:
+                    assert lo.ring_pages_per_warp >= 1, (kv, D, bs, hq, n)
+                    row_bytes = D * {B.PA_F16: 2, B.PA_BF16: 2, B.PA_E4M3: 1, B.PA_INT8: 1, B.PA_INT4: 0.5}[kv]
+                    if wp > bs:  # merged blocks
+                        assert bs == 16 and wp == 32 and row_bytes <= 64 and lo.ring_pages_per_warp >= 2
+                    else:
+                        assert wp % 16 == 0 and bs % wp == 0, (kv, D, bs, hq, n)
+                    if bs == 16 and row_bytes > 64:
                         assert wp == 16

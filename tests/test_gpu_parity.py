@@ -373,6 +373,76 @@ def test_large_blocks_as_work_pages(name, kw, split):
     assert error_bits(ws3) == 0 and torch.equal(out, o3) and torch.equal(lse, l3)
 
 
+# ------------------------------------------------- merged small blocks
+
+MERGED = [
+    ("int4", dict(bs=16, Hq=16, Hkv=2)),                # tokens on M, 1 KB tiles two to a page
+    ("int4", dict(bs=16, Hq=64, Hkv=2)),                # 32 rows: rows on M, two row blocks
+    ("int8", dict(bs=16, D=64, Hq=8, Hkv=1)),
+    ("e4m3", dict(bs=16, D=64, Hq=8, Hkv=2, n=4)),      # causal verify, 16 rows
+]
+
+
+@pytest.mark.parametrize("name,kw", MERGED, ids=lambda x: str(x))
+@pytest.mark.parametrize("split", [0, 5])
+def test_merged_blocks_as_work_pages(name, kw, split):
+    """16-token blocks of short rows run two to a work page: lengths of an odd
+    number of blocks leave the last page half empty (its second block is not
+    copied, nor its table entry read); same results as the oracle, the plan in
+    32-token pages, bitwise stable under relocation and with every unused table
+    entry, padding slot and unreferenced block poisoned."""
+    w = make(name, B=6, L_lo=1, L_hi=700, context_lens=[1, 16, 17, 33, 48, 650], **kw)
+    p = pa.problem(w, grid_ctas=split)
+    lo = pa.binding().pa_workspace_layout(p)
+    assert w.bs == 16 and lo.work_page_tokens == 32
+    out, lse, ws, _ = run_gpu(w, grid_ctas=split)
+    assert error_bits(ws) == 0
+    compare(w, out, lse)
+    raw = ws.cpu().numpy()
+    pl = oracle.plan(w.context_lens.cpu().numpy(), bs=32, block_size=16, Hkv=w.Hkv,
+                     max_context_len=w.max_context_len, max_blocks_per_seq=w.max_blocks_per_seq,
+                     row_blocks=lo.row_blocks, warps=lo.warps)
+    req = raw[lo.requests_offset: lo.requests_offset + 16 * w.B].view(np.int32).reshape(w.B, 4)
+    assert np.array_equal(req[:, 1], pl["pages"]) and np.array_equal(req[:, 2], pl["prefix"])
+    assert np.array_equal(req[:, 3], pl["flags"])
+    o2, l2, _, _ = run_gpu(W.relocate(w, seed=3), grid_ctas=split)
+    assert torch.equal(out, o2) and torch.equal(lse, l2)
+    o3, l3, ws3, _ = run_gpu(W.poison_unreferenced(w, seed=4), grid_ctas=split)
+    assert error_bits(ws3) == 0 and torch.equal(out, o3) and torch.equal(lse, l3)
+
+
+def test_merged_page_bad_second_block():
+    """An invalid id in the second block of a merged work page flags the error
+    and NaN-fills that request only."""
+    w = make("int4", B=3, bs=16, Hq=16, Hkv=2, context_lens=[40, 100, 70])
+    assert pa.binding().pa_workspace_layout(pa.problem(w)).work_page_tokens == 32
+    w.block_table = w.block_table.clone()
+    w.block_table[1, 3] = w.num_blocks + 3   # block 3 = second half of work page 1
+    out, lse, ws, _ = run_gpu(w)
+    assert error_bits(ws) & pa.binding().PA_DEV_ERR_BLOCK_ID
+    o = out.float().cpu()
+    assert torch.isnan(o[1]).all()
+    assert torch.isfinite(o[0]).all() and torch.isfinite(o[2]).all()
+
+
+def test_merged_table_limit_counts_blocks():
+    """With merged pages the plan still counts the table row in blocks: a
+    request one token longer than its 7-block row is flagged and NaN-filled
+    although its four 32-token pages would fit ceil(7 / 2) = 4, and the others
+    are exact."""
+    w = make("int4", B=3, bs=16, Hq=16, Hkv=2, context_lens=[40, 112, 70])
+    assert w.max_blocks_per_seq == 7
+    assert pa.binding().pa_workspace_layout(pa.problem(w)).work_page_tokens == 32
+    ref_out, ref_lse, _, _ = run_gpu(w)
+    w.context_lens = w.context_lens.clone()
+    w.context_lens[1] = 113
+    out, lse, ws, _ = run_gpu(w, max_context_len=200)
+    assert error_bits(ws) & pa.binding().PA_DEV_ERR_CONTEXT_LEN
+    o = out.float().cpu()
+    assert torch.isnan(o[1]).all()
+    assert torch.equal(out[0], ref_out[0]) and torch.equal(out[2], ref_out[2])
+
+
 @pytest.mark.parametrize("name,kw", [
     ("bf16", dict(Hq=128, Hkv=2, n=4)),    # 256 query rows per kv head: 16 row blocks
     ("int8", dict(Hq=64, Hkv=1, n=8)),     # 512 rows, one kv head

@@ -78,3 +78,15 @@ def test_plan_depends_only_on_lengths():
     assert a["pieces"] == b["pieces"]
     one = oracle.plan(L, bs=16, Hkv=1, max_context_len=4000, max_blocks_per_seq=300, warps=1)
     assert all(p["complete"] for p in one["pieces"]) and len(one["pieces"]) == 3
+
+
+def test_merged_work_pages_keep_the_table_limit_in_blocks():
+    # work pages of two 16-token blocks: pages count 32 tokens, but a request is
+    # valid only while its 16-token blocks fit the table row (5 here); 90 tokens
+    # need 6 blocks although ceil(90 / 32) = 3 pages would fit ceil(5 / 2)
+    pl = oracle.plan([90, 80, 17, 0], bs=32, block_size=16, Hkv=1, max_context_len=1000, max_blocks_per_seq=5)
+    assert pl["flags"].tolist() == [1, 0, 0, 0]
+    assert pl["pages"].tolist() == [0, 3, 1, 0]
+    assert pl["prefix"].tolist() == [0, 0, 3, 4]
+    same = oracle.plan([90, 80, 17, 0], bs=16, Hkv=1, max_context_len=1000, max_blocks_per_seq=5)
+    assert same["flags"].tolist() == pl["flags"].tolist()
