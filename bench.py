@@ -23,6 +23,13 @@ With N > 1 (torchrun, one rank per GPU) every rank times its own replica of
 the batch (requests are independent, nothing is exchanged): weak scaling,
 `value` is the sum over ranks of the bytes each processed / the slowest rank.
 
+--op insert times the quantized paged KV insert instead (pa_insert): one
+step writes 16384 new tokens (the largest step size of the Q pad + KV insert
+measurements: B requests x next_n new tokens each) of the workload's shape
+into its full-size pool, quantized to its encoding from rows in the query
+dtype; `value` is the bytes the insert must move (new rows read, codes and
+per-token scales written) divided by the step time.
+
 --impl reference times the CPU fp64 oracle on the host cores instead, each
 step a bounded sample of rows of the same workload, in the same unit.
 """
@@ -81,6 +88,7 @@ KERNEL_SOURCES = {
     "int8": ("pa_attn.cuh", "pa_common.cuh", "pa_attn_launch.cuh", "pa_attn_int8_d128.cu"),
     "int4": ("pa_attn.cuh", "pa_common.cuh", "pa_attn_launch.cuh", "pa_attn_int4_d128_merged.cu"),
 }
+KERNEL_SOURCES.update({"insert_" + k: ("pa_insert.cu",) for k in ("tiny", "bf16", "e4m3", "int8", "int4", "latent")})
 
 
 def _kernel_sha(workload: str) -> str:
@@ -175,6 +183,21 @@ class ClockSampler:
                     reasons.add(n)
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
                 "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# new tokens per request of the insert step: 16384 new tokens in all
+INSERT_NEW_TOKENS = {"tiny": 2, "bf16": 256, "e4m3": 512, "int8": 128, "int4": 128, "latent": 64}
+
+
+def insert_bytes(w) -> int:
+    """Algorithmic bytes of one insert: the new rows read (source dtype) plus
+    the codes and per-token scales written."""
+    rows = w.B * w.n * w.Hkv
+    src = 2  # new rows in the query dtype (f16 / bf16)
+    b = rows * (w.Dk * src + w.k_row_bytes + (4 if w.k_scale_mode == "token" else 0))
+    if not w.v_is_k_prefix:
+        b += rows * (w.Dv * src + w.v_row_bytes + (4 if w.v_scale_mode == "token" else 0))
+    return b
 
 
 # -------------------------------------------------------------- GPU arm
@@ -358,6 +381,168 @@ def gpu_arm(args, rank, world, local_rank):
     }, w
 
 
+def insert_arm(args, rank, world, local_rank):
+    import torch
+    import paged_attention_quantized_gb300 as pa
+    from paged_attention_quantized_gb300 import build as pabuild
+    from paged_attention_quantized_gb300 import workloads as W
+
+    pabuild.build()
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    w = W.make(args.workload, device=dev, B=args.batch, n=INSERT_NEW_TOKENS[args.workload])
+    p = pa.problem(w)
+    kn, vn = W.new_kv_rows(w, w.q_dtype, seed=w.seed + 100)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    nbytes = insert_bytes(w)
+    tokens = w.B * w.n
+    flush = torch.ones(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush_sink = torch.zeros((), dtype=torch.int64, device=dev)
+    s = torch.cuda.Stream(device=dev)
+
+    def flush_l2():
+        flush_sink.copy_(flush.view(torch.int64).sum())
+
+    def dist_barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    with torch.cuda.stream(s):
+        pa.insert(w, p, kn, vn, dev_error=err, stream=s)
+    torch.cuda.synchronize()
+    if int(err.item()):
+        raise RuntimeError(f"device error bits {int(err.item()):#x}")
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        pa.insert(w, p, kn, vn, dev_error=err, stream=s)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(s):
+        for _ in range(args.warmup):
+            flush_l2()
+            g.replay()
+    torch.cuda.synchronize()
+
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    time.sleep(0.3)
+    ev0 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ev1 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    dist_barrier()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(s):
+        for k in range(args.steps):
+            flush_l2()
+            ev0[k].record(s)
+            g.replay()
+            ev1[k].record(s)
+    torch.cuda.synchronize()
+    dist_barrier()
+    step_ms = [a.elapsed_time(b) for a, b in zip(ev0, ev1)]
+    # the kernel alone, eager launches on the same stream
+    a0 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    a1 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    with torch.cuda.stream(s):
+        for k in range(args.steps):
+            flush_l2()
+            a0[k].record(s)
+            pa.insert(w, p, kn, vn, dev_error=err, stream=s)
+            a1[k].record(s)
+    torch.cuda.synchronize()
+    time.sleep(0.2)
+    clk = clocks.stop()
+    kern_ms = [a.elapsed_time(b) for a, b in zip(a0, a1)]
+
+    # end to end: new rows, table and lengths in from pinned memory, the
+    # error word back, every step
+    hk = kn.cpu().pin_memory()
+    hv = None if vn is None else vn.cpu().pin_memory()
+    ht = w.block_table.cpu().pin_memory()
+    hl = w.context_lens.cpu().pin_memory()
+    he = torch.empty(1, dtype=torch.int32).pin_memory()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e2e_ms = []
+    dist_barrier()
+    with torch.cuda.stream(s):
+        for k in range(args.steps):
+            flush_l2()
+            e0.record(s)
+            kn.copy_(hk, non_blocking=True)
+            if hv is not None:
+                vn.copy_(hv, non_blocking=True)
+            w.block_table.copy_(ht, non_blocking=True)
+            w.context_lens.copy_(hl, non_blocking=True)
+            pa.insert(w, p, kn, vn, dev_error=err, stream=s)
+            he.copy_(err, non_blocking=True)
+            e1.record(s)
+            e1.synchronize()
+            e2e_ms.append(e0.elapsed_time(e1))
+    h2d = hk.numel() * hk.element_size() + (0 if hv is None else hv.numel() * hv.element_size()) + \
+        ht.numel() * 4 + hl.numel() * 4
+    total_ms, kern_avg, e2e_avg = max_over_ranks([sum(step_ms), sum(kern_ms) / len(kern_ms),
+                                                  sum(e2e_ms) / len(e2e_ms)], world, dev)
+    ms_per_step = total_ms / args.steps
+    peak, peak_kind = _peaks()
+    achieved = nbytes / (kern_avg * 1e-3) / 1e9
+    line = {
+        "metric": METRIC,
+        "op": "insert",
+        "value": round(job_value(world, nbytes, ms_per_step), 2),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_per_step, 5),
+        "median_ms_per_step": round(statistics.median(step_ms), 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": f"quantized paged KV insert of {tokens} new tokens ({w.B} requests x {w.n}) into "
+                               + WORKLOAD_TEXT[args.workload],
+                   "name": args.workload, "batch": w.B, "new_tokens": tokens, "source_dtype": w.q_dtype,
+                   "insert_bytes": nbytes,
+                   "l2": "a 256 MiB buffer is read before every step to evict the previous step's lines",
+                   "parallelism": f"replicas x{world}"},
+        "tokens_per_s": round(world * tokens / (ms_per_step * 1e-3), 1),
+        "pct_of_hbm_peak": round(100.0 * nbytes / (ms_per_step * 1e-3) / 1e9 / peak, 2),
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "traffic": _traffic("insert_" + args.workload),
+                     "kernel": "pa_insert_kernel", "peak_source": f"{peak_kind} hbm_gbs",
+                     "kernel_ms": round(kern_avg, 5)},
+        "e2e": {"value": round(world * nbytes / (e2e_avg * 1e-3) / 1e9, 2), "unit": "GB/s",
+                "ms_per_step": round(e2e_avg, 5), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": 4},
+        "gpu_launches": args.steps,
+        "clocks": clk,
+    }
+    return line, w, kn, vn
+
+
+def oracle_insert_rate(w, kn, vn, budget_s: float):
+    """Time the insert oracle on a bounded prefix of the requests.  Returns
+    (GB/s equivalent, tokens/s, requests timed, seconds)."""
+    from dataclasses import replace
+    from oracle import insert as OI
+    wc = w.to("cpu")
+    # host pools written in place (the timed work is the insert, not a pool copy)
+    wc = replace(wc, k_pool=wc.k_pool.numpy(), v_pool=None if wc.v_pool is None else wc.v_pool.numpy())
+    kc = kn.cpu()
+    vc = None if vn is None else vn.cpu()
+    nb = 1
+    while True:
+        sub = replace(wc, B=nb, block_table=wc.block_table[:nb], context_lens=wc.context_lens[:nb])
+        t0 = time.perf_counter()
+        OI.insert(sub, kc[:nb], None if vc is None else vc[:nb], in_place=True)
+        dt = time.perf_counter() - t0
+        if dt >= budget_s / 4 or nb >= w.B:
+            break
+        nb = min(w.B, nb * 2)
+    per_req = insert_bytes(w) / w.B
+    return per_req * nb / dt / 1e9, nb * w.n / dt, nb, dt
+
+
 # ---------------------------------------------------------- CPU oracle arm
 
 
@@ -436,6 +621,45 @@ def reference_arm(args):
     }
 
 
+def reference_insert_arm(args):
+    from paged_attention_quantized_gb300 import workloads as W
+    w = W.make(args.workload, device="cpu", B=args.batch, n=INSERT_NEW_TOKENS[args.workload])
+    kn, vn = W.new_kv_rows(w, w.q_dtype, seed=w.seed + 100)
+    for _ in range(args.warmup):
+        oracle_insert_rate(w, kn, vn, budget_s=0.2)
+    vals, secs, toks = [], [], []
+    nb = 1
+    for _ in range(args.steps):
+        v, r, nb, dt = oracle_insert_rate(w, kn, vn, budget_s=args.ref_step_s)
+        vals.append(v)
+        secs.append(dt)
+        toks.append(r)
+    value = statistics.median(vals)
+    return {
+        "impl": "reference",
+        "op": "insert",
+        "metric": METRIC,
+        "value": round(value, 4),
+        "unit": "GB/s",
+        "n_gpus": args.gpus,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(1e3 * statistics.median(secs), 3),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": f"quantized paged KV insert into {WORKLOAD_TEXT[args.workload]}",
+                   "name": args.workload},
+        "tokens_per_s": round(statistics.median(toks), 1),
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": f"the first {nb} of {w.B} requests per step, single-threaded numpy; "
+                                   f"{cpu_model()}"},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
 # -------------------------------------------------------------------- main
 
 
@@ -449,6 +673,8 @@ def main():
     ap.add_argument("--ref-step-s", type=float, default=2.0, help="oracle seconds per reference step")
     ap.add_argument("--cpu-baseline-s", type=float, default=12.0, help="oracle seconds for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--op", default="attention", choices=["attention", "insert"],
+                    help="the step timed: the attention (default) or the quantized paged KV insert")
     ap.add_argument("--batch", type=int, default=None,
                     help="requests of the workload (default: its recipe); a smaller batch is for profiling only")
     args = ap.parse_args()
@@ -461,7 +687,8 @@ def main():
     if args.impl == "reference":
         if rank != 0:
             return
-        print(json.dumps(reference_arm(args)), flush=True)
+        print(json.dumps(reference_arm(args) if args.op == "attention" else reference_insert_arm(args)),
+              flush=True)
         return
 
     if world > 1:
@@ -469,6 +696,21 @@ def main():
         import torch.distributed as dist
         torch.cuda.set_device(local_rank)
         dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    if args.op == "insert":
+        line, w, kn, vn = insert_arm(args, rank, world, local_rank)
+        if rank == 0 and not args.no_cpu_baseline:
+            v, r, nb, dt = oracle_insert_rate(w, kn, vn, args.cpu_baseline_s)
+            line["cpu_baseline"] = {"value": round(v, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                                    "sample": f"the first {nb} of {w.B} requests ({nb * w.n} new tokens), "
+                                              f"{dt:.1f} s, single-threaded numpy; {cpu_model()}",
+                                    "tokens_per_s": round(r, 1)}
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+            dist.destroy_process_group()
+        if rank == 0:
+            print(json.dumps(line), flush=True)
+        return
     line, w = gpu_arm(args, rank, world, local_rank)
     if rank == 0 and not args.no_cpu_baseline:
         wc = w  # the timed batch itself; the oracle reads host copies of it

@@ -262,6 +262,66 @@ PA_API pa_status pa_attention_noalloc(const pa_problem *p, const void *q, const 
                                       const float *v_scale, void *out, float *lse,
                                       pa_stream_t stream);
 
+/* Quantized paged KV insert: write the next_n new K / V rows of every
+ * request into their pool slots, quantized to the pool's encoding -- the step
+ * that precedes the attention of each decode / verify step.
+ *
+ * Sources (page title, section): CentML/vllm PR #167, "Q pad + KV insert",
+ * Design (the per-token quantization and paged insert of the new rows; RoPE
+ * and Q padding are not part of this call); onnxruntime PR #32520, "[CUDA]
+ * Normalize the PER_CHANNEL K scale folded into Q for paged XQA", Description
+ * (symmetric INT8 / INT4 codes with scales max|K| / 127 and max|K| / 7);
+ * 1Cat-vLLM PR #647, "Stop grouped-page4 null-block padding from leaking E4M3
+ * NaN", Root cause (0x7F / 0xFF are NaN, so finite values saturate at 448).
+ *
+ * Positions: context_lens already count the new tokens (as for pa_run), so
+ * new token j of request b goes to logical position L_b - next_n + j, block
+ * block_table[b][pos / bs], slot pos % bs.  Nothing else in the pool is
+ * written: other slots of a partial block keep their bytes.
+ *
+ * Each row x (fp32 values of the source) is stored as codes of x / s, the
+ * quotient rounded once in fp32 (IEEE division):
+ *   PA_SCALE_NONE     s = 1
+ *   PA_SCALE_TENSOR   s = *scale
+ *   PA_SCALE_CHANNEL  s = scale[g][d]
+ *   PA_SCALE_TOKEN    (E4M3 only) s = max_d |x_d| / 448 computed per row (1
+ *                     when it is 0; NaN when the row holds a NaN) and stored
+ *                     in the block's per-token scale slot.
+ * Codes: f16 / bf16 round to nearest even (overflow gives inf); E4M3 rounds
+ * to nearest, ties to even, saturating at +-448 (NaN stays NaN); INT8 / INT4
+ * round half to even and clamp to [-127, 127] / [-7, 7] (NaN gives 0), INT4
+ * packed two per byte, channel 2i in the low nibble.
+ *
+ * Arguments (device pointers unless stated):
+ *  p            host; uses batch, next_n, num_kv_heads, head_dim_k/v (multiples
+ *               of 8, at most 2048), block_size, num_blocks, max_blocks_per_seq,
+ *               max_context_len, kv_dtype, k/v_scale_mode, v_is_k_prefix and
+ *               num_sms (0 = the current device's); the other fields are not
+ *               read.
+ *  src_dtype    PA_F32, PA_F16 or PA_BF16: the dtype of k_new / v_new.
+ *  k_new        [batch][next_n][Hkv][Dk] new K rows, 16-byte aligned.
+ *  v_new        [batch][next_n][Hkv][Dv] new V rows, 16-byte aligned; not
+ *               read when v_is_k_prefix (V is then part of the K rows).
+ *  block_table, context_lens   as for pa_run.
+ *  k_scale, v_scale  per mode: NULL (NONE, TOKEN), 1 fp32 (TENSOR) or
+ *               [Hkv][D] fp32, 16-byte aligned (CHANNEL).
+ *  k_pool, v_pool  the pool planes (layout as for pa_run), written in place;
+ *               v_pool is not written when v_is_k_prefix.
+ *  dev_error    optional device uint32 that the kernel ORs error bits into
+ *               (read it with pa_get_error(dev_error, ...)); NULL to ignore.
+ *
+ * Errors: host-detectable problems return a status and launch nothing.  On
+ * the device, a request with L_b < next_n, L_b > max_context_len or more
+ * pages than table columns is left unwritten (PA_DEV_ERR_CONTEXT_LEN), and a
+ * new token whose block id is outside [1, num_blocks) is left unwritten
+ * (PA_DEV_ERR_BLOCK_ID).  Requests must not share a block at the positions
+ * they write (concurrent writes to one slot race).  One kernel launch on
+ * `stream`; no allocation, no synchronisation. */
+PA_API pa_status pa_insert(const pa_problem *p, int32_t src_dtype, const void *k_new, const void *v_new,
+                           const int32_t *block_table, const int32_t *context_lens, const float *k_scale,
+                           const float *v_scale, void *k_pool, void *v_pool, uint32_t *dev_error,
+                           pa_stream_t stream);
+
 /* Copy the device error word to *bits.  Synchronises `stream`. */
 PA_API pa_status pa_get_error(const void *workspace, uint32_t *bits, pa_stream_t stream);
 

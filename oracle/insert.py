@@ -174,14 +174,15 @@ def quantize_rows(x: np.ndarray, kv_dtype: str, mode: str, scale=None):
     return np.ascontiguousarray(data), tok
 
 
-def insert(w, k_new, v_new=None):
+def insert(w, k_new, v_new=None, in_place: bool = False):
     """The pools after writing the new rows of every request.
 
     w: a workload (its pools, table, lengths, scales, shapes).  k_new: new K
     rows [B, n, Hkv, Dk] (f32 / f16 / bf16); v_new likewise with Dv (None
     when V is the first Dv channels of the K plane).  Returns (k_pool,
     v_pool or None, flags): uint8 arrays [num_blocks, block bytes] and the
-    error bits the contract checks raise."""
+    error bits the contract checks raise.  With in_place, w's pools must be
+    numpy uint8 arrays and are written and returned instead of copies."""
     B, n, Hkv, bs = w.B, w.n, w.Hkv, w.bs
     table = np.asarray(w.block_table.cpu().numpy() if hasattr(w.block_table, "cpu") else w.block_table)
     lens = np.asarray(w.context_lens.cpu().numpy() if hasattr(w.context_lens, "cpu") else w.context_lens)
@@ -191,7 +192,10 @@ def insert(w, k_new, v_new=None):
         nonlocal flags
         if pool is None:
             return None
-        out = np.array(pool.cpu().numpy() if hasattr(pool, "cpu") else pool, dtype=np.uint8, copy=True)
+        if in_place:
+            out = pool
+        else:
+            out = np.array(pool.cpu().numpy() if hasattr(pool, "cpu") else pool, dtype=np.uint8, copy=True)
         x = to_f32(new).reshape(B, n, Hkv, D)
         row = D * _BITS[w.kv_dtype] // 8
         codes_bytes = Hkv * bs * row

@@ -4,7 +4,8 @@ The computation lives in libpa.so (CUDA, sm_103a) behind the C ABI of
 include/pa.h; this package is its thin Python face:
 
   * `_binding`  -- ctypes declarations of pa_workspace_size / pa_plan / pa_run /
-                   pa_combine / pa_attention / pa_get_error (same names);
+                   pa_combine / pa_attention / pa_insert / pa_get_error (same
+                   names);
   * `problem()` / `run()` -- marshal a batch held in torch CUDA tensors into
                    those calls (pointers, sizes, the current stream);
   * `workloads` -- seeded synthetic inputs (no attention arithmetic).
@@ -16,7 +17,7 @@ from __future__ import annotations
 import math
 from typing import Optional
 
-__all__ = ["problem", "workspace_bytes", "run", "stream_handle", "binding"]
+__all__ = ["problem", "workspace_bytes", "run", "insert", "stream_handle", "binding"]
 
 
 def binding():
@@ -75,6 +76,16 @@ def run(w, p, out, workspace, lse=None, stream=None, *, steps: str = "all") -> N
             b.pa_combine(p, _ptr(w.v_scale), ws, wsb, _ptr(out), _ptr(lse), s)
         else:
             raise ValueError(step)
+
+
+def insert(w, p, k_new, v_new=None, dev_error=None, stream=None) -> None:
+    """Enqueue pa_insert: write the new rows k_new / v_new ([B, n, Hkv, D]
+    torch CUDA tensors, f32 / f16 / bf16) into w's pools in place.  dev_error:
+    optional int32 CUDA tensor of one element that collects the error bits."""
+    b = binding()
+    src = {"torch.float32": b.PA_F32, "torch.float16": b.PA_F16, "torch.bfloat16": b.PA_BF16}[str(k_new.dtype)]
+    b.pa_insert(p, src, _ptr(k_new), _ptr(v_new), _ptr(w.block_table), _ptr(w.context_lens), _ptr(w.k_scale),
+                _ptr(w.v_scale), _ptr(w.k_pool), _ptr(w.v_pool), _ptr(dev_error), stream_handle(stream))
 
 
 def out_torch_dtype(name: str):

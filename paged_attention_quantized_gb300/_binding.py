@@ -75,6 +75,8 @@ _lib.pa_attention.restype = ctypes.c_int
 _lib.pa_attention.argtypes = [_P(Problem)] + [_vp] * 8 + [ctypes.c_size_t, _vp, _vp, _vp]
 _lib.pa_attention_noalloc.restype = ctypes.c_int
 _lib.pa_attention_noalloc.argtypes = [_P(Problem)] + [_vp] * 10
+_lib.pa_insert.restype = ctypes.c_int
+_lib.pa_insert.argtypes = [_P(Problem), ctypes.c_int32] + [_vp] * 9 + [_vp]
 _lib.pa_get_error.restype = ctypes.c_int
 _lib.pa_get_error.argtypes = [_vp, _P(ctypes.c_uint32), _vp]
 
@@ -130,6 +132,12 @@ def pa_attention_noalloc(p: Problem, q, k_pool, v_pool, block_table, context_len
     caller workspace (for callers that cannot allocate device memory)."""
     _check(_lib.pa_attention_noalloc(ctypes.byref(p), q, k_pool, v_pool, block_table, context_lens, k_scale,
                                      v_scale, out, lse, stream), "pa_attention_noalloc")
+
+
+def pa_insert(p: Problem, src_dtype: int, k_new, v_new, block_table, context_lens, k_scale, v_scale, k_pool,
+              v_pool, dev_error, stream) -> None:
+    _check(_lib.pa_insert(ctypes.byref(p), int(src_dtype), k_new, v_new, block_table, context_lens, k_scale,
+                          v_scale, k_pool, v_pool, dev_error, stream), "pa_insert")
 
 
 def pa_get_error(workspace: int, stream) -> int:

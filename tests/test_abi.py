@@ -208,3 +208,55 @@ def test_every_block_size_has_a_launch(B):
                         assert wp % 16 == 0 and bs % wp == 0, (kv, D, bs, hq, n)
                     if bs == 16 and row_bytes > 64:
                         assert wp == 16
+
+
+# ------------------------------------------------------------- pa_insert
+
+
+def _insert_status(B, p, src=None, ptrs=None, dev_error=None):
+    """pa_insert's status for problem p with fake (never dereferenced) device
+    pointers; every case here fails validation or has nothing to write, so
+    nothing is launched."""
+    a = 1 << 20                       # 16-byte aligned stand-ins
+    d = dict(k_new=a, v_new=a, table=a, lens=a, ks=a, vs=a, kp=a, vp=a)
+    d.update(ptrs or {})
+    return B.raw_status("pa_insert", ctypes.byref(p), B.PA_BF16 if src is None else src, d["k_new"], d["v_new"],
+                        d["table"], d["lens"], d["ks"], d["vs"], d["kp"], d["vp"], dev_error, None)
+
+
+def test_insert_header_and_export(B):
+    assert "pa_insert" in declared_symbols()
+    assert hasattr(ctypes.CDLL(B.LIB_PATH), "pa_insert")
+
+
+def test_insert_empty_batch_is_a_no_op(B):
+    assert _insert_status(B, _prob(B, batch=0)) == B.PA_OK
+
+
+@pytest.mark.parametrize("case,expect", [
+    (dict(src=7), "INVALID_ARG"),                                     # unknown source dtype
+    (dict(p=dict(next_n=0)), "INVALID_ARG"),
+    (dict(p=dict(num_kv_heads=0)), "INVALID_ARG"),
+    (dict(p=dict(kv_dtype=9)), "INVALID_ARG"),
+    (dict(p=dict(k_scale_mode=5)), "INVALID_ARG"),
+    (dict(p=dict(head_dim_k=100, head_dim_v=100)), "UNSUPPORTED"),        # not a multiple of 8
+    (dict(p=dict(head_dim_k=4096, head_dim_v=4096)), "UNSUPPORTED"),      # beyond 2048 channels
+    (dict(p=dict(k_scale_mode=3, v_scale_mode=3)), "UNSUPPORTED"),        # per-token scales: E4M3 only
+    (dict(p=dict(kv_dtype=4, k_scale_mode=2, v_scale_mode=2), ptrs=dict(ks=None)), "INVALID_ARG"),
+    (dict(p=dict(kv_dtype=4, k_scale_mode=2, v_scale_mode=2), ptrs=dict(vs=(1 << 20) + 4)), "INVALID_ARG"),
+    (dict(p=dict(kv_dtype=3, k_scale_mode=1, v_scale_mode=1), ptrs=dict(ks=(1 << 20) + 2)), "INVALID_ARG"),
+    (dict(ptrs=dict(k_new=(1 << 20) + 8)), "INVALID_ARG"),                # 16-byte alignment
+    (dict(ptrs=dict(vp=(1 << 20) + 8)), "INVALID_ARG"),
+    (dict(ptrs=dict(kp=None)), "INVALID_ARG"),
+    (dict(ptrs=dict(table=None)), "INVALID_ARG"),
+    (dict(ptrs=dict(lens=None)), "INVALID_ARG"),
+    (dict(dev_error=(1 << 20) + 2), "INVALID_ARG"),
+    (dict(p=dict(kv_dtype=3, k_scale_mode=3, v_scale_mode=3, block_size=3, num_kv_heads=1, head_dim_k=8,
+                 head_dim_v=8)), "UNSUPPORTED"),                          # blocks not 16-byte multiples
+    (dict(p=dict(v_is_k_prefix=1, head_dim_k=64, head_dim_v=128)), "INVALID_ARG"),
+    (dict(p=dict(batch=1 << 20, next_n=1 << 10, num_kv_heads=8)), "UNSUPPORTED"),   # > 2^31 rows
+])
+def test_insert_rejects_bad_arguments(B, case, expect):
+    p = _prob(B, **case.get("p", {}))
+    st = _insert_status(B, p, case.get("src"), case.get("ptrs"), case.get("dev_error"))
+    assert st == getattr(B, "PA_ERR_" + expect)
