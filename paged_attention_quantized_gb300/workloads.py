@@ -427,7 +427,7 @@ def referenced_mask(w: Workload) -> np.ndarray:
 # ------------------------------------------------------------ new KV rows
 
 
-def new_kv_rows(w: Workload, src: str = "bf16", seed: int = 0, device=None):
+def new_kv_rows(w: Workload, src: str = "bf16", seed: int = 0, device=None, outliers: bool = True):
     """Seeded new K / V rows [B, n, Hkv, D] for an insert into w's pool, in the
     source dtype `src` ("f32", "f16" or "bf16"); V is None when it is the
     prefix of the K plane.
@@ -436,7 +436,9 @@ def new_kv_rows(w: Workload, src: str = "bf16", seed: int = 0, device=None):
     N(0,1) with 1% of the values times 100 (past the +-448 code range at the
     0.05 scale); per-channel INT8 / INT4 N(0, (c * k_scale[g, d])^2) with
     c = 127/3 or 7/3, 1% of the values times 10 (clamped codes); per-token
-    E4M3 N(0,1) times 10^U(-3,3) per row, 2% of the rows all zero."""
+    E4M3 N(0,1) times 10^U(-3,3) per row, 2% of the rows all zero.  With
+    outliers=False the values follow the pool's own recipe instead (N(0,1),
+    or N(0, (c * k_scale[g, d])^2) for per-channel integer caches)."""
     device = w.k_pool.device if device is None else torch.device(device)
     g = _gen(device, seed)
     dt = TORCH_FLOAT[src]
@@ -444,7 +446,11 @@ def new_kv_rows(w: Workload, src: str = "bf16", seed: int = 0, device=None):
     def rows(D, scale, mode):
         shape = (w.B, w.n, w.Hkv, D)
         x = torch.randn(shape, generator=g, device=device)
-        if w.kv_dtype == "e4m3" and mode == "tensor":
+        if not outliers:
+            if w.kv_dtype in ("int8", "int4") and mode == "channel":
+                c = (127.0 if w.kv_dtype == "int8" else 7.0) / 3.0
+                x = x * c * scale.to(device).float().reshape(1, 1, w.Hkv, D)
+        elif w.kv_dtype == "e4m3" and mode == "tensor":
             big = torch.rand(shape, generator=g, device=device) < 0.01
             x = torch.where(big, x * 100.0, x)
         elif w.kv_dtype in ("int8", "int4") and mode == "channel":

@@ -146,13 +146,15 @@ def test_insert_non_finite_inputs(name):
     got = w2.k_pool.cpu().numpy()
     if w.kv_dtype == "e4m3":
         # NaN codes may carry either sign: compare NaN-ness there, bytes elsewhere
-        nan_ref = (kp & 0x7F) == 0x7F
-        nan_got = (got & 0x7F) == 0x7F
+        codes = w.Hkv * w.bs * w.k_row_bytes
+        gc, rc = got[:, :codes], kp[:, :codes]
+        nan_ref = (rc & 0x7F) == 0x7F
+        nan_got = (gc & 0x7F) == 0x7F
         assert np.array_equal(nan_ref, nan_got)
-        assert np.array_equal(got[~nan_ref], kp[~nan_ref])
+        assert np.array_equal(gc[~nan_ref], rc[~nan_ref])
+        assert np.array_equal(got[:, codes:], kp[:, codes:]) or w.k_scale_mode == "token"
         if w.k_scale_mode == "token":
-            # scales of NaN rows are NaN; the others match bitwise
-            codes = w.Hkv * w.bs * w.k_row_bytes
+            # scales of NaN rows are NaN (any payload); the others match bitwise
             sg = got[:, codes:].copy().view(np.float32)
             sr = kp[:, codes:].copy().view(np.float32)
             assert np.array_equal(np.isnan(sg), np.isnan(sr))
@@ -181,7 +183,9 @@ def test_attention_over_inserted_tokens(name, kw):
     w = W.make(name, device="cuda", **kw)
     if name == "int8":
         w.q = (w.q.float() / 1e7).to(w.q.dtype)   # a softmax that mixes many tokens
-    kn, vn = W.new_kv_rows(w, "bf16", seed=7)
+    # rows drawn like the pool's own values: the absolute tolerance of bf16
+    # outputs assumes outputs of order 1 (half a bf16 step at 8 is 0.016)
+    kn, vn = W.new_kv_rows(w, "bf16", seed=7, outliers=False)
     w2, _ = gpu_insert(w, kn, vn)
     grid = dict(grid_ctas=3) if name == "latent" else {}
     out, lse, ws, _ = run_gpu(w2, **grid)
