@@ -467,3 +467,39 @@ def new_kv_rows(w: Workload, src: str = "bf16", seed: int = 0, device=None, outl
     k = rows(w.Dk, w.k_scale, w.k_scale_mode)
     v = None if w.v_is_k_prefix else rows(w.Dv, w.v_scale, w.v_scale_mode)
     return k, v
+
+
+# ------------------------------------------------------- sparse selections
+
+
+def make_selection(w: Workload, k: int, seed: int = 0, shared: float = 0.9, device=None) -> torch.Tensor:
+    """Seeded token selections [B, next_n, k] int32 for sparse attention: the
+    logical positions each query token attends to, in no particular order,
+    -1 for unused entries.
+
+    Recipe ("highly shared selections"): every request draws one pool of k
+    positions uniformly from its tokens; each query row keeps a `shared`
+    share of that pool and draws the rest from its own visible tokens (which
+    may repeat pool entries), then the row is shuffled.  Rows whose visible
+    length is below k list every visible token once and pad with -1."""
+    device = w.context_lens.device if device is None else torch.device(device)
+    g = _gen("cpu", seed)
+    L = w.context_lens.cpu().tolist()
+    out = torch.full((w.B, w.n, k), -1, dtype=torch.int32)
+    for b, Lb in enumerate(L):
+        pool = torch.randperm(max(Lb, 1), generator=g)[:k].to(torch.int32) if Lb > 0 else torch.zeros(0, dtype=torch.int32)
+        for j in range(w.n):
+            vis = Lb - (w.n - 1 - j) if w.causal else Lb
+            if vis <= 0:
+                continue
+            if vis <= k:
+                row = torch.randperm(vis, generator=g).to(torch.int32)
+                out[b, j, :vis] = row
+                continue
+            keep = pool[pool < vis]
+            nkeep = min(int(round(shared * k)), keep.numel())
+            keep = keep[torch.randperm(keep.numel(), generator=g)[:nkeep]]
+            rest = torch.randint(0, vis, (k - nkeep,), generator=g, dtype=torch.int64).to(torch.int32)
+            row = torch.cat([keep, rest])
+            out[b, j] = row[torch.randperm(k, generator=g)]
+    return out.to(device)
