@@ -322,6 +322,46 @@ PA_API pa_status pa_insert(const pa_problem *p, int32_t src_dtype, const void *k
                            const float *v_scale, void *k_pool, void *v_pool, uint32_t *dev_error,
                            pa_stream_t stream);
 
+/* Sparse (selected-token) paged attention: query token j of request b (all
+ * its heads) attends only to the logical positions sel[b][j][:] names.
+ *
+ * Sources (page title, section): 1Cat-vLLM PR #494, "[Bugfix][SM70]
+ * Stabilize QSA page4 order under KV relocation", Summary / Contract and
+ * limits (sparse attention over per-query selected token ids, work ordered
+ * by logical position, bitwise stable under relocation) and Upstream and
+ * duplicate-work check (unused selection entries are skipped).
+ *
+ *   T_bj = { t in sel[b][j][0..top_k) : 0 <= t < vis_bj }   (a set)
+ *   out[b,j,h,:] = softmax_{t in T_bj}(softmax_scale * q . k^_t) . v^_t
+ * with vis_bj as for pa_run (causal or not); entries < 0 or >= vis_bj are
+ * skipped, a position listed twice counts once, and the order of the
+ * entries does not matter (the result is bitwise the same).  An empty T_bj
+ * gives out = 0, lse = -inf.
+ *
+ * Arguments as for pa_attention, plus:
+ *  top_k      entries per selection row (>= 0).
+ *  sel        device [batch][next_n][top_k] int32 logical positions.
+ *  workspace  caller-owned device memory of pa_sparse_workspace_size()
+ *             bytes, 256-byte aligned: word 0 is the device error word
+ *             (read it with pa_get_error), then the per-token counts and the
+ *             compacted token lists.
+ * Supported: separate K and V planes (not v_is_k_prefix) with Dk = Dv in
+ * {64, 128, 256}, Hq / Hkv <= min(16, 2048 / D), per-token scales for E4M3
+ * only, max_context_len <= 1.8M (the planner's bitmap: one bit per position,
+ * in shared memory); other problems return PA_ERR_UNSUPPORTED.
+ * Device errors: a request whose length breaks the contract
+ * (PA_DEV_ERR_CONTEXT_LEN) or a selected token whose block id is outside
+ * [1, num_blocks) (PA_DEV_ERR_BLOCK_ID) gets NaN rows.  Three stream
+ * operations (a 4-byte memset of the error word and two kernels); no
+ * allocation, no synchronisation. */
+PA_API pa_status pa_sparse_workspace_size(const pa_problem *p, int32_t top_k, size_t *bytes);
+
+PA_API pa_status pa_sparse_attention(const pa_problem *p, int32_t top_k, const int32_t *sel, const void *q,
+                                     const void *k_pool, const void *v_pool, const int32_t *block_table,
+                                     const int32_t *context_lens, const float *k_scale, const float *v_scale,
+                                     void *workspace, size_t workspace_bytes, void *out, float *lse,
+                                     pa_stream_t stream);
+
 /* Copy the device error word to *bits.  Synchronises `stream`. */
 PA_API pa_status pa_get_error(const void *workspace, uint32_t *bits, pa_stream_t stream);
 

@@ -4,8 +4,8 @@ The computation lives in libpa.so (CUDA, sm_103a) behind the C ABI of
 include/pa.h; this package is its thin Python face:
 
   * `_binding`  -- ctypes declarations of pa_workspace_size / pa_plan / pa_run /
-                   pa_combine / pa_attention / pa_insert / pa_get_error (same
-                   names);
+                   pa_combine / pa_attention / pa_insert / pa_sparse_attention /
+                   pa_get_error (same names);
   * `problem()` / `run()` -- marshal a batch held in torch CUDA tensors into
                    those calls (pointers, sizes, the current stream);
   * `workloads` -- seeded synthetic inputs (no attention arithmetic).
@@ -17,7 +17,7 @@ from __future__ import annotations
 import math
 from typing import Optional
 
-__all__ = ["problem", "workspace_bytes", "run", "insert", "stream_handle", "binding"]
+__all__ = ["problem", "workspace_bytes", "run", "insert", "sparse_run", "stream_handle", "binding"]
 
 
 def binding():
@@ -86,6 +86,17 @@ def insert(w, p, k_new, v_new=None, dev_error=None, stream=None) -> None:
     src = {"torch.float32": b.PA_F32, "torch.float16": b.PA_F16, "torch.bfloat16": b.PA_BF16}[str(k_new.dtype)]
     b.pa_insert(p, src, _ptr(k_new), _ptr(v_new), _ptr(w.block_table), _ptr(w.context_lens), _ptr(w.k_scale),
                 _ptr(w.v_scale), _ptr(w.k_pool), _ptr(w.v_pool), _ptr(dev_error), stream_handle(stream))
+
+
+def sparse_run(w, p, sel, out, workspace, lse=None, stream=None) -> None:
+    """Enqueue pa_sparse_attention for workload tensors on the device; sel is
+    an int32 [B, n, top_k] CUDA tensor of selected logical positions and
+    workspace a uint8 tensor of pa_sparse_workspace_size bytes."""
+    b = binding()
+    top_k = int(sel.shape[-1])
+    b.pa_sparse_attention(p, top_k, _ptr(sel), _ptr(w.q), _ptr(w.k_pool), _ptr(w.v_pool), _ptr(w.block_table),
+                          _ptr(w.context_lens), _ptr(w.k_scale), _ptr(w.v_scale), _ptr(workspace),
+                          workspace.numel() * workspace.element_size(), _ptr(out), _ptr(lse), stream_handle(stream))
 
 
 def out_torch_dtype(name: str):

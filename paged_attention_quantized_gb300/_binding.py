@@ -77,6 +77,10 @@ _lib.pa_attention_noalloc.restype = ctypes.c_int
 _lib.pa_attention_noalloc.argtypes = [_P(Problem)] + [_vp] * 10
 _lib.pa_insert.restype = ctypes.c_int
 _lib.pa_insert.argtypes = [_P(Problem), ctypes.c_int32] + [_vp] * 9 + [_vp]
+_lib.pa_sparse_workspace_size.restype = ctypes.c_int
+_lib.pa_sparse_workspace_size.argtypes = [_P(Problem), ctypes.c_int32, _P(ctypes.c_size_t)]
+_lib.pa_sparse_attention.restype = ctypes.c_int
+_lib.pa_sparse_attention.argtypes = [_P(Problem), ctypes.c_int32] + [_vp] * 9 + [ctypes.c_size_t, _vp, _vp, _vp]
 _lib.pa_get_error.restype = ctypes.c_int
 _lib.pa_get_error.argtypes = [_vp, _P(ctypes.c_uint32), _vp]
 
@@ -138,6 +142,19 @@ def pa_insert(p: Problem, src_dtype: int, k_new, v_new, block_table, context_len
               v_pool, dev_error, stream) -> None:
     _check(_lib.pa_insert(ctypes.byref(p), int(src_dtype), k_new, v_new, block_table, context_lens, k_scale,
                           v_scale, k_pool, v_pool, dev_error, stream), "pa_insert")
+
+
+def pa_sparse_workspace_size(p: Problem, top_k: int) -> int:
+    n = ctypes.c_size_t()
+    _check(_lib.pa_sparse_workspace_size(ctypes.byref(p), int(top_k), ctypes.byref(n)), "pa_sparse_workspace_size")
+    return n.value
+
+
+def pa_sparse_attention(p: Problem, top_k: int, sel, q, k_pool, v_pool, block_table, context_lens, k_scale,
+                        v_scale, workspace, workspace_bytes, out, lse, stream) -> None:
+    _check(_lib.pa_sparse_attention(ctypes.byref(p), int(top_k), sel, q, k_pool, v_pool, block_table,
+                                    context_lens, k_scale, v_scale, workspace, workspace_bytes, out, lse, stream),
+           "pa_sparse_attention")
 
 
 def pa_get_error(workspace: int, stream) -> int:

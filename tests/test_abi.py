@@ -260,3 +260,54 @@ def test_insert_rejects_bad_arguments(B, case, expect):
     p = _prob(B, **case.get("p", {}))
     st = _insert_status(B, p, case.get("src"), case.get("ptrs"), case.get("dev_error"))
     assert st == getattr(B, "PA_ERR_" + expect)
+
+
+# --------------------------------------------------------- pa_sparse_attention
+
+
+def _sparse_status(B, p, top_k=16, ws_bytes=1 << 20, ptrs=None):
+    """pa_sparse_attention's status with fake (never dereferenced) device
+    pointers; every case here fails validation or has no rows, so nothing is
+    launched."""
+    a = 1 << 20
+    d = dict(sel=a, q=a, kp=a, vp=a, table=a, lens=a, ks=a, vs=a, ws=a, out=a, lse=a)
+    d.update(ptrs or {})
+    return B.raw_status("pa_sparse_attention", ctypes.byref(p), top_k, d["sel"], d["q"], d["kp"], d["vp"],
+                        d["table"], d["lens"], d["ks"], d["vs"], d["ws"], ctypes.c_size_t(ws_bytes), d["out"],
+                        d["lse"], None)
+
+
+def test_sparse_header_and_workspace_size(B):
+    assert {"pa_sparse_attention", "pa_sparse_workspace_size"} <= set(declared_symbols())
+    p = _prob(B, batch=3, next_n=2)
+    n = B.pa_sparse_workspace_size(p, 100)
+    # error word, then per-token counts, then the token lists (256-byte aligned)
+    assert n == 256 + 256 + ((3 * 2 * 100 * 4 + 255) // 256) * 256
+    assert B.pa_sparse_workspace_size(_prob(B, batch=0), 100) == 256      # the error word only
+
+
+def test_sparse_empty_batch_is_a_no_op(B):
+    assert _sparse_status(B, _prob(B, batch=0)) == B.PA_OK
+
+
+@pytest.mark.parametrize("case,expect", [
+    (dict(top_k=-1), "INVALID_ARG"),
+    (dict(p=dict(q_dtype=0)), "INVALID_ARG"),                                       # f32 queries
+    (dict(p=dict(head_dim_k=96, head_dim_v=96)), "UNSUPPORTED"),
+    (dict(p=dict(head_dim_v=64)), "UNSUPPORTED"),                                   # Dk != Dv
+    (dict(p=dict(num_q_heads=136, num_kv_heads=8)), "UNSUPPORTED"),                  # 17 heads per kv head
+    (dict(p=dict(head_dim_k=256, head_dim_v=256, num_q_heads=72, num_kv_heads=8)), "UNSUPPORTED"),  # 9 > 8
+    (dict(p=dict(v_is_k_prefix=1)), "UNSUPPORTED"),
+    (dict(p=dict(k_scale_mode=3, v_scale_mode=3)), "UNSUPPORTED"),                   # token scales: E4M3 only
+    (dict(p=dict(max_context_len=1 << 21)), "UNSUPPORTED"),                         # planner bitmap > 227 KB
+    (dict(ws_bytes=256), "WORKSPACE"),
+    (dict(ptrs=dict(ws=(1 << 20) + 16)), "WORKSPACE"),
+    (dict(ptrs=dict(sel=None)), "INVALID_ARG"),
+    (dict(ptrs=dict(out=None)), "INVALID_ARG"),
+    (dict(ptrs=dict(kp=(1 << 20) + 8)), "INVALID_ARG"),
+    (dict(p=dict(kv_dtype=4, k_scale_mode=2, v_scale_mode=2), ptrs=dict(vs=None)), "INVALID_ARG"),
+])
+def test_sparse_rejects_bad_arguments(B, case, expect):
+    p = _prob(B, **case.get("p", {}))
+    st = _sparse_status(B, p, case.get("top_k", 16), case.get("ws_bytes", 1 << 20), case.get("ptrs"))
+    assert st == getattr(B, "PA_ERR_" + expect)
