@@ -30,6 +30,11 @@ into its full-size pool, quantized to its encoding from rows in the query
 dtype; `value` is the bytes the insert must move (new rows read, codes and
 per-token scales written) divided by the step time.
 
+--op sparse times sparse (selected-token) attention (pa_sparse_attention) on
+the qsa workload: every query token attends to the positions its top-k
+selection names; `value` is the K and V bytes of the selected tokens (each
+query token and kv head reads its own) divided by the step time.
+
 --impl reference times the CPU fp64 oracle on the host cores instead, each
 step a bounded sample of rows of the same workload, in the same unit.
 """
@@ -63,8 +68,13 @@ WORKLOAD_TEXT = {
     "latent": "single-latent-KV MQA decode: B=256, L~lognormal(median 8192, sigma 1, cap 131072), next_n=2 "
               "causal, 128 q heads / 1 kv head, Dk=576, Dv=512 (first 512 of K), bs=64, E4M3 KV with a "
               "per-token fp32 scale, q~N(0,1) bf16, bf16 out",
+    "qsa": "sparse selected-token attention: 4 requests of 65536 tokens, 256 causal query rows each "
+           "(1024 rows), 6 q / 1 kv heads, D=256, bs=16, fp16 KV, top-k 2048 selections, 90% shared "
+           "per request, fp16 out",
 }
-COMPUTE_DTYPE = {"tiny": "f16", "bf16": "bf16", "e4m3": "f16", "int8": "f16", "int4": "f16", "latent": "f16"}
+SPARSE_TOP_K = 2048
+COMPUTE_DTYPE = {"tiny": "f16", "bf16": "bf16", "e4m3": "f16", "int8": "f16", "int4": "f16", "latent": "f16",
+                 "qsa": "f16"}
 L2_FLUSH_BYTES = 256 << 20
 
 
@@ -520,6 +530,178 @@ def insert_arm(args, rank, world, local_rank):
     return line, w, kn, vn
 
 
+def selected_counts(w, sel) -> "list[int]":
+    """Distinct visible positions each query token's selection names."""
+    import numpy as np
+    sl = sel.cpu().numpy()
+    L = w.context_lens.cpu().numpy()
+    out = []
+    for b in range(w.B):
+        for j in range(w.n):
+            vis = int(L[b]) - (w.n - 1 - j) if w.causal else int(L[b])
+            r = sl[b, j]
+            out.append(int(np.unique(r[(r >= 0) & (r < vis)]).size))
+    return out
+
+
+def sparse_arm(args, rank, world, local_rank):
+    import torch
+    import paged_attention_quantized_gb300 as pa
+    from paged_attention_quantized_gb300 import build as pabuild
+    from paged_attention_quantized_gb300 import workloads as W
+
+    pabuild.build()
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    w = W.make(args.workload, device=dev, B=args.batch)
+    sel = W.make_selection(w, k=SPARSE_TOP_K, seed=w.seed + 200, shared=0.9)
+    p = pa.problem(w)
+    B = pa.binding()
+    ws = torch.zeros(max(256, B.pa_sparse_workspace_size(p, SPARSE_TOP_K)), dtype=torch.uint8, device=dev)
+    out = torch.empty((w.B, w.n, w.Hq, w.Dv), dtype=pa.out_torch_dtype(w.out_dtype), device=dev)
+    lse = torch.empty((w.B, w.n, w.Hq), dtype=torch.float32, device=dev)
+    counts = selected_counts(w, sel)
+    nbytes = sum(counts) * w.Hkv * (w.k_row_bytes + w.v_row_bytes)
+    rows = w.B * w.n
+    flush = torch.ones(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush_sink = torch.zeros((), dtype=torch.int64, device=dev)
+    s = torch.cuda.Stream(device=dev)
+
+    def flush_l2():
+        flush_sink.copy_(flush.view(torch.int64).sum())
+
+    with torch.cuda.stream(s):
+        pa.sparse_run(w, p, sel, out, ws, lse, stream=s)
+    torch.cuda.synchronize()
+    bits = B.pa_get_error(ws.data_ptr(), int(s.cuda_stream))
+    if bits:
+        raise RuntimeError(f"device error bits {bits:#x}")
+    if not torch.isfinite(out.float()).all():
+        raise RuntimeError("non-finite output")
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        pa.sparse_run(w, p, sel, out, ws, lse, stream=s)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(s):
+        for _ in range(args.warmup):
+            flush_l2()
+            g.replay()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    time.sleep(0.3)
+    ev0 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ev1 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(s):
+        for k in range(args.steps):
+            flush_l2()
+            ev0[k].record(s)
+            g.replay()
+            ev1[k].record(s)
+    torch.cuda.synchronize()
+    step_ms = [a.elapsed_time(b) for a, b in zip(ev0, ev1)]
+    # the call alone, eager, on the same stream (planner + attention)
+    a0 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    a1 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    with torch.cuda.stream(s):
+        for k in range(args.steps):
+            flush_l2()
+            a0[k].record(s)
+            pa.sparse_run(w, p, sel, out, ws, lse, stream=s)
+            a1[k].record(s)
+    torch.cuda.synchronize()
+    time.sleep(0.2)
+    clk = clocks.stop()
+    call_ms = [a.elapsed_time(b) for a, b in zip(a0, a1)]
+    # end to end: q, selections, table and lengths in from pinned memory, out back
+    hq = w.q.cpu().pin_memory()
+    hs = sel.cpu().pin_memory()
+    ht = w.block_table.cpu().pin_memory()
+    hl = w.context_lens.cpu().pin_memory()
+    ho = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e2e_ms = []
+    with torch.cuda.stream(s):
+        for k in range(args.steps):
+            flush_l2()
+            e0.record(s)
+            w.q.copy_(hq, non_blocking=True)
+            sel.copy_(hs, non_blocking=True)
+            w.block_table.copy_(ht, non_blocking=True)
+            w.context_lens.copy_(hl, non_blocking=True)
+            pa.sparse_run(w, p, sel, out, ws, lse, stream=s)
+            ho.copy_(out, non_blocking=True)
+            e1.record(s)
+            e1.synchronize()
+            e2e_ms.append(e0.elapsed_time(e1))
+    h2d = hq.numel() * hq.element_size() + hs.numel() * 4 + ht.numel() * 4 + hl.numel() * 4
+    d2h = ho.numel() * ho.element_size()
+    total_ms, call_avg, e2e_avg = max_over_ranks([sum(step_ms), sum(call_ms) / len(call_ms),
+                                                  sum(e2e_ms) / len(e2e_ms)], world, dev)
+    ms_per_step = total_ms / args.steps
+    peak, peak_kind = _peaks()
+    achieved = nbytes / (call_avg * 1e-3) / 1e9
+    return {
+        "metric": METRIC,
+        "op": "sparse",
+        "value": round(job_value(world, nbytes, ms_per_step), 2),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_per_step, 5),
+        "median_ms_per_step": round(statistics.median(step_ms), 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD_TEXT[args.workload], "name": args.workload, "batch": w.B, "next_n": w.n,
+                   "top_k": SPARSE_TOP_K, "selected_tokens": sum(counts), "selected_kv_bytes": nbytes,
+                   "l2": "a 256 MiB buffer is read before every step to evict the previous step's lines",
+                   "parallelism": f"replicas x{world}"},
+        "query_rows_per_s": round(world * rows / (ms_per_step * 1e-3), 1),
+        "pct_of_hbm_peak": round(100.0 * nbytes / (ms_per_step * 1e-3) / 1e9 / peak, 2),
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "traffic": None, "kernel": "pa_sparse_attn_kernel",
+                     "peak_source": f"{peak_kind} hbm_gbs", "call_ms": round(call_avg, 5),
+                     "note": "timed over the whole call (planner + attention); selected rows shared between "
+                             "the query tokens of a request can hit L2"},
+        "e2e": {"value": round(world * nbytes / (e2e_avg * 1e-3) / 1e9, 2), "unit": "GB/s",
+                "ms_per_step": round(e2e_avg, 5), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": 2 * args.steps,
+        "clocks": clk,
+    }, w, sel, nbytes
+
+
+def oracle_sparse_rate(w, sel, nbytes: int, budget_s: float, seed: int = 0):
+    """Time the sparse oracle on a bounded sample of query tokens (all heads).
+    Returns (GB/s equivalent, query rows/s, rows timed, seconds)."""
+    import numpy as np
+    from oracle import sparse as OS
+    wc = w.to("cpu")
+    sc = sel.cpu()
+    rng = np.random.default_rng(seed)
+    order = rng.permutation(w.B * w.n)
+    n = 1
+    while True:
+        pick = order[:n]
+        rows = [(int(r // w.n), int(r % w.n), h) for r in pick for h in range(w.Hq)]
+        t0 = time.perf_counter()
+        OS.sparse_attention(wc, sc, rows=rows)
+        dt = time.perf_counter() - t0
+        if dt >= budget_s / 4 or n >= w.B * w.n:
+            break
+        n = min(w.B * w.n, n * 2)
+    share = n / (w.B * w.n)
+    return nbytes * share / dt / 1e9, n / dt, n, dt
+
+
 def oracle_insert_rate(w, kn, vn, budget_s: float):
     """Time the insert oracle on a bounded prefix of the requests.  Returns
     (GB/s equivalent, tokens/s, requests timed, seconds)."""
@@ -660,6 +842,45 @@ def reference_insert_arm(args):
     }
 
 
+def reference_sparse_arm(args):
+    from paged_attention_quantized_gb300 import workloads as W
+    w = W.make(args.workload, device="cpu", B=args.batch)
+    sel = W.make_selection(w, k=SPARSE_TOP_K, seed=w.seed + 200, shared=0.9)
+    nbytes = sum(selected_counts(w, sel)) * w.Hkv * (w.k_row_bytes + w.v_row_bytes)
+    for _ in range(args.warmup):
+        oracle_sparse_rate(w, sel, nbytes, budget_s=0.2)
+    vals, secs, rs = [], [], []
+    nr = 1
+    for k in range(args.steps):
+        v, r, nr, dt = oracle_sparse_rate(w, sel, nbytes, budget_s=args.ref_step_s, seed=k)
+        vals.append(v)
+        secs.append(dt)
+        rs.append(r)
+    value = statistics.median(vals)
+    return {
+        "impl": "reference",
+        "op": "sparse",
+        "metric": METRIC,
+        "value": round(value, 4),
+        "unit": "GB/s",
+        "n_gpus": args.gpus,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(1e3 * statistics.median(secs), 3),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD_TEXT[args.workload], "name": args.workload, "top_k": SPARSE_TOP_K},
+        "query_rows_per_s": round(statistics.median(rs), 3),
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": f"{nr} of {w.B * w.n} query tokens (all heads) per step, seeded, fp64; "
+                                   f"{cpu_model()}"},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
 # -------------------------------------------------------------------- main
 
 
@@ -673,8 +894,9 @@ def main():
     ap.add_argument("--ref-step-s", type=float, default=2.0, help="oracle seconds per reference step")
     ap.add_argument("--cpu-baseline-s", type=float, default=12.0, help="oracle seconds for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--op", default="attention", choices=["attention", "insert"],
-                    help="the step timed: the attention (default) or the quantized paged KV insert")
+    ap.add_argument("--op", default="attention", choices=["attention", "insert", "sparse"],
+                    help="the step timed: the attention (default), the quantized paged KV insert, or sparse "
+                         "selected-token attention (qsa workload)")
     ap.add_argument("--batch", type=int, default=None,
                     help="requests of the workload (default: its recipe); a smaller batch is for profiling only")
     args = ap.parse_args()
@@ -687,15 +909,35 @@ def main():
     if args.impl == "reference":
         if rank != 0:
             return
-        print(json.dumps(reference_arm(args) if args.op == "attention" else reference_insert_arm(args)),
-              flush=True)
+        if args.op == "sparse" and args.workload == "bf16":
+            args.workload = "qsa"
+        arm = {"attention": reference_arm, "insert": reference_insert_arm, "sparse": reference_sparse_arm}[args.op]
+        print(json.dumps(arm(args)), flush=True)
         return
+    if args.op == "sparse" and args.workload == "bf16":
+        args.workload = "qsa"   # the sparse step's workload unless another is named
 
     if world > 1:
         import torch
         import torch.distributed as dist
         torch.cuda.set_device(local_rank)
         dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    if args.op == "sparse":
+        line, w, sel, nbytes = sparse_arm(args, rank, world, local_rank)
+        if rank == 0 and not args.no_cpu_baseline:
+            v, r, nr, dt = oracle_sparse_rate(w, sel, nbytes, args.cpu_baseline_s)
+            line["cpu_baseline"] = {"value": round(v, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                                    "sample": f"{nr} of {w.B * w.n} query tokens (all heads), seeded, {dt:.1f} s, "
+                                              f"fp64; GB/s scaled by the sampled share of the selected bytes; "
+                                              f"{cpu_model()}",
+                                    "query_rows_per_s": round(r, 3)}
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+            dist.destroy_process_group()
+        if rank == 0:
+            print(json.dumps(line), flush=True)
+        return
     if args.op == "insert":
         line, w, kn, vn = insert_arm(args, rank, world, local_rank)
         if rank == 0 and not args.no_cpu_baseline:

@@ -17,6 +17,9 @@ configurations of this library:
   latent   single-latent MQA, B=256, L~lognormal(median 8192, sigma 1,
            cap 131072), next_n=2, 128/1 heads, Dk=576, Dv=512 (= first 512
            channels of K), bs=64, E4M3 with a per-token fp32 scale
+  qsa      sparse (selected-token) attention: four 64K-token requests, 256
+           causal query rows each, 6 q / 1 kv heads, D=256, bs=16, fp16 KV
+           (selections from make_selection)
 
 Pool layout: every block is [Hkv][bs][row_bytes] codes; with per-token scales
 the block continues with [Hkv][bs] fp32 scales.  INT4 stores channel 2i in the
@@ -38,7 +41,8 @@ TORCH_FLOAT = {"f16": torch.float16, "bf16": torch.bfloat16, "f32": torch.float3
 CONFIG_NAMES = ("tiny", "bf16", "e4m3", "int8", "int4", "latent")
 # seed = 1234 + index of the configuration in the benchmark list (int8 and int4
 # are the two halves of the fourth configuration and share its seed)
-CONFIG_SEED = {"tiny": 1234, "bf16": 1235, "e4m3": 1236, "int8": 1237, "int4": 1237, "latent": 1238}
+CONFIG_SEED = {"tiny": 1234, "bf16": 1235, "e4m3": 1236, "int8": 1237, "int4": 1237, "latent": 1238,
+               "qsa": 1239}
 
 
 @dataclass
@@ -147,6 +151,8 @@ def _poison_bytes(shape, gen, device) -> torch.Tensor:
 def _lengths(name: str, B: int, gen_cpu: torch.Generator, lo=None, hi=None) -> torch.Tensor:
     if name == "tiny" and lo is None and hi is None and B <= 2:
         return torch.tensor([37, 70], dtype=torch.int32)[:B]
+    if name == "qsa" and lo is None and hi is None:
+        return torch.full((B,), 65536, dtype=torch.int32)
     if name == "latent":
         # lognormal, median 8192, sigma 1, capped at 131072, at least next_n
         z = torch.randn(B, generator=gen_cpu, dtype=torch.float64)
@@ -154,7 +160,7 @@ def _lengths(name: str, B: int, gen_cpu: torch.Generator, lo=None, hi=None) -> t
         lo_ = 2 if lo is None else lo
         hi_ = 131072 if hi is None else hi
         return L.round().clamp(lo_, hi_).to(torch.int32)
-    rng = {"tiny": (1, 100), "bf16": (512, 8192), "e4m3": (1024, 32768), "int8": (2048, 16384), "int4": (2048, 16384)}[name]
+    rng = {"tiny": (1, 100), "qsa": (1, 65536), "bf16": (512, 8192), "e4m3": (1024, 32768), "int8": (2048, 16384), "int4": (2048, 16384)}[name]
     lo_ = rng[0] if lo is None else lo
     hi_ = rng[1] if hi is None else hi
     return torch.randint(lo_, hi_ + 1, (B,), generator=gen_cpu, dtype=torch.int64).to(torch.int32)
@@ -168,6 +174,8 @@ _SHAPES = {
     "int8": (128, 1, 64, 8, 128, 128, 16, "f16", "int8", "f32", "channel", "channel", False, False),
     "int4": (128, 1, 64, 8, 128, 128, 16, "f16", "int4", "f32", "channel", "channel", False, False),
     "latent": (256, 2, 128, 1, 576, 512, 64, "bf16", "e4m3", "bf16", "token", "token", True, True),
+    # sparse (selected-token) attention: four 64K-token requests, 256 query rows each
+    "qsa": (4, 256, 6, 1, 256, 256, 16, "f16", "f16", "f16", "none", "none", True, False),
 }
 
 
