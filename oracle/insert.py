@@ -46,6 +46,7 @@ insert(w, k_new, v_new) -> (k_pool, v_pool, flags)   new pools as uint8 arrays
 from __future__ import annotations
 
 import numpy as np
+import torch
 
 from . import e4m3_table
 
@@ -63,7 +64,7 @@ def _host(t):
         t = t.detach().cpu().contiguous()
         name = str(t.dtype)
         if name == "torch.bfloat16":
-            return ("bf16", t.view(__import__("torch").int16).numpy().view(np.uint16))
+            return ("bf16", t.view(torch.int16).numpy().view(np.uint16))
         if name == "torch.float16":
             return ("f16", t.numpy())
         if name == "torch.float32":
