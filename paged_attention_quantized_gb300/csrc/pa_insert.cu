@@ -14,9 +14,10 @@
 //    past 448 saturate instead.
 //
 // The kernel is HBM-bound (16-byte vector loads of the new rows, one store of
-// 4-16 bytes per 8 channels): a persistent grid of 256-thread CTAs, each warp
-// split into row groups of 8, 16 or 32 lanes (the smallest power of two that
-// covers the row's 8-channel chunks, 32 for rows longer than 256 channels).
+// 4-16 bytes per 8 channels): a grid-stride loop over up to 8 CTAs of 256
+// threads per SM, each warp split into row groups of 8, 16 or 32 lanes (the
+// smallest power of two that covers the row's 8-channel chunks, 32 for rows
+// longer than 256 channels).
 // Rows are ordered (token, plane, kv head), so the warps of a CTA write
 // neighbouring slots of the same blocks.
 #include <cuda_bf16.h>
