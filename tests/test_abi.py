@@ -311,3 +311,39 @@ def test_sparse_rejects_bad_arguments(B, case, expect):
     p = _prob(B, **case.get("p", {}))
     st = _sparse_status(B, p, case.get("top_k", 16), case.get("ws_bytes", 1 << 20), case.get("ptrs"))
     assert st == getattr(B, "PA_ERR_" + expect)
+
+
+# ------------------------------------------------- the header from plain C
+
+
+def test_header_compiles_as_c11_and_links(B, tmp_path):
+    import subprocess
+    exe = tmp_path / "abi_check"
+    src = os.path.join(ROOT, "tests", "c", "abi_check.c")
+    libdir = os.path.dirname(B.LIB_PATH)
+    r = subprocess.run(["gcc", "-std=c11", "-Wall", "-Wextra", "-Werror", "-pedantic", "-I",
+                        os.path.join(ROOT, "include"), src, "-o", str(exe), "-L", libdir, "-lpa",
+                        "-Wl,-rpath," + libdir], capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    run = subprocess.run([str(exe)], capture_output=True, text=True)
+    assert run.returncode == 0, run.stdout + run.stderr
+    assert "version" in run.stdout
+
+
+def _prototype_arity():
+    """Argument count of every PA_API prototype in include/pa.h."""
+    hdr = open(os.path.join(ROOT, "include", "pa.h")).read()
+    hdr = re.sub(r"/\*.*?\*/", "", hdr, flags=re.S)
+    out = {}
+    for m in re.finditer(r"PA_API\s+[\w\s\*]+?\b(pa_\w+)\s*\(([^)]*)\)\s*;", hdr):
+        args = m.group(2).strip()
+        out[m.group(1)] = 0 if args in ("", "void") else len(args.split(","))
+    return out
+
+
+def test_binding_declares_every_prototype_with_its_arity(B):
+    arity = _prototype_arity()
+    assert len(arity) == len(declared_symbols())
+    for name, n in arity.items():
+        f = getattr(B._lib, name)
+        assert f.argtypes is not None and len(f.argtypes) == n, (name, n, f.argtypes)
