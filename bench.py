@@ -752,6 +752,15 @@ def oracle_rate(w, budget_s: float, seed: int = 0):
     return eff / dt / 1e9, n / dt, n, dt, threads
 
 
+REFERENCE_TOTAL_S = 150.0  # oracle seconds a whole reference run may take (all timed steps)
+
+
+def ref_step_budget(args) -> float:
+    """Oracle seconds per reference step: --ref-step-s, reduced so that the
+    K timed steps together stay within REFERENCE_TOTAL_S."""
+    return max(0.05, min(args.ref_step_s, REFERENCE_TOTAL_S / max(1, args.steps)))
+
+
 def cpu_model() -> str:
     try:
         out = subprocess.run(["lscpu"], capture_output=True, text=True).stdout
@@ -772,7 +781,7 @@ def reference_arm(args):
     n_rows = 0
     threads = 1
     for k in range(args.steps):
-        v, r, n, dt, threads = oracle_rate(w, budget_s=args.ref_step_s, seed=k)
+        v, r, n, dt, threads = oracle_rate(w, budget_s=ref_step_budget(args), seed=k)
         vals.append(v)
         rows_s.append(r)
         secs.append(dt)
@@ -812,7 +821,7 @@ def reference_insert_arm(args):
     vals, secs, toks = [], [], []
     nb = 1
     for _ in range(args.steps):
-        v, r, nb, dt = oracle_insert_rate(w, kn, vn, budget_s=args.ref_step_s)
+        v, r, nb, dt = oracle_insert_rate(w, kn, vn, budget_s=ref_step_budget(args))
         vals.append(v)
         secs.append(dt)
         toks.append(r)
@@ -852,7 +861,7 @@ def reference_sparse_arm(args):
     vals, secs, rs = [], [], []
     nr = 1
     for k in range(args.steps):
-        v, r, nr, dt = oracle_sparse_rate(w, sel, nbytes, budget_s=args.ref_step_s, seed=k)
+        v, r, nr, dt = oracle_sparse_rate(w, sel, nbytes, budget_s=ref_step_budget(args), seed=k)
         vals.append(v)
         secs.append(dt)
         rs.append(r)
