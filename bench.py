@@ -68,13 +68,16 @@ WORKLOAD_TEXT = {
     "latent": "single-latent-KV MQA decode: B=256, L~lognormal(median 8192, sigma 1, cap 131072), next_n=2 "
               "causal, 128 q heads / 1 kv head, Dk=576, Dv=512 (first 512 of K), bs=64, E4M3 KV with a "
               "per-token fp32 scale, q~N(0,1) bf16, bf16 out",
+    "verify": "FP8 E4M3 verify of 16 draft tokens: B=32, L~U[1024,32768], next_n=16 causal, 32 q / 8 kv heads "
+              "(64 query rows per kv head), D=256, bs=32, per-tensor scales 0.05, NaN-poisoned null/slack/padding, "
+              "bf16 out",
     "qsa": "sparse selected-token attention: 4 requests of 65536 tokens, 256 causal query rows each "
            "(1024 rows), 6 q / 1 kv heads, D=256, bs=16, fp16 KV, top-k 2048 selections, 90% shared "
            "per request, fp16 out",
 }
 SPARSE_TOP_K = 2048
 COMPUTE_DTYPE = {"tiny": "f16", "bf16": "bf16", "e4m3": "f16", "int8": "f16", "int4": "f16", "latent": "f16",
-                 "qsa": "f16"}
+                 "qsa": "f16", "verify": "f16"}
 L2_FLUSH_BYTES = 256 << 20
 
 

@@ -17,6 +17,8 @@ configurations of this library:
   latent   single-latent MQA, B=256, L~lognormal(median 8192, sigma 1,
            cap 131072), next_n=2, 128/1 heads, Dk=576, Dv=512 (= first 512
            channels of K), bs=64, E4M3 with a per-token fp32 scale
+  verify   the e4m3 recipe with next_n=16 (16 draft tokens verified per
+           request: 64 query rows per kv head)
   qsa      sparse (selected-token) attention: four 64K-token requests, 256
            causal query rows each, 6 q / 1 kv heads, D=256, bs=16, fp16 KV
            (selections from make_selection)
@@ -42,7 +44,7 @@ CONFIG_NAMES = ("tiny", "bf16", "e4m3", "int8", "int4", "latent")
 # seed = 1234 + index of the configuration in the benchmark list (int8 and int4
 # are the two halves of the fourth configuration and share its seed)
 CONFIG_SEED = {"tiny": 1234, "bf16": 1235, "e4m3": 1236, "int8": 1237, "int4": 1237, "latent": 1238,
-               "qsa": 1239}
+               "qsa": 1239, "verify": 1236}
 
 
 @dataclass
@@ -160,7 +162,7 @@ def _lengths(name: str, B: int, gen_cpu: torch.Generator, lo=None, hi=None) -> t
         lo_ = 2 if lo is None else lo
         hi_ = 131072 if hi is None else hi
         return L.round().clamp(lo_, hi_).to(torch.int32)
-    rng = {"tiny": (1, 100), "qsa": (1, 65536), "bf16": (512, 8192), "e4m3": (1024, 32768), "int8": (2048, 16384), "int4": (2048, 16384)}[name]
+    rng = {"tiny": (1, 100), "qsa": (1, 65536), "verify": (1024, 32768), "bf16": (512, 8192), "e4m3": (1024, 32768), "int8": (2048, 16384), "int4": (2048, 16384)}[name]
     lo_ = rng[0] if lo is None else lo
     hi_ = rng[1] if hi is None else hi
     return torch.randint(lo_, hi_ + 1, (B,), generator=gen_cpu, dtype=torch.int64).to(torch.int32)
@@ -174,6 +176,8 @@ _SHAPES = {
     "int8": (128, 1, 64, 8, 128, 128, 16, "f16", "int8", "f32", "channel", "channel", False, False),
     "int4": (128, 1, 64, 8, 128, 128, 16, "f16", "int4", "f32", "channel", "channel", False, False),
     "latent": (256, 2, 128, 1, 576, 512, 64, "bf16", "e4m3", "bf16", "token", "token", True, True),
+    # verify of 16 draft tokens per request (many query rows per kv head: 4 row blocks)
+    "verify": (32, 16, 32, 8, 256, 256, 32, "bf16", "e4m3", "bf16", "tensor", "tensor", True, False),
     # sparse (selected-token) attention: four 64K-token requests, 256 query rows each
     "qsa": (4, 256, 6, 1, 256, 256, 16, "f16", "f16", "f16", "none", "none", True, False),
 }
@@ -211,7 +215,7 @@ def make(name: str, device="cpu", seed: Optional[int] = None, *, B: Optional[int
         bs = int(bs)
     else:
         bs = bs0
-    poison = (name == "e4m3") if poison is None else poison
+    poison = (name in ("e4m3", "verify")) if poison is None else poison
     device = torch.device(device)
     gcpu = _gen("cpu", seed)
     gdev = _gen(device, seed + 1)
