@@ -13,7 +13,7 @@ from oracle import sparse as OS
 import paged_attention_quantized_gb300 as pa
 from paged_attention_quantized_gb300 import build as pabuild
 from paged_attention_quantized_gb300 import workloads as W
-from tests.gpu_check import TOL
+from tests.gpu_check import TOL, abs_values
 
 pytestmark = pytest.mark.gpu
 
@@ -44,7 +44,10 @@ def check(w, sel, out, lse):
     o = out.double().cpu().numpy()
     tol = TOL[w.out_dtype]
     if w.kv_dtype in ("int8", "int4"):
-        allow = tol * np.maximum(1.0, np.abs(ref))
+        # per-channel fp32 outputs up to 1e5 with cancellation between tokens:
+        # normwise, against sum_t p_t |v_t| (the same criterion as the dense path)
+        mag, _ = OS.sparse_attention(abs_values(w), sel.cpu())
+        allow = tol * np.maximum(1.0, mag.reshape(ref.shape))
     else:
         allow = tol
     assert np.all(np.abs(o - ref) <= allow)
