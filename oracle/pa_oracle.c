@@ -340,10 +340,9 @@ int orc_attention(const orc_problem *p, const void *q, const void *k_pool, const
     return J.status;
 }
 
-/* Near-tie analysis of one row (used where the softmax is almost one-hot and
- * the argmax token is sensitive to rounding; see the onnxruntime PR #32520
- * page, Validation status: "with nonzero codes a scale that large makes
- * softmax one-hot, and the argmax is then fp16-sensitive").
+/* Near-tie analysis of one row, for rows whose softmax is almost one-hot:
+ * there the token that wins can change with fp16 rounding of the folded
+ * query (onnxruntime PR #32520 page, Validation status).
  *
  * Computes the row's scores s_t exactly, M = max s_t and the gap M - s_(2) to
  * the runner-up (+inf if only one token is visible), and, over the tokens with

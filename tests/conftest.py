@@ -13,5 +13,19 @@ def pytest_configure(config):
 
 
 def pytest_collection_modifyitems(config, items):
-    # the no-allocation entry point's test file must run last
+    # Files named test_zz_* run last.  The no-allocation entry point's test
+    # lives there: a run that stops at the first failure (-x) has then run
+    # every other test before it, and that test also checks that the shared
+    # static scratch gives the same results after all the other work done in
+    # this process.
     items.sort(key=lambda it: 1 if os.path.basename(str(it.fspath)).startswith("test_zz_") else 0)
+
+
+def pytest_terminal_summary(terminalreporter):
+    # counts that GPU tests report (e.g. rows accepted through the near-tie
+    # hull), printed even when the tests pass
+    from tests import notes
+    if notes.LINES:
+        terminalreporter.write_sep("-", "reported by the tests")
+        for ln in notes.LINES:
+            terminalreporter.write_line(ln)

@@ -10,6 +10,7 @@ import oracle
 import paged_attention_quantized_gb300 as pa
 from paged_attention_quantized_gb300 import build as pabuild
 from paged_attention_quantized_gb300 import workloads as W
+from tests import notes
 from tests.gpu_check import compare, error_bits, run_gpu, sample_rows
 
 pytestmark = pytest.mark.gpu
@@ -326,7 +327,14 @@ def test_full_size_sampled_parity(name):
     assert torch.isfinite(out.float()).all()
     rows = sample_rows(w, 160 if name != "e4m3" else 96)
     host = oracle.HostArrays(w)
-    compare(w, out, lse, rows=rows, host=host)
+    rep = {}
+    compare(w, out, lse, rows=rows, host=host, report=rep)
+    notes.add(f"full-size {name}: {rep['rows']} sampled rows, max abs err {rep['max_err']:.3g}, "
+              f"{rep['hull_rows']} accepted through the near-tie hull ({rep['tie_rows']} with an exact top-two "
+              f"gap below 2 eps)")
+    # a near tie needs two tokens within the fold's error of the maximum:
+    # most rows are decided by the normwise bound
+    assert rep["hull_rows"] <= rep["rows"] // 4
     # allocation invariance at full size
     w2 = W.relocate(w, seed=5)
     o2, l2, _, _ = run_gpu(w2)

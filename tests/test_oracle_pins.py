@@ -322,22 +322,112 @@ def test_max_abs_scale():
 # -------------------------------------------------------------------- near ties
 
 
-def test_row_ties_detects_duplicate_maximum():
-    w = W.make("int8", B=1, Hq=2, Hkv=1, context_lens=[20])
-    # copy token 3's K and V rows onto token 11 -> exact tie at the max?
-    blk3, blk11 = int(w.block_table[0, 0]), int(w.block_table[0, 0])
+def _tie_workload(codes0, n=1, causal=False, v_seed=0):
+    """INT8 per-channel cache (scales 1), one kv head, D = 64, softmax scale
+    1/8, q = e_0: the exact score of token t is codes0[t] / 8, so scores are
+    fixed by hand (every value below is exact in binary)."""
+    L = len(codes0)
+    w = W.make("int8", B=1, Hq=1, Hkv=1, D=64, n=n, context_lens=[L])
+    w.causal = causal
+    q = torch.zeros_like(w.q, dtype=torch.float32)
+    q[..., 0] = 1.0
+    w.q = q.to(w.q.dtype)
+    w.k_scale = torch.ones_like(w.k_scale)
+    rng = np.random.default_rng(v_seed)
+    w.v_scale = torch.from_numpy(rng.uniform(0.5, 2.0, size=tuple(w.v_scale.shape)).astype(np.float32))
     k = w.k_pool.clone()
     rb = w.k_row_bytes
-    k[blk11, 11 * rb:12 * rb] = k[blk3, 3 * rb:4 * rb]
+    for t, c in enumerate(codes0):
+        blk = int(w.block_table[0, t // w.bs])
+        slot = t % w.bs
+        row = k[blk, slot * rb:(slot + 1) * rb]
+        row[0] = int(np.int8(c).view(np.uint8))
     w.k_pool = k
-    out, _ = _oracle_full(w)
+    assert w.softmax_scale == 0.125
+    return w
+
+
+def _v_values(w, tokens):
+    """Decoded V rows (code * v_scale) of the given logical tokens."""
+    out = []
+    rb = w.v_row_bytes
+    vs = w.v_scale.numpy().astype(np.float64)[0]
+    for t in tokens:
+        blk = int(w.block_table[0, t // w.bs])
+        slot = t % w.bs
+        codes = w.v_pool[blk, slot * rb:(slot + 1) * rb].numpy().view(np.int8).astype(np.float64)
+        out.append(codes * vs)
+    return np.array(out)
+
+
+# scores (code / 8): 12.5 at token 22 (the maximum), 12.0 at 3 and 11.5 at 37
+# (within 1.0), 11.0 at 17 (exactly 1.5 below), everything else <= 50 / 8
+_TIE_CODES = [((t * 7) % 51) - 20 for t in range(40)]
+for _t, _c in ((3, 96), (17, 88), (22, 100), (37, 92)):
+    _TIE_CODES[_t] = _c
+
+
+def test_row_ties_selects_exactly_within_delta_of_the_maximum():
+    w = _tie_workload(_TIE_CODES)
+    vmin, vmax, gap, cnt = oracle.row_ties(w, 0, 0, 0, delta=1.0)
+    assert cnt == 3                                   # 12.5, 12.0, 11.5 (the bound itself is inside)
+    assert gap == 0.5                                 # exact distance to the runner-up
+    ref = _v_values(w, [3, 22, 37])
+    assert np.array_equal(vmin, ref.min(axis=0)) and np.array_equal(vmax, ref.max(axis=0))
+    vmin, vmax, gap, cnt = oracle.row_ties(w, 0, 0, 0, delta=1.5)
+    assert cnt == 4
+    ref = _v_values(w, [3, 17, 22, 37])
+    assert np.array_equal(vmin, ref.min(axis=0)) and np.array_equal(vmax, ref.max(axis=0))
+    # a delta that puts M - delta one ulp above 11.5 (the ulp of scores in
+    # [8, 16) is 2^-49) drops the token at exactly M - delta; likewise at 12.0
+    _, _, _, cnt = oracle.row_ties(w, 0, 0, 0, delta=1.0 - 2.0 ** -49)
+    assert cnt == 2
+    _, _, _, cnt = oracle.row_ties(w, 0, 0, 0, delta=0.5 - 2.0 ** -49)
+    assert cnt == 1
+    vmin, vmax, _, cnt = oracle.row_ties(w, 0, 0, 0, delta=0.0)
+    assert cnt == 1
+    ref = _v_values(w, [22])[0]
+    assert np.array_equal(vmin, ref) and np.array_equal(vmax, ref)
+
+
+def test_row_ties_exact_tie_and_maximum_at_the_ends():
+    codes = list(_TIE_CODES)
+    codes[0] = 100                                    # ties the maximum, first token
+    w = _tie_workload(codes)
     vmin, vmax, gap, cnt = oracle.row_ties(w, 0, 0, 0, delta=0.0)
-    assert cnt >= 1 and gap >= 0
-    assert np.all(out[0, 0, 0] >= vmin - 1e-9 * np.abs(vmin)) or cnt == 1
-    # with a delta covering everything every token is a candidate
+    assert gap == 0.0 and cnt == 2
+    ref = _v_values(w, [0, 22])
+    assert np.array_equal(vmin, ref.min(axis=0)) and np.array_equal(vmax, ref.max(axis=0))
+    codes = list(_TIE_CODES)
+    codes[39] = 104                                   # a new maximum, last token: 13.0
+    w = _tie_workload(codes)
+    vmin, vmax, gap, cnt = oracle.row_ties(w, 0, 0, 0, delta=1.0)
+    assert gap == 0.5 and cnt == 3                    # 13.0, 12.5, 12.0
+    ref = _v_values(w, [3, 22, 39])
+    assert np.array_equal(vmin, ref.min(axis=0)) and np.array_equal(vmax, ref.max(axis=0))
+
+
+def test_row_ties_respects_the_causal_horizon():
+    codes = list(_TIE_CODES)
+    codes[39] = 104                                   # visible to the last query row only
+    w = _tie_workload(codes, n=2, causal=True)
+    _, _, gap, cnt = oracle.row_ties(w, 0, 0, 0, delta=1.0)   # row 0 sees tokens 0..38
+    assert gap == 0.5 and cnt == 3                    # 12.5, 12.0, 11.5
+    _, _, gap, cnt = oracle.row_ties(w, 0, 1, 0, delta=1.0)   # row 1 sees token 39 too
+    assert gap == 0.5 and cnt == 3                    # 13.0, 12.5, 12.0
+
+
+def test_row_ties_single_token_and_whole_row():
+    w = _tie_workload(_TIE_CODES[:1])
+    vmin, vmax, gap, cnt = oracle.row_ties(w, 0, 0, 0, delta=0.0)
+    assert cnt == 1 and gap == math.inf
+    w = _tie_workload(_TIE_CODES)
+    out, _ = _oracle_full(w)
     vmin, vmax, gap, cnt = oracle.row_ties(w, 0, 0, 0, delta=float("inf"))
-    assert cnt == 20
-    assert np.all(out[0, 0, 0] >= vmin - 1e-9) and np.all(out[0, 0, 0] <= vmax + 1e-9)
+    assert cnt == 40
+    ref = _v_values(w, range(40))
+    assert np.array_equal(vmin, ref.min(axis=0)) and np.array_equal(vmax, ref.max(axis=0))
+    assert np.all(out[0, 0, 0] >= vmin - 1e-12) and np.all(out[0, 0, 0] <= vmax + 1e-12)
 
 
 def test_bad_block_id_is_reported_not_read():
