@@ -13,11 +13,16 @@ would land inside the next timed kernel.  `value` is the effective KV bandwidth:
 single pass must read (real tokens only, codes + scales, K and V once) divided
 by the device time of the step.
 
-The default workload is the bf16 GQA decode batch (B=64, L~U[512,8192], 32 q /
-8 kv heads, D=128, bs=16).  The other workloads of the library can be timed
-with --workload (tiny, e4m3, int8, int4, latent).  The latent workload is a
-dense contraction: its roofline is the tensor rate (flops of S = q K^T and
-O = P V over the visible tokens), with the HBM fraction beside it.
+By default every benchmark configuration is timed in turn and printed as one
+JSON line each -- tiny fp16, bf16 GQA decode, E4M3 verify, INT8 and INT4
+per-channel, and last, as the headline, the single-latent MQA batch (the
+largest in tokens and in work).  --workload NAME times one of them (or the
+verify / qsa workloads).  Before anything is timed, the oracle evaluates a
+seeded sample of rows of the very batch about to be timed and the GPU output
+must match it at the library's tolerances (the run fails otherwise); the
+same oracle run's wall time is the line's cpu_baseline.  The latent workload
+is a dense contraction: its roofline is the tensor rate (flops of S = q K^T
+and O = P V over the visible tokens), with the HBM fraction beside it.
 
 With N > 1 (torchrun, one rank per GPU) every rank times its own replica of
 the batch (requests are independent, nothing is exchanged): weak scaling,
@@ -76,6 +81,9 @@ WORKLOAD_TEXT = {
            "per request, fp16 out",
 }
 SPARSE_TOP_K = 2048
+# the benchmark configurations in order; the last (largest in tokens and in
+# work) is the headline line
+ALL_CONFIGS = ("tiny", "bf16", "e4m3", "int8", "int4", "latent")
 COMPUTE_DTYPE = {"tiny": "f16", "bf16": "bf16", "e4m3": "f16", "int8": "f16", "int4": "f16", "latent": "f16",
                  "qsa": "f16", "verify": "f16"}
 L2_FLUSH_BYTES = 256 << 20
@@ -216,7 +224,9 @@ def insert_bytes(w) -> int:
 # -------------------------------------------------------------- GPU arm
 
 
-def gpu_arm(args, rank, world, local_rank):
+def gpu_arm(args, name, rank, world, local_rank, check=None):
+    """Time workload `name`; `check(w, out, lse)` (rank 0) runs after one
+    untimed pass and before anything is timed, and raises on a mismatch."""
     import torch
     import paged_attention_quantized_gb300 as pa
     from paged_attention_quantized_gb300 import build as pabuild
@@ -225,7 +235,7 @@ def gpu_arm(args, rank, world, local_rank):
     pabuild.build()
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
-    w = W.make(args.workload, device=dev, B=args.batch)
+    w = W.make(name, device=dev, B=args.batch)
     p = pa.problem(w)
     out, lse, ws = pa.alloc(w, p, device=dev)
     B = pa.binding()
@@ -251,6 +261,9 @@ def gpu_arm(args, rank, world, local_rank):
         raise RuntimeError(f"device error bits {bits:#x}")
     if not torch.isfinite(out.float()).all():
         raise RuntimeError("non-finite output")
+    # correctness before timing: the oracle on sampled rows of this very batch
+    extra = check(w, out, lse) if (check is not None and rank == 0) else {}
+    dist_barrier()
 
     # capture one step
     g = torch.cuda.CUDAGraph()
@@ -343,7 +356,7 @@ def gpu_arm(args, rank, world, local_rank):
     value = job_value(world, eff_bytes, ms_per_step)
     peak, peak_kind = _peaks()
     achieved = eff_bytes / (attn_avg * 1e-3) / 1e9
-    traffic = _traffic(args.workload)
+    traffic = _traffic(name)
     roofline = {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
                 "frac": round(achieved / peak, 4), "traffic": traffic,
                 "kernel": "pa_attn_kernel", "peak_source": f"{peak_kind} hbm_gbs",
@@ -374,10 +387,10 @@ def gpu_arm(args, rank, world, local_rank):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": COMPUTE_DTYPE[args.workload],
+        "dtype": COMPUTE_DTYPE[name],
         "data": "synthetic",
-        "config": {"workload": WORKLOAD_TEXT[args.workload] + ("" if args.batch is None else f" (batch {w.B})"),
-                   "name": args.workload, "batch": w.B,
+        "config": {"workload": WORKLOAD_TEXT[name] + ("" if args.batch is None else f" (batch {w.B})"),
+                   "name": name, "batch": w.B,
                    "next_n": w.n, "total_tokens": int(w.context_lens.sum().item()),
                    "effective_kv_bytes": eff_bytes,
                    "l2": "inputs larger than L2; a 256 MiB buffer is read before every step to evict the "
@@ -391,6 +404,7 @@ def gpu_arm(args, rank, world, local_rank):
                 "ms_per_step": round(e2e_avg, 5), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clk,
+        **extra,
     }, w
 
 
@@ -731,12 +745,13 @@ def oracle_insert_rate(w, kn, vn, budget_s: float):
 # ---------------------------------------------------------- CPU oracle arm
 
 
-def oracle_rate(w, budget_s: float, seed: int = 0):
-    """Time the oracle on a bounded, seeded sample of rows of workload w.
-    Returns (GB/s equivalent, rows/s, rows timed, seconds, threads)."""
+def oracle_sample(w, budget_s: float, seed: int = 0, host=None):
+    """Run the oracle on a bounded, seeded sample of (b, j, h) rows of
+    workload w, sized to about budget_s seconds.  Returns (rows, out, lse,
+    seconds of the timed run, threads, all rows)."""
     import numpy as np
     import oracle
-    host = oracle.HostArrays(w)
+    host = host if host is not None else oracle.HostArrays(w)
     threads = len(os.sched_getaffinity(0))
     allrows = np.stack(np.meshgrid(np.arange(w.B), np.arange(w.n), np.arange(w.Hq), indexing="ij"), -1).reshape(-1, 3)
     rng = np.random.default_rng(seed)
@@ -749,10 +764,44 @@ def oracle_rate(w, budget_s: float, seed: int = 0):
     n = int(min(len(allrows), max(n0, n0 * budget_s / dt)))
     rows = allrows[perm[:n]]
     t0 = time.perf_counter()
-    oracle.attention(w, rows=rows, host=host, threads=threads)
+    ref, rlse = oracle.attention(w, rows=rows, host=host, threads=threads)
     dt = time.perf_counter() - t0
-    eff = w.effective_kv_bytes() * (n / len(allrows))
+    return rows, ref, rlse, dt, threads, len(allrows)
+
+
+def oracle_rate(w, budget_s: float, seed: int = 0):
+    """Time the oracle on a bounded, seeded sample of rows of workload w.
+    Returns (GB/s equivalent, rows/s, rows timed, seconds, threads)."""
+    rows, _, _, dt, threads, nall = oracle_sample(w, budget_s, seed)
+    n = len(rows)
+    eff = w.effective_kv_bytes() * (n / nall)
     return eff / dt / 1e9, n / dt, n, dt, threads
+
+
+def parity_and_baseline(w, out, lse, budget_s: float):
+    """The oracle on a seeded sample of rows of the batch about to be timed:
+    its wall time is the cpu_baseline, and its rows are compared with the
+    GPU's output of the same batch at the library's tolerances (fp32 output
+    2e-3, bf16 / fp16 1e-2; per-channel INT8 / INT4 normwise with the near-tie
+    rule) -- a mismatch raises, so nothing is timed."""
+    import oracle
+    from tests.gpu_check import TOL, compare
+    host = oracle.HostArrays(w)
+    rows, ref, rlse, dt, threads, nall = oracle_sample(w, budget_s, host=host)
+    n = len(rows)
+    rep = {}
+    compare(w, out, lse, rows=rows, host=host, report=rep, ref=(ref, rlse))
+    v = w.effective_kv_bytes() * (n / nall) / dt / 1e9
+    return {
+        "parity": {"rows": n, "of_rows": nall, "max_abs_err": rep["max_err"], "tol": TOL[w.out_dtype],
+                   "near_tie_hull_rows": rep["hull_rows"], "checked": "before timing, same batch",
+                   "rule": "normwise |gpu-ref| <= tol * max(1, sum_t p_t |v_t|) with the near-tie hull"
+                           if w.kv_dtype in ("int8", "int4") and w.k_scale_mode == "channel" else "max abs error"},
+        "cpu_baseline": {"value": round(v, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
+                         "sample": f"{n} of {nall} (b, j, h) rows, seeded, {dt:.1f} s; GB/s scaled by the "
+                                   f"sampled share of the effective KV bytes; {cpu_model()}",
+                         "query_rows_per_s": round(n / dt / w.Hq, 3)},
+    }
 
 
 REFERENCE_TOTAL_S = 150.0  # oracle seconds a whole reference run may take (all timed steps)
@@ -775,9 +824,9 @@ def cpu_model() -> str:
     return "unknown"
 
 
-def reference_arm(args):
+def reference_arm(args, name):
     from paged_attention_quantized_gb300 import workloads as W
-    w = W.make(args.workload, device="cpu", B=args.batch)
+    w = W.make(name, device="cpu", B=args.batch)
     for _ in range(args.warmup):
         oracle_rate(w, budget_s=0.5)
     vals, rows_s, secs = [], [], []
@@ -807,7 +856,7 @@ def reference_arm(args):
         "vs_baseline": None,
         "dtype": "f64",
         "data": "synthetic",
-        "config": {"workload": WORKLOAD_TEXT[args.workload], "name": args.workload},
+        "config": {"workload": WORKLOAD_TEXT[name], "name": name},
         "query_rows_per_s": round(statistics.median(rows_s) / w.Hq, 3),
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
                          "sample": sample},
@@ -901,10 +950,12 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
-    ap.add_argument("--workload", default="bf16", choices=sorted(WORKLOAD_TEXT))
+    ap.add_argument("--workload", default="all", choices=["all"] + sorted(WORKLOAD_TEXT),
+                    help="all (default): one line per benchmark configuration, the largest (latent) last")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--ref-step-s", type=float, default=2.0, help="oracle seconds per reference step")
-    ap.add_argument("--cpu-baseline-s", type=float, default=12.0, help="oracle seconds for cpu_baseline")
+    ap.add_argument("--cpu-baseline-s", type=float, default=8.0,
+                    help="oracle seconds (per configuration) for the parity check and cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--op", default="attention", choices=["attention", "insert", "sparse"],
                     help="the step timed: the attention (default), the quantized paged KV insert, or sparse "
@@ -918,16 +969,22 @@ def main():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
 
+    if args.op != "attention" and args.workload == "all":
+        args.workload = {"sparse": "qsa", "insert": "bf16"}[args.op]   # the step's own default workload
+    names = ALL_CONFIGS if args.workload == "all" else (args.workload,)
     if args.impl == "reference":
         if rank != 0:
             return
-        if args.op == "sparse" and args.workload == "bf16":
-            args.workload = "qsa"
-        arm = {"attention": reference_arm, "insert": reference_insert_arm, "sparse": reference_sparse_arm}[args.op]
+        if args.op == "attention":
+            saved = args.ref_step_s
+            args.ref_step_s = saved / len(names)   # the whole run stays within a few minutes
+            for name in names:
+                print(json.dumps(reference_arm(args, name)), flush=True)
+            args.ref_step_s = saved
+            return
+        arm = {"insert": reference_insert_arm, "sparse": reference_sparse_arm}[args.op]
         print(json.dumps(arm(args)), flush=True)
         return
-    if args.op == "sparse" and args.workload == "bf16":
-        args.workload = "qsa"   # the sparse step's workload unless another is named
 
     if world > 1:
         import torch
@@ -965,21 +1022,19 @@ def main():
         if rank == 0:
             print(json.dumps(line), flush=True)
         return
-    line, w = gpu_arm(args, rank, world, local_rank)
-    if rank == 0 and not args.no_cpu_baseline:
-        wc = w  # the timed batch itself; the oracle reads host copies of it
-        v, r, n, dt, threads = oracle_rate(wc, budget_s=args.cpu_baseline_s)
-        line["cpu_baseline"] = {"value": round(v, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
-                                "sample": f"{n} of {wc.B * wc.n * wc.Hq} (b, j, h) rows, seeded, {dt:.1f} s; "
-                                          f"GB/s scaled by the sampled share of the effective KV bytes; "
-                                          f"{cpu_model()}",
-                                "query_rows_per_s": round(r / wc.Hq, 3)}
+    check = None if args.no_cpu_baseline else (lambda w, out, lse: parity_and_baseline(w, out, lse,
+                                                                                      args.cpu_baseline_s))
+    for name in names:
+        line, w = gpu_arm(args, name, rank, world, local_rank, check=check)
+        if len(names) > 1:
+            line["headline"] = name == names[-1]
+        del w
+        if rank == 0:
+            print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist
         dist.barrier()
         dist.destroy_process_group()
-    if rank == 0:
-        print(json.dumps(line), flush=True)
 
 
 if __name__ == "__main__":

@@ -71,7 +71,10 @@
  *  a captured step.
  *
  * ------------------------------------------------------------------- errors
- *  Host-detectable problems return a status and launch nothing.
+ *  Host-detectable problems return a status and launch nothing.  Among
+ *  them: a batch whose table could name more than 2^31 - 1 pages in all
+ *  (batch x max_blocks_per_seq work pages) is PA_ERR_UNSUPPORTED, since the
+ *  plan keeps page counts in 32 bits.
  *  Contract violations only visible on the device (a block id outside
  *  [1, num_blocks) at a visible position, L_b outside [0, max_context_len] or
  *  needing more than max_blocks_per_seq columns, context_lens changed since
@@ -241,8 +244,8 @@ PA_API pa_status pa_attention(const pa_problem *p, const void *q, const void *k_
                               void *out, float *lse, pa_stream_t stream);
 
 /* pa_attention without a workspace argument, for callers that cannot
- * allocate device memory (a host that only passes its plugins input and
- * output buffers, or code that must not allocate while work is recorded).
+ * allocate device memory: for example a plugin whose host application hands
+ * it only its input and output buffers and owns every allocation itself.
  * The pages have no counterpart of this call; it exists for such callers.
  *
  * Its scratch is one static device array of 32 MiB that every GPU loading
@@ -250,7 +253,9 @@ PA_API pa_status pa_attention(const pa_problem *p, const void *q, const void *k_
  * pa_workspace_size exceeds 32 MiB are rejected with PA_ERR_WORKSPACE.  It
  * allocates nothing and calls no allocating routine.  The first call on a
  * device looks up the array's device address (once per device, with that
- * device current): make that first call before any stream capture.  All
+ * device current) and keeps it for the life of the process: make that first
+ * call before any stream capture, and do not call this entry point again on
+ * a device after cudaDeviceReset (the kept address would be stale).  All
  * calls share the one array, which keeps the last call's contents, so calls
  * that may overlap on the GPU (other streams, other host threads) race with
  * each other: order them on one stream.  Device error bits land in the shared

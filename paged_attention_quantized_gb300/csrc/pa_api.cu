@@ -80,6 +80,7 @@ struct Derived {
 };
 
 pa_status derive_grouped(const pa_problem *p, Derived *d);
+int work_pages_per_seq(const pa_problem *p, const Derived &d);
 
 pa_status derive(const pa_problem *p, Derived *d) {
     if (p == nullptr || d == nullptr) return PA_ERR_INVALID_ARG;
@@ -145,6 +146,11 @@ pa_status derive(const pa_problem *p, Derived *d) {
         if (st != PA_OK) return st;
     }
 
+    // Every request has at most the table width of pages (longer ones are
+    // flagged, not planned), and the plan keeps page prefix sums in 32 bits:
+    // problems that could need more are refused here rather than flagged by
+    // the planner on the device.
+    if ((long long)p->batch * work_pages_per_seq(p, *d) > 0x7fffffffll) return PA_ERR_UNSUPPORTED;
     const long long X = (long long)p->num_kv_heads * d->row_blocks;
     d->slots_partial = ((long long)p->batch * (X / d->gs) + d->nwarps / d->gs) * d->gs;
     if (d->slots_partial > (1ll << 31)) return PA_ERR_UNSUPPORTED;

@@ -1,7 +1,7 @@
 // pa_attention_noalloc: the whole attention (plan, split-KV run, combine) for
-// callers that cannot allocate device memory -- for example a host that only
-// hands a plugin its input and output buffers and forbids cudaMalloc, or code
-// that must not create allocations while other work is being recorded.  The
+// callers that cannot allocate device memory -- for example a plugin whose
+// host application hands it only its input and output buffers and owns every
+// allocation itself.  The
 // scratch that pa_attention keeps in a caller-owned workspace (plan records,
 // split partials, the device error word) lives here instead in one static
 // device array, reserved on every GPU that loads this library until the
@@ -26,7 +26,8 @@ std::mutex g_lock;
 void *g_scratch[MAX_DEVICES] = {};
 
 // Device address of the scratch on the current device, looked up once per
-// device (with that device current).
+// device (with that device current) and kept for the life of the process; a
+// cudaDeviceReset makes the kept address stale (the header says so).
 pa_status scratch_address(void **ptr) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= MAX_DEVICES) return PA_ERR_CUDA;

@@ -94,7 +94,7 @@ def abs_values(w):
     return dataclasses.replace(w, v_pool=nv.contiguous(), v_scale=vs)
 
 
-def compare(w, out, lse, rows=None, host=None, report=None, tie_aware=None):
+def compare(w, out, lse, rows=None, host=None, report=None, ref=None):
     """Assert GPU rows match the oracle.  Returns (max_err, n_hull_rows).
 
     fp16 / bf16 / fp32 outputs use the absolute tolerances above.  Per-channel
@@ -106,13 +106,17 @@ def compare(w, out, lse, rows=None, host=None, report=None, tie_aware=None):
     the maximum (the near-tie rule of the onnxruntime PR #32520 page,
     Validation status: the argmax of a near one-hot softmax depends on fp16
     rounding).  `report` (a dict) receives the largest error and the number
-    of rows accepted through the hull."""
+    of rows accepted through the hull.  `ref` = (out, lse) of the oracle on
+    `rows`, when the caller has evaluated them already."""
     if rows is None:
         grid = np.stack(np.meshgrid(np.arange(w.B), np.arange(w.n), np.arange(w.Hq), indexing="ij"), -1)
         rows = grid.reshape(-1, 3)
     rows = np.asarray(rows, dtype=np.int64)
     host = host or oracle.HostArrays(w)
-    ref, rlse = oracle.attention(w, rows=rows, host=host)
+    if ref is None:
+        ref, rlse = oracle.attention(w, rows=rows, host=host)
+    else:
+        ref, rlse = ref  # the oracle's rows, already evaluated by the caller
     o = out.detach().float().cpu().numpy().astype(np.float64)
     l = lse.detach().float().cpu().numpy().astype(np.float64)
     g = o[rows[:, 0], rows[:, 1], rows[:, 2]]

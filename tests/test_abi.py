@@ -133,6 +133,23 @@ def test_unsupported_shapes(B, kw):
     assert st == B.PA_ERR_UNSUPPORTED
 
 
+def test_plan_overflow_refused_on_the_host(B):
+    # 33000 requests x 65536 table columns could name more than 2^31 - 1 pages:
+    # refused before anything is sized or launched; one column less fits
+    big = dict(batch=33000, num_q_heads=1, num_kv_heads=1, head_dim_k=64, head_dim_v=64, num_blocks=2,
+               max_context_len=1 << 20, max_blocks_per_seq=65536)
+    st = B.raw_status("pa_workspace_size", ctypes.byref(_prob(B, **big)), ctypes.byref(ctypes.c_size_t()))
+    assert st == B.PA_ERR_UNSUPPORTED
+    st = B.raw_status("pa_plan", ctypes.byref(_prob(B, **big)), None, None, None, 0, None)
+    assert st == B.PA_ERR_UNSUPPORTED
+    ok = dict(big, max_blocks_per_seq=65072)          # 33000 x 65072 = 2147376000 < 2^31
+    assert B.pa_workspace_size(_prob(B, **ok)) > 0
+    # latent problems count 64-token pages the same way
+    st = B.raw_status("pa_workspace_size", ctypes.byref(_latent(B, batch=1 << 20, max_blocks_per_seq=4096)),
+                      ctypes.byref(ctypes.c_size_t()))
+    assert st == B.PA_ERR_UNSUPPORTED
+
+
 def test_bad_workspace_rejected_before_any_launch(B):
     p = _prob(B)
     need = B.pa_workspace_size(p)

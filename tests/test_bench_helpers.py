@@ -30,3 +30,10 @@ def test_selected_counts_match_the_oracle_sets():
     L = w.context_lens.tolist()
     want = [OS.selected(sel[b, j].numpy(), L[b] - (w.n - 1 - j)).size for b in range(2) for j in range(7)]
     assert got == want and all(0 < c <= 50 for c in got)
+
+
+def test_default_run_covers_every_configuration_largest_last():
+    # one line per benchmark configuration; the last (the headline) is the
+    # largest in tokens and in work: the single-latent MQA batch
+    assert set(bench.ALL_CONFIGS) == set(W.CONFIG_NAMES)
+    assert bench.ALL_CONFIGS[-1] == "latent"

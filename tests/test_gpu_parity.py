@@ -464,33 +464,3 @@ def test_many_query_rows_per_kv_head(name, kw):
         out, lse, ws, _ = run_gpu(w, grid_ctas=split)
         assert error_bits(ws) == 0
         compare(w, out, lse)
-
-
-def test_plan_overflow_sets_error_and_runs_nothing():
-    """More than 2^31 pages in one plan (33000 requests of 2^20 tokens in
-    16-token blocks) cannot be positioned in 32 bits: the plan flags it and
-    records no pages, and the attention and the combine that follow do no
-    work and touch nothing."""
-    b = pa.binding()
-    B, L, bs = 33000, 1 << 20, 16
-    p = b.Problem(batch=B, next_n=1, num_q_heads=1, num_kv_heads=1, head_dim_k=64, head_dim_v=64, block_size=bs,
-                  num_blocks=2, max_blocks_per_seq=L // bs, max_context_len=L, q_dtype=b.PA_F16,
-                  kv_dtype=b.PA_F16, out_dtype=b.PA_F32, k_scale_mode=0, v_scale_mode=0, causal=0,
-                  v_is_k_prefix=0, num_sms=0, grid_ctas=0, softmax_scale=0.125)
-    lens = torch.full((B,), L, dtype=torch.int32, device="cuda")
-    n = b.pa_workspace_size(p)
-    ws = torch.zeros(n, dtype=torch.uint8, device="cuda")
-    q = torch.zeros((B, 1, 1, 64), dtype=torch.float16, device="cuda")
-    pool = torch.zeros((2, bs * 64 * 2), dtype=torch.uint8, device="cuda")
-    table = torch.ones((1, 1), dtype=torch.int32, device="cuda")  # never read: no pages are planned
-    out = torch.full((B, 1, 1, 64), 7.0, dtype=torch.float32, device="cuda")
-    s = pa.stream_handle()
-    b.pa_plan(p, lens.data_ptr(), None, ws.data_ptr(), n, s)
-    b.pa_run(p, q.data_ptr(), pool.data_ptr(), pool.data_ptr(), table.data_ptr(), lens.data_ptr(), None, None,
-             ws.data_ptr(), n, out.data_ptr(), None, s)
-    torch.cuda.synchronize()
-    assert error_bits(ws) & b.PA_DEV_ERR_PLAN_OVERFLOW
-    lo = b.pa_workspace_layout(p)
-    hdr = ws[lo.header_offset: lo.header_offset + 16].cpu().numpy().view(np.uint32)
-    assert hdr[1] == 0
-    assert torch.all(out == 7.0)

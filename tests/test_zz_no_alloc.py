@@ -1,11 +1,14 @@
 """pa_attention_noalloc: the whole attention for callers that cannot allocate
-device memory (no workspace argument; the library's static 32 MiB device
-scratch is used instead).  Checked against pa_attention on the same inputs,
-twice in a row, through the C ABI.  This file is collected last."""
+device memory, such as a plugin whose host application passes it only its
+input and output buffers (no workspace argument; the library's static 32 MiB
+device scratch is used instead).  Checked against pa_attention on the same
+inputs, twice in a row, through the C ABI: the two run the same plan rule,
+kernels and launch shape, so their results must be equal bit for bit.  This
+file is collected last (see conftest), after every other test of the session
+has run in the same process."""
 import ctypes
 import math
 
-import numpy as np
 import pytest
 import torch
 
@@ -14,8 +17,6 @@ from paged_attention_quantized_gb300 import build as pabuild
 from paged_attention_quantized_gb300 import workloads as W
 
 pytestmark = pytest.mark.gpu
-
-TOL = {"f32": 2e-3, "bf16": 1e-2, "f16": 1e-2}
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -26,6 +27,26 @@ def _lib():
 
 def _ptr(t):
     return None if t is None else t.data_ptr()
+
+
+def _noalloc(w, p, out, lse):
+    st = pa.binding().raw_status(
+        "pa_attention_noalloc", ctypes.byref(p), _ptr(w.q), _ptr(w.k_pool), _ptr(w.v_pool), _ptr(w.block_table),
+        _ptr(w.context_lens), _ptr(w.k_scale), _ptr(w.v_scale), _ptr(out), _ptr(lse), pa.stream_handle())
+    assert st == pa.binding().PA_OK
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _stale_scratch(_lib):
+    # a larger split problem first, so the shared scratch holds other plan
+    # records and partials when the cases below run
+    w = W.make("bf16", device="cuda", B=24, L_lo=500, L_hi=6000, Hq=32, Hkv=8, seed=99)
+    p = pa.problem(w)
+    out = torch.empty((w.B, w.n, w.Hq, w.Dv), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((w.B, w.n, w.Hq), dtype=torch.float32, device="cuda")
+    _noalloc(w, p, out, lse)
+    torch.cuda.synchronize()
+    assert torch.isfinite(out.float()).all()
 
 
 @pytest.mark.parametrize("name,kw", [
@@ -41,19 +62,13 @@ def test_noalloc_matches_workspace_path_twice(name, kw):
     pa.run(w, p, ref, ws, ref_lse)
     torch.cuda.synchronize()
     assert B.pa_get_error(ws.data_ptr(), pa.stream_handle()) == 0
-    tol = TOL[w.out_dtype]
     for _ in range(2):
         out = torch.full_like(ref, math.nan)
         lse = torch.full_like(ref_lse, math.nan)
-        B.pa_attention_noalloc(p, _ptr(w.q), _ptr(w.k_pool), _ptr(w.v_pool), _ptr(w.block_table),
-                               _ptr(w.context_lens), _ptr(w.k_scale), _ptr(w.v_scale), _ptr(out), _ptr(lse),
-                               pa.stream_handle())
+        _noalloc(w, p, out, lse)
         torch.cuda.synchronize()
-        o, r = out.double().cpu().numpy(), ref.double().cpu().numpy()
-        assert np.isfinite(o).all()
-        scale = np.maximum(1.0, np.abs(r)) if w.out_dtype == "f32" and name in ("int8", "int4") else 1.0
-        assert np.all(np.abs(o - r) <= tol * scale)
-        assert np.allclose(lse.cpu().numpy(), ref_lse.cpu().numpy(), rtol=1e-5, atol=1e-5)
+        assert torch.isfinite(out.float()).all()
+        assert torch.equal(out, ref) and torch.equal(lse, ref_lse)
 
 
 def test_noalloc_rejects_problems_beyond_its_scratch():
