@@ -515,3 +515,153 @@ def make_selection(w: Workload, k: int, seed: int = 0, shared: float = 0.9, devi
             row = torch.cat([keep, rest])
             out[b, j] = row[torch.randperm(k, generator=g)]
     return out.to(device)
+
+
+# ------------------------------------------------ FP4 paged MQA logits
+
+
+@dataclass
+class Fp4Logits:
+    """Inputs of FP4 (MXFP4) paged MQA logits (see make_fp4)."""
+    name: str
+    B: int
+    n: int
+    H: int
+    D: int
+    bs: int
+    sf_vec: int
+    num_blocks: int
+    max_blocks_per_seq: int
+    max_context_len: int
+    out_dtype: str
+    causal: bool
+    rectify: bool
+    sf_interleaved: bool
+    q: torch.Tensor            # [B, n, H, D/2] uint8, two E2M1 values per byte
+    sf_q: torch.Tensor         # [B, n, H] int32, D/sf_vec UE8M0 bytes
+    kv_fused: torch.Tensor     # [num_blocks, bs * (D/2 + D/sf_vec)] uint8
+    weights: torch.Tensor      # [B * n, H] float32
+    block_table: torch.Tensor  # [B, max_blocks_per_seq] int32
+    context_lens: torch.Tensor  # [B] int32
+    seed: int = 0
+
+    @property
+    def row_bytes(self) -> int:
+        return self.D // 2 + self.D // self.sf_vec
+
+    def kv_bytes(self) -> int:
+        """Algorithmic bytes read: every visible token's packed values and
+        scale bytes once (the tokens of the longest row of each request)."""
+        return int(self.context_lens.sum().item()) * self.row_bytes
+
+    def out_bytes(self) -> int:
+        es = {"f32": 4, "f16": 2, "bf16": 2}[self.out_dtype]
+        return self.B * self.n * self.max_context_len * es
+
+    def to(self, device) -> "Fp4Logits":
+        mv = lambda t: None if t is None else t.to(device)
+        return replace(self, q=mv(self.q), sf_q=mv(self.sf_q), kv_fused=mv(self.kv_fused),
+                       weights=mv(self.weights), block_table=mv(self.block_table),
+                       context_lens=mv(self.context_lens))
+
+
+def _sf_words(shape, gen, device, lo: int, hi: int) -> torch.Tensor:
+    """int32 words of four UE8M0 bytes, each uniform in [lo, hi]."""
+    b = torch.randint(lo, hi + 1, shape + (4,), generator=gen, device=device, dtype=torch.int64)
+    w = b[..., 0] | (b[..., 1] << 8) | (b[..., 2] << 16) | (b[..., 3] << 24)
+    return torch.where(w >= 2 ** 31, w - 2 ** 32, w).to(torch.int32)
+
+
+def make_fp4(device="cpu", seed: int = 1240, *, B: int = 128, n: int = 2, H: int = 64, D: int = 128,
+             bs: int = 64, L_lo: int = 4096, L_hi: int = 65536, context_lens=None, causal: bool = True,
+             rectify: bool = False, sf_interleaved: bool = False, out_dtype: str = "bf16",
+             scale_lo: int = 124, scale_hi: int = 130, slack_frac: float = 0.10) -> Fp4Logits:
+    """Seeded inputs for FP4 paged MQA logits.
+
+    Recipe (the indexer shape of the FlashInfer fp4_paged_mqa_logits page:
+    64 heads of dim 128, MXFP4 with 32-value UE8M0 groups, 64-token blocks):
+    B requests, L ~ U[L_lo, L_hi], next_n query rows (causal: row j sees
+    tokens up to L - n + j), every E2M1 code equally likely in q and K (all
+    16, including -0), scale bytes uniform in [scale_lo, scale_hi], weights
+    N(0, 1).  Physical ids a seeded permutation of 1..num_blocks-1; the table
+    is as wide as the page's precondition round_up(L, 128) / bs asks, extra
+    columns pointing at the null block or slack blocks; unreferenced blocks
+    and the unused slots of last blocks hold random bytes (scale byte 0xFF,
+    NaN, included)."""
+    device = torch.device(device)
+    gcpu = _gen("cpu", seed)
+    gdev = _gen(device, seed + 1)
+    if context_lens is not None:
+        L = torch.as_tensor(context_lens, dtype=torch.int32).cpu()
+        B = int(L.numel())
+    else:
+        L = torch.randint(L_lo, L_hi + 1, (B,), generator=gcpu, dtype=torch.int64).to(torch.int32)
+    sf_vec = 32
+    row = D // 2 + D // sf_vec
+    pages = [(int(l) + bs - 1) // bs for l in L.tolist()]
+    cols = [((int(l) + 127) // 128) * 128 // bs for l in L.tolist()]
+    Wp = sum(pages)
+    num_blocks = 1 + Wp + max(1, int(math.ceil(slack_frac * Wp)))
+    mbps = max(1, max(cols) if cols else 1)
+    max_ctx = max(1, int(L.max().item()) if B else 1)
+    perm = torch.randperm(num_blocks - 1, generator=gcpu).to(torch.int32) + 1
+    table = torch.zeros((max(B, 1), mbps), dtype=torch.int32)
+    slack = perm[Wp:].clone()
+    choices = torch.cat([torch.zeros(1, dtype=torch.int32), slack])
+    ofs = 0
+    for b in range(B):
+        table[b, : pages[b]] = perm[ofs: ofs + pages[b]]
+        ofs += pages[b]
+        k = mbps - pages[b]
+        if k > 0:
+            table[b, pages[b]:] = choices[torch.randint(0, choices.numel(), (k,), generator=gcpu)]
+    table = table[:B]
+
+    q = torch.randint(0, 256, (B, n, H, D // 2), generator=gdev, device=device, dtype=torch.int16).to(torch.uint8)
+    sf_q = _sf_words((B, n, H), gdev, device, scale_lo, scale_hi)
+    weights = torch.randn((B * n, H), generator=gdev, device=device, dtype=torch.float32)
+
+    # every block starts as junk (random bytes, scale bytes included); the
+    # referenced slots are then written with codes and in-range scales
+    kv = torch.randint(0, 256, (num_blocks, bs * row), generator=gdev, device=device,
+                       dtype=torch.int16).to(torch.uint8)
+    data = bs * (D // 2)
+    nsf = D // sf_vec
+    if sf_interleaved and bs % SF_WORD != 0:
+        raise ValueError("interleaved scales need a block size divisible by 4")
+    # word slot of each token inside the scale region
+    slot_of = list(range(bs))
+    if sf_interleaved:
+        for k in range(bs):
+            slot_of[(k % SF_WORD) * (bs // SF_WORD) + k // SF_WORD] = k
+    slot_idx = torch.tensor(slot_of, dtype=torch.int64, device=device)
+    ofs = 0
+    for b in range(B):
+        for p in range(pages[b]):
+            blk = int(perm[ofs + p])
+            ntok = min(bs, int(L[b]) - p * bs)
+            kv[blk, : ntok * (D // 2)] = torch.randint(0, 256, (ntok * (D // 2),), generator=gdev, device=device,
+                                                       dtype=torch.int16).to(torch.uint8)
+            sc = torch.randint(scale_lo, scale_hi + 1, (ntok, nsf), generator=gdev, device=device,
+                               dtype=torch.int16).to(torch.uint8)
+            pos = data + slot_idx[:ntok, None] * nsf + torch.arange(nsf, device=device)[None, :]
+            kv[blk].index_put_((pos.reshape(-1),), sc.reshape(-1))
+        ofs += pages[b]
+    return Fp4Logits(name="fp4", B=B, n=n, H=H, D=D, bs=bs, sf_vec=sf_vec, num_blocks=num_blocks,
+                     max_blocks_per_seq=mbps, max_context_len=max_ctx, out_dtype=out_dtype, causal=causal,
+                     rectify=rectify, sf_interleaved=sf_interleaved, q=q, sf_q=sf_q, kv_fused=kv,
+                     weights=weights, block_table=table.to(device), context_lens=L.to(device), seed=seed)
+
+
+SF_WORD = 4  # UE8M0 bytes in one scale word (one token's scales at D = 128)
+
+
+def relocate_fp4(w: Fp4Logits, seed: int) -> Fp4Logits:
+    """Move every non-null block of an Fp4Logits pool to a new physical id."""
+    g = _gen("cpu", seed)
+    pi = torch.cat([torch.zeros(1, dtype=torch.int64),
+                    torch.randperm(w.num_blocks - 1, generator=g).to(torch.int64) + 1]).to(w.kv_fused.device)
+    inv = torch.empty_like(pi)
+    inv[pi] = torch.arange(w.num_blocks, device=pi.device)
+    table = pi.index_select(0, w.block_table.reshape(-1).to(torch.int64)).to(torch.int32).reshape(w.block_table.shape)
+    return replace(w, kv_fused=w.kv_fused.index_select(0, inv).contiguous(), block_table=table)
