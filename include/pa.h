@@ -169,15 +169,15 @@ typedef struct pa_problem {
  * r = j * (Hq / Hkv) + (h mod (Hq / Hkv)).
  *
  * Two kernels: the grouped kernel (separate K and V planes, per-tensor or
- * per-channel scales) has S = 16 and one worker per warp; the single-latent
- * kernel (v_is_k_prefix: E4M3, PA_SCALE_TOKEN, Dk = 576, Dv = 512, bs = 64)
- * has S = 64 and one worker per CTA (one CTA per SM), and its workers come
- * in groups of G = row_blocks: positions then run over (request, kv head,
- * page), the W / G groups share them as above, and worker g*G + i takes row
- * block i of every page of group g's share (the G workers read the same
- * pages at about the same time, so all but the first read hit L2).  The
- * piece of segment (b, kv head u, row block i) in group g has slot
- * (b*Hkv + u + g)*G + i. */
+ * per-channel scales) has S = 16 and one worker per warp (or pair of warps);
+ * the single-latent kernel (v_is_k_prefix: E4M3, PA_SCALE_TOKEN, Dk = 576,
+ * Dv = 512, bs = 64) has S = 64 and one worker per CTA (one CTA per SM).  In
+ * both, workers come in groups of G = row_blocks: positions run over
+ * (request, kv head, page), the W / G groups share them as above, and worker
+ * g*G + i takes row block i of every page of group g's share (the G workers
+ * read the same pages at about the same time, so all but the first read hit
+ * L2).  The piece of segment (b, kv head u, row block i) in group g has slot
+ * (b*Hkv + u + g)*G + i; with one row block (G = 1) this is the rule above. */
 typedef struct pa_layout {
     size_t total_bytes;
     size_t header_offset;
@@ -190,10 +190,11 @@ typedef struct pa_layout {
     int32_t num_sms;             /* effective */
     int32_t grid_ctas;           /* effective persistent CTAs of pa_run */
     int32_t warps;               /* workers W: grid_ctas * 4 (grouped; * 2 with paired warps at D = 256
-                                    and more than 8 query rows per kv head) or grid_ctas (latent) */
+                                    and more than 8 query rows per kv head) or grid_ctas (latent); the
+                                    launch is sized so that W is a multiple of group_size */
     int32_t ring_pages_per_warp; /* pages each worker keeps in flight */
     int32_t rows_per_segment;    /* S: 16 (grouped) or 64 (latent) */
-    int32_t group_size;          /* G: workers sharing one run of pages (1, or row_blocks for latent) */
+    int32_t group_size;          /* G = row_blocks: workers sharing one run of pages */
     int32_t work_page_tokens;    /* tokens the attention handles as one page: block_size, or an equal
                                     part of a block (>= 16) when two whole blocks per worker do not fit */
 } pa_layout;

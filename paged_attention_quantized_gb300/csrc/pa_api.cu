@@ -193,7 +193,6 @@ pa_status derive_grouped(const pa_problem *p, Derived *d) {
 
     d->D = D;
     d->rows_seg = 16;
-    d->gs = 1;
     d->row_blocks = (d->R + 15) / 16;
     if (d->row_blocks > 65535) return PA_ERR_UNSUPPORTED;
     const int bs = p->block_size;
@@ -265,6 +264,15 @@ pa_status derive_grouped(const pa_problem *p, Derived *d) {
     d->warp_smem = wsm(d->slots, d->wp);
     d->smem = 1024 + (size_t)workers * d->warp_smem;
     d->ctas = p->grid_ctas > 0 ? p->grid_ctas : d->sms * d->minb;
+    // workers come in groups of row_blocks (one per block of 16 query rows of
+    // a kv head, walking the same pages): the launch holds whole groups
+    d->gs = d->row_blocks;
+    {
+        int g = d->gs, w = workers;
+        while (w != 0) { const int t = g % w; g = w; w = t; }  // gcd(gs, workers)
+        const int m = d->gs / g;                               // CTAs per whole number of groups
+        d->ctas = std::max(m, d->ctas / m * m);
+    }
     d->nwarps = (long long)d->ctas * workers;
     return PA_OK;
 }

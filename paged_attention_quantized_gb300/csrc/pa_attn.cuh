@@ -4,6 +4,9 @@
 // the MMA M axis, each pair of warps sharing one ring and splitting the
 // channel segments between them) is an independent worker that streams its
 // share of the logical page sequence for up to 16 query rows of a kv head.
+// With more than 16 query rows per kv head the workers come in groups, one
+// per block of 16 rows, that share one run of pages: each page of the
+// group's share is read from HBM once and from L2 by the other row blocks.
 //
 //  * the worker's lane 0 reads block ids 32 at a time, checks each against
 //    [1, num_blocks) and copies the K and V tiles of its next pages -- [bs][row
@@ -380,7 +383,12 @@ __global__ void __launch_bounds__(ATTN_THREADS, min_blocks(Geo<KVT, D>::BITS, D,
     const int bs = P.bs;
     const int tile_bytes = bs * G::RB;
     const int page_bytes = 2 * tile_bytes;  // K tile then V tile
-    const int X = P.Hkv * P.RBLK;           // segments per request
+    // Workers come in groups of RBLK, one per row block of a kv head: the
+    // cursors run over (request, kv head, page) and every worker of a group
+    // takes its own row block of every page of the group's share, so the
+    // group reads each page at about the same time (all but the first copy
+    // of a page hit L2) instead of every row block streaming the KV again.
+    const int GS = P.RBLK;
 
     // this worker's shared memory: ring of NS pages, q' fragments (each warp of
     // a pair its half), the pair's score exchange and slot flags, barriers
@@ -407,10 +415,14 @@ __global__ void __launch_bounds__(ATTN_THREADS, min_blocks(Geo<KVT, D>::BITS, D,
         if (threadIdx.x == 0) atomic_or_err(P.hdr, PA_DEV_ERR_STALE_PLAN);
         return;
     }
-    const long long Ntot = total * X;
+    const long long Ntot = total * P.Hkv;
     const long long NWt = (long long)gridDim.x * (NWK / WPW);
-    const long long kw = (long long)blockIdx.x * (NWK / WPW) + wk;
-    const long long x0 = kw * Ntot / NWt, x1 = (kw + 1) * Ntot / NWt;
+    const long long kw = (long long)blockIdx.x * (NWK / WPW) + wk;  // worker
+    const long long NG = NWt / GS;                                   // worker groups
+    const long long kg = kw / GS;                                    // this worker's group
+    const int gi = (int)(kw - kg * GS);                              // and its row block
+    if (kg >= NG) return;  // the host sizes the launch in whole groups
+    const long long x0 = kg * Ntot / NG, x1 = (kg + 1) * Ntot / NG;
     if (x0 >= x1) return;
     const int npg = (int)(x1 - x0);
 
@@ -424,7 +436,7 @@ __global__ void __launch_bounds__(ATTN_THREADS, min_blocks(Geo<KVT, D>::BITS, D,
     pair_sync();  // the barriers are initialised before the partner waits on them
 
     uint32_t err = 0;
-    Cursor cc = cursor_at(x0, P.req, P.B, X, P.mbps);  // compute cursor
+    Cursor cc = cursor_at(x0, P.req, P.B, P.Hkv, P.mbps);  // compute cursor (q = kv head)
     if (cc.b >= P.B) {
         if (lane == 0) atomic_or_err(P.hdr, PA_DEV_ERR_STALE_PLAN);
         return;
@@ -464,7 +476,7 @@ __global__ void __launch_bounds__(ATTN_THREADS, min_blocks(Geo<KVT, D>::BITS, D,
                 blk[i] = __shfl_sync(0xffffffffu, idc, bi0 - idc_w0 + i);
                 if (i < nbp) ok = ok && blk[i] >= 1 && blk[i] < P.num_blocks;
             }
-            const int kvh = (P.RBLK == 1) ? ci.q : ci.q / P.RBLK;
+            const int kvh = ci.q;
             if constexpr (PAIR) {
                 if (lane == 0) sflags[slot] = ok ? 0 : 1;
             }
@@ -486,7 +498,7 @@ __global__ void __launch_bounds__(ATTN_THREADS, min_blocks(Geo<KVT, D>::BITS, D,
                 }
             }
             slot_bad = ok ? (slot_bad & ~(1u << slot)) : (slot_bad | (1u << slot));
-            cursor_next<true>(ci, P.req, P.B, X, P.mbps);
+            cursor_next<true>(ci, P.req, P.B, P.Hkv, P.mbps);
             return;
         }
         // work page ci.p: rows [y0, y0 + bs) of block bi of the request
@@ -504,7 +516,7 @@ __global__ void __launch_bounds__(ATTN_THREADS, min_blocks(Geo<KVT, D>::BITS, D,
         }
         const int blk = __shfl_sync(0xffffffffu, idc, bi - idc_w0);
         const bool ok = blk >= 1 && blk < P.num_blocks;
-        const int kvh = (P.RBLK == 1) ? ci.q : ci.q / P.RBLK;
+        const int kvh = ci.q;
         if constexpr (PAIR) {
             if (lane == 0) sflags[slot] = ok ? 0 : 1;  // published with the barrier's phase
         }
@@ -520,7 +532,7 @@ __global__ void __launch_bounds__(ATTN_THREADS, min_blocks(Geo<KVT, D>::BITS, D,
             }
         }
         slot_bad = ok ? (slot_bad & ~(1u << slot)) : (slot_bad | (1u << slot));
-        cursor_next(ci, P.req, P.B, X, P.mbps);
+        cursor_next(ci, P.req, P.B, P.Hkv, P.mbps);
     };
 
     const int npre = min(NS, npg);
@@ -541,8 +553,8 @@ __global__ void __launch_bounds__(ATTN_THREADS, min_blocks(Geo<KVT, D>::BITS, D,
         piece_b = cc.b;
         piece_q = cc.q;
         piece_p0 = cc.p;
-        kvh = cc.q / P.RBLK;
-        rblk = cc.q % P.RBLK;
+        kvh = cc.q;
+        rblk = gi;
         const int4 Rq = P.req[cc.b];
         L = P.context_lens[cc.b];
         pbad = false;
@@ -642,7 +654,7 @@ __global__ void __launch_bounds__(ATTN_THREADS, min_blocks(Geo<KVT, D>::BITS, D,
         }
         const int Pb = planned_pages(P.req, piece_b, P.mbps);
         const bool complete = (piece_p0 == 0 && last_p == Pb - 1);
-        const long long slot_id = (long long)piece_b * X + piece_q + kw;  // partial slot of this piece
+        const long long slot_id = ((long long)piece_b * P.Hkv + piece_q + kg) * GS + gi;  // partial slot of this piece
         const int r0 = rblk * ROWS;
         const float NaN = __int_as_float(0x7fc00000);
         // store value `val` of (row index within the segment, channel d)
@@ -1035,7 +1047,7 @@ __global__ void __launch_bounds__(ATTN_THREADS, min_blocks(Geo<KVT, D>::BITS, D,
         pair_sync();
         fence_proxy_async_smem();
         if (j + NS < npg && hf == 0) issue();
-        cursor_next(cc, P.req, P.B, X, P.mbps);
+        cursor_next(cc, P.req, P.B, P.Hkv, P.mbps);
     }
     if (j < npg && hf == 0) {
         // a wait ran out: let every copy still in flight land before exiting

@@ -163,10 +163,16 @@ def test_plan_matches_oracle_plan(kw):
     assert np.array_equal(req[:, 3], pl["flags"])
 
 
-def test_partial_pieces_match_oracle_plan():
-    # with many warps every segment is cut into pieces: each piece's partial
-    # lse slot is written, the rest of the slots are not touched
-    w = make("bf16", B=3, L_lo=200, L_hi=900, Hq=8, Hkv=2)
+@pytest.mark.parametrize("name,kw", [
+    ("bf16", dict(Hq=8, Hkv=2)),                 # one row block
+    ("bf16", dict(Hq=32, Hkv=2, n=2)),           # 32 rows: groups of 2 workers
+    ("e4m3", dict(Hq=32, Hkv=8, n=16)),          # verify: groups of 4 paired workers
+])
+def test_partial_pieces_match_oracle_plan(name, kw):
+    # with many workers every segment is cut into pieces: each piece's partial
+    # lse slot is written, the rest of the slots are not touched; workers of a
+    # group (one per row block) share one run of pages
+    w = make(name, B=3, L_lo=200, L_hi=900, **kw)
     p = pa.problem(w, grid_ctas=40)
     out, lse, ws = pa.alloc(w, p)
     lo = pa.binding().pa_workspace_layout(p)
@@ -174,15 +180,19 @@ def test_partial_pieces_match_oracle_plan():
     ws_f[lo.partial_lse_offset // 4: lo.partial_lse_offset // 4 + lo.partial_slots * 16] = float("nan")
     pa.run(w, p, out, ws, lse, steps="plan+run")
     torch.cuda.synchronize()
+    assert lo.group_size == lo.row_blocks and lo.warps % lo.group_size == 0
     pl = oracle.plan(w.context_lens.cpu().numpy(), bs=w.bs, Hkv=w.Hkv, max_context_len=w.max_context_len,
-                     max_blocks_per_seq=w.max_blocks_per_seq, row_blocks=lo.row_blocks, warps=lo.warps)
+                     max_blocks_per_seq=w.max_blocks_per_seq, row_blocks=lo.row_blocks, warps=lo.warps,
+                     group_size=lo.group_size)
     lse_parts = ws_f[lo.partial_lse_offset // 4:][: lo.partial_slots * 16].view(-1, 16).cpu().numpy()
-    R = lo.rows_per_kv_head
+    R = min(lo.rows_per_kv_head, 16)
     written = set()
     for pc in pl["pieces"]:
         if not pc["complete"]:
             written.add(pc["slot"])
             assert np.isfinite(lse_parts[pc["slot"], :R]).all(), pc
+    out2, lse2, _, _ = run_gpu(w, grid_ctas=40)
+    compare(w, out2, lse2)
     untouched = [s for s in range(lo.partial_slots) if s not in written]
     assert np.isnan(lse_parts[untouched]).all()
 
