@@ -81,6 +81,9 @@ WORKLOAD_TEXT = {
            "per request, fp16 out",
 }
 SPARSE_TOP_K = 2048
+FP4_TEXT = ("FP4 (MXFP4) paged MQA logits: B=128, L~U[4096,65536], next_n=2 causal, 64 heads, D=128 E2M1 with a "
+            "UE8M0 scale per 32 values, bs=64 kv_fused blocks (68 B per token), per-head fp32 weights, bf16 logits "
+            "[256, max_context_len]")
 # the benchmark configurations in order; the last (largest in tokens and in
 # work) is the headline line
 ALL_CONFIGS = ("tiny", "bf16", "e4m3", "int8", "int4", "latent")
@@ -102,7 +105,8 @@ def _peaks(key: str = "hbm_gbs"):
 # sources that decide each workload's attention kernel (traffic counters are
 # only reported while these are unchanged)
 KERNEL_SOURCES = {
-    "latent": ("pa_latent.cu", "pa_attn.cuh", "pa_common.cuh"),
+    "latent": ("pa_latent.cu", "pa_attn.cuh", "pa_common.cuh", "pa_tc.cuh"),
+    "fp4": ("pa_fp4.cu", "pa_attn.cuh", "pa_common.cuh", "pa_tc.cuh"),
     "tiny": ("pa_attn.cuh", "pa_common.cuh", "pa_attn_launch.cuh", "pa_attn_f16_d64.cu"),
     "bf16": ("pa_attn.cuh", "pa_common.cuh", "pa_attn_launch.cuh", "pa_attn_bf16_d128.cu"),
     "e4m3": ("pa_attn.cuh", "pa_common.cuh", "pa_attn_launch.cuh", "pa_attn_e4m3_d256.cu"),
@@ -696,6 +700,176 @@ def sparse_arm(args, rank, world, local_rank):
     }, w, sel, nbytes
 
 
+def fp4_arm(args, rank, world, local_rank):
+    import torch
+    import paged_attention_quantized_gb300 as pa
+    from paged_attention_quantized_gb300 import build as pabuild
+    from paged_attention_quantized_gb300 import workloads as W
+
+    pabuild.build()
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    kw = {} if args.batch is None else {"B": args.batch}
+    w = W.make_fp4(device=dev, **kw)
+    p = pa.fp4_problem(w)
+    B = pa.binding()
+    ws = torch.zeros(max(256, B.pa_fp4_logits_workspace_size(p)), dtype=torch.uint8, device=dev)
+    out = torch.empty((w.B * w.n, w.max_context_len), dtype=torch.bfloat16, device=dev)
+    nbytes = w.kv_bytes() + w.out_bytes()
+    flush = torch.ones(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    flush_sink = torch.zeros((), dtype=torch.int64, device=dev)
+    s = torch.cuda.Stream(device=dev)
+
+    def flush_l2():
+        flush_sink.copy_(flush.view(torch.int64).sum())
+
+    with torch.cuda.stream(s):
+        pa.fp4_logits(w, p, out, ws, stream=s)
+    torch.cuda.synchronize()
+    bits = B.pa_get_error(ws.data_ptr(), int(s.cuda_stream))
+    if bits:
+        raise RuntimeError(f"device error bits {bits:#x}")
+    extra = {}
+    if rank == 0 and not args.no_cpu_baseline:
+        extra = fp4_parity_and_baseline(w, out, args.cpu_baseline_s)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        pa.fp4_logits(w, p, out, ws, stream=s)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(s):
+        for _ in range(args.warmup):
+            flush_l2()
+            g.replay()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    time.sleep(0.3)
+    ev0 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ev1 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(s):
+        for k in range(args.steps):
+            flush_l2()
+            ev0[k].record(s)
+            g.replay()
+            ev1[k].record(s)
+    torch.cuda.synchronize()
+    step_ms = [a.elapsed_time(b) for a, b in zip(ev0, ev1)]
+    time.sleep(0.2)
+    clk = clocks.stop()
+    # end to end: q, scales, weights, table and lengths in from pinned memory, logits back
+    hq, hs, hw = w.q.cpu().pin_memory(), w.sf_q.cpu().pin_memory(), w.weights.cpu().pin_memory()
+    ht, hl = w.block_table.cpu().pin_memory(), w.context_lens.cpu().pin_memory()
+    ho = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e2e_ms = []
+    with torch.cuda.stream(s):
+        for k in range(args.steps):
+            flush_l2()
+            e0.record(s)
+            w.q.copy_(hq, non_blocking=True)
+            w.sf_q.copy_(hs, non_blocking=True)
+            w.weights.copy_(hw, non_blocking=True)
+            w.block_table.copy_(ht, non_blocking=True)
+            w.context_lens.copy_(hl, non_blocking=True)
+            pa.fp4_logits(w, p, out, ws, stream=s)
+            ho.copy_(out, non_blocking=True)
+            e1.record(s)
+            e1.synchronize()
+            e2e_ms.append(e0.elapsed_time(e1))
+    h2d = sum(t.numel() * t.element_size() for t in (hq, hs, hw, ht, hl))
+    d2h = ho.numel() * ho.element_size()
+    total_ms, e2e_avg = max_over_ranks([sum(step_ms), sum(e2e_ms) / len(e2e_ms)], world, dev)
+    ms_per_step = total_ms / args.steps
+    peak, peak_kind = _peaks()
+    achieved = nbytes / (ms_per_step * 1e-3) / 1e9
+    flops = 2.0 * 128 * w.H * sum(max(0, int(L) - (w.n - 1 - j)) for L in w.context_lens.tolist() for j in range(w.n))
+    tpeak, tkind = _peaks("bf16_tflops")
+    return {
+        "metric": METRIC,
+        "op": "fp4_logits",
+        "value": round(job_value(world, nbytes, ms_per_step), 2),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_per_step, 5),
+        "median_ms_per_step": round(statistics.median(step_ms), 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f16",
+        "data": "synthetic",
+        "config": {"workload": FP4_TEXT + ("" if args.batch is None else f" (batch {w.B})"), "name": "fp4",
+                   "batch": w.B, "next_n": w.n, "total_tokens": int(w.context_lens.sum().item()),
+                   "kv_bytes": w.kv_bytes(), "logit_bytes": w.out_bytes(),
+                   "l2": "inputs larger than L2; a 256 MiB buffer is read before every step",
+                   "parallelism": f"replicas x{world}"},
+        "query_rows_per_s": round(world * w.B * w.n / (ms_per_step * 1e-3), 1),
+        "pct_of_hbm_peak": round(100.0 * achieved / peak, 2),
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "traffic": _traffic("fp4"), "kernel": "pa_fp4_logits_kernel",
+                     "peak_source": f"{peak_kind} hbm_gbs",
+                     "note": "timed over the whole call (plan, -inf fill, logits kernel); bytes = kv_fused of every "
+                             "visible token once + the logits written",
+                     "tensor": {"achieved": round(flops / (ms_per_step * 1e-3) / 1e12, 2), "peak": tpeak,
+                                "unit": "TFLOP/s", "frac": round(flops / (ms_per_step * 1e-3) / 1e12 / tpeak, 4),
+                                "peak_source": f"{tkind} bf16_tflops (f16 MMA, same rate)"}},
+        "e2e": {"value": round(world * nbytes / (e2e_avg * 1e-3) / 1e9, 2), "unit": "GB/s",
+                "ms_per_step": round(e2e_avg, 5), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": 3 * args.steps,
+        "clocks": clk,
+        **extra,
+    }, w
+
+
+def fp4_oracle_sample(w, budget_s: float, seed: int = 0):
+    """The FP4 logits oracle on seeded query rows, about budget_s seconds."""
+    import numpy as np
+    from oracle import mqa_logits as OM
+    wc = w.to("cpu")
+    order = np.random.default_rng(seed).permutation(w.B * w.n)
+    rows, outs = [], []
+    t0 = time.perf_counter()
+    for r in order:
+        outs.append(OM.mqa_logits(wc, rows=[int(r)])[0])
+        rows.append(int(r))
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    return rows, np.stack(outs), time.perf_counter() - t0
+
+
+def fp4_parity_and_baseline(w, out, budget_s: float):
+    """Oracle rows of the batch about to be timed: compared with the GPU's
+    logits (same -inf / NaN pattern; |gpu - ref| <= 1e-2 * max(1, magnitude)
+    for bf16 logits, the magnitude from the oracle on the sign-cleared inputs)
+    before timing, and timed as the cpu_baseline."""
+    import numpy as np
+    from tests.test_fp4_gpu import magnitudes
+    rows, ref, dt = fp4_oracle_sample(w, budget_s)
+    mag = magnitudes(w, rows=rows)
+    g = out[rows].float().cpu().numpy().astype(np.float64)
+    if not (np.array_equal(np.isneginf(g), np.isneginf(ref)) and np.array_equal(np.isnan(g), np.isnan(ref))):
+        raise RuntimeError("fp4 logits: masked / NaN columns differ from the oracle")
+    fin = np.isfinite(ref)
+    ratio = np.abs(g[fin] - ref[fin]) / np.maximum(1.0, mag[fin])
+    if ratio.size and ratio.max() > 1e-2:
+        raise RuntimeError(f"fp4 logits: error {ratio.max():.3g} of the magnitude exceeds 1e-2")
+    L = w.context_lens.cpu().numpy()
+    share = sum(int(L[r // w.n]) for r in rows) / float(w.n * L.sum())
+    v = (w.kv_bytes() + w.out_bytes()) * share / dt / 1e9
+    return {"parity": {"rows": len(rows), "of_rows": w.B * w.n, "max_err_over_magnitude": float(ratio.max(initial=0.0)),
+                       "tol": 1e-2, "checked": "before timing, same batch"},
+            "cpu_baseline": {"value": round(v, 5), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                             "sample": f"{len(rows)} of {w.B * w.n} query rows, seeded, {dt:.1f} s, fp64 numpy; "
+                                       f"GB/s scaled by the sampled share of the tokens; {cpu_model()}",
+                             "query_rows_per_s": round(len(rows) / dt, 4)}}
+
+
 def oracle_sparse_rate(w, sel, nbytes: int, budget_s: float, seed: int = 0):
     """Time the sparse oracle on a bounded sample of query tokens (all heads).
     Returns (GB/s equivalent, query rows/s, rows timed, seconds)."""
@@ -903,6 +1077,46 @@ def reference_insert_arm(args):
     }
 
 
+def reference_fp4_arm(args):
+    from paged_attention_quantized_gb300 import workloads as W
+    kw = {} if args.batch is None else {"B": args.batch}
+    w = W.make_fp4(device="cpu", **kw)
+    L = w.context_lens.numpy()
+    for _ in range(args.warmup):
+        fp4_oracle_sample(w, budget_s=0.2)
+    vals, secs, rs = [], [], []
+    nr = 1
+    for k in range(args.steps):
+        rows, _, dt = fp4_oracle_sample(w, budget_s=ref_step_budget(args), seed=k)
+        share = sum(int(L[r // w.n]) for r in rows) / float(w.n * L.sum())
+        vals.append((w.kv_bytes() + w.out_bytes()) * share / dt / 1e9)
+        secs.append(dt)
+        rs.append(len(rows) / dt)
+        nr = len(rows)
+    value = statistics.median(vals)
+    return {
+        "impl": "reference",
+        "op": "fp4_logits",
+        "metric": METRIC,
+        "value": round(value, 5),
+        "unit": "GB/s",
+        "n_gpus": args.gpus,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(1e3 * statistics.median(secs), 3),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": FP4_TEXT, "name": "fp4"},
+        "query_rows_per_s": round(statistics.median(rs), 4),
+        "cpu_baseline": {"value": round(value, 5), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                         "sample": f"{nr} of {w.B * w.n} query rows per step, seeded, fp64 numpy; {cpu_model()}"},
+        "e2e": {"value": round(value, 5), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
 def reference_sparse_arm(args):
     from paged_attention_quantized_gb300 import workloads as W
     w = W.make(args.workload, device="cpu", B=args.batch)
@@ -957,7 +1171,7 @@ def main():
     ap.add_argument("--cpu-baseline-s", type=float, default=8.0,
                     help="oracle seconds (per configuration) for the parity check and cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--op", default="attention", choices=["attention", "insert", "sparse"],
+    ap.add_argument("--op", default="attention", choices=["attention", "insert", "sparse", "fp4"],
                     help="the step timed: the attention (default), the quantized paged KV insert, or sparse "
                          "selected-token attention (qsa workload)")
     ap.add_argument("--batch", type=int, default=None,
@@ -970,7 +1184,7 @@ def main():
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
 
     if args.op != "attention" and args.workload == "all":
-        args.workload = {"sparse": "qsa", "insert": "bf16"}[args.op]   # the step's own default workload
+        args.workload = {"sparse": "qsa", "insert": "bf16", "fp4": "bf16"}[args.op]   # the step's own workload
     names = ALL_CONFIGS if args.workload == "all" else (args.workload,)
     if args.impl == "reference":
         if rank != 0:
@@ -982,7 +1196,7 @@ def main():
                 print(json.dumps(reference_arm(args, name)), flush=True)
             args.ref_step_s = saved
             return
-        arm = {"insert": reference_insert_arm, "sparse": reference_sparse_arm}[args.op]
+        arm = {"insert": reference_insert_arm, "sparse": reference_sparse_arm, "fp4": reference_fp4_arm}[args.op]
         print(json.dumps(arm(args)), flush=True)
         return
 
@@ -991,6 +1205,15 @@ def main():
         import torch.distributed as dist
         torch.cuda.set_device(local_rank)
         dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    if args.op == "fp4":
+        line, w = fp4_arm(args, rank, world, local_rank)
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+            dist.destroy_process_group()
+        if rank == 0:
+            print(json.dumps(line), flush=True)
+        return
     if args.op == "sparse":
         line, w, sel, nbytes = sparse_arm(args, rank, world, local_rank)
         if rank == 0 and not args.no_cpu_baseline:

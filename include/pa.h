@@ -368,6 +368,79 @@ PA_API pa_status pa_sparse_attention(const pa_problem *p, int32_t top_k, const i
                                      void *workspace, size_t workspace_bytes, void *out, float *lse,
                                      pa_stream_t stream);
 
+/* FP4 (MXFP4) paged MQA logits: for every query row r = b * next_n + j and
+ * token t of request b, a weighted sum over heads of the FP4 dot products.
+ *
+ * Source (page title, section): FlashInfer docs,
+ * "flashinfer.fp4_paged_mqa_logits", Parameters -- q, sf_q, kv_fused, weights,
+ * context_lens, block_table, max_context_len, sf_vec_size,
+ * is_kv_sf_interleaved and a preallocated out of at least max_context_len
+ * columns.
+ *
+ *   q^[h, d]  = e2m1(q[b][j][h] value d) * 2^(byte d / 32 of sf_q[b][j][h] - 127)
+ *   k^[t, d]  = e2m1(value d of token t % bs in block block_table[b][t / bs])
+ *               * 2^(scale byte d / 32 of that token - 127)
+ *   logit[r][t] = sum_h weights[r][h] * f(q^[h, :] . k^[t, :])   for t < vis
+ *   logit[r][t] = -inf                                  for vis <= t < max_context_len
+ * with f the identity, or max(0, .) when rectify = 1 (the page does not print
+ * how the heads combine: a plain weighted sum is this library's reading, the
+ * rectified sum an option), and vis = L_b, or L_b - (next_n - 1 - j) when
+ * causal = 1.  E2M1 is the OCP MX 4-bit float (values 0, 0.5, 1, 1.5, 2, 3,
+ * 4, 6 and their negatives); UE8M0 is a power of two 2^(e - 127), 0xFF NaN.
+ *
+ * Layouts (device pointers):
+ *  q         [batch][next_n][num_heads][64] uint8: 128 E2M1 values, value 2i
+ *            in the low nibble of byte i; 16-byte aligned.
+ *  sf_q      [batch][next_n][num_heads] int32: byte i (little-endian) scales
+ *            values 32i .. 32i + 31.
+ *  kv_fused  [num_blocks][block_size * 68] uint8: a block is block_size rows
+ *            of 64 packed bytes (token order), then block_size 4-byte scale
+ *            words, in token order or, with sf_interleaved = 1, word slot k
+ *            holding token (k % 4) * (block_size / 4) + k / 4; 16-byte aligned.
+ *  weights   [batch * next_n][num_heads] float32.
+ *  context_lens [batch] int32 (<= max_context_len); block_table
+ *            [batch][max_blocks_per_seq] int32 ids in [1, num_blocks) for the
+ *            ceil(L_b / block_size) blocks each request uses (a narrower
+ *            requirement than the page's round_up(L_b, 128) / block_size;
+ *            columns past a request's blocks are never read).
+ *  out       [batch * next_n][out_stride] of out_dtype (f32 / f16 / bf16);
+ *            columns 0 .. max_context_len - 1 of every row are written.
+ *  workspace caller-owned, pa_fp4_logits_workspace_size() bytes, 256-byte
+ *            aligned: word 0 is the device error word (pa_get_error), then
+ *            the plan over 128-token tiles.
+ * Supported: head_dim 128, sf_vec_size 32, block_size 16 / 32 / 64 / 128,
+ * num_heads a multiple of 16, next_n * num_heads <= 192; other problems
+ * return PA_ERR_UNSUPPORTED.  A request whose length breaks the contract
+ * (PA_DEV_ERR_CONTEXT_LEN) or a block id outside [1, num_blocks)
+ * (PA_DEV_ERR_BLOCK_ID) gets NaN logits; nothing outside the buffers is read
+ * or written.  Three kernel launches on `stream`; no allocation, no
+ * synchronisation. */
+typedef struct pa_fp4_problem {
+    int32_t batch;              /* B >= 0 requests */
+    int32_t next_n;             /* query rows per request, >= 1 */
+    int32_t num_heads;          /* H */
+    int32_t head_dim;           /* 128 */
+    int32_t sf_vec_size;        /* values per UE8M0 scale: 32 */
+    int32_t block_size;         /* tokens per kv_fused block */
+    int32_t num_blocks;         /* blocks in the pool (block 0 = null block) */
+    int32_t max_blocks_per_seq; /* block_table columns */
+    int32_t max_context_len;    /* columns of each output row written; bound on context_lens */
+    int32_t out_dtype;          /* PA_F32, PA_F16, PA_BF16 */
+    int32_t out_stride;         /* elements between output rows (>= max_context_len; 0 = max_context_len) */
+    int32_t causal;             /* 1: row j sees tokens [0, L_b - next_n + j] */
+    int32_t rectify;            /* 1: each head's dot product is clamped at 0 before weighting */
+    int32_t sf_interleaved;     /* 1: interleaved scale words (see above) */
+    int32_t num_sms;            /* SMs to size the launch for; 0 = current device's */
+    int32_t grid_ctas;          /* persistent CTAs; 0 = one per SM */
+} pa_fp4_problem;
+
+PA_API pa_status pa_fp4_logits_workspace_size(const pa_fp4_problem *p, size_t *bytes);
+
+PA_API pa_status pa_fp4_logits(const pa_fp4_problem *p, const uint8_t *q, const int32_t *sf_q,
+                               const uint8_t *kv_fused, const float *weights, const int32_t *context_lens,
+                               const int32_t *block_table, void *workspace, size_t workspace_bytes,
+                               void *out, pa_stream_t stream);
+
 /* Copy the device error word to *bits.  Synchronises `stream`. */
 PA_API pa_status pa_get_error(const void *workspace, uint32_t *bits, pa_stream_t stream);
 

@@ -5,7 +5,7 @@ include/pa.h; this package is its thin Python face:
 
   * `_binding`  -- ctypes declarations of pa_workspace_size / pa_plan / pa_run /
                    pa_combine / pa_attention / pa_insert / pa_sparse_attention /
-                   pa_get_error (same names);
+                   pa_fp4_logits / pa_get_error (same names);
   * `problem()` / `run()` -- marshal a batch held in torch CUDA tensors into
                    those calls (pointers, sizes, the current stream);
   * `workloads` -- seeded synthetic inputs (no attention arithmetic).
@@ -17,7 +17,8 @@ from __future__ import annotations
 import math
 from typing import Optional
 
-__all__ = ["problem", "workspace_bytes", "run", "insert", "sparse_run", "stream_handle", "binding"]
+__all__ = ["problem", "workspace_bytes", "run", "insert", "sparse_run", "fp4_problem", "fp4_logits",
+           "stream_handle", "binding"]
 
 
 def binding():
@@ -112,3 +113,23 @@ def alloc(w, p, device="cuda"):
     nbytes = workspace_bytes(p)
     ws = torch.zeros(max(256, nbytes), dtype=torch.uint8, device=device)
     return out, lse, ws
+
+
+def fp4_problem(w, *, num_sms: int = 0, grid_ctas: int = 0, out_stride: int = 0):
+    """pa_fp4_problem for an FP4 MQA-logits batch (see workloads.Fp4Logits)."""
+    b = binding()
+    return b.Fp4Problem(batch=w.B, next_n=w.n, num_heads=w.H, head_dim=w.D, sf_vec_size=w.sf_vec, block_size=w.bs,
+                        num_blocks=w.num_blocks, max_blocks_per_seq=w.max_blocks_per_seq,
+                        max_context_len=w.max_context_len, out_dtype=b.DTYPE[w.out_dtype], out_stride=out_stride,
+                        causal=int(bool(w.causal)), rectify=int(bool(w.rectify)),
+                        sf_interleaved=int(bool(w.sf_interleaved)), num_sms=num_sms, grid_ctas=grid_ctas)
+
+
+def fp4_logits(w, p, out, workspace, stream=None) -> None:
+    """Enqueue pa_fp4_logits for an Fp4Logits batch on the device; out is a
+    [B * next_n, >= max_context_len] tensor of the problem's output dtype
+    (its row stride is taken from p.out_stride, 0 = max_context_len) and
+    workspace a uint8 tensor of pa_fp4_logits_workspace_size bytes."""
+    b = binding()
+    b.pa_fp4_logits(p, _ptr(w.q), _ptr(w.sf_q), _ptr(w.kv_fused), _ptr(w.weights), _ptr(w.context_lens),
+                    _ptr(w.block_table), _ptr(workspace), workspace.numel(), _ptr(out), stream_handle(stream))

@@ -49,6 +49,13 @@ class Layout(ctypes.Structure):
             "rows_per_segment", "group_size", "work_page_tokens")]
 
 
+class Fp4Problem(ctypes.Structure):
+    _fields_ = [(k, ctypes.c_int32) for k in (
+        "batch", "next_n", "num_heads", "head_dim", "sf_vec_size", "block_size", "num_blocks",
+        "max_blocks_per_seq", "max_context_len", "out_dtype", "out_stride", "causal", "rectify",
+        "sf_interleaved", "num_sms", "grid_ctas")]
+
+
 if not os.path.exists(LIB_PATH):
     raise ImportError(f"libpa.so is not built ({LIB_PATH}); run "
                       "`python -m paged_attention_quantized_gb300.build` (nvcc, sm_103a)")
@@ -81,6 +88,10 @@ _lib.pa_sparse_workspace_size.restype = ctypes.c_int
 _lib.pa_sparse_workspace_size.argtypes = [_P(Problem), ctypes.c_int32, _P(ctypes.c_size_t)]
 _lib.pa_sparse_attention.restype = ctypes.c_int
 _lib.pa_sparse_attention.argtypes = [_P(Problem), ctypes.c_int32] + [_vp] * 9 + [ctypes.c_size_t, _vp, _vp, _vp]
+_lib.pa_fp4_logits_workspace_size.restype = ctypes.c_int
+_lib.pa_fp4_logits_workspace_size.argtypes = [_P(Fp4Problem), _P(ctypes.c_size_t)]
+_lib.pa_fp4_logits.restype = ctypes.c_int
+_lib.pa_fp4_logits.argtypes = [_P(Fp4Problem)] + [_vp] * 7 + [ctypes.c_size_t, _vp, _vp]
 _lib.pa_get_error.restype = ctypes.c_int
 _lib.pa_get_error.argtypes = [_vp, _P(ctypes.c_uint32), _vp]
 
@@ -155,6 +166,18 @@ def pa_sparse_attention(p: Problem, top_k: int, sel, q, k_pool, v_pool, block_ta
     _check(_lib.pa_sparse_attention(ctypes.byref(p), int(top_k), sel, q, k_pool, v_pool, block_table,
                                     context_lens, k_scale, v_scale, workspace, workspace_bytes, out, lse, stream),
            "pa_sparse_attention")
+
+
+def pa_fp4_logits_workspace_size(p: Fp4Problem) -> int:
+    n = ctypes.c_size_t()
+    _check(_lib.pa_fp4_logits_workspace_size(ctypes.byref(p), ctypes.byref(n)), "pa_fp4_logits_workspace_size")
+    return n.value
+
+
+def pa_fp4_logits(p: Fp4Problem, q, sf_q, kv_fused, weights, context_lens, block_table, workspace,
+                  workspace_bytes, out, stream) -> None:
+    _check(_lib.pa_fp4_logits(ctypes.byref(p), q, sf_q, kv_fused, weights, context_lens, block_table, workspace,
+                              workspace_bytes, out, stream), "pa_fp4_logits")
 
 
 def pa_get_error(workspace: int, stream) -> int:

@@ -21,6 +21,12 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 OUT_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(OUT_DIR, "libpa.so")
+# A test build of the same sources: every bounded wait gives up after 2 ms
+# instead of 2 s, and a workspace header word can make the copy of one page
+# go missing (PA_FAULT_INJECT), so the timeout path can be exercised on a GPU
+# without any fault.  It is never loaded by the package.
+VARIANTS = {"": ("_build", "libpa.so", []),
+            "fi": ("_build_fi", "libpa_fi.so", ["-DPA_FAULT_INJECT", "-DPA_WAIT_LIMIT_NS=2000000ull"])}
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-fvisibility=hidden",
                      "-I", INCLUDE, "-I", CSRC]
@@ -41,22 +47,30 @@ def _deps():
     return sources() + glob.glob(os.path.join(CSRC, "*.cuh")) + [os.path.join(INCLUDE, "pa.h"), __file__]
 
 
-def up_to_date() -> bool:
-    if not os.path.exists(LIB):
+def lib_path(variant: str = "") -> str:
+    d, name, _ = VARIANTS[variant]
+    return os.path.join(HERE, d, name)
+
+
+def up_to_date(variant: str = "") -> bool:
+    lib = lib_path(variant)
+    if not os.path.exists(lib):
         return False
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     return all(os.path.getmtime(p) <= t for p in _deps())
 
 
-def build(force: bool = False, verbose: bool = False, jobs: int | None = None) -> str:
-    if not force and up_to_date():
-        return LIB
-    os.makedirs(os.path.join(OUT_DIR, "obj"), exist_ok=True)
+def build(force: bool = False, verbose: bool = False, jobs: int | None = None, variant: str = "") -> str:
+    lib = lib_path(variant)
+    if not force and up_to_date(variant):
+        return lib
+    out_dir = os.path.dirname(lib)
+    os.makedirs(os.path.join(out_dir, "obj"), exist_ok=True)
     nvcc = _nvcc()
-    extra = ["-Xptxas", "-v"] if verbose else []
+    extra = (["-Xptxas", "-v"] if verbose else []) + VARIANTS[variant][2]
 
     def compile_one(src):
-        obj = os.path.join(OUT_DIR, "obj", os.path.basename(src) + ".o")
+        obj = os.path.join(out_dir, "obj", os.path.basename(src) + ".o")
         cmd = [nvcc] + NVCC_FLAGS + extra + ["-c", src, "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
@@ -71,13 +85,13 @@ def build(force: bool = False, verbose: bool = False, jobs: int | None = None) -
         for _, log in results:
             if log.strip():
                 sys.stdout.write(log)
-    tmp = LIB + f".{os.getpid()}.tmp"
+    tmp = lib + f".{os.getpid()}.tmp"
     cmd = [nvcc] + ARCH + ["-shared", "-o", tmp] + [o for o, _ in results]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":

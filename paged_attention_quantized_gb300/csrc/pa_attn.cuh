@@ -447,9 +447,20 @@ __global__ void __launch_bounds__(ATTN_THREADS, min_blocks(Geo<KVT, D>::BITS, D,
     unsigned slot_bad = 0;                      // slots whose page had an invalid id
 
     int islot = 0;  // ring slot of the next copy
+#ifdef PA_FAULT_INJECT
+    const unsigned fi_withhold = P.hdr[HDR_WITHHOLD];
+    long long fi_pos = x0;  // position of the next page issued
+#endif
     auto issue = [&]() {
         const int slot = islot;
         islot = (islot + 1 == NS) ? 0 : islot + 1;
+#ifdef PA_FAULT_INJECT
+        if (fi_withhold != 0 && fi_pos++ + 1 == (long long)fi_withhold && ci.b < P.B) {
+            if constexpr (WM == WP_MERGED) cursor_next<true>(ci, P.req, P.B, P.Hkv, P.mbps);
+            else cursor_next(ci, P.req, P.B, P.Hkv, P.mbps);
+            return;  // no copy and no arrive: the waits on this slot run out
+        }
+#endif
         if (ci.b >= P.B) {  // inconsistent records: no copy, the slot still completes
             if constexpr (PAIR) {
                 if (lane == 0) sflags[slot] = 1;
@@ -1052,6 +1063,24 @@ __global__ void __launch_bounds__(ATTN_THREADS, min_blocks(Geo<KVT, D>::BITS, D,
     if (j < npg && hf == 0) {
         // a wait ran out: let every copy still in flight land before exiting
         for (int i = j; i < min(npg, j + NS); ++i) mbar_wait_bounded(&full[i % NS], (i / NS) & 1, nullptr);
+    }
+    if (j < npg) {
+        // every piece this worker still owned -- the one in progress and any
+        // later one of its share -- is written as NaN (outputs, or partials the
+        // combine turns into NaN rows), so no row keeps stale values
+        pbad = true;
+        for (; j < npg && cc.b < P.B; ++j) {
+            if (cc.b != piece_b || cc.q != piece_q) {
+                if (piece_b >= 0) finish_piece();
+                piece_b = cc.b;
+                piece_q = cc.q;
+                piece_p0 = cc.p;
+                kvh = cc.q;
+                rblk = gi;
+            }
+            last_p = cc.p;
+            cursor_next(cc, P.req, P.B, P.Hkv, P.mbps);
+        }
     }
     // the combine may start launching while the last pieces are written
     grid_dependents_launch();

@@ -86,8 +86,17 @@ constexpr int HDR_ERR = 0;
 constexpr int HDR_TOTAL_PAGES = 1;  // sum over requests of their pages
 constexpr int HDR_KMAX = 3;
 
-// bounded waits: give up after this many nanoseconds of %globaltimer
-constexpr unsigned long long WAIT_LIMIT_NS = 2000000000ull;
+// bounded waits: give up after this many nanoseconds of %globaltimer (2 s;
+// a test build sets a shorter limit with -DPA_WAIT_LIMIT_NS=...)
+#ifndef PA_WAIT_LIMIT_NS
+#define PA_WAIT_LIMIT_NS 2000000000ull
+#endif
+constexpr unsigned long long WAIT_LIMIT_NS = PA_WAIT_LIMIT_NS;
+// Test builds only (-DPA_FAULT_INJECT): header word 4 of the workspace names a
+// page (its global position + 1, 0 = none) whose copy every producer that
+// owns it withholds -- neither a copy nor an arrive -- so the waits on that
+// ring slot run out, the way a copy lost on the device would look.
+constexpr int HDR_WITHHOLD = 4;
 
 // ------------------------------------------------------------------ basics
 

@@ -46,9 +46,12 @@
 //    reach P.V (1Cat-vLLM PR #647, "Stop grouped-page4 null-block padding
 //    from leaking E4M3 NaN", Fix).
 #include "pa_attn.cuh"
+#include "pa_tc.cuh"
 
 namespace pa {
 namespace lat {
+
+using namespace tc;
 
 constexpr int DK = 576, DV = 512, BS = 64, LROWS = 64, NSLOT = 2;
 constexpr int NWARPS = 10, THREADS = NWARPS * 32;
@@ -88,69 +91,6 @@ constexpr float ROW_SLACK = 6.0f;                      // lazy maximum: rescale 
 static_assert(SMEM_BYTES <= 227 * 1024, "latent kernel exceeds the shared memory of one CTA");
 static_assert(NSLOT == 2, "barrier counts below assume two ring slots");
 
-// ---------------------------------------------------------- tcgen05 helpers
-
-// shared-memory matrix descriptor: start, leading / stride byte offsets,
-// descriptor version 1, swizzle (2 = 128 B, 4 = 64 B)
-__device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t sbo, uint32_t swz) {
-    return (uint64_t)((saddr >> 4) & 0x3FFF) | ((uint64_t)((lbo >> 4) & 0x3FFF) << 16) |
-           ((uint64_t)((sbo >> 4) & 0x3FFF) << 32) | ((uint64_t)1 << 46) | ((uint64_t)swz << 61);
-}
-
-// instruction descriptor: fp32 accumulator, A/B formats 0 (f16 for kind::f16,
-// E4M3 for kind::f8f6f4), A MN-major flag, N >> 3, M >> 4
-__host__ __device__ constexpr uint32_t idesc(int M, int N, int a_mn) {
-    return (1u << 4) | ((uint32_t)a_mn << 15) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
-}
-
-__device__ __forceinline__ void mma_f8(uint32_t d, uint64_t a, uint64_t b, uint32_t id, uint32_t acc) {
-    asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-                 "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
-                 "l"(a), "l"(b), "r"(id), "r"(acc));
-}
-
-__device__ __forceinline__ void mma_f16(uint32_t d, uint64_t a, uint64_t b, uint32_t id, uint32_t acc) {
-    asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-                 "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
-                 "l"(a), "l"(b), "r"(id), "r"(acc));
-}
-
-__device__ __forceinline__ void mma_commit(uint64_t *bar) {
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
-                 : "memory");
-}
-
-__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
-
-// 32 lanes x 32 columns of 32 bits: lane i of the warp's quarter -> thread i
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float *v) {
-    uint32_t r[32];
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
-          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
-          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-        : "r"(taddr));
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
-}
-
-__device__ __forceinline__ void tmem_st32(uint32_t taddr, const float *v) {
-    asm volatile(
-        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
-        "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
-        "f"(v[0]), "f"(v[1]), "f"(v[2]), "f"(v[3]), "f"(v[4]), "f"(v[5]), "f"(v[6]), "f"(v[7]), "f"(v[8]),
-        "f"(v[9]), "f"(v[10]), "f"(v[11]), "f"(v[12]), "f"(v[13]), "f"(v[14]), "f"(v[15]), "f"(v[16]),
-        "f"(v[17]), "f"(v[18]), "f"(v[19]), "f"(v[20]), "f"(v[21]), "f"(v[22]), "f"(v[23]), "f"(v[24]),
-        "f"(v[25]), "f"(v[26]), "f"(v[27]), "f"(v[28]), "f"(v[29]), "f"(v[30]), "f"(v[31])
-        : "memory");
-    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-}
-
 // two fp32 -> two E4M3 codes (RNE, saturating), lo in the low byte
 __device__ __forceinline__ uint32_t f32x2_e4m3x2(float lo, float hi) {
     uint16_t r;
@@ -165,8 +105,6 @@ __device__ __forceinline__ float2 e4m3x2_f32x2(uint32_t two_codes) {
     return __half22float2(hh);
 }
 
-__device__ __forceinline__ float pow2f(int e) { return __int_as_float((min(max(e, -126), 127) + 127) << 23); }
-
 // byte offset of the 16-byte chunk c (0..35, 16 E4M3 channels each) of row r
 // in a [4 x SW128 [64][128 B] | SW64 [64][64 B]] tile (the copied page layout)
 __device__ __forceinline__ uint32_t e4_off(int r, int c) {
@@ -180,27 +118,6 @@ __device__ __forceinline__ uint32_t v_off(int t, int c) {
     return (uint32_t)((c >> 3) * (64 * 128) + t * 128 + (((c & 7) ^ (t & 7)) << 4));
 }
 
-// Bounded wait by lane 0, outcome shared with the warp; on a timeout the
-// CTA's abort word is raised so every role leaves its loop.
-__device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, volatile int *abort, uint32_t &err) {
-    int ok = 1;
-    if ((threadIdx.x & 31) == 0) {
-        ok = mbar_wait_bounded(bar, parity, abort) ? 1 : 0;
-        if (!ok && *abort == 0) {
-            *abort = 1;
-            err |= PA_DEV_ERR_TIMEOUT;
-        }
-    }
-    ok = __shfl_sync(0xffffffffu, ok, 0);
-    if (ok) (void)mbar_try_wait(bar, parity);  // acquire in every lane
-    return ok != 0;
-}
-
-__device__ __forceinline__ void warp_arrive(uint64_t *bar) {
-    __syncwarp();
-    if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
-}
-
 // two consecutive q values of a packed word (low half first)
 __device__ __forceinline__ float2 q_pair(uint32_t u, int q_dtype) {
     if (q_dtype == PA_BF16) return make_float2(__uint_as_float(u << 16), __uint_as_float(u & 0xFFFF0000u));
@@ -209,6 +126,52 @@ __device__ __forceinline__ float2 q_pair(uint32_t u, int q_dtype) {
 }
 
 }  // namespace lat
+
+// After a wait ran out (or the records ran short): every piece of this CTA's
+// share of positions [x0, x0 + npg) is written as NaN, finished or not, with
+// no access to tensor memory -- outputs, or partial log-sum-exps that the
+// combine turns into NaN rows -- so no row keeps stale values.  Run by the
+// 128 threads of the softmax warps (ti = 0..127); kept out of line so that
+// the main loop's registers are not shaped by it.
+__device__ __noinline__ void latent_nan_share(const LatentParams &P, long long x0, int npg, int U, int GS, long long kg,
+                                              int rb, int ti) {
+    using namespace lat;
+    const float NaN = __int_as_float(0x7fc00000);
+    auto nan_piece = [&](int b_, int q_, int p0_, int pl_) {
+        const int Pb = planned_pages(P.req, b_, P.mbps);
+        const bool complete = (p0_ == 0 && pl_ == Pb - 1);
+        const long long slot_id = ((long long)b_ * U + q_ + kg) * GS + rb;
+        for (int rr = 0; rr < LROWS; ++rr) {
+            const int r = rb * LROWS + rr;
+            if (r >= P.R) break;
+            const int jq = r / P.G, h = q_ * P.G + r % P.G;
+            if (complete) {
+                const size_t row = (((size_t)b_ * P.n + jq) * P.Hq + h) * DV;
+                for (int d = ti; d < DV; d += 128) {
+                    if (P.out_dtype == PA_F32) reinterpret_cast<float *>(P.out)[row + d] = NaN;
+                    else if (P.out_dtype == PA_F16) reinterpret_cast<__half *>(P.out)[row + d] = __float2half_rn(NaN);
+                    else reinterpret_cast<__nv_bfloat16 *>(P.out)[row + d] = __float2bfloat16_rn(NaN);
+                }
+                if (ti == 0 && P.lse != nullptr) P.lse[((size_t)b_ * P.n + jq) * P.Hq + h] = NaN;
+            } else if (ti == 0) {
+                P.part_lse[(size_t)slot_id * LROWS + rr] = NaN;
+            }
+        }
+    };
+    Cursor cw = cursor_at(x0, P.req, P.B, U, P.mbps);
+    int wb = -1, wq = -1, wp0 = 0, wl = 0;
+    for (int j = 0; j < npg && cw.b < P.B; ++j) {
+        if (cw.b != wb || cw.q != wq) {
+            if (wb >= 0) nan_piece(wb, wq, wp0, wl);
+            wb = cw.b;
+            wq = cw.q;
+            wp0 = cw.p;
+        }
+        wl = cw.p;
+        cursor_next(cw, P.req, P.B, U, P.mbps);
+    }
+    if (wb >= 0) nan_piece(wb, wq, wp0, wl);
+}
 
 __global__ void __launch_bounds__(lat::THREADS, 1)
     pa_latent_kernel(const __grid_constant__ CUtensorMap tma, const __grid_constant__ CUtensorMap tmb,
@@ -275,9 +238,19 @@ __global__ void __launch_bounds__(lat::THREADS, 1)
         // ================================================== producer
         Cursor ci = c0;
         int idc_b = -1, idc_w0 = 0, idc = 0, issued = 0;
+#ifdef PA_FAULT_INJECT
+        const unsigned fi_withhold = P.hdr[HDR_WITHHOLD];
+#endif
         for (int j = 0; j < npg; ++j) {
             const int slot = j % NSLOT;
             if (j >= NSLOT && !warp_wait(&bars[B_SLOTFREE + slot], ((j / NSLOT) - 1) & 1, abort, err)) break;
+#ifdef PA_FAULT_INJECT
+            if (fi_withhold != 0 && x0 + j + 1 == (long long)fi_withhold && ci.b < P.B) {
+                ++issued;
+                cursor_next(ci, P.req, P.B, U, P.mbps);
+                continue;  // no copy and no arrive: the waits on this slot run out
+            }
+#endif
             bool ok = false;
             int blk = 0;
             if (ci.b < P.B) {
@@ -680,6 +653,7 @@ __global__ void __launch_bounds__(lat::THREADS, 1)
             cursor_next(cs, P.req, P.B, U, P.mbps);
         }
         if (alive && piece >= 0) (void)epilogue(npg - 1);
+        if (!alive) latent_nan_share(P, x0, npg, U, GS, kg, rb, tid - 32 * W_SM);
     } else {
         // ================================================== V dequant
         const int dt = tid - 32 * W_DQ;  // 0..127

@@ -364,3 +364,41 @@ def test_binding_declares_every_prototype_with_its_arity(B):
     for name, n in arity.items():
         f = getattr(B._lib, name)
         assert f.argtypes is not None and len(f.argtypes) == n, (name, n, f.argtypes)
+
+
+def _fp4(B, **kw):
+    base = dict(batch=4, next_n=2, num_heads=64, head_dim=128, sf_vec_size=32, block_size=64, num_blocks=100,
+                max_blocks_per_seq=16, max_context_len=1000, out_dtype=B.PA_BF16, out_stride=0, causal=1, rectify=0,
+                sf_interleaved=0, num_sms=152, grid_ctas=0)
+    base.update(kw)
+    return B.Fp4Problem(**base)
+
+
+def test_fp4_workspace_and_shapes(B):
+    assert B.pa_fp4_logits_workspace_size(_fp4(B)) == 256 + 256
+    for kw in (dict(head_dim=64), dict(sf_vec_size=16), dict(block_size=48), dict(num_heads=24),
+               dict(next_n=4), dict(batch=1 << 20, max_blocks_per_seq=1 << 14)):
+        st = B.raw_status("pa_fp4_logits_workspace_size", ctypes.byref(_fp4(B, **kw)), ctypes.byref(ctypes.c_size_t()))
+        assert st == B.PA_ERR_UNSUPPORTED, kw
+    for kw in (dict(batch=-1), dict(next_n=0), dict(out_dtype=B.PA_E4M3), dict(causal=2), dict(out_stride=999),
+               dict(max_context_len=-1)):
+        st = B.raw_status("pa_fp4_logits_workspace_size", ctypes.byref(_fp4(B, **kw)), ctypes.byref(ctypes.c_size_t()))
+        assert st == B.PA_ERR_INVALID_ARG, kw
+
+
+def test_fp4_rejects_bad_pointers_before_any_launch(B):
+    p = _fp4(B)
+    args = [0x10000, 0x20000, 0x30000, 0x40000, 0x50000, 0x60000]   # q, sf_q, kv, weights, lens, table
+    assert B.raw_status("pa_fp4_logits", ctypes.byref(p), *args, None, 512, 0x70000, None) == B.PA_ERR_WORKSPACE
+    assert B.raw_status("pa_fp4_logits", ctypes.byref(p), *args, 0x80010, 512, 0x70000, None) == B.PA_ERR_WORKSPACE
+    assert B.raw_status("pa_fp4_logits", ctypes.byref(p), *args, 0x80000, 100, 0x70000, None) == B.PA_ERR_WORKSPACE
+    bad_q = [0x10008] + args[1:]
+    assert B.raw_status("pa_fp4_logits", ctypes.byref(p), *bad_q, 0x80000, 512, 0x70000, None) == B.PA_ERR_INVALID_ARG
+    no_kv = args[:2] + [None] + args[3:]
+    assert B.raw_status("pa_fp4_logits", ctypes.byref(p), *no_kv, 0x80000, 512, 0x70000, None) == B.PA_ERR_INVALID_ARG
+
+
+def test_fp4_empty_batch_is_a_no_op(B):
+    p = _fp4(B, batch=0)
+    assert B.raw_status("pa_fp4_logits", ctypes.byref(p), None, None, None, None, None, None, 0x80000, 512,
+                        None, None) == B.PA_OK
