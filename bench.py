@@ -106,7 +106,8 @@ def _peaks(key: str = "hbm_gbs"):
 # only reported while these are unchanged)
 KERNEL_SOURCES = {
     "latent": ("pa_latent.cu", "pa_attn.cuh", "pa_common.cuh", "pa_tc.cuh"),
-    "fp4": ("pa_fp4.cu", "pa_attn.cuh", "pa_common.cuh", "pa_tc.cuh"),
+    "fp4": ("pa_fp4.cu", "pa_attn.cuh", "pa_common.cuh"),
+    "fp4_rectify": ("pa_fp4.cu", "pa_attn.cuh", "pa_common.cuh", "pa_tc.cuh"),
     "tiny": ("pa_attn.cuh", "pa_common.cuh", "pa_attn_launch.cuh", "pa_attn_f16_d64.cu"),
     "bf16": ("pa_attn.cuh", "pa_common.cuh", "pa_attn_launch.cuh", "pa_attn_bf16_d128.cu"),
     "e4m3": ("pa_attn.cuh", "pa_common.cuh", "pa_attn_launch.cuh", "pa_attn_e4m3_d256.cu"),
@@ -710,7 +711,7 @@ def fp4_arm(args, rank, world, local_rank):
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
     kw = {} if args.batch is None else {"B": args.batch}
-    w = W.make_fp4(device=dev, **kw)
+    w = W.make_fp4(device=dev, rectify=args.rectify, **kw)
     p = pa.fp4_problem(w)
     B = pa.binding()
     ws = torch.zeros(max(256, B.pa_fp4_logits_workspace_size(p)), dtype=torch.uint8, device=dev)
@@ -804,7 +805,10 @@ def fp4_arm(args, rank, world, local_rank):
         "vs_baseline": None,
         "dtype": "f16",
         "data": "synthetic",
-        "config": {"workload": FP4_TEXT + ("" if args.batch is None else f" (batch {w.B})"), "name": "fp4",
+        "config": {"workload": FP4_TEXT + ("" if args.batch is None else f" (batch {w.B})")
+                               + ("; each head's product clamped at 0 (per-head products on the tensor cores)"
+                                  if args.rectify else "; plain weighted sum (heads folded into the query)"),
+                   "name": "fp4" + ("_rectify" if args.rectify else ""), "rectify": bool(args.rectify),
                    "batch": w.B, "next_n": w.n, "total_tokens": int(w.context_lens.sum().item()),
                    "kv_bytes": w.kv_bytes(), "logit_bytes": w.out_bytes(),
                    "l2": "inputs larger than L2; a 256 MiB buffer is read before every step",
@@ -812,7 +816,8 @@ def fp4_arm(args, rank, world, local_rank):
         "query_rows_per_s": round(world * w.B * w.n / (ms_per_step * 1e-3), 1),
         "pct_of_hbm_peak": round(100.0 * achieved / peak, 2),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
-                     "frac": round(achieved / peak, 4), "traffic": _traffic("fp4"), "kernel": "pa_fp4_logits_kernel",
+                     "frac": round(achieved / peak, 4), "traffic": _traffic("fp4_rectify" if args.rectify else "fp4"),
+                     "kernel": "pa_fp4_logits_kernel" if args.rectify else "pa_fp4_logits_sum_kernel",
                      "peak_source": f"{peak_kind} hbm_gbs",
                      "note": "timed over the whole call (plan, -inf fill, logits kernel); bytes = kv_fused of every "
                              "visible token once + the logits written",
@@ -1080,7 +1085,7 @@ def reference_insert_arm(args):
 def reference_fp4_arm(args):
     from paged_attention_quantized_gb300 import workloads as W
     kw = {} if args.batch is None else {"B": args.batch}
-    w = W.make_fp4(device="cpu", **kw)
+    w = W.make_fp4(device="cpu", rectify=args.rectify, **kw)
     L = w.context_lens.numpy()
     for _ in range(args.warmup):
         fp4_oracle_sample(w, budget_s=0.2)
@@ -1174,6 +1179,8 @@ def main():
     ap.add_argument("--op", default="attention", choices=["attention", "insert", "sparse", "fp4"],
                     help="the step timed: the attention (default), the quantized paged KV insert, or sparse "
                          "selected-token attention (qsa workload)")
+    ap.add_argument("--rectify", action="store_true",
+                    help="--op fp4: clamp each head's product at 0 (per-head products, tensor cores)")
     ap.add_argument("--batch", type=int, default=None,
                     help="requests of the workload (default: its recipe); a smaller batch is for profiling only")
     args = ap.parse_args()

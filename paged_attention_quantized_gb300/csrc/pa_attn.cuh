@@ -51,7 +51,10 @@ namespace pa {
 
 constexpr int NWK = 4;                     // warps per CTA, each an independent stream
 enum : int { WP_WHOLE = 0, WP_PART = 1, WP_MERGED = 2 };  // what a work page is (see pa_attn_kernel)
-constexpr int MERGE_BLOCKS = 2;            // blocks per merged work page
+#ifndef PA_MERGE_BLOCKS
+#define PA_MERGE_BLOCKS 2
+#endif
+constexpr int MERGE_BLOCKS = PA_MERGE_BLOCKS;  // blocks per merged work page
 #ifndef PA_MIN_BLOCKS_SMALL_D
 #define PA_MIN_BLOCKS_SMALL_D 2
 #endif

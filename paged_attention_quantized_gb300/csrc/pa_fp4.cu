@@ -441,6 +441,140 @@ __global__ void __launch_bounds__(fp4::THREADS, 1) pa_fp4_logits_kernel(Fp4Param
     if (tid == 0) atomic_or_err(P.hdr, (uint32_t)misc[8]);
 }
 
+// Plain weighted sum (rectify = 0): the logit is linear in the heads, so it
+// equals k^[t] . qw with qw = sum_h w[r, h] * q^[h] -- one 128-wide vector per
+// query row, folded once per request in fp32.  Each token is then a dot
+// product of its 128 decoded values with the row vectors: HBM-bound work for
+// the CUDA cores (no dense contraction left for the tensor cores).  Tiles of
+// 128 tokens in logical order are shared evenly by persistent CTAs of 128
+// threads, one token per thread; a token's 64 packed bytes and its scale word
+// are loaded straight from the pool (the warp reads 2 KB of consecutive rows
+// of a block).  Scale groups are summed separately and scaled by
+// 2^(s - 127) exactly.
+namespace fp4 {
+constexpr int SUM_THREADS = 128;
+constexpr int SUM_MAX_N = 4;       // query rows per request this kernel folds (next_n; more use the MMA kernel)
+constexpr int SUM_CTAS_PER_SM = 8; // persistent CTAs per SM of the launch
+}  // namespace fp4
+
+template <int NQ>
+__global__ void __launch_bounds__(fp4::SUM_THREADS) pa_fp4_logits_sum_kernel(Fp4Params P) {
+    using namespace fp4;
+    __shared__ __align__(16) float qw[NQ][128];  // folded query rows of the current request
+    const int t = threadIdx.x;
+    const float NaN = __int_as_float(0x7fc00000);
+    const long long total = P.hdr[HDR_TOTAL_PAGES];
+    if (total > (long long)P.B * P.mbps) {
+        if (t == 0) atomic_or_err(P.hdr, PA_DEV_ERR_STALE_PLAN);
+        return;
+    }
+    const long long x0 = blockIdx.x * total / gridDim.x, x1 = (blockIdx.x + 1) * total / gridDim.x;
+    if (x0 >= x1) return;
+    Cursor cu = cursor_at(x0, P.req, P.B, 1, P.mbps);
+    if (cu.b >= P.B) {
+        if (t == 0) atomic_or_err(P.hdr, PA_DEV_ERR_STALE_PLAN);
+        return;
+    }
+    uint32_t err = 0;
+    int pb = -1, L = 0, nblk = 0;
+    bool pbad = false;
+    const int q4 = P.bs >> 2;
+    for (long long x = x0; x < x1; ++x) {
+        if (cu.b >= P.B) { err |= PA_DEV_ERR_STALE_PLAN; break; }
+        if (cu.b != pb) {
+            // fold the request's query rows: thread t owns channel t of every row
+            __syncthreads();  // the previous request's rows are no longer read
+            pb = cu.b;
+            L = P.context_lens[pb];
+            const int4 Rq = P.req[pb];
+            pbad = false;
+            if (Rq.w != 0) { pbad = true; err |= PA_DEV_ERR_CONTEXT_LEN; }
+            if (L != Rq.x) { pbad = true; err |= PA_DEV_ERR_STALE_PLAN; }
+            nblk = min((L + P.bs - 1) / P.bs, P.tbl);
+#pragma unroll
+            for (int jq = 0; jq < NQ; ++jq) {
+                float acc = 0.f;
+                for (int h = 0; h < P.H; ++h) {
+                    const size_t qi = ((size_t)pb * NQ + jq) * P.H + h;
+                    const uint32_t h2 = e2m1x2_f16x2(P.q[qi * 64 + (t >> 1)]);
+                    const float2 v = __half22float2(*reinterpret_cast<const __half2 *>(&h2));
+                    const int sb = (int)(((uint32_t)P.sf_q[qi] >> (8 * (t >> 5))) & 0xFFu);
+                    acc = fmaf(P.weights[qi] * ue8m0_f32(sb), (t & 1) ? v.y : v.x, acc);
+                }
+                qw[jq][t] = acc;
+            }
+            __syncthreads();
+        }
+        const int tok = cu.p * TILE + t;
+        float lg[NQ];
+#pragma unroll
+        for (int jq = 0; jq < NQ; ++jq) lg[jq] = 0.f;
+        bool bad = false;
+        if (tok < L) {
+            const int bi = tok / P.bs;
+            const int blk = bi < nblk ? P.block_table[(size_t)pb * P.tbl + bi] : 0;
+            if (blk < 1 || blk >= P.num_blocks) {
+                bad = true;
+                err |= PA_DEV_ERR_BLOCK_ID;
+            } else {
+                const uint8_t *base = P.kv + (size_t)blk * (size_t)P.block_bytes;
+                const int s = tok - bi * P.bs;
+                const uint4 *row = reinterpret_cast<const uint4 *>(base + s * 64);
+                const int ws = P.interleaved ? 4 * (s % q4) + s / q4 : s;
+                const uint32_t sw = *reinterpret_cast<const uint32_t *>(base + P.bs * 64 + ws * 4);
+                uint4 raw[4];
+#pragma unroll
+                for (int k = 0; k < 4; ++k) raw[k] = row[k];
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {  // scale group k: values 32k .. 32k + 31 = bytes 16k .. 16k + 15
+                    float gs[NQ];
+#pragma unroll
+                    for (int jq = 0; jq < NQ; ++jq) gs[jq] = 0.f;
+                    const uint32_t w4[4] = {raw[k].x, raw[k].y, raw[k].z, raw[k].w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        // the 8 values of word e: channels 32k + 8e .. + 7
+                        float v[8];
+#pragma unroll
+                        for (int bb = 0; bb < 4; ++bb) {
+                            const uint32_t h2 = e2m1x2_f16x2(w4[e] >> (8 * bb));
+                            const float2 f = __half22float2(*reinterpret_cast<const __half2 *>(&h2));
+                            v[2 * bb] = f.x;
+                            v[2 * bb + 1] = f.y;
+                        }
+                        const int d = 32 * k + 8 * e;
+#pragma unroll
+                        for (int jq = 0; jq < NQ; ++jq) {
+                            const float4 a = *reinterpret_cast<const float4 *>(&qw[jq][d]);
+                            const float4 b = *reinterpret_cast<const float4 *>(&qw[jq][d + 4]);
+                            float g = gs[jq];
+                            g = fmaf(a.x, v[0], g); g = fmaf(a.y, v[1], g); g = fmaf(a.z, v[2], g); g = fmaf(a.w, v[3], g);
+                            g = fmaf(b.x, v[4], g); g = fmaf(b.y, v[5], g); g = fmaf(b.z, v[6], g); g = fmaf(b.w, v[7], g);
+                            gs[jq] = g;
+                        }
+                    }
+                    const float sc = ue8m0_f32((int)((sw >> (8 * k)) & 0xFFu));
+#pragma unroll
+                    for (int jq = 0; jq < NQ; ++jq) lg[jq] = fmaf(sc, gs[jq], lg[jq]);
+                }
+            }
+        }
+        if (tok < P.max_ctx) {
+#pragma unroll
+            for (int jq = 0; jq < NQ; ++jq) {
+                const int vis = P.causal ? L - (NQ - 1 - jq) : L;
+                const float val = (pbad || bad) ? NaN : (tok < vis ? lg[jq] : -INFINITY);
+                const size_t oi = (size_t)((long long)pb * NQ + jq) * (size_t)P.out_stride + (size_t)tok;
+                if (P.out_dtype == PA_F32) reinterpret_cast<float *>(P.out)[oi] = val;
+                else if (P.out_dtype == PA_F16) reinterpret_cast<__half *>(P.out)[oi] = __float2half_rn(val);
+                else reinterpret_cast<__nv_bfloat16 *>(P.out)[oi] = __float2bfloat16_rn(val);
+            }
+        }
+        cursor_next<true>(cu, P.req, P.B, 1, P.mbps);
+    }
+    if (err) atomic_or_err(P.hdr, err);
+}
+
 // Columns no tile covers: -inf from the last tile of each request to
 // max_context_len, NaN over the whole row of a request the plan flagged.
 __global__ void __launch_bounds__(256) pa_fp4_fill_kernel(Fp4Params P) {
@@ -464,6 +598,17 @@ cudaError_t launch_fp4_logits(const Fp4Params &P, int ctas, cudaStream_t s) {
     pa_fp4_fill_kernel<<<P.B * P.n, 256, 0, s>>>(P);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
+    if (!P.rectify && P.n <= fp4::SUM_MAX_N) {
+        // the plain weighted sum: one folded query vector per row, CUDA cores
+        const dim3 g((unsigned)(ctas * fp4::SUM_CTAS_PER_SM));
+        switch (P.n) {
+            case 1: pa_fp4_logits_sum_kernel<1><<<g, fp4::SUM_THREADS, 0, s>>>(P); break;
+            case 2: pa_fp4_logits_sum_kernel<2><<<g, fp4::SUM_THREADS, 0, s>>>(P); break;
+            case 3: pa_fp4_logits_sum_kernel<3><<<g, fp4::SUM_THREADS, 0, s>>>(P); break;
+            default: pa_fp4_logits_sum_kernel<4><<<g, fp4::SUM_THREADS, 0, s>>>(P); break;
+        }
+        return cudaGetLastError();
+    }
     e = cudaFuncSetAttribute(pa_fp4_logits_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, fp4::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     pa_fp4_logits_kernel<<<ctas, fp4::THREADS, fp4::SMEM_BYTES, s>>>(P);

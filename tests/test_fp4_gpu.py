@@ -67,15 +67,23 @@ def check(w, out, rows=None):
     return float((err / np.maximum(1.0, mag[fin])).max(initial=0.0))
 
 
+# rectify=False runs the folded-query kernel (CUDA cores, next_n <= 4), rectify=True
+# (and next_n > 4) the tensor-core kernel with per-head products
 SMALL = [
     dict(),                                              # bf16 out, causal, 64-token blocks, n = 2, H = 64
     dict(causal=False, out_dtype="f32"),
-    dict(rectify=True, out_dtype="f32"),
     dict(bs=16, sf_interleaved=True),
-    dict(bs=32, n=3),                                    # 192 rows: the widest S^T
+    dict(bs=32, n=3),
     dict(bs=128, n=1, H=16, out_dtype="f16"),
     dict(n=1, H=32, sf_interleaved=True, bs=64),
     dict(scale_lo=100, scale_hi=150, out_dtype="f32"),   # scales spread over 2^50 within rows
+    dict(rectify=True, out_dtype="f32"),
+    dict(rectify=True),
+    dict(rectify=True, bs=16, sf_interleaved=True, causal=False),
+    dict(rectify=True, bs=32, n=3),                      # 192 rows: the widest S^T
+    dict(rectify=True, bs=128, n=1, H=16, out_dtype="f16"),
+    dict(rectify=True, scale_lo=100, scale_hi=150, out_dtype="f32"),
+    dict(n=6, H=16, out_dtype="f32"),                    # more rows than the folded kernel takes
 ]
 
 
@@ -100,8 +108,9 @@ def test_short_and_empty_requests():
     assert torch.all(torch.isneginf(o[2, :]))           # L = 1, causal row 0 sees nothing
 
 
-def test_relocation_and_poisoned_bytes_bitwise():
-    w = W.make_fp4(device="cuda", B=5, L_lo=1, L_hi=900, H=32)
+@pytest.mark.parametrize("rectify", [False, True])
+def test_relocation_and_poisoned_bytes_bitwise(rectify):
+    w = W.make_fp4(device="cuda", B=5, L_lo=1, L_hi=900, H=32, rectify=rectify)
     out, _ = run(w)
     o2, bits = run(W.relocate_fp4(w, seed=4))
     assert bits == 0 and torch.equal(out, o2)
@@ -131,17 +140,20 @@ def test_output_stride_and_columns_past_max_context():
     assert torch.all(out[:, w.max_context_len:].float() == 7.0)
 
 
-def test_bad_block_id_and_over_long_request_are_nan():
-    w = W.make_fp4(device="cuda", context_lens=[200, 300, 150], H=16)
+@pytest.mark.parametrize("rectify", [False, True])
+def test_bad_block_id_and_over_long_request_are_nan(rectify):
+    w = W.make_fp4(device="cuda", context_lens=[200, 300, 150], H=16, rectify=rectify)
     w.block_table = w.block_table.clone()
     w.block_table[1, 2] = w.num_blocks + 5
     out, bits = run(w)
     assert bits & pa.binding().PA_DEV_ERR_BLOCK_ID
     o = out.float().cpu()
-    assert torch.isnan(o[2:4, 128:256]).all()           # tile 1 of request 1 (blocks 2, 3)
+    # the tokens of block 2 are NaN (the tensor-core kernel NaN-fills the whole
+    # 128-token tile holding it, blocks 2 and 3); nothing outside that tile is
+    assert torch.isnan(o[2:4, 128:192]).all()
     assert not torch.isnan(o[2:4, :128]).any() and not torch.isnan(o[2:4, 256:]).any()
     assert not torch.isnan(o[0:2]).any() and not torch.isnan(o[4:6]).any()
-    w2 = W.make_fp4(device="cuda", context_lens=[200, 300, 150], H=16)
+    w2 = W.make_fp4(device="cuda", context_lens=[200, 300, 150], H=16, rectify=rectify)
     p = pa.fp4_problem(w2)
     p.max_context_len = 250                                             # request 1 breaks the contract
     b = pa.binding()
@@ -153,18 +165,20 @@ def test_bad_block_id_and_over_long_request_are_nan():
     assert torch.isnan(out[2:4].float()).all() and not torch.isnan(out[0:2].float()).any()
 
 
-def test_repeat_runs_bitwise():
-    w = W.make_fp4(device="cuda", B=3, L_lo=500, L_hi=3000, n=2, H=64)
+@pytest.mark.parametrize("rectify", [False, True])
+def test_repeat_runs_bitwise(rectify):
+    w = W.make_fp4(device="cuda", B=3, L_lo=500, L_hi=3000, n=2, H=64, rectify=rectify)
     o1, _ = run(w, grid_ctas=7)
     o2, _ = run(w, grid_ctas=7)
     assert torch.equal(o1, o2)
 
 
-def test_full_size_sampled_rows():
+@pytest.mark.parametrize("rectify", [False, True])
+def test_full_size_sampled_rows(rectify):
     """The benchmark's batch (128 requests of 4K-64K tokens, 2 query rows x 64
     heads) in its launch shape, checked on sampled rows including the
     longest request's."""
-    w = W.make_fp4(device="cuda")
+    w = W.make_fp4(device="cuda", rectify=rectify)
     out, bits = run(w)
     assert bits == 0
     L = w.context_lens.cpu().numpy()
@@ -172,4 +186,5 @@ def test_full_size_sampled_rows():
     rng = np.random.default_rng(0)
     rows = sorted({bmax * w.n, bmax * w.n + 1} | {int(x) for x in rng.integers(0, w.B * w.n, 4)})
     worst = check(w, out, rows=rows)
-    notes.add(f"fp4 logits full size: {len(rows)} sampled rows, worst |err| / magnitude {worst:.3g}")
+    notes.add(f"fp4 logits full size (rectify={rectify}): {len(rows)} sampled rows, worst |err| / magnitude "
+              f"{worst:.3g}")

@@ -80,6 +80,19 @@ def test_sparse_matches_oracle(name, kw, k):
     check(w, sel, out, lse)
 
 
+@pytest.mark.parametrize("name", ["int8", "int4"])
+def test_sparse_per_channel_near_one_hot(name):
+    # q ~ N(0, 100^2) with per-channel scales up to 1e3, as in the INT8 / INT4
+    # benchmark batch: scores of order 1e6 make each softmax nearly one-hot;
+    # the sparse kernel scores in fp32 (no f16 fold), so the normwise bound
+    # holds without a near-tie allowance
+    w = W.make(name, device="cuda", B=3, L_lo=200, L_hi=1200, Hq=16, Hkv=2)
+    sel = W.make_selection(w, k=96, seed=4, shared=0.9)
+    out, lse, bits = run_sparse(w, sel)
+    assert bits == 0
+    check(w, sel, out, lse)
+
+
 def test_sparse_relocation_and_selection_order_bitwise():
     w = W.make("e4m3", device="cuda", B=3, L_lo=50, L_hi=900, Hq=16, Hkv=2, n=2)
     sel = W.make_selection(w, k=64, seed=3)

@@ -108,7 +108,7 @@ def test_withheld_copy_times_out_and_leaves_no_stale_rows(fi, name, kw, split):
 
 
 def test_fp4_withheld_tile_times_out(fi):
-    w = W.make_fp4(device="cuda", B=4, L_lo=300, L_hi=1200, H=32)
+    w = W.make_fp4(device="cuda", B=4, L_lo=300, L_hi=1200, H=32, rectify=True)  # the tensor-core kernel
     p = pa.fp4_problem(w, grid_ctas=5)
     b = pa.binding()
     n = b.pa_fp4_logits_workspace_size(p)
