@@ -407,14 +407,18 @@ PA_API pa_status pa_sparse_attention(const pa_problem *p, int32_t top_k, const i
  *            columns 0 .. max_context_len - 1 of every row are written.
  *  workspace caller-owned, pa_fp4_logits_workspace_size() bytes, 256-byte
  *            aligned: word 0 is the device error word (pa_get_error), then
- *            the plan over 128-token tiles.
+ *            the plan over 128-token tiles and, for the plain weighted sum,
+ *            the folded query rows sum_h weights[r][h] * q^[h] (fp32).
  * Supported: head_dim 128, sf_vec_size 32, block_size 16 / 32 / 64 / 128,
  * num_heads a multiple of 16, next_n * num_heads <= 192; other problems
  * return PA_ERR_UNSUPPORTED.  A request whose length breaks the contract
  * (PA_DEV_ERR_CONTEXT_LEN) or a block id outside [1, num_blocks)
  * (PA_DEV_ERR_BLOCK_ID) gets NaN logits; nothing outside the buffers is read
- * or written.  Three kernel launches on `stream`; no allocation, no
- * synchronisation. */
+ * or written.  The plain weighted sum (rectify = 0, next_n <= 4) folds the
+ * heads into one query vector per row first (the logit is linear in the
+ * heads) and runs on the CUDA cores; rectified heads (and next_n > 4) keep
+ * the per-head products on the tensor cores.  Three or four kernel launches
+ * on `stream`; no allocation, no synchronisation. */
 typedef struct pa_fp4_problem {
     int32_t batch;              /* B >= 0 requests */
     int32_t next_n;             /* query rows per request, >= 1 */

@@ -18,6 +18,8 @@
 //
 // Work: 128-token tiles in logical order (request, tile) -- never by block
 // id -- shared evenly by persistent CTAs (one per SM).  Roles (10 warps):
+//  (this kernel serves rectified heads and next_n > 4; the plain weighted sum
+//  runs on pa_fp4_logits_sum_kernel below)
 //  * warp 0 copies each tile's kv_fused blocks (whole blocks, one bulk copy
 //    each; ids range-checked first) into a 4-slot ring;
 //  * warps 6-9 (one token per thread) decode the token's 128 values into the
@@ -44,6 +46,7 @@ struct Fp4Params {
     const int32_t *context_lens;
     uint32_t *hdr;
     const int4 *req;            // plan records over 128-token tiles
+    float *qw;                  // [B][n][128] folded query rows (plain weighted sum)
     void *out;
     long long out_stride;       // elements per output row
     long long block_bytes;      // bs * 68
@@ -457,6 +460,22 @@ constexpr int SUM_MAX_N = 4;       // query rows per request this kernel folds (
 constexpr int SUM_CTAS_PER_SM = 8; // persistent CTAs per SM of the launch
 }  // namespace fp4
 
+// qw[b][j][d] = sum_h w[b * n + j][h] * q^[b][j][h][d] in fp32, one CTA per
+// query row, thread d per channel (heads in ascending order)
+__global__ void __launch_bounds__(128) pa_fp4_fold_kernel(Fp4Params P) {
+    const int r = blockIdx.x;  // b * n + j
+    const int t = threadIdx.x;
+    float acc = 0.f;
+    for (int h = 0; h < P.H; ++h) {
+        const size_t qi = (size_t)r * P.H + h;
+        const uint32_t h2 = fp4::e2m1x2_f16x2(P.q[qi * 64 + (t >> 1)]);
+        const float2 v = __half22float2(*reinterpret_cast<const __half2 *>(&h2));
+        const int sb = (int)(((uint32_t)P.sf_q[qi] >> (8 * (t >> 5))) & 0xFFu);
+        acc = fmaf(P.weights[qi] * fp4::ue8m0_f32(sb), (t & 1) ? v.y : v.x, acc);
+    }
+    P.qw[(size_t)r * 128 + t] = acc;
+}
+
 template <int NQ>
 __global__ void __launch_bounds__(fp4::SUM_THREADS) pa_fp4_logits_sum_kernel(Fp4Params P) {
     using namespace fp4;
@@ -482,7 +501,7 @@ __global__ void __launch_bounds__(fp4::SUM_THREADS) pa_fp4_logits_sum_kernel(Fp4
     for (long long x = x0; x < x1; ++x) {
         if (cu.b >= P.B) { err |= PA_DEV_ERR_STALE_PLAN; break; }
         if (cu.b != pb) {
-            // fold the request's query rows: thread t owns channel t of every row
+            // the request's folded query rows (written by pa_fp4_fold_kernel)
             __syncthreads();  // the previous request's rows are no longer read
             pb = cu.b;
             L = P.context_lens[pb];
@@ -492,17 +511,7 @@ __global__ void __launch_bounds__(fp4::SUM_THREADS) pa_fp4_logits_sum_kernel(Fp4
             if (L != Rq.x) { pbad = true; err |= PA_DEV_ERR_STALE_PLAN; }
             nblk = min((L + P.bs - 1) / P.bs, P.tbl);
 #pragma unroll
-            for (int jq = 0; jq < NQ; ++jq) {
-                float acc = 0.f;
-                for (int h = 0; h < P.H; ++h) {
-                    const size_t qi = ((size_t)pb * NQ + jq) * P.H + h;
-                    const uint32_t h2 = e2m1x2_f16x2(P.q[qi * 64 + (t >> 1)]);
-                    const float2 v = __half22float2(*reinterpret_cast<const __half2 *>(&h2));
-                    const int sb = (int)(((uint32_t)P.sf_q[qi] >> (8 * (t >> 5))) & 0xFFu);
-                    acc = fmaf(P.weights[qi] * ue8m0_f32(sb), (t & 1) ? v.y : v.x, acc);
-                }
-                qw[jq][t] = acc;
-            }
+            for (int jq = 0; jq < NQ; ++jq) qw[jq][t] = P.qw[((size_t)pb * NQ + jq) * 128 + t];
             __syncthreads();
         }
         const int tok = cu.p * TILE + t;
@@ -600,6 +609,9 @@ cudaError_t launch_fp4_logits(const Fp4Params &P, int ctas, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     if (!P.rectify && P.n <= fp4::SUM_MAX_N) {
         // the plain weighted sum: one folded query vector per row, CUDA cores
+        pa_fp4_fold_kernel<<<P.B * P.n, 128, 0, s>>>(P);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
         const dim3 g((unsigned)(ctas * fp4::SUM_CTAS_PER_SM));
         switch (P.n) {
             case 1: pa_fp4_logits_sum_kernel<1><<<g, fp4::SUM_THREADS, 0, s>>>(P); break;
@@ -647,7 +659,10 @@ pa_status fp4_check(const pa_fp4_problem *p) {
     return PA_OK;
 }
 
-size_t fp4_ws_bytes(const pa_fp4_problem *p) { return fp4_align(64) + fp4_align((size_t)p->batch * 16); }
+// header (64 B), request records (16 B each), folded query rows (fp32 [B][n][128])
+size_t fp4_ws_bytes(const pa_fp4_problem *p) {
+    return fp4_align(64) + fp4_align((size_t)p->batch * 16) + fp4_align((size_t)p->batch * p->next_n * 128 * 4);
+}
 
 }  // namespace
 
@@ -709,6 +724,7 @@ PA_API pa_status pa_fp4_logits(const pa_fp4_problem *p, const uint8_t *q, const 
     P.context_lens = context_lens;
     P.hdr = pp.hdr;
     P.req = pp.req;
+    P.qw = reinterpret_cast<float *>(ws + fp4_align(64) + fp4_align((size_t)p->batch * 16));
     P.out = out;
     P.out_stride = p->out_stride > 0 ? p->out_stride : p->max_context_len;
     P.block_bytes = (long long)p->block_size * pa::fp4::ROWB;

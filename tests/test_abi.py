@@ -375,7 +375,7 @@ def _fp4(B, **kw):
 
 
 def test_fp4_workspace_and_shapes(B):
-    assert B.pa_fp4_logits_workspace_size(_fp4(B)) == 256 + 256
+    assert B.pa_fp4_logits_workspace_size(_fp4(B)) == 256 + 256 + 4 * 2 * 512
     for kw in (dict(head_dim=64), dict(sf_vec_size=16), dict(block_size=48), dict(num_heads=24),
                dict(next_n=4), dict(batch=1 << 20, max_blocks_per_seq=1 << 14)):
         st = B.raw_status("pa_fp4_logits_workspace_size", ctypes.byref(_fp4(B, **kw)), ctypes.byref(ctypes.c_size_t()))
@@ -389,13 +389,14 @@ def test_fp4_workspace_and_shapes(B):
 def test_fp4_rejects_bad_pointers_before_any_launch(B):
     p = _fp4(B)
     args = [0x10000, 0x20000, 0x30000, 0x40000, 0x50000, 0x60000]   # q, sf_q, kv, weights, lens, table
-    assert B.raw_status("pa_fp4_logits", ctypes.byref(p), *args, None, 512, 0x70000, None) == B.PA_ERR_WORKSPACE
-    assert B.raw_status("pa_fp4_logits", ctypes.byref(p), *args, 0x80010, 512, 0x70000, None) == B.PA_ERR_WORKSPACE
-    assert B.raw_status("pa_fp4_logits", ctypes.byref(p), *args, 0x80000, 100, 0x70000, None) == B.PA_ERR_WORKSPACE
+    n = B.pa_fp4_logits_workspace_size(p)
+    assert B.raw_status("pa_fp4_logits", ctypes.byref(p), *args, None, n, 0x70000, None) == B.PA_ERR_WORKSPACE
+    assert B.raw_status("pa_fp4_logits", ctypes.byref(p), *args, 0x80010, n, 0x70000, None) == B.PA_ERR_WORKSPACE
+    assert B.raw_status("pa_fp4_logits", ctypes.byref(p), *args, 0x80000, n - 1, 0x70000, None) == B.PA_ERR_WORKSPACE
     bad_q = [0x10008] + args[1:]
-    assert B.raw_status("pa_fp4_logits", ctypes.byref(p), *bad_q, 0x80000, 512, 0x70000, None) == B.PA_ERR_INVALID_ARG
+    assert B.raw_status("pa_fp4_logits", ctypes.byref(p), *bad_q, 0x80000, n, 0x70000, None) == B.PA_ERR_INVALID_ARG
     no_kv = args[:2] + [None] + args[3:]
-    assert B.raw_status("pa_fp4_logits", ctypes.byref(p), *no_kv, 0x80000, 512, 0x70000, None) == B.PA_ERR_INVALID_ARG
+    assert B.raw_status("pa_fp4_logits", ctypes.byref(p), *no_kv, 0x80000, n, 0x70000, None) == B.PA_ERR_INVALID_ARG
 
 
 def test_fp4_empty_batch_is_a_no_op(B):

@@ -157,7 +157,7 @@ def test_bad_block_id_and_over_long_request_are_nan(rectify):
     p = pa.fp4_problem(w2)
     p.max_context_len = 250                                             # request 1 breaks the contract
     b = pa.binding()
-    ws = torch.zeros(256 + 256, dtype=torch.uint8, device="cuda")
+    ws = torch.zeros(b.pa_fp4_logits_workspace_size(p), dtype=torch.uint8, device="cuda")
     out = torch.zeros((6, 250), dtype=torch.bfloat16, device="cuda")
     pa.fp4_logits(w2, p, out, ws)
     torch.cuda.synchronize()
