@@ -16,6 +16,8 @@ cudaError_t launch_plan(const PlanParams &P, const float *k_scale, int k_count, 
 cudaError_t launch_combine(const CombineParams &P, cudaStream_t s);
 cudaError_t launch_latent(const CUtensorMap &ta, const CUtensorMap &tb, const LatentParams &P, int ctas,
                           cudaStream_t s);
+cudaError_t launch_e4m3_tc(const CUtensorMap &tk, const CUtensorMap &tv, const E4TcParams &P, int ctas,
+                           cudaStream_t s);
 }  // namespace pa
 
 namespace {
@@ -68,6 +70,7 @@ pa_status device_sms(int *sms) {
 struct Derived {
     int G, R, row_blocks, sms, ctas, minb;
     bool tokm, latent;
+    bool e4tc;     // the E4M3 tensor-core kernel (head dim 256, 16..64 rows per kv head)
     int rows_seg;  // query rows per segment
     int gs;        // workers per group (they share one run of pages, one row block each)
     long long nwarps, slots_partial;
@@ -113,7 +116,35 @@ pa_status derive(const pa_problem *p, Derived *d) {
         if (st != PA_OK) return st;
     }
     d->latent = p->v_is_k_prefix != 0;
-    if (d->latent) {
+    d->e4tc = !d->latent && p->kv_dtype == PA_E4M3 && p->head_dim_k == 256 && p->head_dim_v == 256 &&
+              (p->k_scale_mode == PA_SCALE_NONE || p->k_scale_mode == PA_SCALE_TENSOR) &&
+              (p->v_scale_mode == PA_SCALE_NONE || p->v_scale_mode == PA_SCALE_TENSOR) && d->R % 16 == 0 &&
+              d->R >= 16 && d->R <= 64 &&
+              (p->block_size == 16 || p->block_size == 32 || p->block_size == 64 || p->block_size == 128) &&
+              p->num_kv_heads <= 65535;
+    if (d->e4tc) {
+        // tokens on the MMA M axis in 128-token chunks (the plan's pages), all R
+        // rows of a kv head in one segment, one CTA per SM
+        d->D = 256;
+        d->rows_seg = d->R;
+        d->row_blocks = 1;
+        d->tokm = false;
+        d->minb = 1;
+        d->RB = 256;
+        d->SW = 128;
+        d->k_block = (size_t)p->num_kv_heads * p->block_size * 256;
+        d->v_block = d->k_block;
+        d->slots = d->R <= 48 ? 3 : 2;  // K stages of a chunk (V: 3 at 16 rows, else 2)
+        d->wp = 128;
+        d->wpb = 1;
+        d->mpb = 128 / p->block_size;
+        d->box_rows = p->block_size;
+        d->warp_smem = 0;
+        d->smem = 0;
+        d->gs = 1;
+        d->ctas = p->grid_ctas > 0 ? p->grid_ctas : d->sms;
+        d->nwarps = d->ctas;
+    } else if (d->latent) {
         // single-latent MQA: one E4M3 plane, V = its first 512 of 576
         // channels, a per-token fp32 scale after the codes of each block
         if (p->kv_dtype != PA_E4M3 || p->k_scale_mode != PA_SCALE_TOKEN || p->head_dim_k != LAT_DK ||
@@ -473,6 +504,51 @@ PA_API pa_status pa_run(const pa_problem *p, const void *q, const void *k_pool, 
         P.causal = p->causal;
         P.softmax_scale = p->softmax_scale;
         cudaError_t e = pa::launch_latent(ta, tb, P, d.ctas, reinterpret_cast<cudaStream_t>(stream));
+        return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+    }
+    if (d.e4tc) {
+        // rows of q are read in 16-byte pieces; the pools are read by tensor copies
+        if ((reinterpret_cast<uintptr_t>(k_pool) & 15) || (reinterpret_cast<uintptr_t>(v_pool) & 15) ||
+            (reinterpret_cast<uintptr_t>(q) & 15))
+            return PA_ERR_INVALID_ARG;
+        if ((p->k_scale_mode == PA_SCALE_TENSOR && k_scale == nullptr) ||
+            (p->v_scale_mode == PA_SCALE_TENSOR && v_scale == nullptr))
+            return PA_ERR_INVALID_ARG;
+        CUtensorMap tk, tv;
+        if ((st = make_tmap(&tk, k_pool, d, p, d.k_block, 128)) != PA_OK) return st;
+        if ((st = make_tmap(&tv, v_pool, d, p, d.v_block, 128)) != PA_OK) return st;
+        pa::E4TcParams P;
+        P.q = static_cast<const uint8_t *>(q);
+        P.k_pool = static_cast<const uint8_t *>(k_pool);
+        P.v_pool = static_cast<const uint8_t *>(v_pool);
+        P.block_table = block_table;
+        P.context_lens = context_lens;
+        P.k_scale = k_scale;
+        P.v_scale = v_scale;
+        P.hdr = at<uint32_t>(workspace, d.L.header_offset);
+        P.req = at<const int4>(workspace, d.L.requests_offset);
+        P.part_o = at<float>(workspace, d.L.partial_o_offset);
+        P.part_lse = at<float>(workspace, d.L.partial_lse_offset);
+        P.out = out;
+        P.lse = lse;
+        P.block_stride = (long long)d.k_block;
+        P.B = p->batch;
+        P.n = p->next_n;
+        P.Hq = p->num_q_heads;
+        P.Hkv = p->num_kv_heads;
+        P.G = d.G;
+        P.R = d.R;
+        P.bs = p->block_size;
+        P.tbl = p->max_blocks_per_seq;
+        P.mbps = work_pages_per_seq(p, d);
+        P.num_blocks = p->num_blocks;
+        P.q_dtype = p->q_dtype;
+        P.out_dtype = p->out_dtype;
+        P.k_mode = p->k_scale_mode;
+        P.v_mode = p->v_scale_mode;
+        P.causal = p->causal;
+        P.softmax_scale = p->softmax_scale;
+        cudaError_t e = pa::launch_e4m3_tc(tk, tv, P, d.ctas, reinterpret_cast<cudaStream_t>(stream));
         return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
     }
     if ((reinterpret_cast<uintptr_t>(k_pool) & 15) || (reinterpret_cast<uintptr_t>(v_pool) & 15) ||

@@ -392,6 +392,9 @@ __global__ void __launch_bounds__(ATTN_THREADS, min_blocks(Geo<KVT, D>::BITS, D,
     // group reads each page at about the same time (all but the first copy
     // of a page hit L2) instead of every row block streaming the KV again.
     const int GS = P.RBLK;
+    // pages read by one worker only stream through L2 (evict first); a group
+    // of row-block workers rereads each page from L2
+    const uint64_t pol = GS > 1 ? l2_evict_normal_policy() : l2_evict_first_policy();
 
     // this worker's shared memory: ring of NS pages, q' fragments (each warp of
     // a pair its half), the pair's score exchange and slot flags, barriers
@@ -503,8 +506,8 @@ __global__ void __launch_bounds__(ATTN_THREADS, min_blocks(Geo<KVT, D>::BITS, D,
 #pragma unroll
                     for (int i = 0; i < MERGE_BLOCKS; ++i) {
                         if (i < nbp) {
-                            tma_load_5d(kt + i * sub, &tmk, &full[slot], 0, 0, 0, kvh, blk[i]);
-                            tma_load_5d(vt + i * sub, &tmv, &full[slot], 0, 0, 0, kvh, blk[i]);
+                            tma_load_5d_hint(kt + i * sub, &tmk, &full[slot], 0, 0, 0, kvh, blk[i], pol);
+                            tma_load_5d_hint(vt + i * sub, &tmv, &full[slot], 0, 0, 0, kvh, blk[i], pol);
                         }
                     }
                 } else {
@@ -539,8 +542,8 @@ __global__ void __launch_bounds__(ATTN_THREADS, min_blocks(Geo<KVT, D>::BITS, D,
             uint8_t *vt = kt + tile_bytes;
             if (ok) {
                 mbar_arrive_expect_tx(&full[slot], (uint32_t)page_bytes);
-                tma_load_5d(kt, &tmk, &full[slot], 0, y0, 0, kvh, blk);  // all segments of the K tile
-                tma_load_5d(vt, &tmv, &full[slot], 0, y0, 0, kvh, blk);
+                tma_load_5d_hint(kt, &tmk, &full[slot], 0, y0, 0, kvh, blk, pol);  // all segments of the K tile
+                tma_load_5d_hint(vt, &tmv, &full[slot], 0, y0, 0, kvh, blk, pol);
             } else {
                 mbar_arrive(&full[slot]);  // no copy: the piece is NaN-filled
             }

@@ -59,6 +59,28 @@ struct LatentParams {
     float softmax_scale;
 };
 
+// The E4M3 tensor-core kernel (head dim 256, 16..64 query rows per kv head):
+// separate K and V planes, per-tensor (or no) scales, 128-token chunks.
+struct E4TcParams {
+    const uint8_t *q;
+    const uint8_t *k_pool;
+    const uint8_t *v_pool;
+    const int32_t *block_table;
+    const int32_t *context_lens;
+    const float *k_scale;  // per-tensor or NULL
+    const float *v_scale;
+    uint32_t *hdr;
+    const int4 *req;       // plan over 128-token chunks
+    float *part_o;         // [slots][R][256]
+    float *part_lse;       // [slots][R]
+    void *out;
+    float *lse;
+    long long block_stride;  // bytes per pool block (Hkv * bs * 256)
+    int B, n, Hq, Hkv, G, R, bs, tbl, mbps, num_blocks;
+    int q_dtype, out_dtype, k_mode, v_mode, causal;
+    float softmax_scale;
+};
+
 struct PlanParams {
     const int32_t *context_lens;
     uint32_t *hdr;
@@ -177,6 +199,32 @@ __device__ __forceinline__ void tma_load_4d(void *dst, const CUtensorMap *tm, ui
         : "memory");
 }
 
+// An L2 policy for data read once (the KV stream): its lines are the first
+// to go, so the stream does not push out what is reused (code, queries,
+// tables, plan records).
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
+// the default L2 policy, as a value (for call sites that pick one at run time)
+__device__ __forceinline__ uint64_t l2_evict_normal_policy() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
+// tma_load_4d with an L2 cache policy
+__device__ __forceinline__ void tma_load_4d_hint(void *dst, const CUtensorMap *tm, uint64_t *bar, int x, int y, int z,
+                                                 int w, uint64_t pol) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3, %4, %5}], [%6], %7;" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(z), "r"(w), "r"(smem_u32(bar)), "l"(pol)
+        : "memory");
+}
+
 // 5-D tiled bulk tensor copy global -> shared, completion counted on `bar`.
 __device__ __forceinline__ void tma_load_5d(void *dst, const CUtensorMap *tm, uint64_t *bar, int c0, int c1, int c2,
                                             int c3, int c4) {
@@ -187,11 +235,31 @@ __device__ __forceinline__ void tma_load_5d(void *dst, const CUtensorMap *tm, ui
         : "memory");
 }
 
+// tma_load_5d with an L2 cache policy
+__device__ __forceinline__ void tma_load_5d_hint(void *dst, const CUtensorMap *tm, uint64_t *bar, int c0, int c1,
+                                                 int c2, int c3, int c4, uint64_t pol) {
+    asm volatile(
+        "cp.async.bulk.tensor.5d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3, %4, %5, %6}], [%7], %8;" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(tm)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(c4), "r"(smem_u32(bar)),
+        "l"(pol)
+        : "memory");
+}
+
 // 1-D bulk copy global -> shared (16-byte aligned addresses, size a multiple of 16)
 __device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
     asm volatile(
         "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(smem_u32(dst)),
         "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+
+// bulk_load with an L2 cache policy
+__device__ __forceinline__ void bulk_load_hint(void *dst, const void *src, uint32_t bytes, uint64_t *bar, uint64_t pol) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(
+            smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar)), "l"(pol)
         : "memory");
 }
 

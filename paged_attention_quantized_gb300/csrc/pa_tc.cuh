@@ -135,6 +135,16 @@ __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, volati
     return ok != 0;
 }
 
+// warp_wait with a warp-uniform fast path: one try_wait in every lane (each
+// lane acquires the completed phase itself; measured at about a third of the
+// cost of a lane-0 poll and broadcast), the bounded lane-0 wait otherwise.
+// For kernels whose waits mostly find the phase complete; in a kernel bound
+// by shared-memory bandwidth the lane-0 poll of warp_wait is kinder.
+__device__ __forceinline__ bool warp_wait_u(uint64_t *bar, uint32_t parity, volatile int *abort, uint32_t &err) {
+    if (__all_sync(0xffffffffu, mbar_try_wait(bar, parity))) return true;
+    return warp_wait(bar, parity, abort, err);
+}
+
 __device__ __forceinline__ void warp_arrive(uint64_t *bar) {
     __syncwarp();
     if ((threadIdx.x & 31) == 0) mbar_arrive(bar);

@@ -207,7 +207,9 @@ def test_every_block_size_has_a_launch(B):
     """Every KV encoding x head dim x block size (multiples of 16 up to 128) x
     rows per kv head gets a launch: whole blocks when two per worker fit,
     else equal work pages of >= 16 tokens; 16-token blocks of rows of at most
-    64 bytes are merged two to a work page when two merged pages fit."""
+    64 bytes are merged two to a work page when two merged pages fit; E4M3 at
+    head dim 256 with 16..64 rows per kv head runs on the tensor-core kernel
+    in 128-token chunks."""
     for kv in (B.PA_F16, B.PA_BF16, B.PA_E4M3, B.PA_INT8, B.PA_INT4):
         for D in (64, 128, 256):
             if kv == B.PA_INT4 and D == 64:
@@ -219,6 +221,12 @@ def test_every_block_size_has_a_launch(B):
                     wp = lo.work_page_tokens
                     assert lo.ring_pages_per_warp >= 1, (kv, D, bs, hq, n)
                     row_bytes = D * {B.PA_F16: 2, B.PA_BF16: 2, B.PA_E4M3: 1, B.PA_INT8: 1, B.PA_INT4: 0.5}[kv]
+                    R = (hq // 8) * n
+                    if kv == B.PA_E4M3 and D == 256 and R % 16 == 0 and 16 <= R <= 64 and bs in (16, 32, 64, 128):
+                        # the tensor-core kernel: 128-token chunks, every row of a kv head in one segment
+                        assert wp == 128 and lo.rows_per_segment == R and lo.row_blocks == 1
+                        assert lo.warps == lo.grid_ctas and lo.ring_pages_per_warp in (2, 3)
+                        continue
                     if wp > bs:  # merged blocks
                         assert bs == 16 and wp == 32 and row_bytes <= 64 and lo.ring_pages_per_warp >= 2
                     else:

@@ -87,7 +87,10 @@ def test_paired_warps_d256(name, kw, split):
     w = make(base, B=4, L_lo=1, L_hi=600, Hq=8, Hkv=2, n=4, **kw)
     p = pa.problem(w, grid_ctas=split)
     lo = pa.binding().pa_workspace_layout(p)
-    assert lo.warps == lo.grid_ctas * 2  # two warps per worker
+    if name == "e4m3":  # E4M3 at D = 256 with 16 rows runs on the tensor-core kernel instead
+        assert lo.rows_per_segment == 16 and lo.work_page_tokens == 128 and lo.warps == lo.grid_ctas
+    else:
+        assert lo.warps == lo.grid_ctas * 2  # two warps per worker
     out, lse, ws, _ = run_gpu(w, grid_ctas=split)
     assert error_bits(ws) == 0
     compare(w, out, lse)
@@ -166,7 +169,8 @@ def test_plan_matches_oracle_plan(kw):
 @pytest.mark.parametrize("name,kw", [
     ("bf16", dict(Hq=8, Hkv=2)),                 # one row block
     ("bf16", dict(Hq=32, Hkv=2, n=2)),           # 32 rows: groups of 2 workers
-    ("e4m3", dict(Hq=32, Hkv=8, n=16)),          # verify: groups of 4 paired workers
+    ("bf16", dict(Hq=64, Hkv=2, n=2, D=256)),    # 64 rows at D = 256: groups of 4 paired workers
+    ("e4m3", dict(Hq=32, Hkv=8, n=16)),          # verify: the tensor-core kernel, 64-row segments
 ])
 def test_partial_pieces_match_oracle_plan(name, kw):
     # with many workers every segment is cut into pieces: each piece's partial
@@ -176,16 +180,17 @@ def test_partial_pieces_match_oracle_plan(name, kw):
     p = pa.problem(w, grid_ctas=40)
     out, lse, ws = pa.alloc(w, p)
     lo = pa.binding().pa_workspace_layout(p)
+    S = lo.rows_per_segment
     ws_f = ws.view(torch.float32)
-    ws_f[lo.partial_lse_offset // 4: lo.partial_lse_offset // 4 + lo.partial_slots * 16] = float("nan")
+    ws_f[lo.partial_lse_offset // 4: lo.partial_lse_offset // 4 + lo.partial_slots * S] = float("nan")
     pa.run(w, p, out, ws, lse, steps="plan+run")
     torch.cuda.synchronize()
     assert lo.group_size == lo.row_blocks and lo.warps % lo.group_size == 0
-    pl = oracle.plan(w.context_lens.cpu().numpy(), bs=w.bs, Hkv=w.Hkv, max_context_len=w.max_context_len,
-                     max_blocks_per_seq=w.max_blocks_per_seq, row_blocks=lo.row_blocks, warps=lo.warps,
-                     group_size=lo.group_size)
-    lse_parts = ws_f[lo.partial_lse_offset // 4:][: lo.partial_slots * 16].view(-1, 16).cpu().numpy()
-    R = min(lo.rows_per_kv_head, 16)
+    pl = oracle.plan(w.context_lens.cpu().numpy(), bs=lo.work_page_tokens, block_size=w.bs, Hkv=w.Hkv,
+                     max_context_len=w.max_context_len, max_blocks_per_seq=w.max_blocks_per_seq,
+                     row_blocks=lo.row_blocks, warps=lo.warps, group_size=lo.group_size)
+    lse_parts = ws_f[lo.partial_lse_offset // 4:][: lo.partial_slots * S].view(-1, S).cpu().numpy()
+    R = min(lo.rows_per_kv_head, S)
     written = set()
     for pc in pl["pieces"]:
         if not pc["complete"]:

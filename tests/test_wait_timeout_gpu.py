@@ -60,11 +60,11 @@ def _attention(lib, w, p, withhold=0):
     return out, lse, bits, total, dt
 
 
-def _owner_rows(w, total, x):
+def _owner_rows(w, total, x, wp):
     """(request, kv head) whose pages position x belongs to: positions run over
-    (request, kv head, page) by the plan's prefix sums."""
+    (request, kv head, page) by the plan's prefix sums (pages of wp tokens)."""
     L = w.context_lens.cpu().numpy().astype(np.int64)
-    bs = w.bs
+    bs = wp
     P = (L + bs - 1) // bs
     base = 0
     for b in range(w.B):
@@ -77,7 +77,8 @@ def _owner_rows(w, total, x):
 
 @pytest.mark.parametrize("name,kw,split", [
     ("bf16", dict(B=5, L_lo=200, L_hi=1500, Hq=16, Hkv=2), 0),
-    ("e4m3", dict(B=4, L_lo=100, L_hi=900, Hq=32, Hkv=8, n=16), 5),   # groups of 4 paired workers
+    ("bf16", dict(B=4, L_lo=100, L_hi=900, Hq=64, Hkv=2, n=2, D=256), 5),  # groups of 4 paired workers
+    ("e4m3", dict(B=4, L_lo=100, L_hi=2000, Hq=32, Hkv=8, n=4), 7),     # the E4M3 tensor-core kernel
     ("latent", dict(B=3, L_lo=200, L_hi=600, Hq=32), 6),
 ])
 def test_withheld_copy_times_out_and_leaves_no_stale_rows(fi, name, kw, split):
@@ -95,7 +96,7 @@ def test_withheld_copy_times_out_and_leaves_no_stale_rows(fi, name, kw, split):
     out, lse, bits, _, dt = _attention(fi, w, p, withhold=x + 1)
     assert bits & pa.binding().PA_DEV_ERR_TIMEOUT
     assert dt < 10.0
-    b, u = _owner_rows(w, total, x)
+    b, u = _owner_rows(w, total, x, pa.binding().pa_workspace_layout(p).work_page_tokens)
     G = w.Hq // w.Hkv
     o = out.float().cpu()
     assert torch.isnan(o[b, :, u * G:(u + 1) * G]).all()
