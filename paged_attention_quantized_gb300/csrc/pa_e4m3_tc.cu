@@ -59,8 +59,8 @@ namespace e4tc {
 using namespace tc;
 
 constexpr int D = 256, CH = 128;  // head dim, tokens per chunk
-constexpr int NWARPS = 7, THREADS = NWARPS * 32;
-constexpr int W_KPROD = 0, W_MMA = 1, W_VPROD = 6;  // warps 2-5: softmax
+constexpr int NWARPS = 11, THREADS = NWARPS * 32;
+constexpr int W_KPROD = 0, W_MMA = 1, W_SM0 = 2, W_VPROD = 10;  // warps 2-9: softmax (two groups of 4)
 constexpr int TILE = 2 * CH * 128;                  // one K or V stage: [2 channel halves][128 tokens][128 B]
 // lazy maximum (exp2 domain): the reference m is moved only when a score
 // passes it by more than SLACK, and then to the chunk's maximum plus HEAD, so
@@ -73,6 +73,7 @@ constexpr float PSCALE = 256.0f, PSCALE_INV = 1.0f / 256.0f;
 
 template <int N>
 struct Lay {
+    static constexpr int NR = N / 2;  // rows of one softmax group
     // tensor memory: SB buffers of S^T (2N columns: the hi and lo halves of
     // q'), then O^T as two channel tiles of 3N columns (one per P^T term)
     static constexpr int SB = (10 * N <= 512) ? 2 : 1;
@@ -94,7 +95,7 @@ struct Lay {
     static constexpr int RS_OFF = M_OFF + 4 * 64 * 4;
     static constexpr int VIS_OFF = RS_OFF + 2 * 64 * 4;
     static constexpr int RED_OFF = VIS_OFF + 2 * 64 * 4;     // [4][64] per-warp reductions
-    static constexpr int NEED_OFF = RED_OFF + 4 * 64 * 4;    // [2][4] votes
+    static constexpr int NEED_OFF = RED_OFF + 4 * 64 * 4;    // [2 groups][2][4] votes
     static constexpr int VBAD_OFF = NEED_OFF + 64;           // [NV] the chunk in V stage s had an invalid block id
     static constexpr int BAR_OFF = VBAD_OFF + 64;
     enum {
@@ -108,8 +109,8 @@ struct Lay {
         B_ODONE = B_PFULL + 2,           // [2] O^T += V^T P^T complete
         B_QFULL = B_ODONE + 2,           // q' of the piece staged
         B_OFREE = B_QFULL + 1,           // O^T of the previous piece read out
-        B_WG = B_OFREE + 1,              // the four softmax warps
-        B_MDONE = B_WG + 1,
+        B_WG = B_OFREE + 1,              // [2] the four warps of a softmax group
+        B_MDONE = B_WG + 2,
         NBARS = B_MDONE + 1
     };
     static constexpr int MISC_OFF = BAR_OFF + NBARS * 8;     // [0] tmem, [1] abort, [4] errors
@@ -157,7 +158,7 @@ __device__ __forceinline__ uint32_t tile_off(int t, int c) {
 
 // After a wait ran out: every piece of the CTA's share is NaN (outputs, or
 // partial log-sum-exps the combine turns into NaN rows).
-__device__ __noinline__ void e4tc_nan_share(const E4TcParams &P, long long x0, int npg, int ti) {
+__device__ __noinline__ void e4tc_nan_share(const E4TcParams &P, long long x0, int npg, int ti, int nth) {
     using namespace e4tc;
     const float NaN = __int_as_float(0x7fc00000);
     const long long kw = blockIdx.x;
@@ -169,7 +170,7 @@ __device__ __noinline__ void e4tc_nan_share(const E4TcParams &P, long long x0, i
             const int jq = r / P.G, h = u_ * P.G + r % P.G;
             if (complete) {
                 const size_t row = (((size_t)b_ * P.n + jq) * P.Hq + h) * D;
-                for (int d = ti; d < D; d += 128) {
+                for (int d = ti; d < D; d += nth) {
                     if (P.out_dtype == PA_F32) reinterpret_cast<float *>(P.out)[row + d] = NaN;
                     else if (P.out_dtype == PA_F16) reinterpret_cast<__half *>(P.out)[row + d] = __float2half_rn(NaN);
                     else reinterpret_cast<__nv_bfloat16 *>(P.out)[row + d] = __float2bfloat16_rn(NaN);
@@ -212,7 +213,7 @@ __global__ void __launch_bounds__(e4tc::THREADS, 1)
     int *vis_s = reinterpret_cast<int *>(smem + Y::VIS_OFF);
     float *red = reinterpret_cast<float *>(smem + Y::RED_OFF);
     volatile int *need = reinterpret_cast<volatile int *>(smem + Y::NEED_OFF);
-    constexpr int NK = Y::NK, NV = Y::NV, SB = Y::SB;
+    constexpr int NK = Y::NK, NV = Y::NV, SB = Y::SB, NR = Y::NR;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const float NaN = __int_as_float(0x7fc00000);
     const int U = P.Hkv;  // segments (kv heads) per request
@@ -238,8 +239,9 @@ __global__ void __launch_bounds__(e4tc::THREADS, 1)
         for (int i = 0; i < Y::NBARS; ++i) {
             uint32_t c = 1;
             if ((i >= Y::B_SFREE && i < Y::B_SFREE + 2) || (i >= Y::B_PFULL && i < Y::B_PFULL + 2) ||
-                i == Y::B_QFULL || i == Y::B_OFREE || i == Y::B_WG)
-                c = 4;
+                i == Y::B_QFULL || i == Y::B_OFREE)
+                c = 8;  // the eight softmax warps
+            if (i >= Y::B_WG && i < Y::B_WG + 2) c = 4;
             mbar_init(&bars[i], c);
         }
         misc[1] = 0;
@@ -395,10 +397,17 @@ __global__ void __launch_bounds__(e4tc::THREADS, 1)
         __syncwarp();
     } else {
         // ================================================== softmax, q' staging, epilogue
+        // two warpgroups, each owning half of the rows (S^T and O^T columns):
+        // rows are independent in the softmax, so each group votes, rescales
+        // and writes P^T for its own rows; one token per thread
+        const int wg = (warp - W_SM0) >> 2;
+        const int rb = wg * NR;                  // the group's first row
         const int qd = warp & 3;                 // tensor-memory lane quarter
         const int t = 32 * qd + lane;            // token of the chunk (S^T) / channel of a tile (O^T)
-        const int ti = t;                        // 0..127 across the four warps
+        const int ti = t;                        // 0..127 within the group
         const uint32_t tl = tmem + ((uint32_t)(32 * qd) << 16);
+        uint64_t *bwg = &bars[Y::B_WG + wg];
+        volatile int *needw = need + 8 * wg;
         const float ksc = (P.k_mode == PA_SCALE_TENSOR) ? P.k_scale[0] : 1.0f;
         const float vsc = (P.v_mode == PA_SCALE_TENSOR) ? P.v_scale[0] : 1.0f;
         Cursor cs = c0;
@@ -408,98 +417,93 @@ __global__ void __launch_bounds__(e4tc::THREADS, 1)
         int4 nx_R = P.req[c0.b];
         int pp = 0, mb = 0;  // buffer of the piece's row constants, running-maximum buffer
         bool pbad = false;
-        float lsum[N];
+        float lsum[NR];
 #pragma unroll
-        for (int r = 0; r < N; ++r) lsum[r] = 0.f;
+        for (int r = 0; r < NR; ++r) lsum[r] = 0.f;
         auto mrow = [&](int ppb, int mbb) -> float * { return m_s + (ppb * 2 + mbb) * 64; };
-        auto wg_sync = [&]() -> bool {  // the four softmax warps (bounded)
+        auto wg_sync = [&]() -> bool {  // the group's four warps (bounded)
             __syncwarp();
-            if (lane == 0) mbar_arrive(&bars[Y::B_WG]);
-            const bool ok = warp_wait_u(&bars[Y::B_WG], wg_phase & 1, abort, err);
+            if (lane == 0) mbar_arrive(bwg);
+            const bool ok = warp_wait_u(bwg, wg_phase & 1, abort, err);
             ++wg_phase;
             return ok;
         };
 
-        // q' of the segment (b, kv head u): TPR threads per row r load the row
-        // together (one round trip), agree on its largest magnitude, and write
-        // two exact E4M3 terms of q * 2^s_r (largest magnitude in [128, 256));
-        // the row's score scale and visible length go to the buffers of parity ppb
-        constexpr int TPR = (N <= 16) ? 8 : 4;       // threads per q row
-        constexpr int QW = 32 / TPR;                  // 16-byte words of the row per thread
-        constexpr int RPR = 128 / TPR;                // rows per round
-        constexpr int ROUNDS = (N + RPR - 1) / RPR;
+        // q' of the segment (b, kv head u) for the group's rows: TPR threads
+        // per row load it together (one round trip), agree on its largest
+        // magnitude, and write two exact E4M3 terms of q * 2^s_r (largest
+        // magnitude in [128, 256)); the row's score scale and visible length
+        // go to the buffers of parity ppb
+        constexpr int TPR = (NR <= 8) ? 16 : (NR <= 16) ? 8 : 4;  // threads per q row
+        constexpr int QW = 32 / TPR;                              // 16-byte words of the row per thread
+        static_assert(NR * TPR <= 128, "one round of q rows");
         auto stage_q = [&](int b, int u, int Lb, int ppb) {
-#pragma unroll 1
-            for (int rd = 0; rd < ROUNDS; ++rd) {
-                const int r = rd * RPR + ti / TPR, part = ti % TPR;
-                const bool rok = r < N && r < P.R;
-                const int jq = rok ? r / P.G : 0, h = u * P.G + (rok ? r % P.G : 0);
-                const uint4 *qrow =
-                    reinterpret_cast<const uint4 *>(P.q + 2 * ((((size_t)b * P.n + jq) * P.Hq + h) * D)) + part * QW;
-                uint4 v[QW];
+            const int r = rb + ti / TPR, part = ti % TPR;
+            const bool rok = ti / TPR < NR && r < P.R;
+            const int jq = rok ? r / P.G : 0, h = u * P.G + (rok ? r % P.G : 0);
+            const uint4 *qrow =
+                reinterpret_cast<const uint4 *>(P.q + 2 * ((((size_t)b * P.n + jq) * P.Hq + h) * D)) + part * QW;
+            uint4 v[QW];
 #pragma unroll
-                for (int i = 0; i < QW; ++i) v[i] = rok ? qrow[i] : make_uint4(0u, 0u, 0u, 0u);
-                float mx = 0.f;
+            for (int i = 0; i < QW; ++i) v[i] = rok ? qrow[i] : make_uint4(0u, 0u, 0u, 0u);
+            float mx = 0.f;
 #pragma unroll
-                for (int i = 0; i < QW; ++i) {
-                    const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+            for (int i = 0; i < QW; ++i) {
+                const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
+                for (int e = 0; e < 4; ++e) {
+                    const float2 f = q_pair2(w[e], P.q_dtype);
+                    mx = fmaxf(mx, fmaxf(fabsf(f.x), fabsf(f.y)));
+                }
+            }
+#pragma unroll
+            for (int o = TPR / 2; o >= 1; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+            int ex = 0;
+            const bool fin = mx > 0.f && mx < 3.0e38f;
+            if (fin) frexpf(mx, &ex);
+            const int sh = fin ? 8 - ex : 0;
+            const float up = pow2f(sh);
+            if (rok) {
+#pragma unroll
+                for (int cc = 0; cc < QW / 2; ++cc) {  // 16 channels = 16 bytes of each term
+                    const int c = part * (QW / 2) + cc;
+                    const uint32_t w[8] = {v[2 * cc].x,     v[2 * cc].y,     v[2 * cc].z,     v[2 * cc].w,
+                                           v[2 * cc + 1].x, v[2 * cc + 1].y, v[2 * cc + 1].z, v[2 * cc + 1].w};
+                    uint32_t hw[4] = {0u, 0u, 0u, 0u}, lw[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
                         const float2 f = q_pair2(w[e], P.q_dtype);
-                        mx = fmaxf(mx, fmaxf(fabsf(f.x), fabsf(f.y)));
+                        const float a = f.x * up, bb = f.y * up;
+                        const uint32_t h2 = f32x2_e4m3x2(a, bb);
+                        const float2 hf = e4m3x2_f32x2(h2);
+                        const uint32_t l2 = f32x2_e4m3x2(a - hf.x, bb - hf.y);
+                        hw[e >> 1] |= h2 << (16 * (e & 1));
+                        lw[e >> 1] |= l2 << (16 * (e & 1));
                     }
+                    // hi in row r, lo in row N + r of the half's [2N][128 B] tile
+                    const uint32_t off = (uint32_t)((c >> 3) * (2 * N * 128) + r * 128 + (((c & 7) ^ (r & 7)) << 4));
+                    *reinterpret_cast<uint4 *>(smem + Y::Q_OFF + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+                    *reinterpret_cast<uint4 *>(smem + Y::Q_OFF + N * 128 + off) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
                 }
-#pragma unroll
-                for (int o = TPR / 2; o >= 1; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-                int ex = 0;
-                const bool fin = mx > 0.f && mx < 3.0e38f;
-                if (fin) frexpf(mx, &ex);
-                const int sh = fin ? 8 - ex : 0;
-                const float up = pow2f(sh);
-                if (rok) {
-#pragma unroll
-                    for (int cc = 0; cc < QW / 2; ++cc) {  // 16 channels = 16 bytes of each term
-                        const int c = part * (QW / 2) + cc;
-                        const uint32_t w[8] = {v[2 * cc].x,     v[2 * cc].y,     v[2 * cc].z,     v[2 * cc].w,
-                                               v[2 * cc + 1].x, v[2 * cc + 1].y, v[2 * cc + 1].z, v[2 * cc + 1].w};
-                        uint32_t hw[4] = {0u, 0u, 0u, 0u}, lw[4] = {0u, 0u, 0u, 0u};
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) {
-                            const float2 f = q_pair2(w[e], P.q_dtype);
-                            const float a = f.x * up, bb = f.y * up;
-                            const uint32_t h2 = f32x2_e4m3x2(a, bb);
-                            const float2 hf = e4m3x2_f32x2(h2);
-                            const uint32_t l2 = f32x2_e4m3x2(a - hf.x, bb - hf.y);
-                            hw[e >> 1] |= h2 << (16 * (e & 1));
-                            lw[e >> 1] |= l2 << (16 * (e & 1));
-                        }
-                        // hi in row r, lo in row N + r of the half's [2N][128 B] tile
-                        const uint32_t off =
-                            (uint32_t)((c >> 3) * (2 * N * 128) + r * 128 + (((c & 7) ^ (r & 7)) << 4));
-                        *reinterpret_cast<uint4 *>(smem + Y::Q_OFF + off) = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-                        *reinterpret_cast<uint4 *>(smem + Y::Q_OFF + N * 128 + off) =
-                            make_uint4(lw[0], lw[1], lw[2], lw[3]);
-                    }
-                }
-                if (r < N && part == 0) {
-                    rs_s[ppb * 64 + r] = rok ? P.softmax_scale * ksc * LOG2E * pow2f(-sh) : 0.f;
-                    vis_s[ppb * 64 + r] = rok ? (P.causal ? Lb - (P.n - 1 - jq) : Lb) : 0;
-                    mrow(ppb, 0)[r] = -INFINITY;
-                    mrow(ppb, 1)[r] = -INFINITY;
-                }
+            }
+            if (ti / TPR < NR && part == 0) {
+                rs_s[ppb * 64 + r] = rok ? P.softmax_scale * ksc * LOG2E * pow2f(-sh) : 0.f;
+                vis_s[ppb * 64 + r] = rok ? (P.causal ? Lb - (P.n - 1 - jq) : Lb) : 0;
+                mrow(ppb, 0)[r] = -INFINITY;
+                mrow(ppb, 1)[r] = -INFINITY;
             }
         };
 
-        // the finished segment's output (or partial) from the three O^T partial
-        // sums and the row sums; its row constants are in the buffers of parity
-        // ppb, maxima in mbb
+        // the finished segment's output (or partial) for the group's rows from
+        // the three O^T partial sums and the row sums; its row constants are in
+        // the buffers of parity ppb, maxima in mbb
         auto epilogue = [&](int jl, int ppb, int mbb) -> bool {
 #pragma unroll
-            for (int r = 0; r < N; ++r) {  // row sums over the 128 tokens
-                float v = lsum[r];
+            for (int k = 0; k < NR; ++k) {  // row sums over the 128 tokens
+                float v = lsum[k];
 #pragma unroll
                 for (int o = 16; o >= 1; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-                if (lane == 0) red[qd * 64 + r] = v;
+                if (lane == 0) red[qd * 64 + rb + k] = v;
             }
             if (!wg_sync()) return false;
             if (!warp_wait_u(&bars[Y::B_ODONE + (jl & 1)], (jl >> 1) & 1, abort, err)) return false;
@@ -507,8 +511,8 @@ __global__ void __launch_bounds__(e4tc::THREADS, 1)
             const bool complete = (p0 == 0 && last_p == pPb - 1);
             const long long slot_id = (long long)pb * U + pq + kw;
             auto row_l = [&](int r) -> float { return (red[r] + red[64 + r]) + (red[128 + r] + red[192 + r]); };
-            if (ti < N && ti < P.R) {
-                const int r = ti;
+            if (ti < NR && rb + ti < P.R) {
+                const int r = rb + ti;
                 const float l = row_l(r);
                 float lse_v = l > 0.f ? (mrow(ppb, mbb)[r] + lg2(l)) * LN2 : -INFINITY;
                 if (pbad) lse_v = NaN;
@@ -524,16 +528,16 @@ __global__ void __launch_bounds__(e4tc::THREADS, 1)
             for (int i = 0; i < 2; ++i) {
                 const int d = 128 * i + t;
 #pragma unroll 1
-                for (int r0 = 0; r0 < N; r0 += 16) {
-                    uint32_t a[16], b2[16], c2[16];
-                    const uint32_t ta = tl + TM_O + (uint32_t)(3 * N * i + r0);
-                    tmem_ld16_nowait(ta, a);
-                    tmem_ld16_nowait(ta + N, b2);
-                    tmem_ld16_nowait(ta + 2 * N, c2);
+                for (int g = 0; g < NR; g += 8) {
+                    uint32_t a[8], b2[8], c2[8];
+                    const uint32_t ta = tl + TM_O + (uint32_t)(3 * N * i + rb + g);
+                    tmem_ld8_nowait(ta, a);
+                    tmem_ld8_nowait(ta + N, b2);
+                    tmem_ld8_nowait(ta + 2 * N, c2);
                     tmem_ld_wait();
 #pragma unroll
-                    for (int k = 0; k < 16; ++k) {
-                        const int r = r0 + k;
+                    for (int k = 0; k < 8; ++k) {
+                        const int r = rb + g + k;
                         if (r >= P.R) break;
                         const float l = row_l(r);
                         const float o = (__uint_as_float(a[k]) + __uint_as_float(b2[k])) + __uint_as_float(c2[k]);
@@ -590,7 +594,7 @@ __global__ void __launch_bounds__(e4tc::THREADS, 1)
                 if (Rq.w != 0) { pbad = true; err |= PA_DEV_ERR_CONTEXT_LEN; }
                 if (L != Rq.x) { pbad = true; err |= PA_DEV_ERR_STALE_PLAN; }
 #pragma unroll
-                for (int r = 0; r < N; ++r) lsum[r] = 0.f;
+                for (int k = 0; k < NR; ++k) lsum[k] = 0.f;
                 {
                     // the segment after this one: its record now, its q rows into L2
                     const int nb = pq + 1 < U ? pb : pb + 1, nq = pq + 1 < U ? pq + 1 : 0;
@@ -600,8 +604,8 @@ __global__ void __launch_bounds__(e4tc::THREADS, 1)
                             nx_L = P.context_lens[nb];
                             nx_R = P.req[nb];
                         }
-                        for (int i = ti; i < 4 * N; i += 128) {
-                            const int rr = i >> 2;
+                        for (int i = ti; i < 4 * NR; i += 128) {
+                            const int rr = rb + (i >> 2);
                             if (rr < P.R) {
                                 const int jq = rr / P.G, h = nq * P.G + rr % P.G;
                                 const uint8_t *qa = P.q + 2 * ((((size_t)nb * P.n + jq) * P.Hq + h) * D) + 128 * (i & 3);
@@ -614,64 +618,66 @@ __global__ void __launch_bounds__(e4tc::THREADS, 1)
             }
             if (!warp_wait_u(&bars[Y::B_SFULL + sbuf], (j / SB) & 1, abort, err)) { alive = false; break; }
             tc_fence_after();
-            float x[N];
+            float x[NR];
+            {
+                uint32_t hi[NR], lo[NR];
 #pragma unroll
-            for (int r0 = 0; r0 < N; r0 += 16) {
-                uint32_t hi[16], lo[16];
-                const uint32_t ta = tl + TM_S + (uint32_t)(2 * N * sbuf + r0);
-                tmem_ld16_nowait(ta, hi);
-                tmem_ld16_nowait(ta + N, lo);
+                for (int g = 0; g < NR; g += 8) {
+                    const uint32_t ta = tl + TM_S + (uint32_t)(2 * N * sbuf + rb + g);
+                    tmem_ld8_nowait(ta, hi + g);
+                    tmem_ld8_nowait(ta + N, lo + g);
+                }
                 tmem_ld_wait();
 #pragma unroll
-                for (int k = 0; k < 16; ++k) x[r0 + k] = __uint_as_float(hi[k]) + __uint_as_float(lo[k]);
+                for (int k = 0; k < NR; ++k) x[k] = __uint_as_float(hi[k]) + __uint_as_float(lo[k]);
             }
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&bars[Y::B_SFREE + sbuf]);
             const int tok = cs.p * CH + t;
-            const float *mc = mrow(pp, mb);
-            const float *rsp = rs_s + pp * 64;
+            const float *mc = mrow(pp, mb) + rb;
+            const float *rsp = rs_s + pp * 64 + rb;
             bool exceed = false;
             if (cs.p * CH + CH <= vmin) {  // every row sees every token of the chunk
 #pragma unroll
-                for (int r = 0; r < N; ++r) {
-                    x[r] *= rsp[r];
-                    exceed |= x[r] > mc[r] + SLACK;  // also true for a finite score and m = -inf
+                for (int k = 0; k < NR; ++k) {
+                    x[k] *= rsp[k];
+                    exceed |= x[k] > mc[k] + SLACK;  // also true for a finite score and m = -inf
                 }
             } else {
-                const int *vp = vis_s + pp * 64;
+                const int *vp = vis_s + pp * 64 + rb;
 #pragma unroll
-                for (int r = 0; r < N; ++r) {
-                    x[r] = (tok < vp[r]) ? x[r] * rsp[r] : -INFINITY;
-                    exceed |= x[r] > mc[r] + SLACK;
+                for (int k = 0; k < NR; ++k) {
+                    x[k] = (tok < vp[k]) ? x[k] * rsp[k] : -INFINITY;
+                    exceed |= x[k] > mc[k] + SLACK;
                 }
             }
             const int vote = __any_sync(0xffffffffu, exceed) ? 1 : 0;
-            if (lane == 0) need[pbuf * 4 + qd] = vote;
+            if (lane == 0) needw[pbuf * 4 + qd] = vote;
             if (!wg_sync()) { alive = false; break; }
-            const bool resc = (need[pbuf * 4] | need[pbuf * 4 + 1] | need[pbuf * 4 + 2] | need[pbuf * 4 + 3]) != 0;
+            const bool resc = (needw[pbuf * 4] | needw[pbuf * 4 + 1] | needw[pbuf * 4 + 2] | needw[pbuf * 4 + 3]) != 0;
             if (resc) {
                 // new row maxima over the chunk's 128 tokens, into the other buffer
 #pragma unroll
-                for (int r = 0; r < N; ++r) {
-                    float v = x[r];
+                for (int k = 0; k < NR; ++k) {
+                    float v = x[k];
 #pragma unroll
                     for (int o = 16; o >= 1; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-                    if (lane == 0) red[qd * 64 + r] = v;
+                    if (lane == 0) red[qd * 64 + rb + k] = v;
                 }
                 if (!wg_sync()) { alive = false; break; }
-                float *mn_s = mrow(pp, mb ^ 1);
-                if (ti < N) {
-                    const int r = ti;
-                    const float mo = mc[r];
+                float *mn_s = mrow(pp, mb ^ 1) + rb;
+                if (ti < NR) {
+                    const int r = rb + ti;
+                    const float mo = mc[ti];
                     const float cm = fmaxf(fmaxf(red[r], red[64 + r]), fmaxf(red[128 + r], red[192 + r]));
-                    mn_s[r] = (mo == -INFINITY || cm > mo + SLACK) ? fmaxf(cm + HEAD, mo) : mo;
+                    mn_s[ti] = (mo == -INFINITY || cm > mo + SLACK) ? fmaxf(cm + HEAD, mo) : mo;
                 }
                 if (!wg_sync()) { alive = false; break; }
 #pragma unroll
-                for (int r = 0; r < N; ++r) {
-                    const float mo = mc[r], mn = mn_s[r];
-                    lsum[r] *= (mn == mo) ? 1.f : ex2(mo - mn);
+                for (int k = 0; k < NR; ++k) {
+                    const float mo = mc[k], mn = mn_s[k];
+                    lsum[k] *= (mn == mo) ? 1.f : ex2(mo - mn);
                 }
                 // O^T (channels on lanes, rows on columns, three partial sums per
                 // tile) takes the same factors once the previous chunk's O MMAs
@@ -684,24 +690,18 @@ __global__ void __launch_bounds__(e4tc::THREADS, 1)
                     tc_fence_after();
 #pragma unroll 1
                     for (int i = 0; i < 6; ++i) {  // (tile, term)
+#pragma unroll 1
+                        for (int g = 0; g < NR; g += 8) {
+                            uint32_t w[8];
+                            const uint32_t ta = tl + TM_O + (uint32_t)(N * i + rb + g);
+                            tmem_ld8_nowait(ta, w);
+                            tmem_ld_wait();
 #pragma unroll
-                        for (int r0 = 0; r0 < N; r0 += 16) {
-                            float o[16];
-                            const uint32_t ta = tl + TM_O + (uint32_t)(N * i + r0);
-                            tmem_ld16(ta, o);
-                            uint32_t w[16];
-#pragma unroll
-                            for (int k = 0; k < 16; ++k) {
-                                const float mo = mc[r0 + k], mn = mn_s[r0 + k];
-                                w[k] = __float_as_uint(o[k] * ((mn == mo) ? 1.f : ex2(mo - mn)));
+                            for (int k = 0; k < 8; ++k) {
+                                const float mo = mc[g + k], mn = mn_s[g + k];
+                                w[k] = __float_as_uint(__uint_as_float(w[k]) * ((mn == mo) ? 1.f : ex2(mo - mn)));
                             }
-                            asm volatile(
-                                "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,"
-                                "%13,%14,%15,%16};" ::"r"(ta),
-                                "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]),
-                                "r"(w[7]), "r"(w[8]), "r"(w[9]), "r"(w[10]), "r"(w[11]), "r"(w[12]), "r"(w[13]),
-                                "r"(w[14]), "r"(w[15])
-                                : "memory");
+                            tmem_st8_u(ta, w);
                         }
                     }
                     tmem_st_wait();
@@ -716,28 +716,31 @@ __global__ void __launch_bounds__(e4tc::THREADS, 1)
             }
             // V of the chunk has landed: flag invalid block ids, and zero the V
             // rows past the request's length (uncopied, or slots of the last
-            // block that may hold NaN codes), so that 0 * NaN cannot reach O^T
+            // block that may hold NaN codes), so that 0 * NaN cannot reach O^T;
+            // each group zeroes one 128-channel half of the row
             if (!warp_wait_u(&bars[Y::B_VFULL + vslot], (j / NV) & 1, abort, err)) { alive = false; break; }
             if (vbad[vslot]) { pbad = true; err |= PA_DEV_ERR_BLOCK_ID; }
             if (tok >= L) {
                 uint8_t *vrow = smem + Y::V_OFF + vslot * TILE;
 #pragma unroll
-                for (int c = 0; c < 16; ++c) *reinterpret_cast<uint4 *>(vrow + tile_off(t, c)) = make_uint4(0, 0, 0, 0);
+                for (int c = 8 * wg; c < 8 * wg + 8; ++c)
+                    *reinterpret_cast<uint4 *>(vrow + tile_off(t, c)) = make_uint4(0u, 0u, 0u, 0u);
             }
             // P^T = 2^(x - m) * 2^8 as three E4M3 terms of 4 significant bits
             // each (rows in pairs, one conversion per pair and term)
             uint8_t *pt = smem + Y::P_OFF + pbuf * Y::P_BUF;
-            const float *mcur = mrow(pp, mb);
+            const float *mcur = mrow(pp, mb) + rb;
 #pragma unroll
-            for (int r = 0; r < N; r += 2) {
-                const float ma = mcur[r], mb2 = mcur[r + 1];
-                const float pa0 = ex2(x[r] - ((ma == -INFINITY) ? 0.f : ma));
-                const float pb0 = ex2(x[r + 1] - ((mb2 == -INFINITY) ? 0.f : mb2));
-                lsum[r] += pa0;
-                lsum[r + 1] += pb0;
-                float ra, rb, sa, sb2;
-                const float ha = split4(pa0 * PSCALE, ra), hb = split4(pb0 * PSCALE, rb);
-                const float ma1 = split4(ra, sa), mb1 = split4(rb, sb2);
+            for (int k = 0; k < NR; k += 2) {
+                const int r = rb + k;
+                const float ma = mcur[k], mb2 = mcur[k + 1];
+                const float pa0 = ex2(x[k] - ((ma == -INFINITY) ? 0.f : ma));
+                const float pb0 = ex2(x[k + 1] - ((mb2 == -INFINITY) ? 0.f : mb2));
+                lsum[k] += pa0;
+                lsum[k + 1] += pb0;
+                float ra, rb2, sa, sb2;
+                const float ha = split4(pa0 * PSCALE, ra), hb = split4(pb0 * PSCALE, rb2);
+                const float ma1 = split4(ra, sa), mb1 = split4(rb2, sb2);
                 const uint32_t ch = f32x2_e4m3x2(ha, hb), cm = f32x2_e4m3x2(ma1, mb1), cl = f32x2_e4m3x2(sa, sb2);
                 // K-major, 128-byte swizzle: row r of 128 tokens, 16-byte chunk
                 // t / 16 lands at (t / 16) ^ (r & 7)
@@ -757,7 +760,7 @@ __global__ void __launch_bounds__(e4tc::THREADS, 1)
             cursor_next(cs, P.req, P.B, U, P.mbps);
         }
         if (alive && piece >= 0 && !epilogue(npg - 1, pp, mb)) alive = false;
-        if (!alive) e4tc_nan_share(P, x0, npg, ti);
+        if (!alive) e4tc_nan_share(P, x0, npg, wg * 128 + ti, 256);
     }
 
     // ---- teardown
