@@ -110,11 +110,28 @@ KERNEL_SOURCES = {
     "fp4_rectify": ("pa_fp4.cu", "pa_attn.cuh", "pa_common.cuh", "pa_tc.cuh"),
     "tiny": ("pa_attn.cuh", "pa_common.cuh", "pa_attn_launch.cuh", "pa_attn_f16_d64.cu"),
     "bf16": ("pa_attn.cuh", "pa_common.cuh", "pa_attn_launch.cuh", "pa_attn_bf16_d128.cu"),
-    "e4m3": ("pa_attn.cuh", "pa_common.cuh", "pa_attn_launch.cuh", "pa_attn_e4m3_d256.cu"),
+    "e4m3": ("pa_e4m3_tc.cu", "pa_attn.cuh", "pa_common.cuh", "pa_tc.cuh"),
+    "verify": ("pa_e4m3_tc.cu", "pa_attn.cuh", "pa_common.cuh", "pa_tc.cuh"),
+    "sparse": ("pa_sparse.cu",),
     "int8": ("pa_attn.cuh", "pa_common.cuh", "pa_attn_launch.cuh", "pa_attn_int8_d128.cu"),
     "int4": ("pa_attn.cuh", "pa_common.cuh", "pa_attn_launch.cuh", "pa_attn_int4_d128_merged.cu"),
 }
 KERNEL_SOURCES.update({"insert_" + k: ("pa_insert.cu",) for k in ("tiny", "bf16", "e4m3", "int8", "int4", "latent")})
+
+
+def attention_kernel_name(w) -> str:
+    """The kernel pa_run launches for a workload (the dispatch rule of the C
+    library: E4M3 at head dim 256 with per-tensor or no scales, 16..64 query
+    rows per kv head in multiples of 16 and blocks of 16..128 tokens run on the
+    tensor-core kernel; the single-latent shape on the latent kernel; the rest
+    on the grouped warp-level kernel)."""
+    if w.v_is_k_prefix:
+        return "pa_latent_kernel"
+    R = (w.Hq // w.Hkv) * w.n
+    if (w.kv_dtype == "e4m3" and w.Dk == 256 and w.Dv == 256 and w.k_scale_mode in ("none", "tensor")
+            and w.v_scale_mode in ("none", "tensor") and R % 16 == 0 and 16 <= R <= 64 and w.bs in (16, 32, 64, 128)):
+        return "pa_e4m3_tc_kernel"
+    return "pa_attn_kernel"
 
 
 def _kernel_sha(workload: str) -> str:
@@ -364,7 +381,7 @@ def gpu_arm(args, name, rank, world, local_rank, check=None):
     traffic = _traffic(name)
     roofline = {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
                 "frac": round(achieved / peak, 4), "traffic": traffic,
-                "kernel": "pa_attn_kernel", "peak_source": f"{peak_kind} hbm_gbs",
+                "kernel": attention_kernel_name(w), "peak_source": f"{peak_kind} hbm_gbs",
                 "attn_ms": round(attn_avg, 5)}
     if w.v_is_k_prefix:
         # the latent path is a dense contraction: 2 (Dk + Dv) flops per
@@ -690,7 +707,7 @@ def sparse_arm(args, rank, world, local_rank):
         "query_rows_per_s": round(world * rows / (ms_per_step * 1e-3), 1),
         "pct_of_hbm_peak": round(100.0 * nbytes / (ms_per_step * 1e-3) / 1e9 / peak, 2),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
-                     "frac": round(achieved / peak, 4), "traffic": None, "kernel": "pa_sparse_attn_kernel",
+                     "frac": round(achieved / peak, 4), "traffic": _traffic("sparse"), "kernel": "pa_sparse_attn_kernel",
                      "peak_source": f"{peak_kind} hbm_gbs", "call_ms": round(call_avg, 5),
                      "note": "timed over the whole call (planner + attention); selected rows shared between "
                              "the query tokens of a request can hit L2"},

@@ -535,8 +535,12 @@ __global__ void __launch_bounds__(e4tc::THREADS, 1)
                     tmem_ld8_nowait(ta + N, b2);
                     tmem_ld8_nowait(ta + 2 * N, c2);
                     tmem_ld_wait();
+                    // row r = rb + g + k is query row jq, head pq G + hg: advanced one
+                    // row at a time instead of a division per element
+                    int jq = (rb + g) / P.G, hg = (rb + g) % P.G;
 #pragma unroll
-                    for (int k = 0; k < 8; ++k) {
+                    for (int k = 0; k < 8; ++k, ++hg) {
+                        if (hg == P.G) { hg = 0; ++jq; }
                         const int r = rb + g + k;
                         if (r >= P.R) break;
                         const float l = row_l(r);
@@ -544,7 +548,7 @@ __global__ void __launch_bounds__(e4tc::THREADS, 1)
                         float y = o * (l > 0.f ? PSCALE_INV / l : 0.f);
                         if (pbad) y = NaN;
                         if (complete) {
-                            const int jq = r / P.G, h = pq * P.G + r % P.G;
+                            const int h = pq * P.G + hg;
                             const size_t oi = (((size_t)pb * P.n + jq) * P.Hq + h) * D + d;
                             const float z = y * vsc;
                             if (P.out_dtype == PA_F32) reinterpret_cast<float *>(P.out)[oi] = z;

@@ -399,7 +399,7 @@ __global__ void __launch_bounds__(lat::THREADS, 1)
             const uint8_t *qrow = P.q + 2 * qbase;
             float mx = 0.f;
             if (rok) {
-#pragma unroll 1
+#pragma unroll 6
                 for (int c = 18 * half; c < 18 * half + 18; ++c) {
                     const uint4 v = *reinterpret_cast<const uint4 *>(qrow + 32 * c);
                     const uint4 w = *reinterpret_cast<const uint4 *>(qrow + 32 * c + 16);
@@ -418,7 +418,7 @@ __global__ void __launch_bounds__(lat::THREADS, 1)
             if (fin) frexpf(mx, &ex);
             const int s = fin ? 8 - ex : 0;
             const float up = pow2f(s);
-#pragma unroll 1
+#pragma unroll 3
             for (int c = 18 * half; c < 18 * half + 18; ++c) {
                 uint32_t hw[4] = {0u, 0u, 0u, 0u}, lw[4] = {0u, 0u, 0u, 0u};
                 if (rok) {
@@ -477,14 +477,18 @@ __global__ void __launch_bounds__(lat::THREADS, 1)
                 for (int half = 0; half < 2; ++half) {
                     float o[32];
                     tmem_ld32(tl + TM_O + 64u * i + 32u * half, o);
+                    // row r = r0 + 32 half + k is query row jq, head kvh G + g: both
+                    // advanced by one row at a time instead of a division per element
+                    int jq = (r0 + 32 * half) / P.G, g = (r0 + 32 * half) % P.G;
 #pragma unroll 4
-                    for (int k = 0; k < 32; ++k) {
+                    for (int k = 0; k < 32; ++k, ++g) {
+                        if (g == P.G) { g = 0; ++jq; }
                         const int rr = 32 * half + k;
                         const int r = r0 + rr;
                         if (r >= P.R) break;
                         const float y = o[k] * stat_f[rr];
                         if (complete) {
-                            const int jq = r / P.G, h = kvh * P.G + r % P.G;
+                            const int h = kvh * P.G + g;
                             const size_t oi = (((size_t)pb * P.n + jq) * P.Hq + h) * DV + d;
                             if (P.out_dtype == PA_F32) reinterpret_cast<float *>(P.out)[oi] = y;
                             else if (P.out_dtype == PA_F16) reinterpret_cast<__half *>(P.out)[oi] = __float2half_rn(y);
@@ -527,6 +531,17 @@ __global__ void __launch_bounds__(lat::THREADS, 1)
                 const int r = rblk * LROWS + row;
                 vis = (r < P.R && P.causal) ? L - (P.n - 1 - r / P.G) : L;
                 rowsc = rowsc_new;
+                {
+                    // the next segment's q rows of this row block into L2, so that its
+                    // q' staging reads L2 rather than DRAM
+                    const int nb = pq + 1 < U ? pb : pb + 1, nq = pq + 1 < U ? pq + 1 : 0;
+                    if (nb < P.B && r < P.R) {
+                        const int jq = r / P.G, h = nq * P.G + r % P.G;
+                        const uint8_t *qa = P.q + 2 * ((((size_t)nb * P.n + jq) * P.Hq + h) * DK) + 576 * half;
+#pragma unroll
+                        for (int k = 0; k < 5; ++k) asm volatile("prefetch.global.L2 [%0];" ::"l"(qa + 128 * k));
+                    }
+                }
                 m = -INFINITY;
                 lsum = 0.f;
                 E_set = false;
