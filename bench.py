@@ -559,7 +559,7 @@ def insert_arm(args, rank, world, local_rank):
         "pct_of_hbm_peak": round(100.0 * nbytes / (ms_per_step * 1e-3) / 1e9 / peak, 2),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": _traffic("insert_" + args.workload),
-                     "kernel": "pa_insert_kernel", "peak_source": f"{peak_kind} hbm_gbs",
+                     "kernel": "pa_insert_staged_kernel", "peak_source": f"{peak_kind} hbm_gbs",
                      "kernel_ms": round(kern_avg, 5)},
         "e2e": {"value": round(world * nbytes / (e2e_avg * 1e-3) / 1e9, 2), "unit": "GB/s",
                 "ms_per_step": round(e2e_avg, 5), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": 4},

@@ -13,13 +13,16 @@
 //    E4M3 NaN", Root cause: 0x7F / 0xFF are E4M3's NaN codes, so finite values
 //    past 448 saturate instead.
 //
-// The kernel is HBM-bound (16-byte vector loads of the new rows, one store of
-// 4-16 bytes per 8 channels): a grid-stride loop over up to 8 CTAs of 256
-// threads per SM, each warp split into row groups of 8, 16 or 32 lanes (the
-// smallest power of two that covers the row's 8-channel chunks, 32 for rows
-// longer than 256 channels).
-// Rows are ordered (token, plane, kv head), so the warps of a CTA write
-// neighbouring slots of the same blocks.
+// The kernel is HBM-bound.  The new rows of each plane are contiguous in
+// their source buffer, so each CTA (3 per SM, 256 threads) takes chunks of
+// up to 32 KB of them: one 1-D bulk copy per chunk into a two-stage shared-
+// memory ring, issued while the previous chunk is quantized, and the next
+// chunk's slots (length check, block id) resolved during the same wait.  Each
+// warp splits into row groups of 8, 16 or 32 lanes (the smallest power of two
+// that covers the row's 8-channel chunks, 32 for rows longer than 256
+// channels) that write one store of 4-16 bytes per 8 channels.  Rows are
+// ordered (token, plane, kv head), so the warps of a CTA write neighbouring
+// slots of the same blocks.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <stdint.h>
@@ -196,103 +199,266 @@ __device__ __forceinline__ Row locate(const InsertParams &P, int r, bool report)
     return w;
 }
 
-// NCK: 8-channel chunks per lane at most; UNR: row groups a warp loads
-// before it encodes any (more bytes in flight for short rows).
-template <int SRC, int KV, int NCK, int UNR>
-__global__ void __launch_bounds__(THREADS, NCK == 1 ? 4 : 2) pa_insert_kernel(const InsertParams P) {
-    const int lane = threadIdx.x & 31;
+// Staged variant: the new rows of each plane are contiguous in their source
+// buffer, so a CTA copies a chunk of up to STAGE_BYTES of them into shared
+// memory with one 1-D bulk copy while it quantizes the previous chunk (two
+// stages), and resolves the next chunk's slots (length, block id) during the
+// same wait.  Every wait is bounded; on a timeout the CTA sets
+// PA_DEV_ERR_TIMEOUT, stops, and waits (bounded) for its copies in flight.
+constexpr int STAGES = 2;
+constexpr int STAGE_BYTES = 32 * 1024;
+constexpr int MAX_CHUNK_ROWS = 512;
+constexpr unsigned long long WAIT_NS = 2000000000ull;
+
+__device__ __forceinline__ uint32_t su32(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+__device__ __forceinline__ bool wait_full(uint64_t *bar, uint32_t parity, volatile int *abort) {
+    const unsigned long long t0 = [] {
+        unsigned long long t;
+        asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+        return t;
+    }();
+    while (true) {
+        uint32_t ok;
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+            "selp.u32 %0, 1, 0, p;\n\t}"
+            : "=r"(ok)
+            : "r"(su32(bar)), "r"(parity)
+            : "memory");
+        if (ok) return true;
+        if (*abort) return false;
+        unsigned long long t;
+        asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+        if (t - t0 > WAIT_NS) return false;
+    }
+}
+
+struct Chunk {
+    int plane, r0, nrows;
+};
+
+__device__ __forceinline__ Chunk chunk_of(int c, int nch0, const int (&cr)[2], int rows_p) {
+    Chunk ch;
+    ch.plane = c < nch0 ? 0 : 1;
+    const int ci = c - (ch.plane ? nch0 : 0);
+    ch.r0 = ci * cr[ch.plane];
+    ch.nrows = min(cr[ch.plane], rows_p - ch.r0);
+    return ch;
+}
+
+template <int SRC>
+__device__ __forceinline__ void issue_chunk(const InsertParams &P, const Chunk &ch, uint8_t *dst, uint64_t *bar) {
+    const uint32_t bytes = (uint32_t)ch.nrows * P.D[ch.plane] * Src<SRC>::BYTES;  // rows are multiples of 16 B
+    const uint8_t *src = P.src[ch.plane] + (long long)ch.r0 * P.D[ch.plane] * Src<SRC>::BYTES;
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(su32(bar)), "r"(bytes) : "memory");
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                 ::"r"(su32(dst)), "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(su32(bar))
+                 : "memory");
+}
+
+// Slot of row i of a chunk: byte offset of its code row in its plane's pool,
+// or -1 when the contract check fails (flags raised here).
+__device__ __forceinline__ long long slot_of(const InsertParams &P, int plane, int rp) {
+    const int t = rp / P.Hkv;
+    const int g = rp - t * P.Hkv;
+    const int b = t / P.n;
+    const int j = t - b * P.n;
+    const int L = __ldg(P.context_lens + b);
+    if (L < P.n || L > P.max_ctx || (L - 1) / P.bs + 1 > P.mbps) {
+        if (j == 0 && g == 0 && plane == 0 && P.err) atomicOr(P.err, PA_DEV_ERR_CONTEXT_LEN);
+        return -1;
+    }
+    const int pos = L - P.n + j;
+    const int page = pos / P.bs;
+    const int slot = pos - page * P.bs;
+    const int blk = __ldg(P.block_table + (long long)b * P.mbps + page);
+    if (blk < 1 || blk >= P.num_blocks) {
+        if (g == 0 && plane == 0 && P.err) atomicOr(P.err, PA_DEV_ERR_BLOCK_ID);
+        return -1;
+    }
+    return (long long)blk * P.block_stride[plane] + (long long)(g * P.bs + slot) * P.row_bytes[plane];
+}
+
+template <int SRC, int KV, int NCK>
+__global__ void __launch_bounds__(THREADS, 3)
+pa_insert_staged_kernel(const InsertParams P, int cr0, int cr1, int nch0, int nch) {
+    extern __shared__ __align__(128) uint8_t stage[];                 // STAGES * STAGE_BYTES
+    __shared__ long long slots[STAGES][MAX_CHUNK_ROWS];
+    __shared__ __align__(8) uint64_t full[STAGES];
+    __shared__ int abort_flag;
+    const int tid = threadIdx.x, lane = tid & 31;
     const int lpr = 1 << P.lpr_log2;
     const int sub = lane & (lpr - 1);
-    const int rpw = 32 >> P.lpr_log2;  // rows per warp and group
-    const long long warp = ((long long)blockIdx.x * THREADS + threadIdx.x) >> 5;
-    const long long nwarps = ((long long)gridDim.x * THREADS) >> 5;
+    const int rows_per_pass = THREADS >> P.lpr_log2;
+    const int cr[2] = {cr0, cr1};  // indexed by plane
+    const int rows_p = P.B * P.n * P.Hkv;
     constexpr int BITS = (KV == PA_F16 || KV == PA_BF16) ? 16 : (KV == PA_INT4 ? 4 : 8);
-    for (long long base = warp * rpw * UNR; base < P.rows; base += nwarps * rpw * UNR) {
-        float x[UNR][NCK][8];
-        Row row[UNR];
+    if (tid == 0) {
+        for (int s = 0; s < STAGES; ++s)
+            asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(su32(&full[s])), "r"(1) : "memory");
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        abort_flag = 0;
+    }
+    __syncthreads();
+    const int first = blockIdx.x, step = gridDim.x;
+    if (first < nch) {
+        const Chunk ch = chunk_of(first, nch0, cr, rows_p);
+        if (tid == 0) issue_chunk<SRC>(P, ch, stage, &full[0]);
+        for (int i = tid; i < ch.nrows; i += THREADS) slots[0][i] = slot_of(P, ch.plane, ch.r0 + i);
+    }
+    int k = 0;
+    bool pending_next = false;
+    for (int c = first; c < nch; c += step, ++k) {
+        const int s = k & 1;
+        const Chunk ch = chunk_of(c, nch0, cr, rows_p);
+        const int nxt = c + step;
+        pending_next = nxt < nch;
+        if (pending_next) {  // stage s^1 and its slots were released by the barrier ending the previous iteration
+            const Chunk cn = chunk_of(nxt, nch0, cr, rows_p);
+            if (tid == 0) issue_chunk<SRC>(P, cn, stage + (s ^ 1) * STAGE_BYTES, &full[s ^ 1]);
+            for (int i = tid; i < cn.nrows; i += THREADS) slots[s ^ 1][i] = slot_of(P, cn.plane, cn.r0 + i);
+        }
+        if (!wait_full(&full[s], (uint32_t)(k >> 1) & 1u, &abort_flag)) abort_flag = 1;
+        __syncthreads();  // slots[s] written, abort decided
+        if (abort_flag) break;
+        const uint8_t *rows = stage + s * STAGE_BYTES;
+        const int D = P.D[ch.plane];
+        const int mode = P.mode[ch.plane];
+        const float *scale = P.scale[ch.plane];
+        uint8_t *pool = P.pool[ch.plane];
+        const int passes = (ch.nrows + rows_per_pass - 1) / rows_per_pass;
+        for (int pass = 0; pass < passes; ++pass) {
+            const int i = pass * rows_per_pass + (tid >> P.lpr_log2);
+            const bool in = i < ch.nrows;
+            float x[NCK][8];
 #pragma unroll
-        for (int u = 0; u < UNR; ++u) {
-            const long long r = base + u * rpw + (lane >> P.lpr_log2);
-            if (r < P.rows) {
-                row[u] = locate<SRC>(P, (int)r, sub == 0);
-            } else {
-                row[u].valid = false;
-                row[u].D = 0;
-            }
+            for (int kk = 0; kk < NCK; ++kk) {
+                const int cc = sub + kk * lpr;
+                if (in && cc * 8 < D) {
+                    const uint8_t *src = rows + ((long long)i * D + cc * 8) * Src<SRC>::BYTES;
+                    if constexpr (SRC == PA_F32) {
+                        const float4 a = *reinterpret_cast<const float4 *>(src);
+                        const float4 b = *reinterpret_cast<const float4 *>(src + 16);
+                        x[kk][0] = a.x; x[kk][1] = a.y; x[kk][2] = a.z; x[kk][3] = a.w;
+                        x[kk][4] = b.x; x[kk][5] = b.y; x[kk][6] = b.z; x[kk][7] = b.w;
+                    } else {
+                        const uint4 u = *reinterpret_cast<const uint4 *>(src);
+                        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
-            for (int k = 0; k < NCK; ++k) {
-                const int c = sub + k * lpr;
-                if (row[u].valid && c * 8 < row[u].D) {
-                    Src<SRC>::load8(row[u].src + (long long)c * 8 * Src<SRC>::BYTES, x[u][k]);
+                        for (int q = 0; q < 4; ++q) {
+                            if constexpr (SRC == PA_F16) {
+                                __half2 h;
+                                memcpy(&h, &w[q], 4);
+                                const float2 f = __half22float2(h);
+                                x[kk][2 * q] = f.x;
+                                x[kk][2 * q + 1] = f.y;
+                            } else {
+                                x[kk][2 * q] = __uint_as_float(w[q] << 16);
+                                x[kk][2 * q + 1] = __uint_as_float(w[q] & 0xFFFF0000u);
+                            }
+                        }
+                    }
                 } else {
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) x[u][k][i] = 0.f;
+                    for (int q = 0; q < 8; ++q) x[kk][q] = 0.f;
                 }
             }
-        }
-#pragma unroll
-        for (int u = 0; u < UNR; ++u) {
             float s_tok = 1.f;
-            if (P.any_token) {  // uniform: every lane of the warp reduces
+            if (P.any_token) {  // every lane of the warp takes part
                 float m = 0.f;
 #pragma unroll
-                for (int k = 0; k < NCK; ++k)
+                for (int kk = 0; kk < NCK; ++kk)
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) m = nan_max(fabsf(x[u][k][i]), m);
+                    for (int q = 0; q < 8; ++q) m = nan_max(fabsf(x[kk][q]), m);
                 for (int o = lpr >> 1; o > 0; o >>= 1) m = nan_max(__shfl_xor_sync(0xffffffffu, m, o), m);
                 s_tok = __fdiv_rn(m, 448.f);
                 if (s_tok == 0.f) s_tok = 1.f;
             }
-            const Row &w = row[u];
-            if (!w.valid) continue;
+            const long long off = in ? slots[s][i] : -1;
+            if (off < 0) continue;
+            const int rp = ch.r0 + i;
+            const int g = rp - (rp / P.Hkv) * P.Hkv;
+            uint8_t *dst = pool + off;
             float ts = 1.f;
-            if (w.mode == PA_SCALE_TENSOR) ts = __ldg(w.scale);
-            if (w.mode == PA_SCALE_TOKEN) ts = s_tok;
+            if (mode == PA_SCALE_TENSOR) ts = __ldg(scale);
+            if (mode == PA_SCALE_TOKEN) ts = s_tok;
 #pragma unroll
-            for (int k = 0; k < NCK; ++k) {
-                const int c = sub + k * lpr;
-                if (c * 8 >= w.D) continue;
+            for (int kk = 0; kk < NCK; ++kk) {
+                const int cc = sub + kk * lpr;
+                if (cc * 8 >= D) continue;
                 float y[8];
-                if (w.mode == PA_SCALE_NONE) {
+                if (mode == PA_SCALE_NONE) {
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) y[i] = x[u][k][i];
-                } else if (w.mode == PA_SCALE_CHANNEL) {
-                    const float4 *sp = reinterpret_cast<const float4 *>(w.scale + (long long)w.g * w.D + c * 8);
+                    for (int q = 0; q < 8; ++q) y[q] = x[kk][q];
+                } else if (mode == PA_SCALE_CHANNEL) {
+                    const float4 *sp = reinterpret_cast<const float4 *>(scale + (long long)g * D + cc * 8);
                     const float4 a = __ldg(sp), b = __ldg(sp + 1);
                     const float s8[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) y[i] = __fdiv_rn(x[u][k][i], s8[i]);
+                    for (int q = 0; q < 8; ++q) y[q] = __fdiv_rn(x[kk][q], s8[q]);
                 } else {
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) y[i] = __fdiv_rn(x[u][k][i], ts);
+                    for (int q = 0; q < 8; ++q) y[q] = __fdiv_rn(x[kk][q], ts);
                 }
-                store8<KV>(w.dst + c * BITS, y);
+                store8<KV>(dst + cc * BITS, y);
             }
-            if (w.mode == PA_SCALE_TOKEN && sub == 0) *w.tok_scale = s_tok;
+            if (mode == PA_SCALE_TOKEN && sub == 0) {
+                // the scale slot: after the block's codes, [Hkv][bs] fp32
+                const long long blk_off = off - (off % P.block_stride[ch.plane]);
+                const long long in_blk = off - blk_off;             // (g * bs + slot) * row_bytes
+                const int gs = (int)(in_blk / P.row_bytes[ch.plane]);
+                *reinterpret_cast<float *>(pool + blk_off + (long long)P.Hkv * P.bs * P.row_bytes[ch.plane] +
+                                           (long long)gs * 4) = s_tok;
+            }
+        }
+        __syncthreads();  // stage s and slots[s] free for the chunk after next
+    }
+    if (abort_flag && tid == 0) {
+        if (P.err) atomicOr(P.err, PA_DEV_ERR_TIMEOUT);
+        // copies still in flight on either stage: wait for them, bounded
+        // (chunk k on stage k & 1, and chunk k + 1 on the other stage if it was issued)
+        volatile int never = 0;
+        for (int d = 0; d < 2; ++d) {
+            const int kk = k + d;
+            if (d == 1 && !pending_next) break;
+            wait_full(&full[kk & 1], (uint32_t)(kk >> 1) & 1u, &never);
         }
     }
 }
 
 template <int SRC, int KV>
-cudaError_t launch_kv(const InsertParams &P, int nck, int ctas, cudaStream_t s) {
+cudaError_t launch_kv(const InsertParams &P, int nck, int ctas, int cr0, int cr1, int nch0, int nch, cudaStream_t s) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)ctas);
     cfg.blockDim = dim3(THREADS);
-    cfg.dynamicSmemBytes = 0;
+    cfg.dynamicSmemBytes = STAGES * STAGE_BYTES;
     cfg.stream = s;
-    if (nck == 1) return cudaLaunchKernelEx(&cfg, pa_insert_kernel<SRC, KV, 1, 2>, P);
-    if (nck == 4) return cudaLaunchKernelEx(&cfg, pa_insert_kernel<SRC, KV, 4, 1>, P);
-    return cudaLaunchKernelEx(&cfg, pa_insert_kernel<SRC, KV, 8, 1>, P);
+    if (nck == 1) {
+        cudaFuncSetAttribute(pa_insert_staged_kernel<SRC, KV, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             STAGES * STAGE_BYTES);
+        return cudaLaunchKernelEx(&cfg, pa_insert_staged_kernel<SRC, KV, 1>, P, cr0, cr1, nch0, nch);
+    }
+    if (nck == 4) {
+        cudaFuncSetAttribute(pa_insert_staged_kernel<SRC, KV, 4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             STAGES * STAGE_BYTES);
+        return cudaLaunchKernelEx(&cfg, pa_insert_staged_kernel<SRC, KV, 4>, P, cr0, cr1, nch0, nch);
+    }
+    cudaFuncSetAttribute(pa_insert_staged_kernel<SRC, KV, 8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         STAGES * STAGE_BYTES);
+    return cudaLaunchKernelEx(&cfg, pa_insert_staged_kernel<SRC, KV, 8>, P, cr0, cr1, nch0, nch);
 }
 
 template <int SRC>
-cudaError_t launch_src(const InsertParams &P, int kv, int nck, int ctas, cudaStream_t s) {
+cudaError_t launch_src(const InsertParams &P, int kv, int nck, int ctas, int cr0, int cr1, int nch0, int nch,
+                       cudaStream_t s) {
     switch (kv) {
-        case PA_F16: return launch_kv<SRC, PA_F16>(P, nck, ctas, s);
-        case PA_BF16: return launch_kv<SRC, PA_BF16>(P, nck, ctas, s);
-        case PA_E4M3: return launch_kv<SRC, PA_E4M3>(P, nck, ctas, s);
-        case PA_INT8: return launch_kv<SRC, PA_INT8>(P, nck, ctas, s);
-        case PA_INT4: return launch_kv<SRC, PA_INT4>(P, nck, ctas, s);
+        case PA_F16: return launch_kv<SRC, PA_F16>(P, nck, ctas, cr0, cr1, nch0, nch, s);
+        case PA_BF16: return launch_kv<SRC, PA_BF16>(P, nck, ctas, cr0, cr1, nch0, nch, s);
+        case PA_E4M3: return launch_kv<SRC, PA_E4M3>(P, nck, ctas, cr0, cr1, nch0, nch, s);
+        case PA_INT8: return launch_kv<SRC, PA_INT8>(P, nck, ctas, cr0, cr1, nch0, nch, s);
+        case PA_INT4: return launch_kv<SRC, PA_INT4>(P, nck, ctas, cr0, cr1, nch0, nch, s);
         default: return cudaErrorInvalidValue;
     }
 }
@@ -400,22 +566,27 @@ extern "C" PA_API pa_status pa_insert(const pa_problem *p, int32_t src_dtype, co
     P.lpr_log2 = lg;
     const int per_lane = (chunks + (1 << lg) - 1) >> lg;
     const int nck = per_lane <= 1 ? 1 : (per_lane <= 4 ? 4 : 8);
-    const int unr = nck == 1 ? 2 : 1;
 
     int sms = p->num_sms;
     if (sms == 0) {
         const pa_status st = sm_count(&sms);
         if (st != PA_OK) return st;
     }
-    const long long rows_per_cta = (long long)(THREADS / 32) * (32 >> lg) * unr;
-    const long long want = (rows + rows_per_cta - 1) / rows_per_cta;
-    const int ctas = (int)std::min<long long>(want, (long long)sms * (2048 / THREADS));
+    const int esize = src_dtype == PA_F32 ? 4 : 2;
+    int cr[2] = {1, 1}, nch_p[2] = {0, 0};
+    const int rows_p = (int)(rows / planes);
+    for (int i = 0; i < planes; ++i) {
+        cr[i] = std::min(MAX_CHUNK_ROWS, STAGE_BYTES / (Ds[i] * esize));
+        nch_p[i] = (rows_p + cr[i] - 1) / cr[i];
+    }
+    const int nch = nch_p[0] + nch_p[1];
+    const int ctas = std::min(nch, sms * 3);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     cudaError_t e;
     switch (src_dtype) {
-        case PA_F32: e = launch_src<PA_F32>(P, p->kv_dtype, nck, ctas, s); break;
-        case PA_F16: e = launch_src<PA_F16>(P, p->kv_dtype, nck, ctas, s); break;
-        default: e = launch_src<PA_BF16>(P, p->kv_dtype, nck, ctas, s); break;
+        case PA_F32: e = launch_src<PA_F32>(P, p->kv_dtype, nck, ctas, cr[0], cr[1], nch_p[0], nch, s); break;
+        case PA_F16: e = launch_src<PA_F16>(P, p->kv_dtype, nck, ctas, cr[0], cr[1], nch_p[0], nch, s); break;
+        default: e = launch_src<PA_BF16>(P, p->kv_dtype, nck, ctas, cr[0], cr[1], nch_p[0], nch, s); break;
     }
     return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }

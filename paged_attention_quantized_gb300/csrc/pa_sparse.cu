@@ -18,10 +18,12 @@
 //      ids.
 //  pa_sparse_attn_kernel  one CTA per (query token, kv head): its G heads
 //      share the token list.  Four warps take contiguous quarters of the
-//      list; per token the warp loads the K and V rows coalesced (lane i
-//      holds channels [i*D/32, (i+1)*D/32)), dequantizes them in fp32, forms
-//      the G scores with a shuffle reduction and updates an fp32 online
-//      softmax; the quarters are merged in warp order.  All arithmetic is
+//      list, in groups of 2 or 4 tokens: the list entries, block ids and K
+//      and V rows of a group are loaded together (coalesced: lane i holds
+//      channels [i*D/32, (i+1)*D/32)), so their latencies overlap; the rows
+//      are dequantized in fp32, the G scores formed with shuffle reductions
+//      and an fp32 online softmax updated once per head and group; the
+//      quarters are merged in warp order.  All arithmetic is
 //      fp32 (the per-channel K scale is applied to q in fp32, so no fold can
 //      overflow), there are no waits, and every index is checked before use.
 #include <cuda_bf16.h>
@@ -227,42 +229,79 @@ __global__ void __launch_bounds__(ATTN_THREADS) pa_sparse_attn_kernel(const Spar
     const int hi = (int)((long long)total * (warp + 1) / ATTN_WARPS);
     const int32_t *list = P.lists + (long long)bj * P.top_k;
     const int32_t *tab = P.block_table + (long long)b * P.mbps;
-    for (int idx = lo; idx < hi; ++idx) {
-        const int t = __ldg(list + idx);               // the same for every lane
-        const int blk = __ldg(tab + t / P.bs);          // t < L, and the plan checked L's pages fit the table
-        if (blk < 1 || blk >= P.num_blocks) {
-            bad = true;
-            continue;
+    // groups of TK tokens: the list entries, block ids and rows of a group are
+    // loaded together, then one rescale per head and group
+    constexpr int TK = NH >= 16 ? 2 : 4;
+    for (int idx0 = lo; idx0 < hi; idx0 += TK) {
+        int t[TK], blk[TK];
+        bool ok[TK];
+#pragma unroll
+        for (int u = 0; u < TK; ++u) t[u] = idx0 + u < hi ? __ldg(list + idx0 + u) : -1;
+#pragma unroll
+        for (int u = 0; u < TK; ++u) {
+            blk[u] = t[u] >= 0 ? __ldg(tab + t[u] / P.bs) : 0;  // t < L: the table holds its page
+            ok[u] = t[u] >= 0 && blk[u] >= 1 && blk[u] < P.num_blocks;
+            if (t[u] >= 0 && !ok[u]) bad = true;
         }
-        const int slot = t - (t / P.bs) * P.bs;
-        const long long row_off = (long long)(g * P.bs + slot) * P.row_bytes + lane * LB;
-        const uint8_t *kb = P.k_pool + (long long)blk * P.k_block;
-        const uint8_t *vb = P.v_pool + (long long)blk * P.v_block;
-        uint32_t kw[4], vw[4];
-        load_codes<KV, CPL>(kb + row_off, kw);
-        load_codes<KV, CPL>(vb + row_off, vw);
-        float ks = 1.f, vs = 1.f;
-        if (P.k_mode == PA_SCALE_TOKEN) ks = __ldg(reinterpret_cast<const float *>(kb + P.k_codes) + g * P.bs + slot);
-        if (P.v_mode == PA_SCALE_TOKEN) vs = __ldg(reinterpret_cast<const float *>(vb + P.v_codes) + g * P.bs + slot);
-        float kx[CPL], vx[CPL];
-        decode<KV, CPL>(kw, kx);
-        decode<KV, CPL>(vw, vx);
+        uint32_t kw[TK][4], vw[TK][4];
+        float ks[TK], vs[TK];
+#pragma unroll
+        for (int u = 0; u < TK; ++u) {
+            ks[u] = vs[u] = 1.f;
+            if (!ok[u]) {
+                kw[u][0] = kw[u][1] = kw[u][2] = kw[u][3] = 0u;
+                vw[u][0] = vw[u][1] = vw[u][2] = vw[u][3] = 0u;
+                continue;
+            }
+            const int slot = t[u] - (t[u] / P.bs) * P.bs;
+            const long long row_off = (long long)(g * P.bs + slot) * P.row_bytes + lane * LB;
+            const uint8_t *kb = P.k_pool + (long long)blk[u] * P.k_block;
+            const uint8_t *vb = P.v_pool + (long long)blk[u] * P.v_block;
+            load_codes<KV, CPL>(kb + row_off, kw[u]);
+            load_codes<KV, CPL>(vb + row_off, vw[u]);
+            if (P.k_mode == PA_SCALE_TOKEN) ks[u] = __ldg(reinterpret_cast<const float *>(kb + P.k_codes) + g * P.bs + slot);
+            if (P.v_mode == PA_SCALE_TOKEN) vs[u] = __ldg(reinterpret_cast<const float *>(vb + P.v_codes) + g * P.bs + slot);
+        }
+        float sc[TK][NH];
+#pragma unroll
+        for (int u = 0; u < TK; ++u) {
+            float kx[CPL];
+            decode<KV, CPL>(kw[u], kx);
+#pragma unroll
+            for (int h = 0; h < NH; ++h) {
+                sc[u][h] = -INFINITY;
+                if (h >= G) continue;
+                float s = 0.f;
+#pragma unroll
+                for (int i = 0; i < CPL; ++i) s = fmaf(qv[h][i], kx[i], s);
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+                if (ok[u]) sc[u][h] = s * ks[u];
+            }
+        }
+        float vx[TK][CPL];
+#pragma unroll
+        for (int u = 0; u < TK; ++u) decode<KV, CPL>(vw[u], vx[u]);
 #pragma unroll
         for (int h = 0; h < NH; ++h) {
             if (h >= G) break;
-            float s = 0.f;
+            float gm = sc[0][h];
 #pragma unroll
-            for (int i = 0; i < CPL; ++i) s = fmaf(qv[h][i], kx[i], s);
+            for (int u = 1; u < TK; ++u) gm = fmaxf(gm, sc[u][h]);
+            const float mn = fmaxf(m[h], gm);
+            if (mn == -INFINITY) continue;               // nothing visible yet
+            const float corr = expf(m[h] - mn);         // 0 while m = -inf
+            l[h] *= corr;
 #pragma unroll
-            for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
-            s *= ks;
-            const float mn = fmaxf(m[h], s);
-            const float corr = expf(m[h] - mn);         // 0 for the first token (m = -inf)
-            const float p = expf(s - mn);
-            l[h] = l[h] * corr + p;
-            const float pv = p * vs;
+            for (int i = 0; i < CPL; ++i) o[h][i] *= corr;
 #pragma unroll
-            for (int i = 0; i < CPL; ++i) o[h][i] = fmaf(pv, vx[i], o[h][i] * corr);
+            for (int u = 0; u < TK; ++u) {
+                const float p = expf(sc[u][h] - mn);    // 0 for a skipped token
+                l[h] += p;
+                const float pv = p * vs[u];
+#pragma unroll
+                for (int i = 0; i < CPL; ++i) o[h][i] = fmaf(pv, vx[u][i], o[h][i]);
+            }
             m[h] = mn;
         }
     }
