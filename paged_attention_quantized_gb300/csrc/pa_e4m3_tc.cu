@@ -26,18 +26,18 @@
 // piece, whole pieces write `out`, cut ones a normalised partial for the
 // combine (one segment per kv head: all R rows).
 //
-// Roles (7 warps):
-//  * warps 0 and 6 copy K and V of each chunk into their own rings (tensor
-//    copies of one block's 128-channel half, 128-byte swizzled: the K-major
+// Roles (3 + 4 G warps, G = 2 softmax groups, 4 at 64 rows):
+//  * warp 0 and the last warp copy K and V of each chunk into their own rings
+//    (tensor copies of one block's 128-channel half, 128-byte swizzled: the K-major
 //    operand layout), with an L2 evict-first policy since every page is read
 //    once; K is released as soon as the chunk's S MMAs are done, V after its
 //    O MMAs.  Blocks past the request's length and blocks with an invalid id
 //    are not copied;
 //  * warp 1 issues the MMAs: S(j+1) before O(j), so the tensor pipe works
 //    while chunk j's softmax runs;
-//  * warps 2-5 (one token per thread: S^T has tokens on the tensor-memory
-//    lanes) run the online softmax in the exp2 domain with a lazy reference
-//    maximum (a chunk reduces the maxima across the 128 tokens, and rescales
+//  * warps 2 .. 4G+1, G groups of four (one token per thread: S^T has tokens
+//    on the tensor-memory lanes; each group owns R/G rows) run the online
+//    softmax in the exp2 domain with a lazy reference maximum (a chunk reduces the maxima across the 128 tokens, and rescales
 //    O^T, only when some score passes its row's reference by more than 0.75;
 //    the reference then moves to one above the chunk's maximum), zero the V
 //    rows past the request's length before the chunk's O MMAs (uncopied rows,
@@ -59,21 +59,23 @@ namespace e4tc {
 using namespace tc;
 
 constexpr int D = 256, CH = 128;  // head dim, tokens per chunk
-constexpr int NWARPS = 11, THREADS = NWARPS * 32;
-constexpr int W_KPROD = 0, W_MMA = 1, W_SM0 = 2, W_VPROD = 10;  // warps 2-9: softmax (two groups of 4)
+constexpr int W_KPROD = 0, W_MMA = 1, W_SM0 = 2;  // then the softmax groups of 4 warps, then the V producer
 constexpr int TILE = 2 * CH * 128;                  // one K or V stage: [2 channel halves][128 tokens][128 B]
 // lazy maximum (exp2 domain): the reference m is moved only when a score
 // passes it by more than SLACK, and then to the chunk's maximum plus HEAD, so
 // that p = 2^(s - m) stays below 2^SLACK and a new maximum must climb
-// HEAD + SLACK before O^T is rescaled again; P^T is stored as p * 2^8 (at most
-// 431 < 448) so that weights down to 2^-14 of the maximum are E4M3 normals in
-// every term
+// HEAD + SLACK before O^T is rescaled again; P^T is stored as p * 2^8 =
+// 2^(s - m + 8) (at most 431 < 448) so that weights down to 2^-14 of the
+// maximum are E4M3 normals in every term; the row sums carry the same 2^8
 constexpr float SLACK = 0.75f, HEAD = 1.0f;
-constexpr float PSCALE = 256.0f, PSCALE_INV = 1.0f / 256.0f;
+constexpr float PSHIFT = 8.0f;
 
 template <int N>
 struct Lay {
-    static constexpr int NR = N / 2;  // rows of one softmax group
+    static constexpr int NWG = (N >= 64) ? 4 : 2;   // softmax warpgroups, each owning NR rows
+    static constexpr int NR = N / NWG;
+    static constexpr int W_VPROD = W_SM0 + 4 * NWG;
+    static constexpr int NWARPS = W_VPROD + 1, THREADS = NWARPS * 32;
     // tensor memory: SB buffers of S^T (2N columns: the hi and lo halves of
     // q'), then O^T as two channel tiles of 3N columns (one per P^T term)
     static constexpr int SB = (10 * N <= 512) ? 2 : 1;
@@ -95,8 +97,9 @@ struct Lay {
     static constexpr int RS_OFF = M_OFF + 4 * 64 * 4;
     static constexpr int VIS_OFF = RS_OFF + 2 * 64 * 4;
     static constexpr int RED_OFF = VIS_OFF + 2 * 64 * 4;     // [4][64] per-warp reductions
-    static constexpr int NEED_OFF = RED_OFF + 4 * 64 * 4;    // [2 groups][2][4] votes
-    static constexpr int VBAD_OFF = NEED_OFF + 64;           // [NV] the chunk in V stage s had an invalid block id
+    static constexpr int NEED_OFF = RED_OFF + 4 * 64 * 4;    // [4 groups][2][4] votes
+    static constexpr int ALPHA_OFF = NEED_OFF + 128;         // [64] O^T factors of a rescale
+    static constexpr int VBAD_OFF = ALPHA_OFF + 256;           // [NV] the chunk in V stage s had an invalid block id
     static constexpr int BAR_OFF = VBAD_OFF + 64;
     enum {
         B_KFULL = 0,                     // [3] K of a chunk landed (tensor copies)
@@ -109,8 +112,8 @@ struct Lay {
         B_ODONE = B_PFULL + 2,           // [2] O^T += V^T P^T complete
         B_QFULL = B_ODONE + 2,           // q' of the piece staged
         B_OFREE = B_QFULL + 1,           // O^T of the previous piece read out
-        B_WG = B_OFREE + 1,              // [2] the four warps of a softmax group
-        B_MDONE = B_WG + 2,
+        B_WG = B_OFREE + 1,              // [4] the four warps of a softmax group
+        B_MDONE = B_WG + 4,
         NBARS = B_MDONE + 1
     };
     static constexpr int MISC_OFF = BAR_OFF + NBARS * 8;     // [0] tmem, [1] abort, [4] errors
@@ -132,12 +135,11 @@ __device__ __forceinline__ float2 e4m3x2_f32x2(uint32_t two) {
     return __half22float2(*reinterpret_cast<const __half2 *>(&h));
 }
 
-// Splits x into a + r with a rounded to 4 significant bits and r = x - a
-// exact (Veltkamp's splitting with the constant 2^20 + 1; the operations are
-// kept apart so that no multiply-add contracts them)
+// Splits x >= 0 into a + r with a = x truncated to 4 significant bits (sign,
+// exponent and the top 3 stored mantissa bits kept) and r = x - a, exact in
+// fp32 (x and a share their exponent)
 __device__ __forceinline__ float split4(float x, float &r) {
-    const float t = __fmul_rn(x, 1048577.0f);
-    const float a = __fsub_rn(t, __fsub_rn(t, x));
+    const float a = __uint_as_float(__float_as_uint(x) & 0xFFF00000u);
     r = __fsub_rn(x, a);
     return a;
 }
@@ -197,7 +199,7 @@ __device__ __noinline__ void e4tc_nan_share(const E4TcParams &P, long long x0, i
 }
 
 template <int N>
-__global__ void __launch_bounds__(e4tc::THREADS, 1)
+__global__ void __launch_bounds__(e4tc::Lay<N>::THREADS, 1)
     pa_e4m3_tc_kernel(const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv, E4TcParams P) {
     using namespace e4tc;
     using Y = Lay<N>;
@@ -213,6 +215,7 @@ __global__ void __launch_bounds__(e4tc::THREADS, 1)
     int *vis_s = reinterpret_cast<int *>(smem + Y::VIS_OFF);
     float *red = reinterpret_cast<float *>(smem + Y::RED_OFF);
     volatile int *need = reinterpret_cast<volatile int *>(smem + Y::NEED_OFF);
+    float *alpha_s = reinterpret_cast<float *>(smem + Y::ALPHA_OFF);
     constexpr int NK = Y::NK, NV = Y::NV, SB = Y::SB, NR = Y::NR;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const float NaN = __int_as_float(0x7fc00000);
@@ -240,8 +243,8 @@ __global__ void __launch_bounds__(e4tc::THREADS, 1)
             uint32_t c = 1;
             if ((i >= Y::B_SFREE && i < Y::B_SFREE + 2) || (i >= Y::B_PFULL && i < Y::B_PFULL + 2) ||
                 i == Y::B_QFULL || i == Y::B_OFREE)
-                c = 8;  // the eight softmax warps
-            if (i >= Y::B_WG && i < Y::B_WG + 2) c = 4;
+                c = 4 * Y::NWG;  // every softmax warp
+            if (i >= Y::B_WG && i < Y::B_WG + 4) c = 4;
             mbar_init(&bars[i], c);
         }
         misc[1] = 0;
@@ -261,6 +264,7 @@ __global__ void __launch_bounds__(e4tc::THREADS, 1)
     constexpr uint32_t TM_S = 0, TM_O = Y::TM_O;
     uint32_t err = 0;
 
+    constexpr int W_VPROD = Y::W_VPROD, NWG = Y::NWG;
     if (warp == W_KPROD || warp == W_VPROD) {
         // ================================================== producers: K (warp 0) and V (warp 6)
         // of each chunk, one tensor copy per block and 128-channel half (the
@@ -397,7 +401,7 @@ __global__ void __launch_bounds__(e4tc::THREADS, 1)
         __syncwarp();
     } else {
         // ================================================== softmax, q' staging, epilogue
-        // two warpgroups, each owning half of the rows (S^T and O^T columns):
+        // NWG warpgroups, each owning NR = N / NWG rows (S^T and O^T columns):
         // rows are independent in the softmax, so each group votes, rescales
         // and writes P^T for its own rows; one token per thread
         const int wg = (warp - W_SM0) >> 2;
@@ -514,7 +518,7 @@ __global__ void __launch_bounds__(e4tc::THREADS, 1)
             if (ti < NR && rb + ti < P.R) {
                 const int r = rb + ti;
                 const float l = row_l(r);
-                float lse_v = l > 0.f ? (mrow(ppb, mbb)[r] + lg2(l)) * LN2 : -INFINITY;
+                float lse_v = l > 0.f ? (mrow(ppb, mbb)[r] + lg2(l) - PSHIFT) * LN2 : -INFINITY;
                 if (pbad) lse_v = NaN;
                 const int jq = r / P.G, h = pq * P.G + r % P.G;
                 if (complete) {
@@ -545,7 +549,7 @@ __global__ void __launch_bounds__(e4tc::THREADS, 1)
                         if (r >= P.R) break;
                         const float l = row_l(r);
                         const float o = (__uint_as_float(a[k]) + __uint_as_float(b2[k])) + __uint_as_float(c2[k]);
-                        float y = o * (l > 0.f ? PSCALE_INV / l : 0.f);
+                        float y = o * (l > 0.f ? 1.0f / l : 0.f);
                         if (pbad) y = NaN;
                         if (complete) {
                             const int h = pq * P.G + hg;
@@ -671,18 +675,18 @@ __global__ void __launch_bounds__(e4tc::THREADS, 1)
                 }
                 if (!wg_sync()) { alive = false; break; }
                 float *mn_s = mrow(pp, mb ^ 1) + rb;
+                float *al = alpha_s + rb;  // the factor of each row, exp2(m_old - m_new)
                 if (ti < NR) {
                     const int r = rb + ti;
                     const float mo = mc[ti];
                     const float cm = fmaxf(fmaxf(red[r], red[64 + r]), fmaxf(red[128 + r], red[192 + r]));
-                    mn_s[ti] = (mo == -INFINITY || cm > mo + SLACK) ? fmaxf(cm + HEAD, mo) : mo;
+                    const float mn = (mo == -INFINITY || cm > mo + SLACK) ? fmaxf(cm + HEAD, mo) : mo;
+                    mn_s[ti] = mn;
+                    al[ti] = (mn == mo) ? 1.f : ex2(mo - mn);
                 }
                 if (!wg_sync()) { alive = false; break; }
 #pragma unroll
-                for (int k = 0; k < NR; ++k) {
-                    const float mo = mc[k], mn = mn_s[k];
-                    lsum[k] *= (mn == mo) ? 1.f : ex2(mo - mn);
-                }
+                for (int k = 0; k < NR; ++k) lsum[k] *= al[k];
                 // O^T (channels on lanes, rows on columns, three partial sums per
                 // tile) takes the same factors once the previous chunk's O MMAs
                 // are in; the first chunk of a piece overwrites O^T
@@ -693,20 +697,16 @@ __global__ void __launch_bounds__(e4tc::THREADS, 1)
                     }
                     tc_fence_after();
 #pragma unroll 1
-                    for (int i = 0; i < 6; ++i) {  // (tile, term)
-#pragma unroll 1
-                        for (int g = 0; g < NR; g += 8) {
-                            uint32_t w[8];
-                            const uint32_t ta = tl + TM_O + (uint32_t)(N * i + rb + g);
-                            tmem_ld8_nowait(ta, w);
-                            tmem_ld_wait();
+                    for (int i = 0; i < 6; ++i) {  // (tile, term): the group's NR columns in one round trip
+                        uint32_t w[NR];
+                        const uint32_t ta = tl + TM_O + (uint32_t)(N * i + rb);
 #pragma unroll
-                            for (int k = 0; k < 8; ++k) {
-                                const float mo = mc[g + k], mn = mn_s[g + k];
-                                w[k] = __float_as_uint(__uint_as_float(w[k]) * ((mn == mo) ? 1.f : ex2(mo - mn)));
-                            }
-                            tmem_st8_u(ta, w);
-                        }
+                        for (int g = 0; g < NR; g += 8) tmem_ld8_nowait(ta + g, w + g);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int k = 0; k < NR; ++k) w[k] = __float_as_uint(__uint_as_float(w[k]) * al[k]);
+#pragma unroll
+                        for (int g = 0; g < NR; g += 8) tmem_st8_u(ta + g, w + g);
                     }
                     tmem_st_wait();
                     tc_fence_before();
@@ -727,23 +727,24 @@ __global__ void __launch_bounds__(e4tc::THREADS, 1)
             if (tok >= L) {
                 uint8_t *vrow = smem + Y::V_OFF + vslot * TILE;
 #pragma unroll
-                for (int c = 8 * wg; c < 8 * wg + 8; ++c)
+                for (int c = (16 / NWG) * wg; c < (16 / NWG) * (wg + 1); ++c)
                     *reinterpret_cast<uint4 *>(vrow + tile_off(t, c)) = make_uint4(0u, 0u, 0u, 0u);
             }
-            // P^T = 2^(x - m) * 2^8 as three E4M3 terms of 4 significant bits
-            // each (rows in pairs, one conversion per pair and term)
+            // P^T = 2^(x - m + 8) as three E4M3 terms of 4 significant bits each
+            // (rows in pairs, one conversion per pair and term); the row sums add
+            // the same values
             uint8_t *pt = smem + Y::P_OFF + pbuf * Y::P_BUF;
             const float *mcur = mrow(pp, mb) + rb;
 #pragma unroll
             for (int k = 0; k < NR; k += 2) {
                 const int r = rb + k;
                 const float ma = mcur[k], mb2 = mcur[k + 1];
-                const float pa0 = ex2(x[k] - ((ma == -INFINITY) ? 0.f : ma));
-                const float pb0 = ex2(x[k + 1] - ((mb2 == -INFINITY) ? 0.f : mb2));
+                const float pa0 = ex2(x[k] - ((ma == -INFINITY) ? 0.f : ma - PSHIFT));
+                const float pb0 = ex2(x[k + 1] - ((mb2 == -INFINITY) ? 0.f : mb2 - PSHIFT));
                 lsum[k] += pa0;
                 lsum[k + 1] += pb0;
                 float ra, rb2, sa, sb2;
-                const float ha = split4(pa0 * PSCALE, ra), hb = split4(pb0 * PSCALE, rb2);
+                const float ha = split4(pa0, ra), hb = split4(pb0, rb2);
                 const float ma1 = split4(ra, sa), mb1 = split4(rb2, sb2);
                 const uint32_t ch = f32x2_e4m3x2(ha, hb), cm = f32x2_e4m3x2(ma1, mb1), cl = f32x2_e4m3x2(sa, sb2);
                 // K-major, 128-byte swizzle: row r of 128 tokens, 16-byte chunk
@@ -764,7 +765,7 @@ __global__ void __launch_bounds__(e4tc::THREADS, 1)
             cursor_next(cs, P.req, P.B, U, P.mbps);
         }
         if (alive && piece >= 0 && !epilogue(npg - 1, pp, mb)) alive = false;
-        if (!alive) e4tc_nan_share(P, x0, npg, wg * 128 + ti, 256);
+        if (!alive) e4tc_nan_share(P, x0, npg, wg * 128 + ti, 128 * NWG);
     }
 
     // ---- teardown
@@ -784,7 +785,7 @@ cudaError_t launch_e4tc_n(const CUtensorMap &tk, const CUtensorMap &tv, const E4
     using Y = e4tc::Lay<N>;
     cudaError_t e = cudaFuncSetAttribute(pa_e4m3_tc_kernel<N>, cudaFuncAttributeMaxDynamicSharedMemorySize, Y::SMEM);
     if (e != cudaSuccess) return e;
-    e = launch_pdl(pa_e4m3_tc_kernel<N>, dim3((unsigned)ctas), dim3(e4tc::THREADS), (size_t)Y::SMEM, s, tk, tv, P);
+    e = launch_pdl(pa_e4m3_tc_kernel<N>, dim3((unsigned)ctas), dim3(Y::THREADS), (size_t)Y::SMEM, s, tk, tv, P);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
