@@ -39,6 +39,9 @@ SMALL = [
     ("e4m3", dict(B=4, L_lo=4, L_hi=900, Hq=16, Hkv=4), 0),
     ("e4m3", dict(B=4, L_lo=4, L_hi=900, Hq=16, Hkv=4), 2),
     ("e4m3", dict(B=3, L_lo=1, L_hi=70, Hq=4, Hkv=1, n=4), 1),
+    ("e4m3", dict(B=4, L_lo=4, L_hi=900, Hq=16, Hkv=2), 3),     # tensor-core kernel, 32 rows (two groups of 16)
+    ("e4m3", dict(B=3, L_lo=4, L_hi=700, Hq=24, Hkv=2), 0),     # 48 rows (two groups of 24)
+    ("e4m3", dict(B=3, L_lo=4, L_hi=700, Hq=16, Hkv=1, bs=16), 4),  # 64 rows (four groups of 16), 16-token blocks
     ("int8", dict(B=4, L_lo=1, L_hi=600, Hq=16, Hkv=2), 0),
     ("int8", dict(B=4, L_lo=1, L_hi=600, Hq=16, Hkv=2), 2),
     ("int4", dict(B=4, L_lo=1, L_hi=600, Hq=16, Hkv=2), 0),

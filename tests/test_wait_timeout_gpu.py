@@ -79,6 +79,7 @@ def _owner_rows(w, total, x, wp):
     ("bf16", dict(B=5, L_lo=200, L_hi=1500, Hq=16, Hkv=2), 0),
     ("bf16", dict(B=4, L_lo=100, L_hi=900, Hq=64, Hkv=2, n=2, D=256), 5),  # groups of 4 paired workers
     ("e4m3", dict(B=4, L_lo=100, L_hi=2000, Hq=32, Hkv=8, n=4), 7),     # the E4M3 tensor-core kernel
+    ("e4m3", dict(B=3, L_lo=100, L_hi=1500, Hq=32, Hkv=8, n=16), 5),    # the same with four softmax groups
     ("latent", dict(B=3, L_lo=200, L_hi=600, Hq=32), 6),
 ])
 def test_withheld_copy_times_out_and_leaves_no_stale_rows(fi, name, kw, split):
