@@ -293,6 +293,8 @@ __global__ void __launch_bounds__(lat::THREADS, 1)
         // ================================================== MMA issue
         constexpr uint32_t ID_QK = idesc(64, 64, 0), ID_PV = idesc(128, 64, 1);
         Cursor cq = c0, cp = c0;
+        const uint64_t qh128 = sdesc(sb + QH_OFF, 16, 1024, 2), qh64 = sdesc(sb + QH_OFF, 16, 512, 4);
+        const uint64_t ql128 = sdesc(sb + QL_OFF, 16, 1024, 2), ql64 = sdesc(sb + QL_OFF, 16, 512, 4);
         int q_piece = -1, q_pb = -1, q_pq = -1;  // pieces seen by the S stream
         int p_piece = -1, p_pb = -1, p_pq = -1;  // pieces seen by the O stream
         auto issue_s = [&](int j) -> bool {
@@ -307,20 +309,23 @@ __global__ void __launch_bounds__(lat::THREADS, 1)
             if (!warp_wait(&bars[B_FULL + slot], (j / NSLOT) & 1, abort, err)) return false;
             if (j >= 2 && !warp_wait(&bars[B_SFREE + sbuf], ((j >> 1) - 1) & 1, abort, err)) return false;
             tc_fence_after();
+            // descriptors of the step's operands: the tile base's descriptor plus
+            // the step's offset in 16-byte units (no carry out of the 14-bit
+            // address field: shared memory ends below 256 KB)
+            const uint32_t ring = sb + RING_OFF + slot * SLOT_BYTES;
+            const uint64_t r128 = sdesc(ring, 16, 1024, 2), r64 = sdesc(ring, 16, 512, 4);
             if (lane == 0) {
-                const uint32_t ring = sb + RING_OFF + slot * SLOT_BYTES;
                 const uint32_t dS = tmem + TM_S + 64u * sbuf;
                 uint32_t acc = 0;
 #pragma unroll
                 for (int cb = 0; cb < 5; ++cb) {
-                    const uint32_t swz = cb < 4 ? 2u : 4u, sbo = cb < 4 ? 1024u : 512u;
-                    const uint32_t boff = (uint32_t)cb * (64 * 128);
 #pragma unroll
                     for (int ks = 0; ks < (cb < 4 ? 4 : 2); ++ks) {
-                        const uint64_t bdesc = sdesc(ring + boff + 32 * ks, 16, sbo, swz);
-                        mma_f8(dS, sdesc(sb + QH_OFF + boff + 32 * ks, 16, sbo, swz), bdesc, ID_QK, acc);
+                        const uint64_t off = (uint64_t)(cb * 512 + 2 * ks);
+                        const uint64_t bdesc = (cb < 4 ? r128 : r64) + off;
+                        mma_f8(dS, (cb < 4 ? qh128 : qh64) + off, bdesc, ID_QK, acc);
                         acc = 1;
-                        mma_f8(dS, sdesc(sb + QL_OFF + boff + 32 * ks, 16, sbo, swz), bdesc, ID_QK, 1);
+                        mma_f8(dS, (cb < 4 ? ql128 : ql64) + off, bdesc, ID_QK, 1);
                     }
                 }
                 mma_commit(&bars[B_SFULL + sbuf]);
@@ -343,14 +348,15 @@ __global__ void __launch_bounds__(lat::THREADS, 1)
             if (!warp_wait(&bars[B_PFULL + pbuf], (j >> 1) & 1, abort, err)) return false;
             if (!warp_wait(&bars[B_VFULL], j & 1, abort, err)) return false;
             tc_fence_after();
+            const uint64_t vb = sdesc(sb + V_OFF, 8192, 1024, 2), pbd = sdesc(sb + P_OFF + pbuf * 8192, 16, 1024, 2);
             if (lane == 0) {
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
                     const uint32_t dO = tmem + TM_O + 64u * i;
 #pragma unroll
                     for (int k = 0; k < 4; ++k) {
-                        const uint64_t adesc = sdesc(sb + V_OFF + (2 * i) * (64 * 128) + 2048 * k, 8192, 1024, 2);
-                        const uint64_t bdesc = sdesc(sb + P_OFF + pbuf * 8192 + 32 * k, 16, 1024, 2);
+                        const uint64_t adesc = vb + (uint64_t)(((2 * i) * (64 * 128) + 2048 * k) >> 4);
+                        const uint64_t bdesc = pbd + (uint64_t)((32 * k) >> 4);
                         mma_f16(dO, adesc, bdesc, ID_PV, (first && k == 0) ? 0u : 1u);
                     }
                 }
