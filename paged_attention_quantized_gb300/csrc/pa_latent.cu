@@ -304,17 +304,17 @@ __global__ void __launch_bounds__(lat::THREADS, 1)
                 ++q_piece;
                 q_pb = cq.b;
                 q_pq = cq.q;
-                if (!warp_wait(&bars[B_QFULL], q_piece & 1, abort, err)) return false;
+                if (!lane_wait(&bars[B_QFULL], q_piece & 1, abort, err)) return false;
             }
-            if (!warp_wait(&bars[B_FULL + slot], (j / NSLOT) & 1, abort, err)) return false;
-            if (j >= 2 && !warp_wait(&bars[B_SFREE + sbuf], ((j >> 1) - 1) & 1, abort, err)) return false;
+            if (!lane_wait(&bars[B_FULL + slot], (j / NSLOT) & 1, abort, err)) return false;
+            if (j >= 2 && !lane_wait(&bars[B_SFREE + sbuf], ((j >> 1) - 1) & 1, abort, err)) return false;
             tc_fence_after();
             // descriptors of the step's operands: the tile base's descriptor plus
             // the step's offset in 16-byte units (no carry out of the 14-bit
             // address field: shared memory ends below 256 KB)
             const uint32_t ring = sb + RING_OFF + slot * SLOT_BYTES;
             const uint64_t r128 = sdesc(ring, 16, 1024, 2), r64 = sdesc(ring, 16, 512, 4);
-            if (lane == 0) {
+            {
                 const uint32_t dS = tmem + TM_S + 64u * sbuf;
                 uint32_t acc = 0;
 #pragma unroll
@@ -331,7 +331,6 @@ __global__ void __launch_bounds__(lat::THREADS, 1)
                 mma_commit(&bars[B_SFULL + sbuf]);
                 mma_commit(&bars[B_SLOTFREE + slot]);
             }
-            __syncwarp();
             cursor_next(cq, P.req, P.B, U, P.mbps);
             return true;
         };
@@ -343,13 +342,13 @@ __global__ void __launch_bounds__(lat::THREADS, 1)
                 p_pb = cp.b;
                 p_pq = cp.q;
                 first = true;
-                if (p_piece > 0 && !warp_wait(&bars[B_OFREE], (p_piece - 1) & 1, abort, err)) return false;
+                if (p_piece > 0 && !lane_wait(&bars[B_OFREE], (p_piece - 1) & 1, abort, err)) return false;
             }
-            if (!warp_wait(&bars[B_PFULL + pbuf], (j >> 1) & 1, abort, err)) return false;
-            if (!warp_wait(&bars[B_VFULL], j & 1, abort, err)) return false;
+            if (!lane_wait(&bars[B_PFULL + pbuf], (j >> 1) & 1, abort, err)) return false;
+            if (!lane_wait(&bars[B_VFULL], j & 1, abort, err)) return false;
             tc_fence_after();
             const uint64_t vb = sdesc(sb + V_OFF, 8192, 1024, 2), pbd = sdesc(sb + P_OFF + pbuf * 8192, 16, 1024, 2);
-            if (lane == 0) {
+            {
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
                     const uint32_t dO = tmem + TM_O + 64u * i;
@@ -362,18 +361,19 @@ __global__ void __launch_bounds__(lat::THREADS, 1)
                 }
                 mma_commit(&bars[B_PVDONE + pbuf]);
             }
-            __syncwarp();
             cursor_next(cp, P.req, P.B, U, P.mbps);
             return true;
         };
-        if (issue_s(0)) {
-            for (int j = 0; j < npg; ++j) {
-                if (j + 1 < npg && !issue_s(j + 1)) break;
-                if (!issue_o(j)) break;
-            }
-        }
-        // every MMA issued so far is complete before tensor memory is released
+        // lane 0 runs this role alone (its waits need no broadcast); the other
+        // lanes wait at the warp barrier below
         if (lane == 0) {
+            if (issue_s(0)) {
+                for (int j = 0; j < npg; ++j) {
+                    if (j + 1 < npg && !issue_s(j + 1)) break;
+                    if (!issue_o(j)) break;
+                }
+            }
+            // every MMA issued so far is complete before tensor memory is released
             mma_commit(&bars[B_MDONE]);
             (void)mbar_wait_bounded(&bars[B_MDONE], 0, nullptr);
         }

@@ -159,6 +159,17 @@ __device__ __forceinline__ bool warp_wait_u(uint64_t *bar, uint32_t parity, vola
     return warp_wait(bar, parity, abort, err);
 }
 
+// Bounded wait of one thread (a role run by a single lane, such as MMA
+// issue): no broadcast and no acquire by the other lanes
+__device__ __forceinline__ bool lane_wait(uint64_t *bar, uint32_t parity, volatile int *abort, uint32_t &err) {
+    const bool ok = mbar_wait_bounded(bar, parity, abort);
+    if (!ok && *abort == 0) {
+        *abort = 1;
+        err |= PA_DEV_ERR_TIMEOUT;
+    }
+    return ok;
+}
+
 __device__ __forceinline__ void warp_arrive(uint64_t *bar) {
     __syncwarp();
     if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
