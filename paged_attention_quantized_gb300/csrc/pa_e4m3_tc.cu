@@ -334,12 +334,12 @@ __global__ void __launch_bounds__(e4tc::Lay<N>::THREADS, 1)
                 ++q_piece;
                 q_pb = cq.b;
                 q_pq = cq.q;
-                if (!warp_wait_u(&bars[Y::B_QFULL], q_piece & 1, abort, err)) return false;
+                if (!lane_wait(&bars[Y::B_QFULL], q_piece & 1, abort, err)) return false;
             }
-            if (!warp_wait_u(&bars[Y::B_KFULL + kslot], (j / NK) & 1, abort, err)) return false;
-            if (j >= SB && !warp_wait_u(&bars[Y::B_SFREE + sbuf], ((j / SB) - 1) & 1, abort, err)) return false;
+            if (!lane_wait(&bars[Y::B_KFULL + kslot], (j / NK) & 1, abort, err)) return false;
+            if (j >= SB && !lane_wait(&bars[Y::B_SFREE + sbuf], ((j / SB) - 1) & 1, abort, err)) return false;
             tc_fence_after();
-            if (lane == 0) {
+            {
                 const uint32_t kst = sb + Y::K_OFF + kslot * TILE;
                 const uint32_t dS = tmem + TM_S + (uint32_t)(2 * N * sbuf);
 #pragma unroll
@@ -352,7 +352,6 @@ __global__ void __launch_bounds__(e4tc::Lay<N>::THREADS, 1)
                 mma_commit(&bars[Y::B_SFULL + sbuf]);
                 mma_commit(&bars[Y::B_KFREE + kslot]);
             }
-            __syncwarp();
             cursor_next(cq, P.req, P.B, U, P.mbps);
             return true;
         };
@@ -364,12 +363,12 @@ __global__ void __launch_bounds__(e4tc::Lay<N>::THREADS, 1)
                 p_pb = cp.b;
                 p_pq = cp.q;
                 first = true;
-                if (p_piece > 0 && !warp_wait_u(&bars[Y::B_OFREE], (p_piece - 1) & 1, abort, err)) return false;
+                if (p_piece > 0 && !lane_wait(&bars[Y::B_OFREE], (p_piece - 1) & 1, abort, err)) return false;
             }
-            if (!warp_wait_u(&bars[Y::B_PFULL + pbuf], (j >> 1) & 1, abort, err)) return false;
-            if (!warp_wait_u(&bars[Y::B_VFULL + vslot], (j / NV) & 1, abort, err)) return false;
+            if (!lane_wait(&bars[Y::B_PFULL + pbuf], (j >> 1) & 1, abort, err)) return false;
+            if (!lane_wait(&bars[Y::B_VFULL + vslot], (j / NV) & 1, abort, err)) return false;
             tc_fence_after();
-            if (lane == 0) {
+            {
                 const uint32_t vst = sb + Y::V_OFF + vslot * TILE;
                 const uint32_t pst = sb + Y::P_OFF + pbuf * Y::P_BUF;
 #pragma unroll
@@ -384,17 +383,18 @@ __global__ void __launch_bounds__(e4tc::Lay<N>::THREADS, 1)
                 mma_commit(&bars[Y::B_ODONE + pbuf]);
                 mma_commit(&bars[Y::B_VFREE + vslot]);
             }
-            __syncwarp();
             cursor_next(cp, P.req, P.B, U, P.mbps);
             return true;
         };
-        if (issue_s(0)) {
-            for (int j = 0; j < npg; ++j) {
-                if (j + 1 < npg && !issue_s(j + 1)) break;
-                if (!issue_o(j)) break;
-            }
-        }
+        // lane 0 runs this role alone (its waits need no broadcast); the other
+        // lanes wait at the warp barrier below
         if (lane == 0) {
+            if (issue_s(0)) {
+                for (int j = 0; j < npg; ++j) {
+                    if (j + 1 < npg && !issue_s(j + 1)) break;
+                    if (!issue_o(j)) break;
+                }
+            }
             mma_commit(&bars[Y::B_MDONE]);
             (void)mbar_wait_bounded(&bars[Y::B_MDONE], 0, nullptr);
         }
