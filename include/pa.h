@@ -132,7 +132,8 @@ typedef struct pa_problem {
     int32_t num_kv_heads;       /* Hkv, divides Hq */
     int32_t head_dim_k;         /* Dk */
     int32_t head_dim_v;         /* Dv */
-    int32_t block_size;         /* bs, tokens per block (grouped kernel: a multiple of 16, <= 128; latent: 64) */
+    int32_t block_size;         /* bs, tokens per block (grouped kernel: a multiple of 16, <= 128; latent: 64;
+                                   the E4M3 tensor-core kernel: 16, 32, 64 or 128) */
     int32_t num_blocks;         /* blocks in the pool (block 0 = null block) */
     int32_t max_blocks_per_seq; /* block_table columns */
     int32_t max_context_len;    /* bound on every context_lens entry */
@@ -168,11 +169,15 @@ typedef struct pa_problem {
  * row S * (row block) + i of the kv head, query row
  * r = j * (Hq / Hkv) + (h mod (Hq / Hkv)).
  *
- * Two kernels: the grouped kernel (separate K and V planes, per-tensor or
+ * Three kernels: the grouped kernel (separate K and V planes, per-tensor or
  * per-channel scales) has S = 16 and one worker per warp (or pair of warps);
- * the single-latent kernel (v_is_k_prefix: E4M3, PA_SCALE_TOKEN, Dk = 576,
- * Dv = 512, bs = 64) has S = 64 and one worker per CTA (one CTA per SM).  In
- * both, workers come in groups of G = row_blocks: positions run over
+ * the E4M3 tensor-core kernel (E4M3 K and V at Dk = Dv = 256, per-tensor or no
+ * scales, 16, 32, 48 or 64 query rows per kv head, bs = 16, 32, 64 or 128) has
+ * S = all rows of a kv head, pages of 128 tokens (work_page_tokens = 128,
+ * whole blocks) and one worker per CTA (one CTA per SM); the single-latent
+ * kernel (v_is_k_prefix: E4M3, PA_SCALE_TOKEN, Dk = 576, Dv = 512, bs = 64)
+ * has S = 64 and one worker per CTA (one CTA per SM).  In all three, workers
+ * come in groups of G = row_blocks (G = 1 on the E4M3 tensor-core kernel): positions run over
  * (request, kv head, page), the W / G groups share them as above, and worker
  * g*G + i takes row block i of every page of group g's share (the G workers
  * read the same pages at about the same time, so all but the first read hit
@@ -190,10 +195,10 @@ typedef struct pa_layout {
     int32_t num_sms;             /* effective */
     int32_t grid_ctas;           /* effective persistent CTAs of pa_run */
     int32_t warps;               /* workers W: grid_ctas * 4 (grouped; * 2 with paired warps at D = 256
-                                    and more than 8 query rows per kv head) or grid_ctas (latent); the
-                                    launch is sized so that W is a multiple of group_size */
-    int32_t ring_pages_per_warp; /* pages each worker keeps in flight */
-    int32_t rows_per_segment;    /* S: 16 (grouped) or 64 (latent) */
+                                    and more than 8 query rows per kv head) or grid_ctas (latent, E4M3
+                                    tensor-core); the launch is sized so that W is a multiple of group_size */
+    int32_t ring_pages_per_warp; /* pages each worker keeps in flight (E4M3 tensor-core: K stages) */
+    int32_t rows_per_segment;    /* S: 16 (grouped), 64 (latent) or all rows of a kv head (E4M3 tensor-core) */
     int32_t group_size;          /* G = row_blocks: workers sharing one run of pages */
     int32_t work_page_tokens;    /* tokens the attention handles as one page: block_size, or an equal
                                     part of a block (>= 16) when two whole blocks per worker do not fit */
