@@ -87,6 +87,10 @@ struct Lay {
     static constexpr int P_OFF = Q_OFF + Q_BYTES;    // P^T [2 buffers][3 terms x N rows][128 B]
     static constexpr int P_TERM = N * 128;
     static constexpr int P_BUF = 3 * P_TERM;
+    // at 64 rows P^T is stored MN-major (each token's 64 row values of a term
+    // contiguous, 64-byte swizzle, one 8 KB block per term), so a softmax
+    // group writes its 16 rows of a term with one 16-byte store
+    static constexpr bool PMN = (N == 64);
     static constexpr int NK = (N <= 48) ? 3 : 2;     // K stages
     static constexpr int NV = (N <= 16) ? 3 : 2;     // V stages
     static constexpr int K_OFF = P_OFF + 2 * P_BUF;
@@ -323,7 +327,9 @@ __global__ void __launch_bounds__(e4tc::Lay<N>::THREADS, 1)
     } else if (warp == W_MMA) {
         // ================================================== MMA issue
         // S^T = K [q'_hi | q'_lo]^T (N' = 2N), O^T += V^T [P_0 | P_1 | P_2]^T (N' = 3N)
-        constexpr uint32_t ID_S = idesc(128, 2 * N, 0), ID_O = idesc(128, 3 * N, 1);
+        constexpr uint32_t ID_S = idesc(128, 2 * N, 0);
+        // O^T: A = V^T read MN-major; B = P^T K-major, or MN-major (bit 16) at 64 rows
+        constexpr uint32_t ID_O = idesc(128, 3 * N, 1) | (Y::PMN ? (1u << 16) : 0u);
         Cursor cq = c0, cp = c0;
         int q_piece = -1, q_pb = -1, q_pq = -1;
         int p_piece = -1, p_pb = -1, p_pq = -1;
@@ -377,7 +383,9 @@ __global__ void __launch_bounds__(e4tc::Lay<N>::THREADS, 1)
 #pragma unroll
                     for (int k = 0; k < 4; ++k) {  // 32 tokens per step
                         const uint64_t ad = sdesc(vst + (uint32_t)(i * (CH * 128) + k * 32 * 128), 16, 1024, 2);
-                        mma_f8(dO, ad, sdesc(pst + 32 * k, 16, 1024, 2), ID_O, (first && k == 0) ? 0u : 1u);
+                        const uint64_t bd = Y::PMN ? sdesc(pst + 2048 * k, 8192, 512, 4)  // 32 tokens x 64 B per step
+                                                   : sdesc(pst + 32 * k, 16, 1024, 2);
+                        mma_f8(dO, ad, bd, ID_O, (first && k == 0) ? 0u : 1u);
                     }
                 }
                 mma_commit(&bars[Y::B_ODONE + pbuf]);
@@ -735,6 +743,7 @@ __global__ void __launch_bounds__(e4tc::Lay<N>::THREADS, 1)
             // the same values
             uint8_t *pt = smem + Y::P_OFF + pbuf * Y::P_BUF;
             const float *mcur = mrow(pp, mb) + rb;
+            uint32_t pw[3][NR / 4];  // MN-major: the group's bytes of each term, 4 rows per word
 #pragma unroll
             for (int k = 0; k < NR; k += 2) {
                 const int r = rb + k;
@@ -747,17 +756,36 @@ __global__ void __launch_bounds__(e4tc::Lay<N>::THREADS, 1)
                 const float ha = split4(pa0, ra), hb = split4(pb0, rb2);
                 const float ma1 = split4(ra, sa), mb1 = split4(rb2, sb2);
                 const uint32_t ch = f32x2_e4m3x2(ha, hb), cm = f32x2_e4m3x2(ma1, mb1), cl = f32x2_e4m3x2(sa, sb2);
-                // K-major, 128-byte swizzle: row r of 128 tokens, 16-byte chunk
-                // t / 16 lands at (t / 16) ^ (r & 7)
-                const uint32_t oa = (uint32_t)r * 128 + ((((t >> 4) ^ (r & 7)) << 4) | (t & 15));
-                const uint32_t ob = (uint32_t)(r + 1) * 128 + ((((t >> 4) ^ ((r + 1) & 7)) << 4) | (t & 15));
-                pt[oa] = (uint8_t)(ch & 0xFF);
-                pt[ob] = (uint8_t)(ch >> 8);
-                pt[Y::P_TERM + oa] = (uint8_t)(cm & 0xFF);
-                pt[Y::P_TERM + ob] = (uint8_t)(cm >> 8);
-                pt[2 * Y::P_TERM + oa] = (uint8_t)(cl & 0xFF);
-                pt[2 * Y::P_TERM + ob] = (uint8_t)(cl >> 8);
+                if constexpr (Y::PMN) {
+                    const int wi = k >> 2, sh = 8 * (k & 3);  // rows k, k + 1 go to bytes k % 4 .. of word k / 4
+                    if ((k & 3) == 0) { pw[0][wi] = 0u; pw[1][wi] = 0u; pw[2][wi] = 0u; }
+                    pw[0][wi] |= ch << sh;
+                    pw[1][wi] |= cm << sh;
+                    pw[2][wi] |= cl << sh;
+                } else {
+                    // K-major, 128-byte swizzle: row r of 128 tokens, 16-byte chunk
+                    // t / 16 lands at (t / 16) ^ (r & 7)
+                    const uint32_t oa = (uint32_t)r * 128 + ((((t >> 4) ^ (r & 7)) << 4) | (t & 15));
+                    const uint32_t ob = (uint32_t)(r + 1) * 128 + ((((t >> 4) ^ ((r + 1) & 7)) << 4) | (t & 15));
+                    pt[oa] = (uint8_t)(ch & 0xFF);
+                    pt[ob] = (uint8_t)(ch >> 8);
+                    pt[Y::P_TERM + oa] = (uint8_t)(cm & 0xFF);
+                    pt[Y::P_TERM + ob] = (uint8_t)(cm >> 8);
+                    pt[2 * Y::P_TERM + oa] = (uint8_t)(cl & 0xFF);
+                    pt[2 * Y::P_TERM + ob] = (uint8_t)(cl >> 8);
+                }
             }
+            if constexpr (Y::PMN) {
+                // token t's row of a term: 64 bytes (rows 0..63), 16-byte chunk wg at
+                // wg ^ ((t / 2) & 3) (64-byte swizzle); one 8 KB block per term
+                static_assert(NR == 16, "one 16-byte chunk per group and term");
+                const uint32_t off = (uint32_t)t * 64 + ((uint32_t)(wg ^ ((t >> 1) & 3)) << 4);
+#pragma unroll
+                for (int tm = 0; tm < 3; ++tm)
+                    *reinterpret_cast<uint4 *>(pt + tm * (CH * 64) + off) =
+                        make_uint4(pw[tm][0], pw[tm][1], pw[tm][2], pw[tm][3]);
+            }
+
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) mbar_arrive(&bars[Y::B_PFULL + pbuf]);
