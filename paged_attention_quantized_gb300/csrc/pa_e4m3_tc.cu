@@ -27,25 +27,26 @@
 // combine (one segment per kv head: all R rows).
 //
 // Roles (3 + 4 G warps, G = 2 softmax groups, 4 at 64 rows):
-//  * warp 0 and the last warp copy K and V of each chunk into their own rings
-//    (tensor copies of one block's 128-channel half, 128-byte swizzled: the K-major
-//    operand layout), with an L2 evict-first policy since every page is read
-//    once; K is released as soon as the chunk's S MMAs are done, V after its
-//    O MMAs.  Blocks past the request's length and blocks with an invalid id
-//    are not copied;
-//  * warp 1 issues the MMAs: S(j+1) before O(j), so the tensor pipe works
-//    while chunk j's softmax runs;
+//  * warp 0 and the last warp copy K and V of each chunk into their own
+//    rings (tensor copies of one block's 128-channel half, 128-byte swizzled:
+//    the K-major operand layout), with an L2 evict-first policy since every
+//    page is read once; K is released as soon as the chunk's S MMAs are
+//    done, V after its O MMAs.  Blocks past the request's length and blocks
+//    with an invalid id are not copied;
+//  * lane 0 of warp 1 issues the MMAs: S(j+1) before O(j), so the tensor
+//    pipe works while chunk j's softmax runs;
 //  * warps 2 .. 4G+1, G groups of four (one token per thread: S^T has tokens
 //    on the tensor-memory lanes; each group owns R/G rows) run the online
-//    softmax in the exp2 domain with a lazy reference maximum (a chunk reduces the maxima across the 128 tokens, and rescales
-//    O^T, only when some score passes its row's reference by more than 0.75;
-//    the reference then moves to one above the chunk's maximum), zero the V
-//    rows past the request's length before the chunk's O MMAs (uncopied rows,
-//    or slots of the last block that may hold NaN codes: 1Cat-vLLM PR #647,
-//    "Stop grouped-page4 null-block padding from leaking E4M3 NaN", Fix), write
-//    P^T (times 2^8, so small weights stay E4M3 normals), stage q' at each
-//    piece (and fetch the next piece's record and q rows ahead) and write the
-//    output at its end.
+//    softmax in the exp2 domain with a lazy reference maximum (a chunk
+//    reduces the maxima across the 128 tokens, and rescales O^T, only when
+//    some score passes its row's reference by more than 0.75; the reference
+//    then moves to one above the chunk's maximum), zero the V rows past the
+//    request's length before the chunk's O MMAs (uncopied rows, or slots of
+//    the last block that may hold NaN codes: 1Cat-vLLM PR #647, "Stop
+//    grouped-page4 null-block padding from leaking E4M3 NaN", Fix), write
+//    P^T (times 2^8, so small weights stay E4M3 normals; K-major, or MN-major
+//    at 64 rows), stage q' at each piece (and fetch the next piece's record
+//    and q rows ahead) and write the output at its end.
 // Every wait is bounded (PA_DEV_ERR_TIMEOUT); after a timeout every piece of
 // the CTA's share is written as NaN.
 #include "pa_attn.cuh"
