@@ -215,7 +215,7 @@ def test_every_block_size_has_a_launch(B):
             if kv == B.PA_INT4 and D == 64:
                 continue
             for bs in range(16, 129, 16):
-                for hq, n in ((8, 1), (32, 1), (64, 1), (32, 4), (128, 2)):
+                for hq, n in ((8, 1), (32, 1), (64, 1), (32, 4), (128, 2), (96, 4), (32, 16)):
                     p = _prob(B, kv_dtype=kv, head_dim_k=D, head_dim_v=D, block_size=bs, num_q_heads=hq, next_n=n)
                     lo = B.pa_workspace_layout(p)
                     wp = lo.work_page_tokens
@@ -225,7 +225,7 @@ def test_every_block_size_has_a_launch(B):
                     if kv == B.PA_E4M3 and D == 256 and R % 16 == 0 and 16 <= R <= 64 and bs in (16, 32, 64, 128):
                         # the tensor-core kernel: 128-token chunks, every row of a kv head in one segment
                         assert wp == 128 and lo.rows_per_segment == R and lo.row_blocks == 1
-                        assert lo.warps == lo.grid_ctas and lo.ring_pages_per_warp in (2, 3)
+                        assert lo.warps == lo.grid_ctas and lo.ring_pages_per_warp in (2, 3) and lo.group_size == 1
                         continue
                     if wp > bs:  # merged blocks
                         assert bs == 16 and wp == 32 and row_bytes <= 64 and lo.ring_pages_per_warp >= 2
