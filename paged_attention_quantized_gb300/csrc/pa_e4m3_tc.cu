@@ -45,7 +45,7 @@
 //    the last block that may hold NaN codes: 1Cat-vLLM PR #647, "Stop
 //    grouped-page4 null-block padding from leaking E4M3 NaN", Fix), write
 //    P^T (times 2^8, so small weights stay E4M3 normals; K-major, or MN-major
-//    at 64 rows), stage q' at each piece (and fetch the next piece's record
+//    at 32 and 64 rows), stage q' at each piece (and fetch the next piece's record
 //    and q rows ahead) and write the output at its end.
 // Every wait is bounded (PA_DEV_ERR_TIMEOUT); after a timeout every piece of
 // the CTA's share is written as NaN.
@@ -88,10 +88,12 @@ struct Lay {
     static constexpr int P_OFF = Q_OFF + Q_BYTES;    // P^T [2 buffers][3 terms x N rows][128 B]
     static constexpr int P_TERM = N * 128;
     static constexpr int P_BUF = 3 * P_TERM;
-    // at 64 rows P^T is stored MN-major (each token's 64 row values of a term
-    // contiguous, 64-byte swizzle, one 8 KB block per term), so a softmax
-    // group writes its 16 rows of a term with one 16-byte store
-    static constexpr bool PMN = (N == 64);
+    // at 32 and 64 rows P^T is stored MN-major (each token's N row values of
+    // a term contiguous, a 32- or 64-byte swizzle, one block of 128 N bytes
+    // per term), so a softmax group writes its 16 rows of a term with one
+    // 16-byte store
+    static constexpr bool PMN = (N == 64 || N == 32);
+    static constexpr uint32_t PMN_SWZ = (N == 64) ? 4u : 6u;  // descriptor swizzle: 64 B, 32 B
     static constexpr int NK = (N <= 48) ? 3 : 2;     // K stages
     static constexpr int NV = (N <= 16) ? 3 : 2;     // V stages
     static constexpr int K_OFF = P_OFF + 2 * P_BUF;
@@ -384,7 +386,9 @@ __global__ void __launch_bounds__(e4tc::Lay<N>::THREADS, 1)
 #pragma unroll
                     for (int k = 0; k < 4; ++k) {  // 32 tokens per step
                         const uint64_t ad = sdesc(vst + (uint32_t)(i * (CH * 128) + k * 32 * 128), 16, 1024, 2);
-                        const uint64_t bd = Y::PMN ? sdesc(pst + 2048 * k, 8192, 512, 4)  // 32 tokens x 64 B per step
+                        // MN-major: 32 tokens x N bytes per step, terms CH * N bytes apart,
+                        // 8-token groups 8 N bytes apart
+                        const uint64_t bd = Y::PMN ? sdesc(pst + 32 * N * k, CH * N, 8 * N, Y::PMN_SWZ)
                                                    : sdesc(pst + 32 * k, 16, 1024, 2);
                         mma_f8(dO, ad, bd, ID_O, (first && k == 0) ? 0u : 1u);
                     }
@@ -777,13 +781,15 @@ __global__ void __launch_bounds__(e4tc::Lay<N>::THREADS, 1)
                 }
             }
             if constexpr (Y::PMN) {
-                // token t's row of a term: 64 bytes (rows 0..63), 16-byte chunk wg at
-                // wg ^ ((t / 2) & 3) (64-byte swizzle); one 8 KB block per term
+                // token t's row of a term: N bytes (rows 0..N-1), 16-byte chunk wg at
+                // wg ^ ((t / 2) & 3) (64-byte swizzle, N = 64) or wg ^ ((t / 4) & 1)
+                // (32-byte swizzle, N = 32); one block of 128 N bytes per term
                 static_assert(NR == 16, "one 16-byte chunk per group and term");
-                const uint32_t off = (uint32_t)t * 64 + ((uint32_t)(wg ^ ((t >> 1) & 3)) << 4);
+                const uint32_t sw = (N == 64) ? (uint32_t)((t >> 1) & 3) : (uint32_t)((t >> 2) & 1);
+                const uint32_t off = (uint32_t)t * N + ((uint32_t)wg ^ sw) * 16u;
 #pragma unroll
                 for (int tm = 0; tm < 3; ++tm)
-                    *reinterpret_cast<uint4 *>(pt + tm * (CH * 64) + off) =
+                    *reinterpret_cast<uint4 *>(pt + tm * (CH * N) + off) =
                         make_uint4(pw[tm][0], pw[tm][1], pw[tm][2], pw[tm][3]);
             }
 
